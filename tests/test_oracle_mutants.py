@@ -1,0 +1,75 @@
+"""The pins have teeth: plant one plausible mistake at a time in a copy of the
+oracle's C source (on the CPU), build it, and check that at least one pin in
+``test_oracle_pins`` fails against the mutant.  The real oracle is untouched."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "bit1_oracle.c")
+
+# (name, text in the source, replacement, pins expected to catch it)
+MUTANTS = [
+    ("msb_first_bit_order", "return (bits[n * (K / 8) + k / 8] >> (k % 8)) & 1;",
+     "return (bits[n * (K / 8) + k / 8] >> (7 - k % 8)) & 1;",
+     [lambda o: pins.test_gemv_brute_force_matches_dense(o, 8, 256, 1, 0),
+      lambda o: pins.test_closed_form_single_bit(o)]),
+    ("sign_polarity", "if (orc_bit(bits, K, n, k))", "if (!orc_bit(bits, K, n, k))",
+     [lambda o: pins.test_gemv_brute_force_matches_dense(o, 8, 256, 1, 0),
+      lambda o: pins.test_closed_form_all_bits_set_and_clear(o)]),
+    ("scale_index_transposed", "double s = orc_half_to_double(scales[n * G + g]);",
+     "double s = orc_half_to_double(scales[g * N + n]);",
+     [lambda o: pins.test_gemv_scales_are_per_row_and_group(o)]),
+    ("last_group_dropped", "for (int64_t g = 0; g < G; g++) {\n                double s",
+     "for (int64_t g = 0; g < G - 1; g++) {\n                double s",
+     [lambda o: pins.test_gemv_brute_force_matches_dense(o, 5, 256, 3, 1)]),
+    ("batch_row_ignored", "double xv = orc_bf16_to_double(x[b * K + k]);",
+     "double xv = orc_bf16_to_double(x[k]);",
+     [lambda o: pins.test_gemv_brute_force_matches_dense(o, 5, 256, 3, 1)]),
+    ("half_exponent_bias", "v = ldexp((double)(m + 1024), e - 25);",
+     "v = ldexp((double)(m + 1024), e - 24);",
+     [lambda o: pins.test_half_decode_all_patterns(o)]),
+    ("bf16_subnormal_scale", "v = ldexp((double)m, -133);", "v = ldexp((double)m, -126);",
+     [lambda o: pins.test_bf16_decode_all_patterns(o)]),
+    ("half_rounding_truncates", "n = nearbyint(a / q);", "n = floor(a / q);",
+     [lambda o: pins.test_double_to_half_matches_numpy(o)]),
+    ("xor_skips_last_byte", "for (int64_t j = 0; j < K / 8; j++)\n            bits[r * (K / 8) + j] ^= 0xFF;",
+     "for (int64_t j = 0; j < K / 8 - 1; j++)\n            bits[r * (K / 8) + j] ^= 0xFF;",
+     [lambda o: pins.test_xor_patch_flips_listed_rows_only(o)]),
+    ("xor_range_error_swallowed", "if (rows[i] < 0 || (int64_t)rows[i] >= N)\n            return ORC_ERANGE;",
+     "if (rows[i] < 0 || (int64_t)rows[i] >= N)\n            return ORC_OK;",
+     [lambda o: pins.test_xor_patch_range_checked_before_any_change(o)]),
+    ("pack_wrong_divisor", "mean = sum / 128.0;", "mean = sum / 127.0;",
+     [lambda o: pins.test_pack_scale_is_fp16_of_mean_abs(o), lambda o: pins.test_pack_round_trip(o)]),
+    ("pack_zero_is_negative", "if (!(v < 0.0))", "if (v > 0.0)",
+     [lambda o: pins.test_pack_bits_are_sign_test_little_endian(o)]),
+    ("footprint_scale_bytes", "return N * K / 8 + 2 * N * (K / 128);", "return N * K / 8 + N * (K / 128);",
+     [lambda o: pins.test_footprint_is_1_125_bits_per_weight(o)]),
+]
+
+
+@pytest.mark.parametrize("name,old,new,checks", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new, checks):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not unique/found"
+    mpath = tmp_path / "mutant.c"
+    mpath.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-D_GNU_SOURCE", "-shared", "-fPIC", "-pthread",
+                    str(mpath), "-o", str(so), "-lm"], check=True)
+    saved = oracle._lib
+    oracle._lib = oracle.configure(ctypes.CDLL(str(so)))
+    caught = 0
+    try:
+        for chk in checks:
+            try:
+                chk(oracle)
+            except (AssertionError, oracle.OracleError):
+                caught += 1
+    finally:
+        oracle._lib = saved
+    assert caught >= 1, f"mutant {name} survived every pin"

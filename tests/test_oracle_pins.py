@@ -1,0 +1,392 @@
+"""Pins for the CPU oracle, against things other than the oracle itself.
+
+Each test ties one part of the oracle to a fact the pages or plain mathematics
+fix: library routines for the special cases that reduce to them (numpy's
+float16 conversion, numpy's little-endian unpackbits plus a dense fp64 matmul),
+closed forms (all bits set, all bits clear, one bit set), invariants (a whole
+row flipped negates that output exactly; the XOR patch is its own inverse),
+the footprint figures printed on the pages, and brute force over every 16-bit
+pattern.  A plausible slip in the oracle (bit order, sign polarity, scale
+index, a dropped group, a double rounding) fails at least one of them.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from bit_weight_gemv_sign_b300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "pages_figures.json")
+
+
+# ---------------------------------------------------------------- decoding
+
+def test_half_decode_all_patterns(orc):
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = pats.view(np.float16).astype(np.float64)        # library conversion
+    got = np.array([orc.half_to_double(int(p)) for p in pats])
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all()
+    assert np.array_equal(np.signbit(got[~np.isnan(got)]), np.signbit(ref[~np.isnan(ref)]))
+
+
+def test_bf16_decode_all_patterns(orc):
+    pats = np.arange(65536, dtype=np.int64).astype(np.uint16)
+    ref = torch.from_numpy(pats.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([orc.bf16_to_double(int(p)) for p in pats])
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all()
+
+
+# ---------------------------------------------------------------- rounding
+
+def _edge_doubles(rng, n):
+    mags = np.exp2(rng.uniform(-30, 20, size=n))
+    sgn = np.where(rng.integers(0, 2, size=n) == 1, 1.0, -1.0)
+    return mags * sgn
+
+
+def test_double_to_half_matches_numpy(orc):
+    rng = np.random.default_rng(1)
+    vals = list(_edge_doubles(rng, 4000))
+    # exact ties between neighbouring fp16 values (normal and subnormal),
+    # the overflow boundary and signed zeros
+    grid = np.arange(0, 0x7c00, 97, dtype=np.uint16).view(np.float16).astype(np.float64)
+    vals += list((grid[:-1] + grid[1:]) / 2)
+    sub = np.arange(0, 1024, dtype=np.uint16).view(np.float16).astype(np.float64)
+    vals += list((sub[:-1] + sub[1:]) / 2)
+    vals += [65504.0, 65519.99, 65520.0, 70000.0, 0.0, -0.0, 2.0 ** -25, 2.0 ** -26, -2.0 ** -25 * 3]
+    vals = np.array(vals, dtype=np.float64)
+    ref = vals.astype(np.float16).view(np.uint16)          # numpy: direct RNE
+    got = np.array([orc.double_to_half(v) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def _bf16_grid():
+    """Every finite non-negative bf16 value, plus IEEE's virtual next grid
+    point 2^128 standing for +inf (pattern 0x7f80, even), so that overflow
+    follows the same nearest/ties-to-even rule."""
+    pats = np.arange(0, 0x7f80, dtype=np.int64)  # +0 .. max finite
+    vals = torch.from_numpy(pats.astype(np.uint16).view(np.int16)).view(torch.bfloat16)
+    vals = vals.to(torch.float64).numpy()
+    return np.append(pats, 0x7f80), np.append(vals, 2.0 ** 128)
+
+
+def test_double_to_bf16_is_nearest_even(orc):
+    pats, grid = _bf16_grid()
+    rng = np.random.default_rng(2)
+    vals = list(np.abs(_edge_doubles(rng, 3000)))
+    vals += list((grid[:-2:37] + grid[1:-1:37]) / 2)         # exact ties
+    vals += [0.0, 2.0 ** -140, 1e-45, 3.0e38, 3.4e38, 2.0 ** 128 - 2.0 ** 119,
+             2.0 ** 128 - 2.0 ** 119 - 2.0 ** 90]
+    for v in vals:
+        got = orc.double_to_bf16(v)
+        i = np.searchsorted(grid, v)
+        cands = [j for j in (i - 1, i) if 0 <= j < len(grid)]
+        dist = [abs(grid[j] - v) for j in cands]
+        best = min(dist)
+        near = [cands[t] for t in range(len(cands)) if dist[t] == best]
+        if len(near) > 1:
+            near = [j for j in near if pats[j] % 2 == 0]
+        exp = int(pats[near[0]])
+        assert got == exp, (v, hex(got), hex(exp))
+        neg = orc.double_to_bf16(-v)
+        assert neg == (exp | 0x8000)
+
+
+# ---------------------------------------------------------------- GEMV
+
+def _dense(bits, scales, x, N, K):
+    """Independent route: numpy's little-endian unpackbits, dequantise to a
+    dense fp64 matrix, then a library matmul."""
+    b = np.unpackbits(bits.reshape(N, K // 8), axis=1, bitorder="little")
+    sgn = np.where(b == 1, 1.0, -1.0)
+    s = scales.reshape(N, K // 128).view(np.float16).astype(np.float64)
+    W = sgn * np.repeat(s, 128, axis=1)
+    X = torch.from_numpy(x.reshape(-1, K).view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    return X @ W.T, W, X
+
+
+def _bound(W, X):
+    return np.abs(X) @ np.abs(W).T
+
+
+@pytest.mark.parametrize("N,K,B", [(1, 128, 1), (3, 128, 2), (5, 256, 3), (8, 256, 1), (7, 384, 2)])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_gemv_brute_force_matches_dense(orc, N, K, B, seed):
+    g = synth.rng(100 + seed)
+    bits = synth.sign_bits(N, K, g)
+    scales = synth.group_scales(N, K, g, offset=1e-3)
+    x = synth.activations(B, K, g)
+    y = orc.gemv(bits, scales, x, B, N, K)
+    ref, W, X = _dense(bits, scales, x, N, K)
+    tol = 1e-12 * _bound(W, X) + 1e-300
+    assert np.all(np.abs(y - ref) <= tol)
+    # third route: torch fp64 matmul on the same dense matrix
+    ref2 = (torch.from_numpy(X) @ torch.from_numpy(W).T).numpy()
+    assert np.all(np.abs(y - ref2) <= tol)
+
+
+def test_gemv_scales_are_per_row_and_group(orc):
+    """Distinct scale per (row, group): a transposed or shifted scale index
+    changes the result."""
+    N, K, B = 3, 384, 1
+    bits = np.full((N, K // 8), 0xFF, dtype=np.uint8)
+    svals = np.array([[1, 2, 4], [8, 16, 32], [64, 128, 256]], dtype=np.float16)
+    x = synth.to_bf16_bits(np.concatenate([np.full(128, 1.0), np.full(128, 3.0),
+                                           np.full(128, 5.0)]).astype(np.float32)[None])
+    y = orc.gemv(bits, svals.view(np.uint16), x, B, N, K)
+    want = np.array([[128 * (1 * 1 + 2 * 3 + 4 * 5), 128 * (8 + 16 * 3 + 32 * 5),
+                      128 * (64 + 128 * 3 + 256 * 5)]], dtype=np.float64)
+    assert np.array_equal(y, want)
+
+
+def test_closed_form_all_bits_set_and_clear(orc):
+    N, K, B = 6, 512, 2
+    g = synth.rng(7)
+    scales = synth.group_scales(N, K, g)
+    x = synth.activations(B, K, g)
+    ones = np.full((N, K // 8), 0xFF, dtype=np.uint8)
+    zeros = np.zeros((N, K // 8), dtype=np.uint8)
+    y1 = orc.gemv(ones, scales, x, B, N, K)
+    y0 = orc.gemv(zeros, scales, x, B, N, K)
+    s = scales.view(np.float16).astype(np.float64)
+    X = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    gs = X.reshape(B, K // 128, 128).sum(axis=2)            # sum_k x_k per group
+    closed = gs @ s.T                                        # sum_g s_g * sum_k x_k
+    bound = np.abs(X).reshape(B, K // 128, 128).sum(axis=2) @ s.T
+    assert np.all(np.abs(y1 - closed) <= 1e-12 * bound)
+    assert np.array_equal(y0, -y1)                           # exact negation
+
+
+def test_closed_form_single_bit(orc):
+    N, K, B = 1, 256, 1
+    g = synth.rng(8)
+    scales = synth.group_scales(N, K, g, offset=1e-3)
+    x = synth.activations(B, K, g)
+    s = scales.view(np.float16).astype(np.float64)[0]
+    X = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()[0]
+    base = -(s[0] * X[:128].sum() + s[1] * X[128:].sum())
+    for k in (0, 1, 7, 8, 127, 128, 200, 255):
+        bits = np.zeros((1, K // 8), dtype=np.uint8)
+        bits[0, k // 8] = 1 << (k % 8)
+        y = orc.gemv(bits, scales, x, B, N, K)[0, 0]
+        want = base + 2 * s[k // 128] * X[k]
+        assert abs(y - want) <= 1e-12 * (np.abs(X[:128]).sum() * s[0] + np.abs(X[128:]).sum() * s[1])
+
+
+def test_row_flip_negates_exactly(orc):
+    N, K, B = 9, 1024, 2
+    bits, scales = synth.matrix(N, K, 11)
+    x = synth.x_for(B, K, 11)
+    y = orc.gemv(bits, scales, x, B, N, K)
+    for r in (0, 4, 8):
+        fl = bits.copy()
+        fl[r] ^= 0xFF
+        yf = orc.gemv(fl, scales, x, B, N, K)
+        assert np.array_equal(yf[:, r], -y[:, r])
+        others = [i for i in range(N) if i != r]
+        assert np.array_equal(yf[:, others], y[:, others])
+
+
+def test_gemv_select_and_threads_agree(orc):
+    N, K, B = 37, 1024, 2
+    bits, scales = synth.matrix(N, K, 12)
+    x = synth.x_for(B, K, 12)
+    y = orc.gemv(bits, scales, x, B, N, K)
+    rows = [0, 5, 36, 5]
+    ys = orc.gemv_select(bits, scales, x, B, N, K, rows)
+    assert np.array_equal(ys, y[:, rows])
+    yt = orc.gemv_threads(bits, scales, x, B, N, K, 4)
+    assert np.array_equal(yt, y)
+
+
+def test_gemv_rejects_bad_shapes(orc):
+    bits = np.zeros((2, 24), dtype=np.uint8)
+    scales = np.zeros((2, 2), dtype=np.uint16)
+    x = np.zeros((1, 192), dtype=np.uint16)
+    with pytest.raises(orc.OracleError) as e:
+        orc.gemv(bits, scales, x, 1, 2, 192)
+    assert e.value.status == orc.ESHAPE
+
+
+# ---------------------------------------------------------------- XOR patch
+
+def test_xor_patch_flips_listed_rows_only(orc):
+    N, K = 16, 1024
+    bits, _ = synth.matrix(N, K, 13)
+    rows = [3, 9, 15]
+    p = orc.xor_patch(bits, N, K, rows)
+    ub = np.unpackbits(bits, axis=1, bitorder="little")
+    up = np.unpackbits(p, axis=1, bitorder="little")
+    for r in range(N):
+        if r in rows:
+            assert np.array_equal(up[r], 1 - ub[r])           # every bit complemented
+        else:
+            assert np.array_equal(up[r], ub[r])
+
+
+def test_xor_patch_is_self_inverse_and_duplicates_cancel(orc):
+    N, K = 32, 512
+    bits, _ = synth.matrix(N, K, 14)
+    rows = synth.distinct_rows(N, 8, 0)
+    once = orc.xor_patch(bits, N, K, rows)
+    twice = orc.xor_patch(once, N, K, rows)
+    assert np.array_equal(twice, bits)
+    assert not np.array_equal(once, bits)
+    dup = orc.xor_patch(bits, N, K, [5, 5, 7])
+    assert np.array_equal(dup, orc.xor_patch(bits, N, K, [7]))
+
+
+def test_xor_patch_range_checked_before_any_change(orc):
+    N, K = 8, 256
+    bits, _ = synth.matrix(N, K, 15)
+    for bad in ([1, 8], [-1], [0, 2, 100]):
+        assert orc.xor_patch_status(bits, N, K, bad) == orc.ERANGE
+    with pytest.raises(orc.OracleError):
+        orc.xor_patch(bits, N, K, [8])
+
+
+def test_xor_patch_negates_gemv_rows(orc):
+    N, K, B = 12, 1024, 1
+    bits, scales = synth.matrix(N, K, 16)
+    x = synth.x_for(B, K, 16)
+    rows = [2, 7]
+    y = orc.gemv(bits, scales, x, B, N, K)
+    yp = orc.gemv(orc.xor_patch(bits, N, K, rows), scales, x, B, N, K)
+    assert np.array_equal(yp[:, rows], -y[:, rows])
+    keep = [i for i in range(N) if i not in rows]
+    assert np.array_equal(yp[:, keep], y[:, keep])
+
+
+# ---------------------------------------------------------------- packing
+
+def test_pack_round_trip(orc):
+    """Dequantise (bits, s) with s > 0, pack again: identical bits and scales
+    (the mean of 128 equal magnitudes is exact)."""
+    N, K = 6, 512
+    bits, scales = synth.matrix(N, K, 17, scale_offset=1e-3)
+    _, W, _ = _dense(bits, scales, np.zeros((1, K), dtype=np.uint16), N, K)
+    for dtype, arr in ((orc.F32, W.astype(np.float32)),
+                       (orc.F16, W.astype(np.float16).view(np.uint16)),
+                       (orc.BF16, None)):
+        if dtype == orc.BF16:
+            continue  # fp16 scales are not all exactly representable in bf16
+        st, b2, s2 = orc.pack(arr, dtype, N, K)
+        assert st == orc.OK
+        assert np.array_equal(b2, bits)
+        assert np.array_equal(s2, scales)
+
+
+def test_pack_bits_are_sign_test_little_endian(orc):
+    N, K = 4, 256
+    w = synth.fp_weights(N, K, 18)
+    w[0, :5] = [0.0, -0.0, 1e-30, -1e-30, 3.0]
+    st, b, _ = orc.pack(w, orc.F32, N, K)
+    assert st == orc.OK
+    want = np.packbits(~(w < 0), axis=1, bitorder="little")   # library packing
+    assert np.array_equal(b, want)
+    assert np.unpackbits(b[:1, :1], bitorder="little")[:5].tolist() == [1, 1, 1, 0, 1]
+
+
+def test_pack_scale_is_fp16_of_mean_abs(orc):
+    N, K = 5, 384
+    w = synth.fp_weights(N, K, 19)
+    st, _, s = orc.pack(w, orc.F32, N, K)
+    assert st == orc.OK
+    mean = np.abs(w.astype(np.float64)).reshape(N, K // 128, 128).mean(axis=2)
+    assert np.array_equal(s, mean.astype(np.float16).view(np.uint16))
+    # all-equal magnitudes: the scale is that magnitude exactly
+    w2 = np.full((1, 128), -0.375, dtype=np.float32)
+    st, b2, s2 = orc.pack(w2, orc.F32, 1, 128)
+    assert st == orc.OK and s2[0, 0] == np.float16(0.375).view(np.uint16) and not b2.any()
+
+
+def test_pack_scale_minimises_squared_error(orc):
+    """mean|w| minimises sum (w - s*sign(w))^2 over s (least squares); no
+    perturbation of the unrounded mean does better."""
+    w = synth.fp_weights(1, 128, 20).astype(np.float64)[0]
+    sg = np.where(w < 0, -1.0, 1.0)
+    m = np.abs(w).sum() / 128
+    err = lambda s: ((w - s * sg) ** 2).sum()
+    for d in (1e-2, 1e-4, 1e-6):
+        assert err(m) <= err(m * (1 + d)) and err(m) <= err(m * (1 - d))
+
+
+def test_pack_flags_nan_and_overflow(orc):
+    w = synth.fp_weights(2, 128, 21)
+    w[1, 3] = np.nan
+    st, _, _ = orc.pack(w, orc.F32, 2, 128)
+    assert st == orc.ENAN
+    w = np.full((1, 128), 70000.0, dtype=np.float32)
+    st, _, _ = orc.pack(w, orc.F32, 1, 128)
+    assert st == orc.ERANGE
+    w = np.full((1, 128), 65504.0, dtype=np.float32)
+    st, _, s = orc.pack(w, orc.F32, 1, 128)
+    assert st == orc.OK and s[0, 0] == 0x7bff
+
+
+def test_pack_accepts_bf16_and_fp16_inputs(orc):
+    N, K = 3, 256
+    w32 = synth.fp_weights(N, K, 22)
+    wb = synth.to_bf16_bits(w32)
+    wh = w32.astype(np.float16)
+    st, bb, sb = orc.pack(wb, orc.BF16, N, K)
+    assert st == orc.OK
+    wb64 = torch.from_numpy(wb.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(sb, np.abs(wb64).reshape(N, 2, 128).mean(axis=2).astype(np.float16).view(np.uint16))
+    assert np.array_equal(bb, np.packbits(~(wb64 < 0), axis=1, bitorder="little"))
+    st, bh, sh = orc.pack(wh.view(np.uint16), orc.F16, N, K)
+    assert st == orc.OK
+    assert np.array_equal(bh, np.packbits(~(wh < 0), axis=1, bitorder="little"))
+
+
+# ---------------------------------------------------------------- footprint
+
+def test_footprint_is_1_125_bits_per_weight(orc):
+    fig = json.load(open(GOLDEN))
+    beff = fig["b_eff_binary_bits_per_weight"]["value"]
+    for N, K in ((1, 128), (256, 1024), (12288, 4096), (4096, 12288), (17408, 5120)):
+        assert orc.footprint_bytes(N, K) * 8 == beff * N * K
+        assert orc.footprint_bytes(N, K) == N * K // 8 + 2 * N * (K // 128)
+    assert round(16 / beff, fig["compression_binary_vs_fp16"]["printed_digits"]) == \
+        fig["compression_binary_vs_fp16"]["value"]
+    hn = fig["hn_group_framing"]
+    assert 1 + hn["scale_bits"] / hn["group_size"] == hn["bits_per_weight"]
+
+
+def test_footprint_8b_class_matches_printed_size(orc):
+    """The 8B-class decoder shapes plus the embedding (151936 x 4096, also
+    1-bit) give about 8.2 B parameters in about 1.15 GB."""
+    fig = json.load(open(GOLDEN))
+    mats = synth.sweep_8b()
+    params = sum(m.N * m.K for m in mats) + 151936 * 4096
+    nbytes = sum(orc.footprint_bytes(m.N, m.K) for m in mats) + orc.footprint_bytes(151936, 4096)
+    assert round(params / 1e9, 1) == fig["bonsai_8b_parameters"]["value"] / 1e9
+    assert round(nbytes / 1e9, 2) == fig["bonsai_8b_gigabytes"]["value"]
+    assert nbytes == 1_151_778_816
+    swept = sum(orc.footprint_bytes(m.N, m.K) for m in mats)
+    assert swept == 1_064_263_680
+
+
+def test_footprint_27b_matches_printed_size(orc):
+    fig = json.load(open(GOLDEN))
+    sp = fig["bonsai_27b_parameter_split"]
+    total = sp["language_model"] + sp["vision_tower"] + sp["embedding_and_lm_head"]
+    gb = total * fig["b_eff_binary_bits_per_weight"]["value"] / 8 / 1e9
+    assert round(gb, 1) == fig["bonsai_27b_binary_gigabytes"]["value"]
+    assert round(total * 2 / 1e9) == pytest.approx(fig["bonsai_27b_fp16_gigabytes"]["value"], abs=2)
+    swept = sum(orc.footprint_bytes(m.N, m.K) for m in synth.sweep_27b())
+    assert swept == 2_972_712_960
+
+
+def test_patch_list_size_is_kilobyte_scale():
+    """100 (layer u16, projection u8, row u32) entries are 700 bytes of
+    payload: the same order as the 840 B - 1.1 KB patches on the page."""
+    fig = json.load(open(GOLDEN))["bankai_patch_bytes"]
+    entries = synth.patch_entries_27b(100, 0)
+    assert len(set(entries)) == 100
+    payload = len(entries) * (2 + 1 + 4)
+    assert fig["min"] / 2 <= payload <= fig["max"]
