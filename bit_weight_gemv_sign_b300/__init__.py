@@ -1,1 +1,199 @@
-"""placeholder"""
+"""Python binding of the bit1 C ABI (include/bit1.h): true 1-bit weights
+(sign bit + one fp16 scale per 128 inputs) on NVIDIA B300.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libbit1.so``.  PyTorch provides device memory and streams.  If the
+library has not been built (``python -m bit_weight_gemv_sign_b300.build``)
+every call raises; there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "Bit1Error", "OK", "EINVAL", "ESHAPE", "ERANGE", "ECUDA", "ENAN",
+    "F32", "BF16", "F16", "AUTO", "SIMPLE", "LUT", "SPLITK", "TC", "FLAG_PDL",
+    "bit1_pack", "bit1_pack_flags_status", "bit1_gemv", "bit1_gemv_ex",
+    "bit1_gemv_workspace_bytes", "bit1_gemv_pick", "bit1_gemv_launches",
+    "bit1_xor_patch", "bit1_status_str", "bit1_version", "library_path", "load",
+]
+
+OK, EINVAL, ESHAPE, ERANGE, ECUDA, ENAN = 0, 1, 2, 3, 4, 5
+F32, BF16, F16 = 0, 1, 2
+AUTO, SIMPLE, LUT, SPLITK, TC = 0, 1, 2, 3, 4
+FLAG_PDL = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libbit1.so")
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+class Bit1Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {bit1_status_str(status)} (status {status})")
+
+
+def load():
+    """Load libbit1.so (raises if it is missing: the CUDA path is the only path)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"bit1 CUDA library not found at {_LIB_PATH}; build it with "
+                "`python -m bit_weight_gemv_sign_b300.build` (no CPU fallback exists)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        p, i64, i32, u32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32, ctypes.c_size_t
+        lib.bit1_pack.argtypes = [p, i32, i64, i64, p, p, p, p]
+        lib.bit1_pack.restype = i32
+        lib.bit1_pack_flags_status.argtypes = [u32]
+        lib.bit1_pack_flags_status.restype = i32
+        lib.bit1_gemv.argtypes = [p, p, p, i64, i64, i64, p, i32, p, sz, p]
+        lib.bit1_gemv.restype = i32
+        lib.bit1_gemv_ex.argtypes = [p, p, p, i64, i64, i64, p, i32, p, sz, i32, ctypes.c_uint, p]
+        lib.bit1_gemv_ex.restype = i32
+        lib.bit1_gemv_workspace_bytes.argtypes = [i64, i64, i64]
+        lib.bit1_gemv_workspace_bytes.restype = sz
+        lib.bit1_gemv_pick.argtypes = [i64, i64, i64, sz]
+        lib.bit1_gemv_pick.restype = i32
+        lib.bit1_gemv_launches.argtypes = [i64, i64, i64, i32]
+        lib.bit1_gemv_launches.restype = i32
+        lib.bit1_xor_patch.argtypes = [p, i64, i64, p, i64, p]
+        lib.bit1_xor_patch.restype = i32
+        lib.bit1_status_str.argtypes = [i32]
+        lib.bit1_status_str.restype = ctypes.c_char_p
+        lib.bit1_version.argtypes = []
+        lib.bit1_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def bit1_status_str(status: int) -> str:
+    return load().bit1_status_str(int(status)).decode()
+
+
+def bit1_version() -> str:
+    return load().bit1_version().decode()
+
+
+# ---------------------------------------------------------------- helpers
+
+def _stream(stream) -> int:
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dptr(t, name: str, dtype=None) -> int:
+    import torch
+    if t is None:
+        return 0
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    if dtype is not None and t.dtype not in dtype:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtype}")
+    return t.data_ptr()
+
+
+def _check(st: int, where: str):
+    if st != OK:
+        raise Bit1Error(st, where)
+
+
+_DT = {"float32": F32, "bfloat16": BF16, "float16": F16}
+
+
+# ---------------------------------------------------------------- entry points
+
+def bit1_pack(w, bits=None, scales=None, flags=None, stream=None):
+    """Pack fp32/bf16/fp16 weights [N, K] (CUDA tensor) into (bits uint8 [N, K/8],
+    scales int16 [N, K/128] holding fp16 patterns).  ``flags`` (int32 [1] CUDA
+    tensor) receives the NaN / range flag word; read it with
+    ``bit1_pack_flags_status(int(flags.item()))`` after synchronising."""
+    import torch
+    N, K = w.shape
+    if bits is None:
+        bits = torch.empty((N, K // 8), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((N, max(K // 128, 1)), dtype=torch.int16, device=w.device)
+    dt = _DT.get(str(w.dtype).replace("torch.", ""))
+    if dt is None:
+        raise TypeError(f"unsupported weight dtype {w.dtype}")
+    st = load().bit1_pack(_dptr(w, "w"), dt, N, K, _dptr(bits, "bits"), _dptr(scales, "scales"),
+                          _dptr(flags, "flags"), _stream(stream))
+    _check(st, "bit1_pack")
+    return bits, scales
+
+
+def bit1_pack_flags_status(flags: int) -> int:
+    return int(load().bit1_pack_flags_status(int(flags) & 0xFFFFFFFF))
+
+
+def bit1_gemv_ex(bits, scales, x, y=None, y_dtype=None, workspace=None, variant=AUTO, flags=0,
+                 stream=None, N=None, K=None):
+    """y[B, N] = x[B, K] (bf16) times the packed 1-bit matrix (bits [N, K/8],
+    scales [N, K/128] fp16 patterns).  Returns y (fp32 unless y_dtype/BF16)."""
+    import torch
+    B = x.shape[0] if x.dim() == 2 else 1
+    K = x.shape[-1] if K is None else K
+    N = bits.shape[0] if N is None else N
+    if y is None:
+        yt = torch.bfloat16 if y_dtype == BF16 else torch.float32
+        y = torch.empty((B, N), dtype=yt, device=x.device)
+    ydt = BF16 if y.dtype == torch.bfloat16 else F32
+    if y.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("y must be float32 or bfloat16")
+    ws_ptr, ws_bytes = 0, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dptr(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    st = load().bit1_gemv_ex(_dptr(bits, "bits"), _dptr(scales, "scales"), _dptr(x, "x"),
+                             B, N, K, _dptr(y, "y"), ydt, ws_ptr, ws_bytes, int(variant),
+                             int(flags), _stream(stream))
+    _check(st, "bit1_gemv")
+    return y
+
+
+def bit1_gemv(bits, scales, x, y=None, y_dtype=None, workspace=None, stream=None):
+    return bit1_gemv_ex(bits, scales, x, y=y, y_dtype=y_dtype, workspace=workspace,
+                        variant=AUTO, flags=0, stream=stream)
+
+
+def bit1_gemv_workspace_bytes(B: int, N: int, K: int) -> int:
+    return int(load().bit1_gemv_workspace_bytes(B, N, K))
+
+
+def bit1_gemv_pick(B: int, N: int, K: int, ws_bytes: int = 0) -> int:
+    return int(load().bit1_gemv_pick(B, N, K, ws_bytes))
+
+
+def bit1_gemv_launches(B: int, N: int, K: int, variant: int = AUTO) -> int:
+    return int(load().bit1_gemv_launches(B, N, K, variant))
+
+
+def bit1_xor_patch(bits, rows, N=None, K=None, stream=None):
+    """Flip every sign bit of the listed rows of ``bits`` in place (rows: a
+    host sequence of ints).  Applying the same list again removes the patch."""
+    import numpy as np
+    N = bits.shape[0] if N is None else N
+    K = bits.shape[1] * 8 if K is None else K
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1))
+    st = load().bit1_xor_patch(_dptr(bits, "bits"), N, K, r.ctypes.data if r.size else None,
+                               r.size, _stream(stream))
+    _check(st, "bit1_xor_patch")
+    return bits

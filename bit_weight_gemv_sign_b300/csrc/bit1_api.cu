@@ -1,0 +1,165 @@
+// C ABI of the bit1 library: argument validation (on the host, before any
+// CUDA call, so that a rejected call launches and modifies nothing), kernel
+// selection and launch.  Declarations and their documentation: bit1.h.
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace bit1 {
+
+cudaError_t launch(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                   bool pdl, void** args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelExC(&cfg, func, args);
+}
+
+int sm_count() {
+    static int cached[64];
+    static std::once_flag once[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+    std::call_once(once[dev], [dev] {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        cached[dev] = v;
+    });
+    return cached[dev];
+}
+
+}  // namespace bit1
+
+using namespace bit1;
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool shape_ok(int64_t B, int64_t N, int64_t K) {
+    return B >= 1 && N >= 1 && K >= 128 && K % 128 == 0 && B <= 0x7fffffffLL &&
+           N <= 0x7fffffffLL && K <= (1LL << 24);
+}
+
+bit1_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BIT1_OK : BIT1_ECUDA; }
+
+int pick_variant(int64_t B, int64_t N, int64_t K, size_t ws_bytes) {
+    (void)ws_bytes;
+    if (lut_supported(B, N, K)) return BIT1_GEMV_LUT;
+    return BIT1_GEMV_SIMPLE;
+}
+
+}  // namespace
+
+extern "C" {
+
+bit1_status bit1_pack(const void* w, int w_dtype, int64_t N, int64_t K, uint8_t* bits,
+                      uint16_t* scales, uint32_t* d_flags, bit1_stream_t stream) {
+    if (!shape_ok(1, N, K)) return BIT1_ESHAPE;
+    if (!w || !bits || !scales) return BIT1_EINVAL;
+    if (w_dtype != BIT1_F32 && w_dtype != BIT1_BF16 && w_dtype != BIT1_F16) return BIT1_EINVAL;
+    if (!aligned16(w) || !aligned16(bits) || !aligned16(scales)) return BIT1_EINVAL;
+    if (d_flags && ((uintptr_t)d_flags & 3u)) return BIT1_EINVAL;
+    return from_cuda(launch_pack(w, w_dtype, N, K, bits, scales, d_flags, (cudaStream_t)stream));
+}
+
+bit1_status bit1_pack_flags_status(uint32_t flags) {
+    if (flags & 1u) return BIT1_ENAN;
+    if (flags & 2u) return BIT1_ERANGE;
+    return BIT1_OK;
+}
+
+bit1_status bit1_gemv_ex(const uint8_t* bits, const uint16_t* scales, const uint16_t* x,
+                         int64_t B, int64_t N, int64_t K, void* y, int y_dtype, void* workspace,
+                         size_t ws_bytes, int variant, unsigned flags, bit1_stream_t stream) {
+    if (!shape_ok(B, N, K)) return BIT1_ESHAPE;
+    if (!bits || !scales || !x || !y) return BIT1_EINVAL;
+    if (!aligned16(bits) || !aligned16(scales) || !aligned16(x) || !aligned16(y)) return BIT1_EINVAL;
+    if (y_dtype != BIT1_F32 && y_dtype != BIT1_BF16) return BIT1_EINVAL;
+    if (ws_bytes > 0 && (!workspace || !aligned16(workspace))) return BIT1_EINVAL;
+    if (flags & ~BIT1_FLAG_PDL) return BIT1_EINVAL;
+    if (variant == BIT1_GEMV_AUTO) variant = pick_variant(B, N, K, ws_bytes);
+    GemvArgs a;
+    a.bits = bits; a.scales = scales; a.x = x;
+    a.B = B; a.N = N; a.K = K;
+    a.y = y; a.y_bf16 = (y_dtype == BIT1_BF16);
+    a.workspace = workspace; a.ws_bytes = ws_bytes;
+    a.pdl = (flags & BIT1_FLAG_PDL) != 0;
+    a.stream = (cudaStream_t)stream;
+    switch (variant) {
+        case BIT1_GEMV_SIMPLE:
+            return from_cuda(launch_gemv_simple(a));
+        case BIT1_GEMV_LUT:
+            if (!lut_supported(B, N, K)) return BIT1_ESHAPE;
+            return from_cuda(launch_gemv_lut(a));
+        case BIT1_GEMV_SPLITK:
+        case BIT1_GEMV_TC:
+            return BIT1_ESHAPE;  // not available for any shape in this build
+        default:
+            return BIT1_EINVAL;
+    }
+}
+
+bit1_status bit1_gemv(const uint8_t* bits, const uint16_t* scales, const uint16_t* x, int64_t B,
+                      int64_t N, int64_t K, void* y, int y_dtype, void* workspace, size_t ws_bytes,
+                      bit1_stream_t stream) {
+    return bit1_gemv_ex(bits, scales, x, B, N, K, y, y_dtype, workspace, ws_bytes, BIT1_GEMV_AUTO,
+                        0u, stream);
+}
+
+size_t bit1_gemv_workspace_bytes(int64_t B, int64_t N, int64_t K) {
+    if (!shape_ok(B, N, K)) return 0;
+    return 0;
+}
+
+int bit1_gemv_pick(int64_t B, int64_t N, int64_t K, size_t ws_bytes) {
+    if (!shape_ok(B, N, K)) return 0;
+    return pick_variant(B, N, K, ws_bytes);
+}
+
+int bit1_gemv_launches(int64_t B, int64_t N, int64_t K, int variant) {
+    if (!shape_ok(B, N, K)) return 0;
+    if (variant == BIT1_GEMV_AUTO) variant = pick_variant(B, N, K, 0);
+    switch (variant) {
+        case BIT1_GEMV_SIMPLE: return 1;
+        case BIT1_GEMV_LUT: return lut_supported(B, N, K) ? 1 : 0;
+        default: return 0;
+    }
+}
+
+bit1_status bit1_xor_patch(uint8_t* bits, int64_t N, int64_t K, const int32_t* rows,
+                           int64_t n_rows, bit1_stream_t stream) {
+    if (!shape_ok(1, N, K)) return BIT1_ESHAPE;
+    if (n_rows < 0) return BIT1_EINVAL;
+    if (n_rows == 0) return BIT1_OK;
+    if (!bits || !rows || !aligned16(bits)) return BIT1_EINVAL;
+    for (int64_t i = 0; i < n_rows; ++i)
+        if (rows[i] < 0 || (int64_t)rows[i] >= N) return BIT1_ERANGE;
+    return from_cuda(launch_xor_patch(bits, N, K, rows, n_rows, (cudaStream_t)stream));
+}
+
+const char* bit1_status_str(bit1_status s) {
+    switch (s) {
+        case BIT1_OK: return "ok";
+        case BIT1_EINVAL: return "invalid argument (null or misaligned pointer, unknown dtype, variant or flag)";
+        case BIT1_ESHAPE: return "unsupported shape (B, N >= 1; K a positive multiple of 128; variant limits)";
+        case BIT1_ERANGE: return "value out of range (patch row outside [0, N) or packed scale not finite)";
+        case BIT1_ECUDA: return "CUDA runtime or launch error";
+        case BIT1_ENAN: return "NaN in the weights given to bit1_pack";
+        default: return "unknown status";
+    }
+}
+
+const char* bit1_version(void) { return "bit1 0.1 (sm_103a)"; }
+
+}  // extern "C"

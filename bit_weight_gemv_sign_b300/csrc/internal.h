@@ -1,0 +1,42 @@
+// Host-side launchers of the bit1 kernels (called by the C ABI in bit1_api.cu
+// after argument validation; they only configure and launch).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bit1 {
+
+struct GemvArgs {
+    const uint8_t* bits;
+    const uint16_t* scales;
+    const uint16_t* x;
+    int64_t B, N, K;
+    void* y;
+    int y_bf16;          // 1: bf16 output, 0: fp32 output
+    void* workspace;
+    size_t ws_bytes;
+    bool pdl;            // launch with programmatic stream serialization
+    cudaStream_t stream;
+};
+
+// Launch helper: grid/block/smem with optional PDL attribute.
+cudaError_t launch(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                   bool pdl, void** args);
+
+cudaError_t launch_pack(const void* w, int dtype, int64_t N, int64_t K, uint8_t* bits,
+                        uint16_t* scales, uint32_t* flags, cudaStream_t stream);
+
+cudaError_t launch_xor_patch(uint8_t* bits, int64_t N, int64_t K, const int32_t* rows,
+                             int64_t n_rows, cudaStream_t stream);
+
+cudaError_t launch_gemv_simple(const GemvArgs& a);
+
+// Table-lookup batch-1..8 kernel. Returns cudaErrorNotSupported if the shape
+// is outside its limits (checked by lut_supported first).
+bool lut_supported(int64_t B, int64_t N, int64_t K);
+cudaError_t launch_gemv_lut(const GemvArgs& a);
+
+int sm_count();
+
+}  // namespace bit1

@@ -1,0 +1,127 @@
+"""A decode-step weight sweep: many packed 1-bit matrices resident in HBM,
+each multiplied by its own activation vector, captured once into a CUDA graph
+and replayed (one replay = one decode token's worth of linear layers).
+
+The pages state that autoregressive decode reads essentially the whole weight
+set for every token and that at batch 1 the time goes to memory traffic and to
+kernel launch/synchronisation latency (web page "Bonsai 27B: 노트북과 폰에서
+실행되는 27B급 이진 및 삼진 저비트 LLM", sections "27B 규모에서 효율은 선택이
+아닌 제약" and "하이브리드 어텐션을 위한 저비트 커널").  The sweep therefore
+keeps every matrix resident in one device arena and removes host launch cost
+with a CUDA graph; with programmatic dependent launch each kernel starts
+streaming its weights while the previous one finishes, and waits for it only
+before reading its activations (the data dependence of a real decode step).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import synth
+from . import BF16, F32, FLAG_PDL, AUTO, bit1_gemv_ex, bit1_gemv_launches, bit1_xor_patch
+
+
+def _align(n: int, a: int = 256) -> int:
+    return (n + a - 1) // a * a
+
+
+class Sweep:
+    def __init__(self, mats, seed0: int = 0, batch: int = 1, y_dtype: int = BF16,
+                 device: str = "cuda", variant: int = AUTO):
+        self.mats = list(mats)
+        self.seed0 = seed0
+        self.B = batch
+        self.y_dtype = y_dtype
+        self.variant = variant
+        self.device = device
+        ysz = 2 if y_dtype == BF16 else 4
+        self.bits_off, self.sc_off, self.x_off, self.y_off = [], [], [], []
+        nb = ns = nx = ny = 0
+        for m in self.mats:
+            self.bits_off.append(nb); nb += _align(m.N * m.K // 8)
+            self.sc_off.append(ns); ns += _align(m.N * (m.K // 128) * 2)
+            self.x_off.append(nx); nx += _align(batch * m.K * 2)
+            self.y_off.append(ny); ny += _align(batch * m.N * ysz)
+        self.bits = torch.empty(nb, dtype=torch.uint8, device=device)
+        self.scales = torch.empty(ns // 2, dtype=torch.int16, device=device)
+        self.x = torch.empty(nx // 2, dtype=torch.bfloat16, device=device)
+        self.y = torch.empty(ny, dtype=torch.uint8, device=device)
+        self.weight_bytes = sum(m.N * m.K // 8 + 2 * m.N * (m.K // 128) for m in self.mats)
+        self.x_bytes = sum(batch * m.K * 2 for m in self.mats)
+        self.graph = None
+        self.stream = None
+
+    # ---- views ---------------------------------------------------------
+    def bits_of(self, i):
+        m = self.mats[i]
+        return self.bits[self.bits_off[i]: self.bits_off[i] + m.N * m.K // 8].view(m.N, m.K // 8)
+
+    def scales_of(self, i):
+        m = self.mats[i]
+        o = self.sc_off[i] // 2
+        return self.scales[o: o + m.N * (m.K // 128)].view(m.N, m.K // 128)
+
+    def x_of(self, i):
+        m = self.mats[i]
+        o = self.x_off[i] // 2
+        return self.x[o: o + self.B * m.K].view(self.B, m.K)
+
+    def y_of(self, i):
+        m = self.mats[i]
+        if self.y_dtype == BF16:
+            return self.y[self.y_off[i]: self.y_off[i] + 2 * self.B * m.N].view(torch.bfloat16).view(self.B, m.N)
+        return self.y[self.y_off[i]: self.y_off[i] + 4 * self.B * m.N].view(torch.float32).view(self.B, m.N)
+
+    # ---- data ------------------------------------------------------------
+    def host_matrix(self, i):
+        """The seeded host copy of matrix i (bits, scales) and its input x."""
+        m = self.mats[i]
+        bits, scales = synth.matrix(m.N, m.K, self.seed0 + i)
+        x = synth.x_for(self.B, m.K, self.seed0 + i)
+        return bits, scales, x
+
+    def fill(self):
+        """Generate every matrix on the host (seeded) and copy it to the arena."""
+        for i in range(len(self.mats)):
+            bits, scales, x = self.host_matrix(i)
+            self.bits_of(i).copy_(torch.from_numpy(bits), non_blocking=False)
+            self.scales_of(i).copy_(torch.from_numpy(scales.view(np.int16)))
+            self.x_of(i).copy_(torch.from_numpy(x.view(np.int16)).view(torch.bfloat16))
+        torch.cuda.synchronize()
+        return self
+
+    # ---- execution ---------------------------------------------------------
+    def launches_per_step(self) -> int:
+        return sum(bit1_gemv_launches(self.B, m.N, m.K, self.variant) for m in self.mats)
+
+    def run_eager(self, stream=None, pdl: bool = True):
+        for i, m in enumerate(self.mats):
+            bit1_gemv_ex(self.bits_of(i), self.scales_of(i), self.x_of(i), y=self.y_of(i),
+                         variant=self.variant, flags=FLAG_PDL if pdl else 0, stream=stream,
+                         N=m.N, K=m.K)
+
+    def capture(self, pdl: bool = True):
+        self.stream = torch.cuda.Stream()
+        self.stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(self.stream):
+            self.run_eager(self.stream, pdl)       # warm-up (attributes, module load)
+        self.stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            self.run_eager(self.stream, pdl)
+        self.graph = g
+        return self
+
+    def replay(self):
+        self.graph.replay()
+
+    def apply_patch(self, entries, proj_count: int = 7):
+        """Apply (or, applied again, remove) a list of (layer, projection, row)
+        entries: each is routed to its matrix and XOR-flipped there."""
+        by_mat = {}
+        for layer, proj, row in entries:
+            by_mat.setdefault(layer * proj_count + proj, []).append(row)
+        for i, rows in sorted(by_mat.items()):
+            m = self.mats[i]
+            bit1_xor_patch(self.bits_of(i), rows, N=m.N, K=m.K)
+        return by_mat

@@ -1,0 +1,169 @@
+/*
+ * bit1.h -- C ABI of the true 1-bit linear-layer library for NVIDIA B300
+ * (sm_103a).
+ *
+ * The weight format (web page "Bonsai 27B: 노트북과 폰에서 실행되는 27B급 이진
+ * 및 삼진 저비트 LLM (feat. PrismML)", section "이진(Binary) 가중치 형식"):
+ * every weight is w = s_g * b with b in {-1, +1}; each run of 128 consecutive
+ * input-dimension weights of a row shares one FP16 scale s_g, so a weight
+ * costs 1 + 16/128 = 1.125 bits.  The same page ("저장 공간과 실제 배포 크기")
+ * deploys binary weights in their native 1-bit layout, and its kernel section
+ * ("하이브리드 어텐션을 위한 저비트 커널") decodes the sign codes and applies
+ * the group scale inside the fused product, never rebuilding a dense FP16
+ * matrix, with high-precision accumulation.  The row-wise XOR patch follows
+ * "LocalLLaMA, true 1-bit LLM용 XOR patch 방식 \"Bankai\" 실험에 주목",
+ * section "LocalLLaMA가 본 핵심 포인트".
+ *
+ * Layout (the pages do not fix one; this library's reading):
+ *   bits   : uint8 [N][K/8], row-major; bit k of row n is
+ *            (bits[n*K/8 + k/8] >> (k%8)) & 1, i.e. least significant bit
+ *            first; bit 1 means +1, bit 0 means -1.  Seen as little-endian
+ *            32-bit words, bit k of a row is bit (k%32) of word k/32, and the
+ *            16 bytes at offset 16*g of a row hold group g exactly.
+ *   scales : IEEE binary16 bit patterns [N][K/128], row-major.
+ *   x      : bfloat16 [B][K], row-major (activations).
+ *   y      : [B][N] row-major, fp32 or bf16 (round to nearest even).
+ *   K must be a positive multiple of 128.
+ *
+ * Ownership and execution: the caller owns every buffer.  Device pointers
+ * must point to device memory of the current device and be 16-byte aligned.
+ * No entry point allocates device memory; bit1_gemv takes an optional
+ * caller-owned workspace.  Every call is asynchronous on `stream` (NULL means
+ * the legacy default stream) and validates its arguments on the host before
+ * launching anything: a call that returns an error has launched nothing and
+ * modified nothing.  Errors of kernels that have already been launched
+ * surface at the caller's next synchronisation, as usual in CUDA.
+ */
+#ifndef BIT1_H
+#define BIT1_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *bit1_stream_t;
+
+typedef enum bit1_status {
+    BIT1_OK = 0,
+    BIT1_EINVAL = 1, /* null or misaligned pointer, unknown dtype/variant, bad count */
+    BIT1_ESHAPE = 2, /* B, N < 1; K not a positive multiple of 128; shape beyond a variant's limits */
+    BIT1_ERANGE = 3, /* patch row outside [0, N); packed scale not finite */
+    BIT1_ECUDA = 4,  /* a CUDA runtime call or kernel launch failed */
+    BIT1_ENAN = 5    /* NaN among the weights given to bit1_pack */
+} bit1_status;
+
+enum bit1_dtype {
+    BIT1_F32 = 0,
+    BIT1_BF16 = 1,
+    BIT1_F16 = 2
+};
+
+/* Kernel selection for bit1_gemv_ex.  AUTO picks by shape (the same choice
+ * bit1_gemv makes); the others force one kernel and return BIT1_ESHAPE if
+ * that kernel cannot take the shape. */
+enum bit1_gemv_variant {
+    BIT1_GEMV_AUTO = 0,
+    BIT1_GEMV_SIMPLE = 1,  /* any shape; one warp per row (reference-quality) */
+    BIT1_GEMV_LUT = 2,     /* batch 1..8: CUDA-core table-lookup kernel */
+    BIT1_GEMV_SPLITK = 3,  /* batch 1..8, short N: K split over CTAs, workspace reduction */
+    BIT1_GEMV_TC = 4       /* batch >= 16: tcgen05 tensor-core kernel */
+};
+
+/* bit1_gemv_ex flags. */
+#define BIT1_FLAG_PDL 1u   /* launch with programmatic dependent launch: the
+                              kernel prefetches its weights before waiting for
+                              the preceding kernel in the stream */
+
+/* ------------------------------------------------------------------------
+ * bit1_pack -- floating-point weights -> packed sign bits + fp16 scales.
+ * Follows the binary weight format above.  The pages do not say how a scale
+ * is chosen from real weights; this library's reading: bit = !(w < 0) (so
+ * +0 and -0 give +1), s_g = fp16 round-to-nearest-even of mean(|w|) over
+ * the group, the 128 magnitudes summed in fp64 in ascending k order
+ * (the least-squares scale for w ~ s*sign(w)).
+ *   w       : device, [N][K] of w_dtype (BIT1_F32, BIT1_BF16 or BIT1_F16)
+ *   bits    : device, N*K/8 bytes (written)
+ *   scales  : device, N*(K/128) fp16 patterns (written)
+ *   d_flags : device pointer to one uint32, or NULL.  The call zeroes it on
+ *             `stream`; the kernel sets bit 0 if any weight is NaN and bit 1
+ *             if any scale is not finite (|mean| beyond fp16 range).  After
+ *             synchronising, bit1_pack_flags_status() maps it to a status.
+ * Returns BIT1_ESHAPE / BIT1_EINVAL on bad arguments (nothing launched),
+ * BIT1_ECUDA on launch failure, else BIT1_OK.
+ */
+bit1_status bit1_pack(const void *w, int w_dtype, int64_t N, int64_t K,
+                      uint8_t *bits, uint16_t *scales, uint32_t *d_flags,
+                      bit1_stream_t stream);
+
+/* BIT1_ENAN if bit 0 is set, else BIT1_ERANGE if bit 1 is set, else BIT1_OK. */
+bit1_status bit1_pack_flags_status(uint32_t flags);
+
+/* ------------------------------------------------------------------------
+ * bit1_gemv -- y[b][n] = sum_g s[n][g] * sum_{k in group g} (bit(n,k) ? +x[b][k]
+ *                                                             : -x[b][k])
+ * The product of the binary weight format above with bf16 activations, the
+ * sign decoded and the group scale applied inside the kernel, fp32
+ * accumulation (kernel section of the Bonsai 27B page).  Result within
+ * 1e-3 * sum_k |s*x_k| + 1e-6 of the exact value (plus the bf16 output
+ * rounding for y_dtype = BIT1_BF16).
+ *   bits, scales : device, layout above
+ *   x            : device, bf16 [B][K]
+ *   y            : device, [B][N] of y_dtype (BIT1_F32 or BIT1_BF16), written
+ *   workspace    : device scratch of ws_bytes bytes, or NULL/0.  Some shapes
+ *                  run faster with bit1_gemv_workspace_bytes(B, N, K) bytes;
+ *                  with less, a kernel without scratch is chosen.  Its
+ *                  contents on entry do not matter.
+ * B >= 1, N >= 1, K a positive multiple of 128.  The inputs must not overlap
+ * y or the workspace.
+ */
+bit1_status bit1_gemv(const uint8_t *bits, const uint16_t *scales,
+                      const uint16_t *x, int64_t B, int64_t N, int64_t K,
+                      void *y, int y_dtype, void *workspace, size_t ws_bytes,
+                      bit1_stream_t stream);
+
+/* bit1_gemv with an explicit kernel choice (enum bit1_gemv_variant) and
+ * flags (BIT1_FLAG_*). */
+bit1_status bit1_gemv_ex(const uint8_t *bits, const uint16_t *scales,
+                         const uint16_t *x, int64_t B, int64_t N, int64_t K,
+                         void *y, int y_dtype, void *workspace, size_t ws_bytes,
+                         int variant, unsigned flags, bit1_stream_t stream);
+
+/* Scratch bytes that let bit1_gemv use its fastest kernel for this shape
+ * (0 when no kernel needs scratch). */
+size_t bit1_gemv_workspace_bytes(int64_t B, int64_t N, int64_t K);
+
+/* The variant bit1_gemv picks for this shape and workspace size, and the
+ * number of kernel launches one call makes (0 on bad arguments). */
+int bit1_gemv_pick(int64_t B, int64_t N, int64_t K, size_t ws_bytes);
+int bit1_gemv_launches(int64_t B, int64_t N, int64_t K, int variant);
+
+/* ------------------------------------------------------------------------
+ * bit1_xor_patch -- the Bankai row-wise sign-flip patch, in place.
+ * Every listed row has all of its K sign bits inverted (bytes ^= 0xFF);
+ * scales are untouched.  Applying the same list again removes the patch.
+ * A row listed twice is flipped twice (no change).
+ *   bits   : device, [N][K/8] (modified in place)
+ *   rows   : HOST array of n_rows row indices (the patch list is a small
+ *            host-side object; it is checked on the host and passed to the
+ *            kernel by value, so no device copy is needed)
+ * Returns BIT1_ERANGE, with nothing modified, if any row is outside [0, N).
+ */
+bit1_status bit1_xor_patch(uint8_t *bits, int64_t N, int64_t K,
+                           const int32_t *rows, int64_t n_rows,
+                           bit1_stream_t stream);
+
+/* Static description of a status code. */
+const char *bit1_status_str(bit1_status status);
+
+/* Library version string. */
+const char *bit1_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BIT1_H */

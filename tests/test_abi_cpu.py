@@ -1,0 +1,119 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function include/bit1.h declares, and rejects bad arguments on the host
+before any CUDA call (so these run on a machine without a device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_weight_gemv_sign_b300 as b1
+from bit_weight_gemv_sign_b300 import build as b1build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bit1.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    b1build.build()
+    return b1.load()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(bit1_[a-z0-9_]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_abi():
+    names = _declared_functions()
+    for want in ("bit1_pack", "bit1_gemv", "bit1_gemv_ex", "bit1_xor_patch",
+                 "bit1_gemv_workspace_bytes", "bit1_status_str"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(b1.library_path())
+    missing = [n for n in _declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert len(b1.bit1_status_str(s)) >= 2
+    assert "unknown" in b1.bit1_status_str(99)
+    assert "sm_103a" in b1.bit1_version()
+
+
+def test_pack_flags_mapping(lib):
+    assert b1.bit1_pack_flags_status(0) == b1.OK
+    assert b1.bit1_pack_flags_status(1) == b1.ENAN
+    assert b1.bit1_pack_flags_status(2) == b1.ERANGE
+    assert b1.bit1_pack_flags_status(3) == b1.ENAN
+
+
+FAKE = 1 << 20  # aligned non-null address: never dereferenced by the checks below
+
+
+def test_gemv_rejects_bad_shapes_on_host(lib):
+    f = lib.bit1_gemv_ex
+    for B, N, K in ((1, 1, 100), (1, 1, 0), (0, 8, 128), (1, 0, 128), (1, 8, -128), (1, 8, 129)):
+        assert f(FAKE, FAKE, FAKE, B, N, K, FAKE, b1.F32, None, 0, 0, 0, None) == b1.ESHAPE
+
+
+def test_gemv_rejects_bad_pointers_and_types_on_host(lib):
+    f = lib.bit1_gemv_ex
+    assert f(None, FAKE, FAKE, 1, 8, 128, FAKE, b1.F32, None, 0, 0, 0, None) == b1.EINVAL
+    assert f(FAKE, FAKE, FAKE, 1, 8, 128, None, b1.F32, None, 0, 0, 0, None) == b1.EINVAL
+    assert f(FAKE + 2, FAKE, FAKE, 1, 8, 128, FAKE, b1.F32, None, 0, 0, 0, None) == b1.EINVAL
+    assert f(FAKE, FAKE, FAKE + 8, 1, 8, 128, FAKE, b1.F32, None, 0, 0, 0, None) == b1.EINVAL
+    assert f(FAKE, FAKE, FAKE, 1, 8, 128, FAKE, 7, None, 0, 0, 0, None) == b1.EINVAL
+    assert f(FAKE, FAKE, FAKE, 1, 8, 128, FAKE, b1.F16, None, 0, 0, 0, None) == b1.EINVAL
+    assert f(FAKE, FAKE, FAKE, 1, 8, 128, FAKE, b1.F32, None, 0, 99, 0, None) == b1.EINVAL
+    assert f(FAKE, FAKE, FAKE, 1, 8, 128, FAKE, b1.F32, None, 0, 0, 0x80, None) == b1.EINVAL
+    assert f(FAKE, FAKE, FAKE, 1, 8, 128, FAKE, b1.F32, None, 64, 0, 0, None) == b1.EINVAL
+
+
+def test_gemv_variant_limits_on_host(lib):
+    f = lib.bit1_gemv_ex
+    # the table-lookup kernel takes batch 1 and K a multiple of 1024 up to its table limit
+    assert f(FAKE, FAKE, FAKE, 2, 8, 1024, FAKE, b1.F32, None, 0, b1.LUT, 0, None) == b1.ESHAPE
+    assert f(FAKE, FAKE, FAKE, 1, 8, 1152, FAKE, b1.F32, None, 0, b1.LUT, 0, None) == b1.ESHAPE
+
+
+def test_pick_and_launch_counts(lib):
+    assert b1.bit1_gemv_pick(1, 4096, 4096) == b1.LUT
+    assert b1.bit1_gemv_pick(1, 4096, 1152) == b1.SIMPLE
+    assert b1.bit1_gemv_pick(0, 4096, 4096) == 0
+    assert b1.bit1_gemv_launches(1, 4096, 4096, b1.AUTO) == 1
+    assert b1.bit1_gemv_launches(1, 4096, 100, b1.AUTO) == 0
+    assert b1.bit1_gemv_workspace_bytes(1, 4096, 100) == 0
+
+
+def test_pack_rejects_on_host(lib):
+    f = lib.bit1_pack
+    assert f(FAKE, b1.F32, 8, 100, FAKE, FAKE, None, None) == b1.ESHAPE
+    assert f(None, b1.F32, 8, 128, FAKE, FAKE, None, None) == b1.EINVAL
+    assert f(FAKE, 9, 8, 128, FAKE, FAKE, None, None) == b1.EINVAL
+    assert f(FAKE, b1.F32, 8, 128, FAKE + 4, FAKE, None, None) == b1.EINVAL
+
+
+def test_xor_patch_range_checked_on_host(lib):
+    import numpy as np
+    f = lib.bit1_xor_patch
+    rows = np.array([0, 5, 8], dtype=np.int32)
+    assert f(FAKE, 8, 128, rows.ctypes.data, 3, None) == b1.ERANGE
+    rows = np.array([-1], dtype=np.int32)
+    assert f(FAKE, 8, 128, rows.ctypes.data, 1, None) == b1.ERANGE
+    assert f(FAKE, 8, 128, None, 0, None) == b1.OK      # empty patch: nothing to do
+    assert f(FAKE, 8, 128, None, -1, None) == b1.EINVAL
+    assert f(FAKE, 8, 100, None, 0, None) == b1.ESHAPE
+
+
+def test_binding_fails_loudly_without_cuda_tensors(lib):
+    import torch
+    x = torch.zeros(1, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        b1.bit1_gemv(torch.zeros(8, 16, dtype=torch.uint8), torch.zeros(8, 1, dtype=torch.int16), x)
