@@ -14,15 +14,16 @@ import threading
 
 __all__ = [
     "Bit1Error", "OK", "EINVAL", "ESHAPE", "ERANGE", "ECUDA", "ENAN",
-    "F32", "BF16", "F16", "AUTO", "SIMPLE", "LUT", "SPLITK", "TC", "FLAG_PDL",
+    "F32", "BF16", "F16", "AUTO", "SIMPLE", "LUT", "SPLITK", "TC", "LUT6", "FLAG_PDL",
     "bit1_pack", "bit1_pack_flags_status", "bit1_gemv", "bit1_gemv_ex",
     "bit1_gemv_workspace_bytes", "bit1_gemv_pick", "bit1_gemv_launches",
-    "bit1_xor_patch", "bit1_status_str", "bit1_version", "library_path", "load",
+    "bit1_xor_patch", "bit1_status_str", "bit1_version", "bit1_device_wait_timeouts",
+    "library_path", "load",
 ]
 
 OK, EINVAL, ESHAPE, ERANGE, ECUDA, ENAN = 0, 1, 2, 3, 4, 5
 F32, BF16, F16 = 0, 1, 2
-AUTO, SIMPLE, LUT, SPLITK, TC = 0, 1, 2, 3, 4
+AUTO, SIMPLE, LUT, SPLITK, TC, LUT6 = 0, 1, 2, 3, 4, 5
 FLAG_PDL = 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -73,6 +74,8 @@ def load():
         lib.bit1_status_str.restype = ctypes.c_char_p
         lib.bit1_version.argtypes = []
         lib.bit1_version.restype = ctypes.c_char_p
+        lib.bit1_device_wait_timeouts.argtypes = []
+        lib.bit1_device_wait_timeouts.restype = ctypes.c_uint
         _lib = lib
         return lib
 
@@ -83,6 +86,10 @@ def bit1_status_str(status: int) -> str:
 
 def bit1_version() -> str:
     return load().bit1_version().decode()
+
+
+def bit1_device_wait_timeouts() -> int:
+    return int(load().bit1_device_wait_timeouts())
 
 
 # ---------------------------------------------------------------- helpers

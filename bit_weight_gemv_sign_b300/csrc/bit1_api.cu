@@ -55,6 +55,7 @@ bit1_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BIT1_OK : BIT1_
 
 int pick_variant(int64_t B, int64_t N, int64_t K, size_t ws_bytes) {
     (void)ws_bytes;
+    if (t6_supported(B, N, K)) return BIT1_GEMV_LUT6;
     if (lut_supported(B, N, K)) return BIT1_GEMV_LUT;
     return BIT1_GEMV_SIMPLE;
 }
@@ -102,6 +103,9 @@ bit1_status bit1_gemv_ex(const uint8_t* bits, const uint16_t* scales, const uint
         case BIT1_GEMV_LUT:
             if (!lut_supported(B, N, K)) return BIT1_ESHAPE;
             return from_cuda(launch_gemv_lut(a));
+        case BIT1_GEMV_LUT6:
+            if (!t6_supported(B, N, K)) return BIT1_ESHAPE;
+            return from_cuda(launch_gemv_t6(a));
         case BIT1_GEMV_SPLITK:
         case BIT1_GEMV_TC:
             return BIT1_ESHAPE;  // not available for any shape in this build
@@ -133,6 +137,7 @@ int bit1_gemv_launches(int64_t B, int64_t N, int64_t K, int variant) {
     switch (variant) {
         case BIT1_GEMV_SIMPLE: return 1;
         case BIT1_GEMV_LUT: return lut_supported(B, N, K) ? 1 : 0;
+        case BIT1_GEMV_LUT6: return t6_supported(B, N, K) ? 1 : 0;
         default: return 0;
     }
 }
@@ -160,6 +165,8 @@ const char* bit1_status_str(bit1_status s) {
     }
 }
 
-const char* bit1_version(void) { return "bit1 0.1 (sm_103a)"; }
+const char* bit1_version(void) { return "bit1 0.2 (sm_103a)"; }
+
+unsigned int bit1_device_wait_timeouts(void) { return t6_take_timeouts(); }
 
 }  // extern "C"

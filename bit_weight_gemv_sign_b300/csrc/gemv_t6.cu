@@ -1,0 +1,405 @@
+// Batch-1 GEMV over packed sign bits with 6-bit fp16 lookup tables, one row
+// per lane, TMA-staged weights and split-K over a thread-block cluster
+// (CUDA cores, sm_103a).
+//
+// What it computes: y[n] = sum_g s[n][g] * sum_{k in g} (bit(n,k) ? x[k] : -x[k])
+// (web page "Bonsai 27B: 노트북과 폰에서 실행되는 27B급 이진 및 삼진 저비트 LLM",
+// section "이진(Binary) 가중치 형식"), the fp16 group scale applied inside the
+// product and fp32 accumulation (section "하이브리드 어텐션을 위한 저비트 커널").
+// No multiply per weight: six weights cost one table lookup and one add (the
+// ±1 weights of "PrismML Bonsai — 1.15GB짜리 8B 모델이 말이 되나?", section
+// "1-bit이 뭔지부터", turn the product into additions and subtractions).
+//
+// Design (B300: LDS serves 32 lanes per clock per SM, integer ALU ops issue at
+// half rate, so a per-weight instruction is unaffordable at HBM speed):
+//  * A group of 128 weights is cut into 21 six-bit fields and one two-bit
+//    field.  For every field the CTA precomputes the 64 sums
+//    T[e] = sum_t (bit t of e ? +x'_t : -x'_t) once, rounded to fp16 and packed
+//    two per word: a table is 128 contiguous bytes = the 32 banks, so a warp
+//    whose lanes pick any 32 entries of the same table is conflict-free.
+//  * Lane l of a warp owns row 32*b + l; all lanes walk the same fields in
+//    lockstep, so one shared table serves the whole warp and every CTA.
+//  * x' = x * 2^-m_g per group (exact power-of-two prescale) keeps every entry
+//    within fp16 range; the entry rounding error is <= 2^-12 of the sum of the
+//    six |x'|, i.e. a relative 2.4e-4 of sum|s x| at most, inside the 1e-3
+//    budget.  The group's fp32 partial is multiplied by s_g and 2^m_g.
+//  * Weights and scales of 32-row blocks are copied by TMA into per-warp
+//    rings (mbarrier completion, bounded waits).  Bits arrive as 2-D boxes of
+//    [32 rows][128 B] (8 groups) with 128-byte swizzle: row r's 16-byte chunk
+//    c lands at r*128 + ((c ^ (r % 8)) * 16), so the 32 lanes' 16-byte reads
+//    of one group are bank-conflict-free.
+//  * K is split over the Q CTAs of a cluster: each builds only its K/Q slice of
+//    tables; the per-row partials are summed in a fixed order through
+//    distributed shared memory (deterministic, so a flipped row negates
+//    exactly).
+//  * The weight stream of the first stages is issued before
+//    griddepcontrol.wait (programmatic dependent launch): only x depends on
+//    the preceding kernel.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+#include "t6_common.cuh"
+
+namespace bit1 {
+
+constexpr int kT6MaxWarps = 16;
+constexpr int kT6MaxSmem = 227 * 1024;
+
+__device__ unsigned int g_bit1_wait_timeouts = 0;
+
+struct T6Params {
+    const uint16_t* x;
+    void* y;
+    int N, K, Gc, Q, S, stage_bytes, y_bf16;
+    uint32_t off_tables, off_factors, off_x, off_partials, off_bars;
+};
+
+// ---------------------------------------------------------------- kernel
+__global__ void __launch_bounds__(kT6MaxWarps * 32)
+k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ CUtensorMap tm_sc,
+          const __grid_constant__ T6Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (base - raw);
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
+    uint32_t q;
+    asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(q));
+    const int ncl = gridDim.x / p.Q, cl = blockIdx.x / p.Q;
+    const int RB = (p.N + 31) >> 5;
+    const int rb0 = (int)((int64_t)RB * cl / ncl), rb1 = (int)((int64_t)RB * (cl + 1) / ncl);
+    const int Gc = p.Gc, S = p.S;
+    const int g0 = (int)q * Gc;
+    const uint32_t bits_tile = 32u * Gc * 16u, sc_tile = 32u * Gc * 2u;
+    const uint32_t bars = base + p.off_bars + (uint32_t)(warp * S) * 8u;
+
+    auto issue = [&](int k) {  // lane 0: block rb0 + warp + k*W -> stage k % S
+        const int b = rb0 + warp + k * W;
+        if (b >= rb1) return;
+        const uint32_t st = base + (uint32_t)(warp * S + (k % S)) * p.stage_bytes;
+        const uint32_t bar = bars + 8u * (k % S);
+        mbar_expect_tx(bar, bits_tile + sc_tile);
+        for (int j = 0; j < Gc / 8; ++j)   // 128-byte column j of the slice: groups g0+8j .. g0+8j+7
+            tma_2d(st + 4096u * j, &tm_bits, (g0 + 8 * j) * 16, b * 32, bar);
+        tma_2d(st + bits_tile, &tm_sc, g0, b * 32, bar);
+    };
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(bars + 8u * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int k = 0; k < S; ++k) issue(k);
+    }
+    __syncwarp();
+
+    // Activations come from the preceding kernel of a decode step.
+    pdl_wait();
+    float* fac = reinterpret_cast<float*>(sm + p.off_factors);   // [Gc] 2^m_g
+    float* xs = reinterpret_cast<float*>(sm + p.off_x);           // [Gc*128] x, then x'
+    const uint16_t* xc = p.x + (size_t)g0 * 128;
+    for (int i = threadIdx.x; i < Gc * 32; i += blockDim.x) {     // 4 activations per thread
+        const uint2 xv = *reinterpret_cast<const uint2*>(xc + 4 * i);
+        *reinterpret_cast<float4*>(xs + 4 * i) =
+            make_float4(bf16_bits_to_f32(xv.x & 0xffffu), bf16_bits_to_f32(xv.x >> 16),
+                        bf16_bits_to_f32(xv.y & 0xffffu), bf16_bits_to_f32(xv.y >> 16));
+    }
+    __syncthreads();
+    for (int g = warp; g < Gc; g += W) {
+        const float4 xv = *reinterpret_cast<const float4*>(xs + g * 128 + 4 * lane);
+        float m = fmaxf(fmaxf(fabsf(xv.x), fabsf(xv.y)), fmaxf(fabsf(xv.z), fabsf(xv.w)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        int mg = 0;
+        if (m > 0.f) {
+            const int e = (int)((__float_as_uint(m) >> 23) & 0xffu) - 127;  // floor(log2 m), normal m
+            mg = min(max(e - 11, -126), 127);                                // max|x'| < 2^12
+        }
+        const float finv = __uint_as_float((uint32_t)(127 - mg) << 23);      // exact power of two
+        *reinterpret_cast<float4*>(xs + g * 128 + 4 * lane) =
+            make_float4(xv.x * finv, xv.y * finv, xv.z * finv, xv.w * finv);
+        if (lane == 0) fac[g] = __uint_as_float((uint32_t)(mg + 127) << 23);
+    }
+    __syncthreads();
+    uint8_t* tabs = sm + p.off_tables;
+    for (int t = threadIdx.x; t < Gc * kT6Fields; t += blockDim.x) {
+        const int g = t / kT6Fields, f = t - g * kT6Fields;
+        t6_build(tabs + g * kT6GroupBytes + f * kT6TableBytes, xs + g * 128, f);
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    float* partials = reinterpret_cast<float*>(sm + p.off_partials);
+    const uint32_t tb = base + p.off_tables;
+    const uint32_t fac_s = base + p.off_factors;
+    bool ok = true;
+    int k = 0;
+    for (;; ++k) {
+        const int b = rb0 + warp + k * W;
+        if (b >= rb1) break;
+        const int s = k % S;
+        if (!mbar_wait(bars + 8u * s, (uint32_t)(k / S) & 1u)) {
+            if (lane == 0) atomicOr(&g_bit1_wait_timeouts, 1u);
+            ok = false;
+            break;
+        }
+        const uint32_t st = base + (uint32_t)(warp * S + s) * p.stage_bytes;
+        const uint32_t sts = st + bits_tile + (uint32_t)lane * Gc * 2u;
+        float acc = 0.f;
+        for (int g8 = 0; g8 < Gc; g8 += 8) {
+            const uint4 sv = lds128(sts + 2u * g8);
+            const uint4 fa = lds128(fac_s + 4u * g8), fb = lds128(fac_s + 4u * g8 + 16u);
+            const uint32_t svw[4] = {sv.x, sv.y, sv.z, sv.w};
+            const uint32_t fw[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int g = g8 + j;
+                // box g8/8 holds [32 rows][128 B]; 128-byte swizzle of chunk j in row `lane`
+                const uint32_t L = ((uint32_t)g8 << 9) + (uint32_t)lane * 128u +
+                                   ((uint32_t)(j ^ (lane & 7)) << 4);
+                const uint4 wv = lds128(st + L);
+                const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+                const float part = t6_group(w, tb + (uint32_t)g * kT6GroupBytes, std::make_index_sequence<kT6Fields>{});
+                const float sc = f16_bits_to_f32((uint16_t)(svw[j >> 1] >> (16 * (j & 1))));
+                acc = fmaf(part * sc, __uint_as_float(fw[j]), acc);
+            }
+        }
+        partials[(b - rb0) * 32 + lane] = acc;
+        __syncwarp();
+        if (lane == 0) issue(k + S);
+    }
+    if (!ok && lane == 0) {
+        // Give copies still in flight a bounded chance to land before exit.
+        for (int kk = k + 1; kk < k + S; ++kk)
+            if (rb0 + warp + kk * W < rb1) (void)mbar_wait(bars + 8u * (kk % S), (uint32_t)(kk / S) & 1u);
+    }
+
+    // Sum the Q partials of every row in a fixed order.
+    __syncthreads();
+    cluster_sync();
+    const int R = (rb1 - rb0) * 32;
+    const int lo = (int)((int64_t)R * q / p.Q), hi = (int)((int64_t)R * (q + 1) / p.Q);
+    const uint32_t part_s = base + p.off_partials;
+    for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+        float v = 0.f;
+        for (int r = 0; r < p.Q; ++r) v += ld_cluster_f32(part_s + 4u * i, (uint32_t)r);
+        const int row = rb0 * 32 + i;
+        if (row < p.N) {
+            if (p.y_bf16) reinterpret_cast<uint16_t*>(p.y)[row] = f32_to_bf16_bits(v);
+            else reinterpret_cast<float*>(p.y)[row] = v;
+        }
+    }
+    cluster_sync();
+}
+
+// ---------------------------------------------------------------- host side
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+struct T6Plan {
+    int Q = 0, Gc = 0, W = 0, S = 0, ncl = 0, stage_bytes = 0;
+    size_t smem = 0;
+    T6Params p{};
+};
+
+// Cluster sizes that split G into slices of a multiple of 8 groups whose
+// tables fit comfortably in shared memory, most preferred first.
+int q_candidates(int64_t G, int* out) {
+    int n = 0;
+    if (G % 8 != 0) return 0;
+    const int64_t u = G / 8;  // units of 8 groups
+    for (int q : {4, 2, 1, 5, 3, 7, 6, 8})
+        if (u % q == 0 && (G / q) * kT6GroupBytes <= 120 * 1024) out[n++] = q;
+    return n;
+}
+
+// Clusters of size Q that can be resident at once with this block size and
+// shared memory (clusters must fit inside one GPC, so this can be less than
+// SMs / Q); cached per configuration.
+int active_clusters(int Q, int threads, size_t smem) {
+    static std::mutex mu;
+    static std::vector<std::pair<std::pair<int, int>, std::pair<size_t, int>>> cache;
+    std::lock_guard<std::mutex> lk(mu);
+    for (auto& c : cache)
+        if (c.first.first == Q && c.first.second == threads && c.second.first == smem) return c.second.second;
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(Q * (sm_count() / Q)));
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)Q;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaFuncSetAttribute((const void*)k_gemv_t6, cudaFuncAttributeMaxDynamicSharedMemorySize, kT6MaxSmem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, (const void*)k_gemv_t6, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = sm_count() / Q;  // no device (host-only checks): assume every SM
+    }
+    cache.push_back({{Q, threads}, {smem, n}});
+    return n;
+}
+
+bool plan_t6_q(int64_t N, int64_t K, int Q, T6Plan& pl) {
+    const int64_t G = K / 128;
+    pl.Q = Q;
+    pl.Gc = (int)(G / Q);
+    pl.stage_bytes = (32 * pl.Gc * 18 + 1023) & ~1023;
+    const int tables = pl.Gc * kT6GroupBytes;
+    const int factors = pl.Gc * 4;
+    const int xbytes = pl.Gc * 128 * 4;
+    const int64_t RB = (N + 31) / 32;
+    auto total = [&](int W, int S, int bpc) {
+        return (size_t)1024 + (size_t)W * S * pl.stage_bytes + tables + factors + xbytes +
+               (size_t)bpc * 128 + (size_t)W * S * 8 + 64;
+    };
+    // first guess with every SM, then shrink to the clusters that fit at once
+    int ncl = sm_count() / Q;
+    if (ncl < 1) return false;
+    int W = 0, S = 0, bpc = 0;
+    for (int iter = 0; iter < 3; ++iter) {
+        bpc = (int)((RB + ncl - 1) / ncl);
+        W = bpc < kT6MaxWarps ? bpc : kT6MaxWarps;
+        if (W < 4) W = 4;  // at least 4 warps: they share the table build
+        S = (bpc + W - 1) / W;
+        if (S > 3) S = 3;
+        while (total(W, S, bpc) > kT6MaxSmem && S > 1) --S;
+        while (total(W, S, bpc) > kT6MaxSmem && W > 4) --W;
+        if (total(W, S, bpc) > kT6MaxSmem) return false;
+        const int act = active_clusters(Q, W * 32, total(W, S, bpc));
+        if (act >= ncl) break;
+        ncl = act < 1 ? 1 : act;
+    }
+    pl.ncl = ncl;
+    pl.W = W;
+    pl.S = S;
+    pl.smem = total(W, S, bpc);
+    uint32_t off = (uint32_t)(W * S * pl.stage_bytes);
+    pl.p.off_tables = off;        off += tables;           // multiple of 128 (stages are 1 KB multiples)
+    pl.p.off_factors = off;       off += factors;          // 16-byte aligned (tables multiple of 128)
+    off = (off + 15u) & ~15u;
+    pl.p.off_x = off;             off += xbytes;
+    pl.p.off_partials = off;      off += bpc * 128;
+    off = (off + 7u) & ~7u;
+    pl.p.off_bars = off;
+    pl.p.N = (int)N;
+    pl.p.K = (int)K;
+    pl.p.Gc = pl.Gc;
+    pl.p.Q = Q;
+    pl.p.S = S;
+    pl.p.stage_bytes = pl.stage_bytes;
+    return true;
+}
+
+// Among the usable cluster sizes, take the plan that keeps the most SMs busy.
+bool plan_t6(int64_t N, int64_t K, T6Plan& best) {
+    if (N < 1 || N > (1LL << 30)) return false;
+    int qs[8];
+    const int nq = q_candidates(K / 128, qs);
+    bool found = false;
+    for (int i = 0; i < nq; ++i) {
+        T6Plan pl;
+        if (!plan_t6_q(N, K, qs[i], pl)) continue;
+        if (!found || pl.ncl * pl.Q > best.ncl * best.Q) {
+            best = pl;
+            found = true;
+        }
+    }
+    return found;
+}
+
+}  // namespace
+
+bool t6_supported(int64_t B, int64_t N, int64_t K) {
+    int qs[8];
+    return B == 1 && K % 1024 == 0 && K <= (1LL << 20) && q_candidates(K / 128, qs) > 0 && N >= 1 &&
+           N <= (1LL << 30);
+}
+
+cudaError_t launch_gemv_t6(const GemvArgs& a) {
+    T6Plan pl;
+    if (a.B != 1 || !plan_t6(a.N, a.K, pl)) return cudaErrorNotSupported;
+    auto enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int64_t G = a.K / 128;
+    CUtensorMap tm_bits, tm_sc;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 8), (cuuint64_t)a.N};
+        const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 8)};
+        const cuuint32_t box[2] = {128, 32};
+        const cuuint32_t es[2] = {1, 1};
+        if (enc(&tm_bits, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void*)a.bits, dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)G, (cuuint64_t)a.N};
+        const cuuint64_t strides[1] = {(cuuint64_t)(G * 2)};
+        const cuuint32_t box[2] = {(cuuint32_t)pl.Gc, 32};
+        const cuuint32_t es[2] = {1, 1};
+        if (enc(&tm_sc, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (void*)a.scales, dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cudaError_t e = cudaFuncSetAttribute((const void*)k_gemv_t6,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kT6MaxSmem);
+        if (e != cudaSuccess) return e;
+    }
+
+    T6Params prm = pl.p;
+    prm.x = a.x;
+    prm.y = a.y;
+    prm.y_bf16 = a.y_bf16;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(pl.ncl * pl.Q));
+    cfg.blockDim = dim3((unsigned)(pl.W * 32));
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)pl.Q;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    int na = 1;
+    if (a.pdl) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        na = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    void* args[] = {(void*)&tm_bits, (void*)&tm_sc, (void*)&prm};
+    return cudaLaunchKernelExC(&cfg, (const void*)k_gemv_t6, args);
+}
+
+unsigned int t6_take_timeouts() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_bit1_wait_timeouts, sizeof(v)) != cudaSuccess) return 0xffffffffu;
+    cudaMemcpyToSymbol(g_bit1_wait_timeouts, &zero, sizeof(zero));
+    return v;
+}
+
+}  // namespace bit1

@@ -1,0 +1,125 @@
+// Device helpers shared by the 6-bit-table GEMV kernels: TMA / mbarrier
+// wrappers, the table builder and the table lookup.  See gemv_t6.cu for the
+// method and the numerical argument.
+#pragma once
+
+#include <cuda.h>
+
+#include <utility>
+
+#include "common.cuh"
+
+namespace bit1 {
+
+constexpr int kT6Fields = 22;                     // 21 six-bit + 1 two-bit field per group
+constexpr int kT6TableBytes = 128;                // 64 fp16 entries
+constexpr int kT6GroupBytes = kT6Fields * kT6TableBytes;  // 2816
+
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// Bounded wait on an mbarrier phase: false if it did not complete in time.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < (1u << 22); ++i) {
+        uint32_t done;
+        asm volatile("{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p;}"
+                     : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// ---------------------------------------------------------------- tables
+// Table for field f of one group, from the group's 128 prescaled activations
+// x' (fp32, shared memory): 6 of them (f < 21) or the last two (f = 21).
+// Entry e sits at byte 2e; complementary indices hold exact negatives (every
+// sum is formed symmetrically).
+__device__ __forceinline__ void t6_build(uint8_t* tab, const float* xg, int f) {
+    if (f < 21) {
+        const float* xs = xg + 6 * f;
+        const float v0 = xs[0], v1 = xs[1], v2 = xs[2], v3 = xs[3], v4 = xs[4], v5 = xs[5];
+        const float a = v0 + v1, b = v0 - v1, c = v3 + v4, d = v3 - v4;
+        const float lo[8] = {-a - v2, b - v2, -b - v2, a - v2, -a + v2, b + v2, -b + v2, a + v2};
+        const float hi[8] = {-c - v5, d - v5, -d - v5, c - v5, -c + v5, d + v5, -d + v5, c + v5};
+        uint4* dst = reinterpret_cast<uint4*>(tab);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t wd[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int e0 = 8 * i + 2 * j, e1 = e0 + 1;
+                const __half2 h = __floats2half2_rn(lo[e0 & 7] + hi[e0 >> 3], lo[e1 & 7] + hi[e1 >> 3]);
+                wd[j] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            dst[i] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        }
+    } else {
+        const float v0 = xg[126], v1 = xg[127];
+        const __half2 h0 = __floats2half2_rn(-v0 - v1, v0 - v1);
+        const __half2 h1 = __floats2half2_rn(-v0 + v1, v0 + v1);
+        *reinterpret_cast<uint2*>(tab) = make_uint2(*reinterpret_cast<const uint32_t*>(&h0),
+                                                    *reinterpret_cast<const uint32_t*>(&h1));
+    }
+}
+
+// Field F of the 128-bit group w[0..3]: its value times 2 (byte offset of the
+// fp16 entry), or'ed into the 128-byte aligned table base of the group; the
+// entry is loaded here and added by t6_add.  The load is an ordinary
+// (non-volatile) shared load so that the compiler can issue the 22 loads of a
+// group back to back; its address depends on w, which is only read after the
+// stage's mbarrier completed, which orders it after the table build.
+template <int F>
+__device__ __forceinline__ unsigned short t6_ld(const uint32_t (&w)[4], uint32_t tg) {
+    constexpr int O = 6 * F, QW = O >> 5, S = O & 31;
+    uint32_t v;
+    if constexpr (F == 21) v = (w[3] >> 29) & 0x6u;
+    else if constexpr (S == 0) v = (w[QW] << 1) & 0x7Eu;
+    else if constexpr (S + 6 <= 32) v = (w[QW] >> (S - 1)) & 0x7Eu;
+    else v = __funnelshift_r(w[QW], w[QW + 1], S - 1) & 0x7Eu;
+    unsigned short t;
+    asm("ld.shared.b16 %0, [%1+%2];" : "=h"(t) : "r"(v | tg), "n"(F * kT6TableBytes));
+    return t;
+}
+
+// acc + (fp32) t, the fp16 -> fp32 widening exact, in one mixed-precision FMA.
+__device__ __forceinline__ float t6_add(unsigned short t, float acc) {
+    const unsigned short one = 0x3C00;
+    asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc) : "h"(t), "h"(one));
+    return acc;
+}
+
+template <size_t... F>
+__device__ __forceinline__ float t6_group(const uint32_t (&w)[4], uint32_t tg, std::index_sequence<F...>) {
+    unsigned short t[sizeof...(F)];
+    ((t[F] = t6_ld<(int)F>(w, tg)), ...);
+    float acc[2] = {0.f, 0.f};
+    ((acc[F & 1] = t6_add(t[F], acc[F & 1])), ...);
+    return acc[0] + acc[1];
+}
+
+
+}  // namespace bit1

@@ -70,7 +70,10 @@ enum bit1_gemv_variant {
     BIT1_GEMV_SIMPLE = 1,  /* any shape; one warp per row (reference-quality) */
     BIT1_GEMV_LUT = 2,     /* batch 1..8: CUDA-core table-lookup kernel */
     BIT1_GEMV_SPLITK = 3,  /* batch 1..8, short N: K split over CTAs, workspace reduction */
-    BIT1_GEMV_TC = 4       /* batch >= 16: tcgen05 tensor-core kernel */
+    BIT1_GEMV_TC = 4,      /* batch >= 16: tcgen05 tensor-core kernel */
+    BIT1_GEMV_LUT6 = 5     /* batch 1, K a multiple of 1024: one row per lane,
+                              6-bit fp16 tables, TMA-staged weights, K split over
+                              a thread-block cluster */
 };
 
 /* bit1_gemv_ex flags. */
@@ -155,6 +158,13 @@ int bit1_gemv_launches(int64_t B, int64_t N, int64_t K, int variant);
 bit1_status bit1_xor_patch(uint8_t *bits, int64_t N, int64_t K,
                            const int32_t *rows, int64_t n_rows,
                            bit1_stream_t stream);
+
+/* Kernels bound every wait on an asynchronous copy; a wait that gives up
+ * skips the remaining work and records the event on the device instead of
+ * hanging.  Returns how many such events happened since the previous call
+ * (and resets the count); synchronises with the device.  0xffffffff if the
+ * count could not be read. */
+unsigned int bit1_device_wait_timeouts(void);
 
 /* Static description of a status code. */
 const char *bit1_status_str(bit1_status status);

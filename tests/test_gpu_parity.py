@@ -35,12 +35,15 @@ def _run(bits, scales, x, N, K, B, variant, y_dtype=b1.F32, flags=0):
 # ---------------------------------------------------------------- GEMV
 
 SHAPES_B1 = [(1, 1024), (7, 1024), (256, 1024), (149, 2048), (300, 3072), (1025, 4096),
-             (37, 5120), (64, 6144), (33, 7168), (513, 12288), (40, 13312)]
+             (37, 5120), (64, 6144), (33, 7168), (513, 12288), (40, 13312),
+             (151, 3072), (4097, 4096), (32, 4096), (33, 12288), (5000, 12288)]
 
 
 @pytest.mark.parametrize("N,K", SHAPES_B1)
-@pytest.mark.parametrize("variant", [b1.LUT, b1.SIMPLE, b1.AUTO])
+@pytest.mark.parametrize("variant", [b1.LUT6, b1.LUT, b1.SIMPLE, b1.AUTO])
 def test_gemv_b1_matches_oracle(orc, N, K, variant):
+    if variant == b1.LUT6 and b1.bit1_gemv_launches(1, N, K, b1.LUT6) == 0:
+        pytest.skip("shape outside the 6-bit table kernel's limits")
     bits, scales, x = _problem(N, K, 1, 1000 + N + K)
     ref = orc.gemv(bits, scales, x, 1, N, K)
     y = _run(bits, scales, x, N, K, 1, variant)
@@ -58,7 +61,7 @@ def test_gemv_simple_any_shape(orc, N, K, B):
     assert_gemv_close(y, ref, abs_bound(scales, x, K), f"auto N={N} K={K} B={B}")
 
 
-@pytest.mark.parametrize("variant", [b1.LUT, b1.SIMPLE])
+@pytest.mark.parametrize("variant", [b1.LUT6, b1.LUT, b1.SIMPLE])
 def test_gemv_bf16_output(orc, variant):
     N, K = 777, 4096
     bits, scales, x = _problem(N, K, 1, 3001)
@@ -68,7 +71,7 @@ def test_gemv_bf16_output(orc, variant):
     assert_gemv_close(y, ref, abs_bound(scales, x, K), "bf16 out")
 
 
-@pytest.mark.parametrize("variant", [b1.LUT, b1.SIMPLE])
+@pytest.mark.parametrize("variant", [b1.LUT6, b1.LUT, b1.SIMPLE])
 def test_gemv_row_flip_negates_exactly(variant):
     """Flipping all bits of a row negates its output bit for bit: the kernels
     sum +-x symmetrically (the table entries of complementary nibbles are exact
@@ -97,18 +100,38 @@ def test_gemv_special_values(orc):
     x = x.copy()
     x[0, :128] = 0                 # a whole group of zero activations
     ref = orc.gemv(bits, scales, x, 1, N, K)
-    for v in (b1.LUT, b1.SIMPLE):
+    for v in (b1.LUT6, b1.LUT, b1.SIMPLE):
         y = _run(bits, scales, x, N, K, 1, v)
         assert_gemv_close(y, ref, abs_bound(scales, x, K), f"special {v}")
         assert float(y[0, 2]) == 0.0
 
 
-def test_gemv_pdl_flag_same_result(orc):
+@pytest.mark.parametrize("variant", [b1.LUT6, b1.LUT])
+def test_gemv_pdl_flag_same_result(orc, variant):
     N, K = 999, 4096
     bits, scales, x = _problem(N, K, 1, 3004)
-    a = _run(bits, scales, x, N, K, 1, b1.LUT)
-    b = _run(bits, scales, x, N, K, 1, b1.LUT, flags=b1.FLAG_PDL)
+    a = _run(bits, scales, x, N, K, 1, variant)
+    b = _run(bits, scales, x, N, K, 1, variant, flags=b1.FLAG_PDL)
     assert torch.equal(a, b)
+    assert b1.bit1_device_wait_timeouts() == 0
+
+
+def test_gemv_lut6_extreme_activation_ranges(orc):
+    """Groups whose activations are tiny, huge or mixed in magnitude: the
+    per-group power-of-two prescale keeps the fp16 table entries in range."""
+    N, K = 96, 4096
+    bits, scales, x = _problem(N, K, 1, 3005)
+    xf = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).float().numpy()
+    xf[0, 0:128] *= 2.0 ** -100
+    xf[0, 128:256] *= 2.0 ** 60
+    xf[0, 256:384] *= np.where(np.arange(128) % 2 == 0, 2.0 ** 20, 2.0 ** -20)
+    xf[0, 384:512] = 0.0
+    xf[0, 512:640] = 65504.0 * 4
+    x2 = synth.to_bf16_bits(xf)
+    ref = orc.gemv(bits, scales, x2, 1, N, K)
+    for v in (b1.LUT6, b1.SIMPLE):
+        y = _run(bits, scales, x2, N, K, 1, v)
+        assert_gemv_close(y, ref, abs_bound(scales, x2, K), f"extreme ranges {v}")
 
 
 @pytest.mark.parametrize("m", synth.PROJ_8B, ids=[m.name for m in synth.PROJ_8B])
