@@ -14,17 +14,24 @@ import threading
 
 __all__ = [
     "Bit1Error", "OK", "EINVAL", "ESHAPE", "ERANGE", "ECUDA", "ENAN",
-    "F32", "BF16", "F16", "AUTO", "SIMPLE", "LUT", "SPLITK", "TC", "LUT6", "FLAG_PDL",
+    "F32", "BF16", "F16", "AUTO", "SIMPLE", "LUT", "SPLITK", "TC", "LUT6", "STREAM", "FLAG_PDL",
     "bit1_pack", "bit1_pack_flags_status", "bit1_gemv", "bit1_gemv_ex",
     "bit1_gemv_workspace_bytes", "bit1_gemv_pick", "bit1_gemv_launches",
     "bit1_xor_patch", "bit1_status_str", "bit1_version", "bit1_device_wait_timeouts",
+    "bit1_group_plan_bytes", "bit1_group_plan", "bit1_gemv_group", "GroupPlan",
     "library_path", "load",
 ]
 
 OK, EINVAL, ESHAPE, ERANGE, ECUDA, ENAN = 0, 1, 2, 3, 4, 5
 F32, BF16, F16 = 0, 1, 2
-AUTO, SIMPLE, LUT, SPLITK, TC, LUT6 = 0, 1, 2, 3, 4, 5
+AUTO, SIMPLE, LUT, SPLITK, TC, LUT6, STREAM = 0, 1, 2, 3, 4, 5, 6
 FLAG_PDL = 1
+
+class _Problem(ctypes.Structure):
+    _fields_ = [("bits", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("x", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("y_dtype", ctypes.c_int)]
+
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libbit1.so")
@@ -76,6 +83,12 @@ def load():
         lib.bit1_version.restype = ctypes.c_char_p
         lib.bit1_device_wait_timeouts.argtypes = []
         lib.bit1_device_wait_timeouts.restype = ctypes.c_uint
+        lib.bit1_group_plan_bytes.argtypes = [i32]
+        lib.bit1_group_plan_bytes.restype = sz
+        lib.bit1_group_plan.argtypes = [ctypes.POINTER(_Problem), i32, p, sz]
+        lib.bit1_group_plan.restype = i32
+        lib.bit1_gemv_group.argtypes = [p, p, ctypes.c_uint, p]
+        lib.bit1_gemv_group.restype = i32
         _lib = lib
         return lib
 
@@ -204,3 +217,50 @@ def bit1_xor_patch(bits, rows, N=None, K=None, stream=None):
                                r.size, _stream(stream))
     _check(st, "bit1_xor_patch")
     return bits
+
+
+# ---------------------------------------------------------------- grouped GEMV
+
+def bit1_group_plan_bytes(count: int) -> int:
+    return int(load().bit1_group_plan_bytes(int(count)))
+
+
+def bit1_group_plan(problems, host_plan_ptr: int, plan_bytes: int) -> None:
+    """problems: sequence of (bits, scales, x, y) CUDA tensors (batch 1)."""
+    import torch
+    arr = (_Problem * len(problems))()
+    for i, (bits, scales, x, y) in enumerate(problems):
+        if y.dtype not in (torch.float32, torch.bfloat16):
+            raise TypeError("y must be float32 or bfloat16")
+        arr[i] = _Problem(_dptr(bits, "bits"), _dptr(scales, "scales"), _dptr(x, "x"), _dptr(y, "y"),
+                          bits.shape[0], x.shape[-1], BF16 if y.dtype == torch.bfloat16 else F32)
+    st = load().bit1_group_plan(arr, len(problems), host_plan_ptr, plan_bytes)
+    _check(st, "bit1_group_plan")
+
+
+def bit1_gemv_group(device_plan_ptr: int, host_plan_ptr: int, flags: int = 0, stream=None) -> None:
+    st = load().bit1_gemv_group(device_plan_ptr, host_plan_ptr, int(flags), _stream(stream))
+    _check(st, "bit1_gemv_group")
+
+
+class GroupPlan:
+    """A grouped-GEMV plan: the encoded host copy and its device copy (both
+    128-byte aligned).  The tensors named in ``problems`` must stay alive and
+    in place while the plan is used."""
+
+    def __init__(self, problems, device="cuda"):
+        import numpy as np
+        import torch
+        self.problems = list(problems)
+        self.nbytes = bit1_group_plan_bytes(len(self.problems))
+        self._host_raw = np.zeros(self.nbytes + 128, dtype=np.uint8)
+        off = (-self._host_raw.ctypes.data) % 128
+        self.host = self._host_raw[off: off + self.nbytes]
+        bit1_group_plan(self.problems, self.host.ctypes.data, self.nbytes)
+        self._dev_raw = torch.empty(self.nbytes + 128, dtype=torch.uint8, device=device)
+        doff = (-self._dev_raw.data_ptr()) % 128
+        self.dev = self._dev_raw[doff: doff + self.nbytes]
+        self.dev.copy_(torch.from_numpy(self.host))
+
+    def run(self, flags: int = 0, stream=None) -> None:
+        bit1_gemv_group(self.dev.data_ptr(), self.host.ctypes.data, flags, stream)

@@ -106,6 +106,9 @@ bit1_status bit1_gemv_ex(const uint8_t* bits, const uint16_t* scales, const uint
         case BIT1_GEMV_LUT6:
             if (!t6_supported(B, N, K)) return BIT1_ESHAPE;
             return from_cuda(launch_gemv_t6(a));
+        case BIT1_GEMV_STREAM:
+            if (!group1_supported(B, N, K)) return BIT1_ESHAPE;
+            return from_cuda(launch_gemv_group1(a));
         case BIT1_GEMV_SPLITK:
         case BIT1_GEMV_TC:
             return BIT1_ESHAPE;  // not available for any shape in this build
@@ -138,6 +141,7 @@ int bit1_gemv_launches(int64_t B, int64_t N, int64_t K, int variant) {
         case BIT1_GEMV_SIMPLE: return 1;
         case BIT1_GEMV_LUT: return lut_supported(B, N, K) ? 1 : 0;
         case BIT1_GEMV_LUT6: return t6_supported(B, N, K) ? 1 : 0;
+        case BIT1_GEMV_STREAM: return group1_supported(B, N, K) ? 1 : 0;
         default: return 0;
     }
 }
@@ -167,6 +171,25 @@ const char* bit1_status_str(bit1_status s) {
 
 const char* bit1_version(void) { return "bit1 0.2 (sm_103a)"; }
 
-unsigned int bit1_device_wait_timeouts(void) { return t6_take_timeouts(); }
+unsigned int bit1_device_wait_timeouts(void) {
+    const unsigned int a = t6_take_timeouts(), b = group_take_timeouts();
+    if (a == 0xffffffffu || b == 0xffffffffu) return 0xffffffffu;
+    return a + b;
+}
+
+size_t bit1_group_plan_bytes(int count) { return group_plan_bytes(count); }
+
+bit1_status bit1_group_plan(const bit1_gemv_problem* problems, int count, void* host_plan,
+                            size_t plan_bytes) {
+    return group_plan(problems, count, host_plan, plan_bytes);
+}
+
+bit1_status bit1_gemv_group(const void* device_plan, const void* host_plan, unsigned flags,
+                            bit1_stream_t stream) {
+    if (!device_plan || !host_plan || ((uintptr_t)device_plan & 127) || ((uintptr_t)host_plan & 127))
+        return BIT1_EINVAL;
+    if (flags & ~BIT1_FLAG_PDL) return BIT1_EINVAL;
+    return from_cuda(launch_group(device_plan, host_plan, (flags & BIT1_FLAG_PDL) != 0, (cudaStream_t)stream));
+}
 
 }  // extern "C"

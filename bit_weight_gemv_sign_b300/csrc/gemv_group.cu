@@ -1,0 +1,474 @@
+// Grouped batch-1 GEMV: many independent packed-1-bit problems in one
+// persistent launch (CUDA cores, sm_103a).
+//
+// Each problem is y = W x with W in the binary g128 format of the web page
+// "Bonsai 27B: 노트북과 폰에서 실행되는 27B급 이진 및 삼진 저비트 LLM" (section
+// "이진(Binary) 가중치 형식"), computed with the 6-bit fp16 tables of
+// gemv_t6.cu (one row per lane, TMA-staged weights, fp32 accumulation).
+//
+// Why one launch: autoregressive decode reads every weight once per token and
+// at batch 1 the time goes to weight traffic and to kernel launch /
+// synchronisation latency (same page, sections "27B 규모에서 효율은 선택이
+// 아닌 제약" and "하이브리드 어텐션을 위한 저비트 커널").  Launching every
+// matrix separately pays launch, table-build and drain latency per matrix.
+// Here the concatenated list of 32-row blocks of all problems is cut into
+// one contiguous, cost-balanced range per CTA (one CTA per SM, no clusters,
+// no split-K: every row is produced by exactly one lane, deterministically).
+// A CTA builds tables only for the problems its range touches, K split into
+// chunks of at most 32 groups (4096 inputs); its per-warp TMA rings run ahead
+// across problem and chunk boundaries, so the weight stream does not stall
+// while the next problem's tables are built.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstddef>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+#include "t6_common.cuh"
+
+namespace bit1 {
+
+__device__ unsigned int g_group_wait_timeouts = 0;
+
+constexpr int kGChunkGroups = 32;            // K chunk: 32 groups = 4096 inputs
+constexpr int kGStageBytes = 5120;           // 4 KB bits box + 512 B scales box, 1 KB aligned
+constexpr int kGMaxCtas = 160;
+constexpr int kGWarps = 8;
+constexpr int kGMaxSmem = 227 * 1024;
+
+struct GHeader {            // 64 bytes
+    int count, nctas, W, S;
+    uint32_t off_tables, off_x, off_fac, off_part, off_bars;
+    int part_rows, smem_bytes, ranges_off, probs_off;
+    int pad[3];
+};
+static_assert(sizeof(GHeader) == 64, "header size");
+
+struct GRange {             // blocks from (p0, b0) up to, not including, (p1, b1)
+    int p0, b0, p1, b1;
+};
+
+struct alignas(128) GProb {
+    CUtensorMap tm_bits;    // 2-D [N][K/8] uint8, box {128, 32}, 128-byte swizzle
+    CUtensorMap tm_sc;      // 2-D [N][G] uint16, box {8, 32}
+    const uint16_t* x;
+    void* y;
+    int N, K, G, RB, y_bf16, nch;
+};
+
+struct GSingle {            // whole plan of a one-problem call, passed by value
+    GHeader h;
+    GRange r[kGMaxCtas];
+    GProb p;
+};
+
+// ---------------------------------------------------------------- device
+struct GIter {               // position in one warp's sequence of stages
+    int p, c, b, j;
+};
+
+struct GCtx {
+    const GProb* P;
+    GRange R;
+    int w, W;
+    __device__ __forceinline__ int bs(int p) const { return p == R.p0 ? R.b0 : 0; }
+    __device__ __forceinline__ int be(int p) const { return p == R.p1 ? R.b1 : P[p].RB; }
+    __device__ __forceinline__ int slices(int p, int c) const {
+        const int cg = min(kGChunkGroups, P[p].G - kGChunkGroups * c);
+        return cg >> 3;
+    }
+    __device__ __forceinline__ bool done(const GIter& it) const {
+        return it.p > R.p1 || (it.p == R.p1 && it.b >= R.b1);
+    }
+    // Move to the first valid stage at or after `it` (block of this warp in a
+    // non-empty segment).
+    __device__ __forceinline__ void settle(GIter& it) const {
+        while (it.p <= R.p1) {
+            if (it.b < be(it.p)) return;
+            ++it.c;
+            if (it.c < P[it.p].nch) {
+                it.b = bs(it.p) + w;
+            } else {
+                ++it.p;
+                it.c = 0;
+                if (it.p > R.p1) return;
+                it.b = bs(it.p) + w;
+            }
+            it.j = 0;
+        }
+    }
+    __device__ __forceinline__ GIter first() const {
+        GIter it{R.p0, 0, bs(R.p0) + w, 0};
+        settle(it);
+        return it;
+    }
+    __device__ __forceinline__ void next(GIter& it) const {
+        if (++it.j < slices(it.p, it.c)) return;
+        it.j = 0;
+        it.b += W;
+        settle(it);
+    }
+};
+
+__device__ __forceinline__ void g_issue(const GProb* P, const GIter& it, uint32_t st, uint32_t bar) {
+    const GProb& pr = P[it.p];
+    const int g = kGChunkGroups * it.c + 8 * it.j;
+    mbar_expect_tx(bar, 4096u + 512u);
+    tma_2d(st, &pr.tm_bits, g * 16, it.b * 32, bar);
+    tma_2d(st + 4096u, &pr.tm_sc, g, it.b * 32, bar);
+}
+
+__device__ __forceinline__ void g_body(const uint8_t* plan) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (base - raw);
+
+    const GHeader* H = reinterpret_cast<const GHeader*>(plan);
+    const int W = H->W, S = H->S;
+    GCtx cx;
+    cx.P = reinterpret_cast<const GProb*>(plan + H->probs_off);
+    cx.R = reinterpret_cast<const GRange*>(plan + H->ranges_off)[blockIdx.x];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    cx.w = warp;
+    cx.W = W;
+    const GProb* P = cx.P;
+    const uint32_t bars = base + H->off_bars + (uint32_t)(warp * S) * 8u;
+    const uint32_t stages = base + (uint32_t)(warp * S) * kGStageBytes;
+
+    // Producer (lane 0): start the warp's weight stream before anything else.
+    GIter prod = cx.first();
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(bars + 8u * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int s = 0; s < S && !cx.done(prod); ++s) {
+            g_issue(P, prod, stages + (uint32_t)s * kGStageBytes, bars + 8u * s);
+            cx.next(prod);
+        }
+    } else {
+        for (int s = 0; s < S && !cx.done(prod); ++s) cx.next(prod);
+    }
+    __syncwarp();
+
+    pdl_wait();   // inputs may come from the preceding kernel
+    float* fac = reinterpret_cast<float*>(sm + H->off_fac);
+    float* xs = reinterpret_cast<float*>(sm + H->off_x);
+    float* part = reinterpret_cast<float*>(sm + H->off_part);
+    uint8_t* tabs = sm + H->off_tables;
+    const uint32_t tb = base + H->off_tables;
+    const uint32_t fac_s = base + H->off_fac;
+
+    int k = 0;          // stages consumed by this warp
+    int kfail = -1;     // stage whose bounded wait gave up
+    bool ok = true;
+    for (int p = cx.R.p0; p <= cx.R.p1; ++p) {
+        const int bs = cx.bs(p), be = cx.be(p);
+        if (bs >= be) continue;
+        const GProb& pr = P[p];
+        for (int c = 0; c < pr.nch; ++c) {
+            const int cg = min(kGChunkGroups, pr.G - kGChunkGroups * c);
+            // --- tables for (problem p, chunk c): every thread of the CTA
+            __syncthreads();                                   // old tables no longer read
+            const uint16_t* xc = pr.x + (size_t)c * kGChunkGroups * 128;
+            for (int g = warp; g < cg; g += W) {               // one group per warp pass
+                const uint2 xv = *reinterpret_cast<const uint2*>(xc + g * 128 + 4 * lane);
+                const float x0 = bf16_bits_to_f32(xv.x & 0xffffu), x1 = bf16_bits_to_f32(xv.x >> 16);
+                const float x2 = bf16_bits_to_f32(xv.y & 0xffffu), x3 = bf16_bits_to_f32(xv.y >> 16);
+                float m = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                int mg = 0;
+                if (m > 0.f) {
+                    const int e = (int)((__float_as_uint(m) >> 23) & 0xffu) - 127;
+                    mg = min(max(e - 11, -126), 127);          // max|x'| < 2^12
+                }
+                const float finv = __uint_as_float((uint32_t)(127 - mg) << 23);
+                *reinterpret_cast<float4*>(xs + g * 128 + 4 * lane) =
+                    make_float4(x0 * finv, x1 * finv, x2 * finv, x3 * finv);
+                if (lane == 0) fac[g] = __uint_as_float((uint32_t)(mg + 127) << 23);
+            }
+            __syncthreads();
+            for (int t = threadIdx.x; t < cg * kT6Fields; t += blockDim.x) {
+                const int g = t / kT6Fields, f = t - g * kT6Fields;
+                t6_build(tabs + g * kT6GroupBytes + f * kT6TableBytes, xs + g * 128, f);
+            }
+            __syncthreads();
+            if (p == cx.R.p0 && c == 0) pdl_launch_dependents();
+
+            // --- this warp's blocks of the segment, for chunk c
+            const int nsl = cg >> 3;
+            for (int b = bs + warp; b < be; b += W) {
+                float acc = 0.f;
+                for (int j = 0; j < nsl; ++j, ++k) {
+                    const int s = k % S;
+                    if (ok && !mbar_wait(bars + 8u * s, (uint32_t)(k / S) & 1u)) {
+                        if (lane == 0) atomicOr(&g_group_wait_timeouts, 1u);
+                        ok = false;
+                        kfail = k;
+                    }
+                    if (ok) {
+                        const uint32_t st = stages + (uint32_t)s * kGStageBytes;
+                        const uint4 sv = lds128(st + 4096u + 16u * lane);       // 8 scales of row `lane`
+                        const uint4 fa = lds128(fac_s + 32u * j), fb = lds128(fac_s + 32u * j + 16u);
+                        const uint32_t svw[4] = {sv.x, sv.y, sv.z, sv.w};
+                        const uint32_t fw[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const uint32_t L = (uint32_t)lane * 128u + ((uint32_t)(jj ^ (lane & 7)) << 4);
+                            const uint4 wv = lds128(st + L);
+                            const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+                            const float pt = t6_group(w4, tb + (uint32_t)(8 * j + jj) * kT6GroupBytes,
+                                                      std::make_index_sequence<kT6Fields>{});
+                            const float sc = f16_bits_to_f32((uint16_t)(svw[jj >> 1] >> (16 * (jj & 1))));
+                            acc = fmaf(pt * sc, __uint_as_float(fw[jj]), acc);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0 && ok && !cx.done(prod))
+                        g_issue(P, prod, stages + (uint32_t)(k % S) * kGStageBytes, bars + 8u * (k % S));
+                    if (!cx.done(prod)) cx.next(prod);
+                }
+                const int row = b * 32 + lane;
+                const int li = (b - bs) * 32 + lane;           // row within the segment
+                if (pr.nch > 1) {
+                    const float v = (c == 0) ? acc : part[li] + acc;
+                    if (c + 1 < pr.nch) {
+                        part[li] = v;
+                        continue;
+                    }
+                    acc = v;
+                }
+                if (row < pr.N) {
+                    if (pr.y_bf16) reinterpret_cast<uint16_t*>(pr.y)[row] = f32_to_bf16_bits(acc);
+                    else reinterpret_cast<float*>(pr.y)[row] = acc;
+                }
+            }
+        }
+    }
+    if (!ok && lane == 0) {
+        // Give copies still in flight a bounded chance to land before exit.
+        for (int kk = kfail + 1; kk < kfail + S; ++kk)
+            (void)mbar_wait(bars + 8u * (kk % S), (uint32_t)(kk / S) & 1u);
+    }
+}
+
+__global__ void __launch_bounds__(kGWarps * 32, 1) k_gemv_group(const uint8_t* __restrict__ plan) {
+    g_body(plan);
+}
+
+__global__ void __launch_bounds__(kGWarps * 32, 1) k_gemv_group1(const __grid_constant__ GSingle plan) {
+    g_body(reinterpret_cast<const uint8_t*>(&plan));
+}
+
+// ---------------------------------------------------------------- host
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+bool encode_prob(GProb& g, const bit1_gemv_problem& pb) {
+    auto enc = g_encode();
+    if (!enc) return false;
+    const int64_t G = pb.K / 128;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)(pb.K / 8), (cuuint64_t)pb.N};
+        const cuuint64_t strides[1] = {(cuuint64_t)(pb.K / 8)};
+        const cuuint32_t box[2] = {128, 32};
+        const cuuint32_t es[2] = {1, 1};
+        if (enc(&g.tm_bits, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void*)pb.bits, dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)G, (cuuint64_t)pb.N};
+        const cuuint64_t strides[1] = {(cuuint64_t)(G * 2)};
+        const cuuint32_t box[2] = {8, 32};
+        const cuuint32_t es[2] = {1, 1};
+        if (enc(&g.tm_sc, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (void*)pb.scales, dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    g.x = pb.x;
+    g.y = pb.y;
+    g.N = (int)pb.N;
+    g.K = (int)pb.K;
+    g.G = (int)G;
+    g.RB = (int)((pb.N + 31) / 32);
+    g.y_bf16 = pb.y_dtype == BIT1_BF16;
+    g.nch = (int)((G + kGChunkGroups - 1) / kGChunkGroups);
+    return true;
+}
+
+// Cost-balanced contiguous block ranges (cost of a block ~ its bytes ~ K),
+// then the shared memory layout; false if some segment that needs a
+// cross-chunk partial buffer would not fit.
+bool plan_layout(const std::vector<GProb>& probs, int nctas, GHeader& h, std::vector<GRange>& ranges) {
+    const int n = (int)probs.size();
+    std::vector<double> cum(n + 1, 0.0);
+    for (int i = 0; i < n; ++i) cum[i + 1] = cum[i] + (double)probs[i].RB * probs[i].K;
+    const double total = cum[n];
+    auto locate = [&](double c, int& p, int& b) {   // first block whose start cost >= c
+        if (c >= total) { p = n - 1; b = probs[n - 1].RB; return; }
+        p = (int)(std::upper_bound(cum.begin(), cum.end(), c) - cum.begin()) - 1;
+        if (p < 0) p = 0;
+        const double per = (double)probs[p].K;
+        b = (int)((c - cum[p] + per - 1e-9) / per);
+        if (b > probs[p].RB) b = probs[p].RB;
+        if (b == probs[p].RB && p + 1 < n) { ++p; b = 0; }
+    };
+    ranges.resize(nctas);
+    int part_rows = 0;
+    for (int i = 0; i < nctas; ++i) {
+        GRange r;
+        locate(total * i / nctas, r.p0, r.b0);
+        locate(total * (i + 1) / nctas, r.p1, r.b1);
+        if (i == nctas - 1) { r.p1 = n - 1; r.b1 = probs[n - 1].RB; }
+        ranges[i] = r;
+        for (int p = r.p0; p <= r.p1 && p < n; ++p) {
+            if (probs[p].nch <= 1) continue;
+            const int bs = p == r.p0 ? r.b0 : 0, be = p == r.p1 ? r.b1 : probs[p].RB;
+            if (be > bs) part_rows = std::max(part_rows, (be - bs) * 32);
+        }
+    }
+    h.count = n;
+    h.nctas = nctas;
+    h.W = kGWarps;
+    h.part_rows = part_rows;
+    const int tables = kGChunkGroups * kT6GroupBytes;
+    const int xbytes = kGChunkGroups * 128 * 4;
+    for (int S = 3; S >= 1; --S) {
+        uint32_t off = (uint32_t)(kGWarps * S * kGStageBytes);
+        const uint32_t off_tables = off;  off += tables;
+        const uint32_t off_x = off;       off += xbytes;
+        const uint32_t off_fac = off;     off += kGChunkGroups * 4;
+        const uint32_t off_part = off;    off += (uint32_t)part_rows * 4;
+        off = (off + 7u) & ~7u;
+        const uint32_t off_bars = off;    off += kGWarps * S * 8;
+        const size_t smem = 1024 + (size_t)off;
+        if (smem <= (size_t)kGMaxSmem) {
+            h.S = S;
+            h.off_tables = off_tables;
+            h.off_x = off_x;
+            h.off_fac = off_fac;
+            h.off_part = off_part;
+            h.off_bars = off_bars;
+            h.smem_bytes = (int)smem;
+            return true;
+        }
+    }
+    return false;
+}
+
+bool problem_ok(const bit1_gemv_problem& pb) {
+    return pb.bits && pb.scales && pb.x && pb.y && pb.N >= 1 && pb.N <= (1LL << 30) && pb.K >= 1024 &&
+           pb.K % 1024 == 0 && pb.K <= (1LL << 20) && (pb.y_dtype == BIT1_F32 || pb.y_dtype == BIT1_BF16) &&
+           ((uintptr_t)pb.bits & 15) == 0 && ((uintptr_t)pb.scales & 15) == 0 && ((uintptr_t)pb.x & 15) == 0 &&
+           ((uintptr_t)pb.y & 15) == 0;
+}
+
+cudaError_t set_smem_attr(const void* f) {
+    return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kGMaxSmem);
+}
+
+}  // namespace
+
+size_t group_plan_bytes(int count) {
+    if (count < 1) return 0;
+    const size_t ranges = 64 + (size_t)kGMaxCtas * sizeof(GRange);
+    const size_t probs_off = (ranges + 127) & ~(size_t)127;
+    return probs_off + (size_t)count * sizeof(GProb);
+}
+
+bit1_status group_plan(const bit1_gemv_problem* problems, int count, void* host_plan, size_t bytes) {
+    if (count < 1 || !problems || !host_plan) return BIT1_EINVAL;
+    if (bytes < group_plan_bytes(count) || ((uintptr_t)host_plan & 127)) return BIT1_EINVAL;
+    for (int i = 0; i < count; ++i)
+        if (!problem_ok(problems[i])) return BIT1_ESHAPE;
+    std::vector<GProb> probs(count);
+    for (int i = 0; i < count; ++i)
+        if (!encode_prob(probs[i], problems[i])) return BIT1_ECUDA;
+    GHeader h{};
+    std::vector<GRange> ranges;
+    const int nctas = std::min(sm_count(), kGMaxCtas);
+    if (!plan_layout(probs, nctas, h, ranges)) return BIT1_ESHAPE;
+    const size_t r_off = 64;
+    const size_t p_off = (r_off + (size_t)kGMaxCtas * sizeof(GRange) + 127) & ~(size_t)127;
+    h.ranges_off = (int)r_off;
+    h.probs_off = (int)p_off;
+    uint8_t* out = static_cast<uint8_t*>(host_plan);
+    std::memset(out, 0, bytes);
+    std::memcpy(out, &h, sizeof(h));
+    std::memcpy(out + r_off, ranges.data(), ranges.size() * sizeof(GRange));
+    std::memcpy(out + p_off, probs.data(), probs.size() * sizeof(GProb));
+    return BIT1_OK;
+}
+
+cudaError_t launch_group(const void* device_plan, const void* host_plan, bool pdl, cudaStream_t stream) {
+    const GHeader* h = static_cast<const GHeader*>(host_plan);
+    cudaError_t e = set_smem_attr((const void*)k_gemv_group);
+    if (e != cudaSuccess) return e;
+    const uint8_t* dp = static_cast<const uint8_t*>(device_plan);
+    void* args[] = {(void*)&dp};
+    return launch((const void*)k_gemv_group, dim3((unsigned)h->nctas), dim3((unsigned)(h->W * 32)),
+                  (size_t)h->smem_bytes, stream, pdl, args);
+}
+
+bool group1_supported(int64_t B, int64_t N, int64_t K) {
+    return B == 1 && N >= 1 && N <= (1LL << 30) && K >= 1024 && K % 1024 == 0 && K <= (1LL << 20);
+}
+
+cudaError_t launch_gemv_group1(const GemvArgs& a) {
+    bit1_gemv_problem pb;
+    pb.bits = a.bits;
+    pb.scales = a.scales;
+    pb.x = a.x;
+    pb.y = a.y;
+    pb.N = a.N;
+    pb.K = a.K;
+    pb.y_dtype = a.y_bf16 ? BIT1_BF16 : BIT1_F32;
+    if (!problem_ok(pb)) return cudaErrorInvalidValue;
+    std::vector<GProb> probs(1);
+    if (!encode_prob(probs[0], pb)) return cudaErrorInvalidValue;
+    static GSingle single;  // large: keep off the stack; filled and copied into the launch
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    std::memset(&single, 0, sizeof(single));
+    std::vector<GRange> ranges;
+    const int nctas = std::min(sm_count(), kGMaxCtas);
+    if (!plan_layout(probs, nctas, single.h, ranges)) return cudaErrorInvalidValue;
+    single.h.ranges_off = (int)offsetof(GSingle, r);
+    single.h.probs_off = (int)offsetof(GSingle, p);
+    std::memcpy(single.r, ranges.data(), ranges.size() * sizeof(GRange));
+    single.p = probs[0];
+    cudaError_t e = set_smem_attr((const void*)k_gemv_group1);
+    if (e != cudaSuccess) return e;
+    void* args[] = {(void*)&single};
+    return launch((const void*)k_gemv_group1, dim3((unsigned)single.h.nctas), dim3((unsigned)(single.h.W * 32)),
+                  (size_t)single.h.smem_bytes, a.stream, a.pdl, args);
+}
+
+unsigned int group_take_timeouts() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_group_wait_timeouts, sizeof(v)) != cudaSuccess) return 0xffffffffu;
+    cudaMemcpyToSymbol(g_group_wait_timeouts, &zero, sizeof(zero));
+    return v;
+}
+
+}  // namespace bit1

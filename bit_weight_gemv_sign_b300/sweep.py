@@ -18,7 +18,8 @@ import numpy as np
 import torch
 
 from . import synth
-from . import BF16, F32, FLAG_PDL, AUTO, bit1_gemv_ex, bit1_gemv_launches, bit1_xor_patch
+from . import (BF16, F32, FLAG_PDL, AUTO, GroupPlan, bit1_gemv_ex, bit1_gemv_launches,
+               bit1_xor_patch)
 
 
 def _align(n: int, a: int = 256) -> int:
@@ -114,6 +115,13 @@ class Sweep:
 
     def replay(self):
         self.graph.replay()
+
+    def group_plan(self):
+        """One grouped launch over every matrix of the sweep (each with its own
+        input): the plan is built once; run() is one kernel launch."""
+        probs = [(self.bits_of(i), self.scales_of(i), self.x_of(i), self.y_of(i))
+                 for i in range(len(self.mats))]
+        return GroupPlan(probs, device=self.device)
 
     def apply_patch(self, entries, proj_count: int = 7):
         """Apply (or, applied again, remove) a list of (layer, projection, row)

@@ -71,9 +71,12 @@ enum bit1_gemv_variant {
     BIT1_GEMV_LUT = 2,     /* batch 1..8: CUDA-core table-lookup kernel */
     BIT1_GEMV_SPLITK = 3,  /* batch 1..8, short N: K split over CTAs, workspace reduction */
     BIT1_GEMV_TC = 4,      /* batch >= 16: tcgen05 tensor-core kernel */
-    BIT1_GEMV_LUT6 = 5     /* batch 1, K a multiple of 1024: one row per lane,
+    BIT1_GEMV_LUT6 = 5,    /* batch 1, K a multiple of 1024: one row per lane,
                               6-bit fp16 tables, TMA-staged weights, K split over
                               a thread-block cluster */
+    BIT1_GEMV_STREAM = 6   /* batch 1, K a multiple of 1024: the grouped kernel
+                              below with one problem (one CTA per SM streaming a
+                              contiguous row range, full-K tables, no clusters) */
 };
 
 /* bit1_gemv_ex flags. */
@@ -143,6 +146,41 @@ size_t bit1_gemv_workspace_bytes(int64_t B, int64_t N, int64_t K);
  * number of kernel launches one call makes (0 on bad arguments). */
 int bit1_gemv_pick(int64_t B, int64_t N, int64_t K, size_t ws_bytes);
 int bit1_gemv_launches(int64_t B, int64_t N, int64_t K, int variant);
+
+/* ------------------------------------------------------------------------
+ * Grouped GEMV: many independent batch-1 products in one persistent launch.
+ * A decode step reads every weight once, and at batch 1 launch and
+ * synchronisation latency, not bandwidth, dominates per-matrix launches (web
+ * page "Bonsai 27B: 노트북과 폰에서 실행되는 27B급 이진 및 삼진 저비트 LLM",
+ * section "하이브리드 어텐션을 위한 저비트 커널").  Each problem is one
+ * bit1_gemv with B = 1; the problems must not depend on each other (no y is
+ * another problem's x).  K must be a multiple of 1024; y_dtype BIT1_F32 or
+ * BIT1_BF16; all pointers device pointers, 16-byte aligned.
+ *
+ * Use: bit1_group_plan() encodes the problems (TMA descriptors and a
+ * cost-balanced split of all rows over the SMs) into a caller-owned HOST
+ * buffer of bit1_group_plan_bytes(count) bytes (128-byte aligned).  The caller
+ * copies it, unchanged, into a DEVICE buffer of the same size (128-byte
+ * aligned) and then calls bit1_gemv_group(device_plan, host_plan, ...) as
+ * often as it likes (the plan embeds the problems' pointers and shapes: it is
+ * valid while those buffers are).  Results are bit-identical to running the
+ * problems one by one with BIT1_GEMV_STREAM.
+ */
+typedef struct bit1_gemv_problem {
+    const uint8_t *bits;     /* [N][K/8] sign bits */
+    const uint16_t *scales;  /* [N][K/128] fp16 scales */
+    const uint16_t *x;       /* [K] bf16 activations */
+    void *y;                 /* [N] output of y_dtype */
+    int64_t N, K;
+    int y_dtype;
+} bit1_gemv_problem;
+
+size_t bit1_group_plan_bytes(int count);
+bit1_status bit1_group_plan(const bit1_gemv_problem *problems, int count,
+                            void *host_plan, size_t plan_bytes);
+/* flags: BIT1_FLAG_PDL or 0. */
+bit1_status bit1_gemv_group(const void *device_plan, const void *host_plan,
+                            unsigned flags, bit1_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * bit1_xor_patch -- the Bankai row-wise sign-flip patch, in place.

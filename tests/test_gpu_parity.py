@@ -243,3 +243,55 @@ def test_pack_then_gemv_round_trip(orc):
     y = b1.bit1_gemv(bits, scales, dev_bf16(x).view(1, K))
     st, rb, rs = orc.pack(w, orc.F32, N, K)
     assert_gemv_close(y, orc.gemv(rb, rs, x, 1, N, K), abs_bound(rs, x, K), "pack+gemv")
+
+
+# ---------------------------------------------------------------- grouped GEMV
+
+GROUP_SHAPES = [(33, 5120), (1, 1024), (999, 12288), (40, 2048), (4096, 4096), (7, 17408),
+                (1025, 4096), (300, 3072), (64, 6144)]
+
+
+def test_group_matches_stream_and_oracle(orc):
+    """Many independent problems in one launch: every output bit-identical to
+    the one-problem launches of the same kernel, and within tolerance of the
+    oracle (mixed K, ragged N, fp32 and bf16 outputs)."""
+    probs, host = [], []
+    for i, (N, K) in enumerate(GROUP_SHAPES):
+        bits, scales, x = _problem(N, K, 1, 7000 + i)
+        yd = torch.float32 if i % 2 == 0 else torch.bfloat16
+        y = torch.empty(1, N, dtype=yd, device="cuda")
+        probs.append((dev_u8(bits), dev_u16(scales), dev_bf16(x).view(1, K), y))
+        host.append((bits, scales, x, N, K))
+    plan = b1.GroupPlan(probs)
+    plan.run()
+    torch.cuda.synchronize()
+    for (bits, scales, x, N, K), (db, ds, dx, y) in zip(host, probs):
+        ref = orc.gemv(bits, scales, x, 1, N, K)
+        assert_gemv_close(y, ref, abs_bound(scales, x, K), f"group N={N} K={K}")
+        y1 = b1.bit1_gemv_ex(db, ds, dx, y=torch.empty_like(y), variant=b1.STREAM)
+        torch.cuda.synchronize()
+        assert torch.equal(y1, y), f"group vs single N={N} K={K}"
+    # a second run of the same plan gives the same bits
+    before = [p[3].clone() for p in probs]
+    plan.run(flags=b1.FLAG_PDL)
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, p[3]) for a, p in zip(before, probs))
+    assert b1.bit1_device_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("N,K", [(1, 1024), (151936, 4096), (4096, 12288), (5120, 17408), (37, 5120)])
+def test_stream_variant_matches_oracle(orc, N, K):
+    bits, scales, x = _problem(N, K, 1, 7100 + N)
+    ref = orc.gemv_threads(bits, scales, x, 1, N, K, 8)
+    y = _run(bits, scales, x, N, K, 1, b1.STREAM)
+    assert_gemv_close(y, ref, abs_bound(scales, x, K), f"stream N={N} K={K}")
+
+
+def test_stream_row_flip_negates_exactly():
+    N, K = 300, 12288
+    bits, scales, x = _problem(N, K, 1, 7200)
+    y0 = _run(bits, scales, x, N, K, 1, b1.STREAM).cpu()
+    fl = bits.copy()
+    fl[[5, 299]] ^= 0xFF
+    y1 = _run(fl, scales, x, N, K, 1, b1.STREAM).cpu()
+    assert torch.equal(y1[0, [5, 299]], -y0[0, [5, 299]])
