@@ -38,14 +38,16 @@ __device__ unsigned int g_group_wait_timeouts = 0;
 constexpr int kGChunkGroups = 32;            // K chunk: 32 groups = 4096 inputs
 constexpr int kGStageBytes = 5120;           // 4 KB bits box + 512 B scales box, 1 KB aligned
 constexpr int kGMaxCtas = 160;
-constexpr int kGWarps = 8;
+constexpr int kGWarps = 16;
 constexpr int kGMaxSmem = 227 * 1024;
+constexpr int kGSegBlocks = 128;             // sub-segment cap: 4096 rows of partials
 
 struct GHeader {            // 64 bytes
     int count, nctas, W, S;
     uint32_t off_tables, off_x, off_fac, off_part, off_bars;
     int part_rows, smem_bytes, ranges_off, probs_off;
-    int pad[3];
+    int seg_blocks;         // row blocks per sub-segment of a problem with K > 4096
+    int pad[2];
 };
 static_assert(sizeof(GHeader) == 64, "header size");
 
@@ -69,41 +71,48 @@ struct GSingle {            // whole plan of a one-problem call, passed by value
 
 // ---------------------------------------------------------------- device
 struct GIter {               // position in one warp's sequence of stages
-    int p, c, b, j;
+    int p, sb, c, b, j;      // problem, sub-segment start block, chunk, block, slice
 };
 
+// A CTA's work: for each problem p of its range, the blocks [bs(p), be(p)),
+// cut into sub-segments of at most mb(p) blocks (only problems with more than
+// one K chunk are cut: their row partials live in shared memory between
+// chunks); per sub-segment, chunk by chunk; per chunk, this warp's blocks
+// (every W-th); per block, the chunk's 8-group slices.
 struct GCtx {
     const GProb* P;
     GRange R;
-    int w, W;
+    int w, W, seg_blocks;
     __device__ __forceinline__ int bs(int p) const { return p == R.p0 ? R.b0 : 0; }
     __device__ __forceinline__ int be(int p) const { return p == R.p1 ? R.b1 : P[p].RB; }
+    __device__ __forceinline__ int mb(int p) const { return P[p].nch > 1 ? seg_blocks : 0x3fffffff; }
+    __device__ __forceinline__ int se(int p, int sb) const { return min(be(p), sb + mb(p)); }
     __device__ __forceinline__ int slices(int p, int c) const {
         const int cg = min(kGChunkGroups, P[p].G - kGChunkGroups * c);
         return cg >> 3;
     }
-    __device__ __forceinline__ bool done(const GIter& it) const {
-        return it.p > R.p1 || (it.p == R.p1 && it.b >= R.b1);
-    }
-    // Move to the first valid stage at or after `it` (block of this warp in a
-    // non-empty segment).
+    __device__ __forceinline__ bool done(const GIter& it) const { return it.p > R.p1; }
+    // Move to the first valid stage at or after `it` (a block of this warp).
     __device__ __forceinline__ void settle(GIter& it) const {
         while (it.p <= R.p1) {
-            if (it.b < be(it.p)) return;
-            ++it.c;
-            if (it.c < P[it.p].nch) {
-                it.b = bs(it.p) + w;
+            if (it.sb < be(it.p) && it.b < se(it.p, it.sb)) return;
+            if (it.sb < be(it.p) && ++it.c < P[it.p].nch) {
+                it.b = it.sb + w;              // next chunk, same sub-segment
+            } else if (it.sb < be(it.p) && (it.sb += mb(it.p)) < be(it.p)) {
+                it.c = 0;                      // next sub-segment
+                it.b = it.sb + w;
             } else {
-                ++it.p;
-                it.c = 0;
+                ++it.p;                        // next problem
                 if (it.p > R.p1) return;
-                it.b = bs(it.p) + w;
+                it.sb = bs(it.p);
+                it.c = 0;
+                it.b = it.sb + w;
             }
             it.j = 0;
         }
     }
     __device__ __forceinline__ GIter first() const {
-        GIter it{R.p0, 0, bs(R.p0) + w, 0};
+        GIter it{R.p0, bs(R.p0), 0, bs(R.p0) + w, 0};
         settle(it);
         return it;
     }
@@ -137,6 +146,7 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     cx.w = warp;
     cx.W = W;
+    cx.seg_blocks = H->seg_blocks;
     const GProb* P = cx.P;
     const uint32_t bars = base + H->off_bars + (uint32_t)(warp * S) * 8u;
     const uint32_t stages = base + (uint32_t)(warp * S) * kGStageBytes;
@@ -167,9 +177,9 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
     int kfail = -1;     // stage whose bounded wait gave up
     bool ok = true;
     for (int p = cx.R.p0; p <= cx.R.p1; ++p) {
-        const int bs = cx.bs(p), be = cx.be(p);
-        if (bs >= be) continue;
-        const GProb& pr = P[p];
+      const GProb& pr = P[p];
+      for (int sb = cx.bs(p); sb < cx.be(p); sb += cx.mb(p)) {
+        const int be = cx.se(p, sb);
         for (int c = 0; c < pr.nch; ++c) {
             const int cg = min(kGChunkGroups, pr.G - kGChunkGroups * c);
             // --- tables for (problem p, chunk c): every thread of the CTA
@@ -193,16 +203,16 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
                 if (lane == 0) fac[g] = __uint_as_float((uint32_t)(mg + 127) << 23);
             }
             __syncthreads();
-            for (int t = threadIdx.x; t < cg * kT6Fields; t += blockDim.x) {
-                const int g = t / kT6Fields, f = t - g * kT6Fields;
-                t6_build(tabs + g * kT6GroupBytes + f * kT6TableBytes, xs + g * 128, f);
+            for (int t = threadIdx.x; t < cg * kT6Fields * 8; t += blockDim.x) {
+                const int tt = t >> 3, g = tt / kT6Fields, f = tt - g * kT6Fields;
+                t6_build_chunk(tabs + g * kT6GroupBytes + f * kT6TableBytes, xs + g * 128, f, t & 7);
             }
             __syncthreads();
-            if (p == cx.R.p0 && c == 0) pdl_launch_dependents();
+            if (p == cx.R.p0 && sb == cx.bs(p) && c == 0) pdl_launch_dependents();
 
-            // --- this warp's blocks of the segment, for chunk c
+            // --- this warp's blocks of the sub-segment, for chunk c
             const int nsl = cg >> 3;
-            for (int b = bs + warp; b < be; b += W) {
+            for (int b = sb + warp; b < be; b += W) {
                 float acc = 0.f;
                 for (int j = 0; j < nsl; ++j, ++k) {
                     const int s = k % S;
@@ -234,7 +244,7 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
                     if (!cx.done(prod)) cx.next(prod);
                 }
                 const int row = b * 32 + lane;
-                const int li = (b - bs) * 32 + lane;           // row within the segment
+                const int li = (b - sb) * 32 + lane;           // row within the sub-segment
                 if (pr.nch > 1) {
                     const float v = (c == 0) ? acc : part[li] + acc;
                     if (c + 1 < pr.nch) {
@@ -249,6 +259,7 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
                 }
             }
         }
+      }
     }
     if (!ok && lane == 0) {
         // Give copies still in flight a bounded chance to land before exit.
@@ -344,33 +355,36 @@ bool plan_layout(const std::vector<GProb>& probs, int nctas, GHeader& h, std::ve
         for (int p = r.p0; p <= r.p1 && p < n; ++p) {
             if (probs[p].nch <= 1) continue;
             const int bs = p == r.p0 ? r.b0 : 0, be = p == r.p1 ? r.b1 : probs[p].RB;
-            if (be > bs) part_rows = std::max(part_rows, (be - bs) * 32);
+            if (be > bs) part_rows = std::max(part_rows, std::min(be - bs, kGSegBlocks) * 32);
         }
     }
     h.count = n;
     h.nctas = nctas;
-    h.W = kGWarps;
     h.part_rows = part_rows;
+    h.seg_blocks = kGSegBlocks;
     const int tables = kGChunkGroups * kT6GroupBytes;
     const int xbytes = kGChunkGroups * 128 * 4;
-    for (int S = 3; S >= 1; --S) {
-        uint32_t off = (uint32_t)(kGWarps * S * kGStageBytes);
-        const uint32_t off_tables = off;  off += tables;
-        const uint32_t off_x = off;       off += xbytes;
-        const uint32_t off_fac = off;     off += kGChunkGroups * 4;
-        const uint32_t off_part = off;    off += (uint32_t)part_rows * 4;
-        off = (off + 7u) & ~7u;
-        const uint32_t off_bars = off;    off += kGWarps * S * 8;
-        const size_t smem = 1024 + (size_t)off;
-        if (smem <= (size_t)kGMaxSmem) {
-            h.S = S;
-            h.off_tables = off_tables;
-            h.off_x = off_x;
-            h.off_fac = off_fac;
-            h.off_part = off_part;
-            h.off_bars = off_bars;
-            h.smem_bytes = (int)smem;
-            return true;
+    for (int W : {kGWarps, kGWarps / 2}) {
+        for (int S = 3; S >= 1; --S) {
+            uint32_t off = (uint32_t)(W * S * kGStageBytes);
+            const uint32_t off_tables = off;  off += tables;
+            const uint32_t off_x = off;       off += xbytes;
+            const uint32_t off_fac = off;     off += kGChunkGroups * 4;
+            const uint32_t off_part = off;    off += (uint32_t)part_rows * 4;
+            off = (off + 7u) & ~7u;
+            const uint32_t off_bars = off;    off += W * S * 8;
+            const size_t smem = 1024 + (size_t)off;
+            if (smem <= (size_t)kGMaxSmem) {
+                h.W = W;
+                h.S = S;
+                h.off_tables = off_tables;
+                h.off_x = off_x;
+                h.off_fac = off_fac;
+                h.off_part = off_part;
+                h.off_bars = off_bars;
+                h.smem_bytes = (int)smem;
+                return true;
+            }
         }
     }
     return false;

@@ -126,9 +126,9 @@ k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
     }
     __syncthreads();
     uint8_t* tabs = sm + p.off_tables;
-    for (int t = threadIdx.x; t < Gc * kT6Fields; t += blockDim.x) {
-        const int g = t / kT6Fields, f = t - g * kT6Fields;
-        t6_build(tabs + g * kT6GroupBytes + f * kT6TableBytes, xs + g * 128, f);
+    for (int t = threadIdx.x; t < Gc * kT6Fields * 8; t += blockDim.x) {
+        const int tt = t >> 3, g = tt / kT6Fields, f = tt - g * kT6Fields;
+        t6_build_chunk(tabs + g * kT6GroupBytes + f * kT6TableBytes, xs + g * 128, f, t & 7);
     }
     __syncthreads();
     pdl_launch_dependents();

@@ -54,30 +54,30 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t ra
 }
 
 // ---------------------------------------------------------------- tables
-// Table for field f of one group, from the group's 128 prescaled activations
-// x' (fp32, shared memory): 6 of them (f < 21) or the last two (f = 21).
+// Chunk c (16 bytes: entries 8c..8c+7) of the table of field f of one group,
+// from the group's 128 prescaled activations x' (fp32, shared memory): six of
+// them (f < 21) or the last two (f = 21, an 8-byte table written by c = 0).
 // Entry e sits at byte 2e; complementary indices hold exact negatives (every
-// sum is formed symmetrically).
-__device__ __forceinline__ void t6_build(uint8_t* tab, const float* xg, int f) {
+// sum is formed symmetrically).  Eight threads build one table, so the eight
+// threads of a quarter warp store 128 contiguous bytes (no bank conflicts).
+__device__ __forceinline__ void t6_build_chunk(uint8_t* tab, const float* xg, int f, int c) {
     if (f < 21) {
         const float* xs = xg + 6 * f;
         const float v0 = xs[0], v1 = xs[1], v2 = xs[2], v3 = xs[3], v4 = xs[4], v5 = xs[5];
-        const float a = v0 + v1, b = v0 - v1, c = v3 + v4, d = v3 - v4;
+        const float a = v0 + v1, b = v0 - v1;
         const float lo[8] = {-a - v2, b - v2, -b - v2, a - v2, -a + v2, b + v2, -b + v2, a + v2};
-        const float hi[8] = {-c - v5, d - v5, -d - v5, c - v5, -c + v5, d + v5, -d + v5, c + v5};
-        uint4* dst = reinterpret_cast<uint4*>(tab);
+        // hi part of entries 8c..8c+7: bits (3,4,5) of e = bits of c
+        const float s3 = (c & 1) ? v3 : -v3, s4 = (c & 2) ? v4 : -v4, s5 = (c & 4) ? v5 : -v5;
+        const float hc = (s3 + s4) + s5;
+        // the same value as the full-table form hi[c]: +-v3 +-v4 first, then +-v5
+        uint32_t wd[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            uint32_t wd[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int e0 = 8 * i + 2 * j, e1 = e0 + 1;
-                const __half2 h = __floats2half2_rn(lo[e0 & 7] + hi[e0 >> 3], lo[e1 & 7] + hi[e1 >> 3]);
-                wd[j] = *reinterpret_cast<const uint32_t*>(&h);
-            }
-            dst[i] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        for (int j = 0; j < 4; ++j) {
+            const __half2 h = __floats2half2_rn(lo[2 * j] + hc, lo[2 * j + 1] + hc);
+            wd[j] = *reinterpret_cast<const uint32_t*>(&h);
         }
-    } else {
+        reinterpret_cast<uint4*>(tab)[c] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    } else if (c == 0) {
         const float v0 = xg[126], v1 = xg[127];
         const __half2 h0 = __floats2half2_rn(-v0 - v1, v0 - v1);
         const __half2 h1 = __floats2half2_rn(-v0 + v1, v0 + v1);
@@ -116,9 +116,9 @@ template <size_t... F>
 __device__ __forceinline__ float t6_group(const uint32_t (&w)[4], uint32_t tg, std::index_sequence<F...>) {
     unsigned short t[sizeof...(F)];
     ((t[F] = t6_ld<(int)F>(w, tg)), ...);
-    float acc[2] = {0.f, 0.f};
-    ((acc[F & 1] = t6_add(t[F], acc[F & 1])), ...);
-    return acc[0] + acc[1];
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    ((acc[F & 3] = t6_add(t[F], acc[F & 3])), ...);
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
 
