@@ -41,13 +41,15 @@ constexpr int kGMaxCtas = 160;
 constexpr int kGWarps = 16;
 constexpr int kGMaxSmem = 227 * 1024;
 constexpr int kGSegBlocks = 128;             // sub-segment cap: 4096 rows of partials
+constexpr int kGMaxProbsPerCta = 64;         // problems one CTA's range may touch
 
 struct GHeader {            // 64 bytes
     int count, nctas, W, S;
     uint32_t off_tables, off_x, off_fac, off_part, off_bars;
     int part_rows, smem_bytes, ranges_off, probs_off;
     int seg_blocks;         // row blocks per sub-segment of a problem with K > 4096
-    int pad[2];
+    uint32_t off_xraw;      // raw bf16 activations of the next phase (bulk copy target)
+    uint32_t off_pinfo;     // per-problem {RB, G, nch, N} of the CTA's range
 };
 static_assert(sizeof(GHeader) == 64, "header size");
 
@@ -81,14 +83,17 @@ struct GIter {               // position in one warp's sequence of stages
 // (every W-th); per block, the chunk's 8-group slices.
 struct GCtx {
     const GProb* P;
+    const int4* I;          // shared memory: {RB, G, nch, N} of problems R.p0.. (index p - R.p0)
     GRange R;
     int w, W, seg_blocks;
+    __device__ __forceinline__ int4 info(int p) const { return I[p - R.p0]; }
     __device__ __forceinline__ int bs(int p) const { return p == R.p0 ? R.b0 : 0; }
-    __device__ __forceinline__ int be(int p) const { return p == R.p1 ? R.b1 : P[p].RB; }
-    __device__ __forceinline__ int mb(int p) const { return P[p].nch > 1 ? seg_blocks : 0x3fffffff; }
+    __device__ __forceinline__ int be(int p) const { return p == R.p1 ? R.b1 : info(p).x; }
+    __device__ __forceinline__ int nch(int p) const { return info(p).z; }
+    __device__ __forceinline__ int mb(int p) const { return nch(p) > 1 ? seg_blocks : 0x3fffffff; }
     __device__ __forceinline__ int se(int p, int sb) const { return min(be(p), sb + mb(p)); }
     __device__ __forceinline__ int slices(int p, int c) const {
-        const int cg = min(kGChunkGroups, P[p].G - kGChunkGroups * c);
+        const int cg = min(kGChunkGroups, info(p).y - kGChunkGroups * c);
         return cg >> 3;
     }
     __device__ __forceinline__ bool done(const GIter& it) const { return it.p > R.p1; }
@@ -96,7 +101,7 @@ struct GCtx {
     __device__ __forceinline__ void settle(GIter& it) const {
         while (it.p <= R.p1) {
             if (it.sb < be(it.p) && it.b < se(it.p, it.sb)) return;
-            if (it.sb < be(it.p) && ++it.c < P[it.p].nch) {
+            if (it.sb < be(it.p) && ++it.c < nch(it.p)) {
                 it.b = it.sb + w;              // next chunk, same sub-segment
             } else if (it.sb < be(it.p) && (it.sb += mb(it.p)) < be(it.p)) {
                 it.c = 0;                      // next sub-segment
@@ -110,6 +115,26 @@ struct GCtx {
             }
             it.j = 0;
         }
+    }
+    // CTA-level phases (problem, sub-segment, chunk), in execution order.
+    __device__ __forceinline__ bool next_phase(int& p, int& sb, int& c) const {
+        if (++c < nch(p)) return true;
+        c = 0;
+        sb += mb(p);
+        if (sb < be(p)) return true;
+        for (++p; p <= R.p1; ++p) {
+            sb = bs(p);
+            if (sb < be(p)) return true;
+        }
+        return false;
+    }
+    __device__ __forceinline__ bool first_phase(int& p, int& sb, int& c) const {
+        c = 0;
+        for (p = R.p0; p <= R.p1; ++p) {
+            sb = bs(p);
+            if (sb < be(p)) return true;
+        }
+        return false;
     }
     __device__ __forceinline__ GIter first() const {
         GIter it{R.p0, bs(R.p0), 0, bs(R.p0) + w, 0};
@@ -147,6 +172,13 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
     cx.w = warp;
     cx.W = W;
     cx.seg_blocks = H->seg_blocks;
+    int4* pinfo = reinterpret_cast<int4*>(sm + H->off_pinfo);
+    for (int i = threadIdx.x; i <= cx.R.p1 - cx.R.p0 && i < kGMaxProbsPerCta; i += blockDim.x) {
+        const GProb& q = cx.P[cx.R.p0 + i];
+        pinfo[i] = make_int4(q.RB, q.G, q.nch, q.N);
+    }
+    cx.I = pinfo;
+    __syncthreads();
     const GProb* P = cx.P;
     const uint32_t bars = base + H->off_bars + (uint32_t)(warp * S) * 8u;
     const uint32_t stages = base + (uint32_t)(warp * S) * kGStageBytes;
@@ -165,7 +197,25 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
     }
     __syncwarp();
 
+    // The activations of each phase are bulk-copied into shared memory one
+    // phase ahead (mbarrier xbar, one completion per phase).
+    const uint32_t xbar = base + H->off_bars + (uint32_t)(W * S) * 8u;
+    const uint32_t xraw = base + H->off_xraw;
+    auto prefetch_x = [&](int p, int c) {
+        const GProb& q = P[p];
+        const int cg = min(kGChunkGroups, q.G - kGChunkGroups * c);
+        mbar_expect_tx(xbar, (uint32_t)cg * 256u);
+        bulk_g2s(xraw, q.x + (size_t)c * kGChunkGroups * 128, (uint32_t)cg * 256u, xbar);
+    };
     pdl_wait();   // inputs may come from the preceding kernel
+    if (threadIdx.x == 0) {
+        mbar_init(xbar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        int fp, fsb, fc;
+        if (cx.first_phase(fp, fsb, fc)) prefetch_x(fp, fc);
+    }
+    int xphase = 0;
+    const uint16_t* xr = reinterpret_cast<const uint16_t*>(sm + H->off_xraw);
     float* fac = reinterpret_cast<float*>(sm + H->off_fac);
     float* xs = reinterpret_cast<float*>(sm + H->off_x);
     float* part = reinterpret_cast<float*>(sm + H->off_part);
@@ -178,15 +228,20 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
     bool ok = true;
     for (int p = cx.R.p0; p <= cx.R.p1; ++p) {
       const GProb& pr = P[p];
+      const int4 pi = cx.info(p);             // RB, G, nch, N
       for (int sb = cx.bs(p); sb < cx.be(p); sb += cx.mb(p)) {
         const int be = cx.se(p, sb);
-        for (int c = 0; c < pr.nch; ++c) {
-            const int cg = min(kGChunkGroups, pr.G - kGChunkGroups * c);
+        for (int c = 0; c < pi.z; ++c) {
+            const int cg = min(kGChunkGroups, pi.y - kGChunkGroups * c);
             // --- tables for (problem p, chunk c): every thread of the CTA
             __syncthreads();                                   // old tables no longer read
-            const uint16_t* xc = pr.x + (size_t)c * kGChunkGroups * 128;
+            if (!mbar_wait(xbar, (uint32_t)(xphase & 1))) {     // this phase's activations
+                if (lane == 0) atomicOr(&g_group_wait_timeouts, 2u);
+                ok = false;
+            }
+            ++xphase;
             for (int g = warp; g < cg; g += W) {               // one group per warp pass
-                const uint2 xv = *reinterpret_cast<const uint2*>(xc + g * 128 + 4 * lane);
+                const uint2 xv = *reinterpret_cast<const uint2*>(xr + g * 128 + 4 * lane);
                 const float x0 = bf16_bits_to_f32(xv.x & 0xffffu), x1 = bf16_bits_to_f32(xv.x >> 16);
                 const float x2 = bf16_bits_to_f32(xv.y & 0xffffu), x3 = bf16_bits_to_f32(xv.y >> 16);
                 float m = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
@@ -203,9 +258,13 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
                 if (lane == 0) fac[g] = __uint_as_float((uint32_t)(mg + 127) << 23);
             }
             __syncthreads();
-            for (int t = threadIdx.x; t < cg * kT6Fields * 8; t += blockDim.x) {
-                const int tt = t >> 3, g = tt / kT6Fields, f = tt - g * kT6Fields;
-                t6_build_chunk(tabs + g * kT6GroupBytes + f * kT6TableBytes, xs + g * 128, f, t & 7);
+            if (threadIdx.x == 0) {                            // raw x consumed: fetch the next phase's
+                int np = p, nsb = sb, nc = c;
+                if (cx.next_phase(np, nsb, nc)) prefetch_x(np, nc);
+            }
+            for (int t = threadIdx.x; t < cg * kT6Fields * 4; t += blockDim.x) {
+                const int tt = t >> 2, g = tt / kT6Fields, f = tt - g * kT6Fields;
+                t6_build_pair(tabs + g * kT6GroupBytes + f * kT6TableBytes, xs + g * 128, f, t & 3, tt & 1);
             }
             __syncthreads();
             if (p == cx.R.p0 && sb == cx.bs(p) && c == 0) pdl_launch_dependents();
@@ -245,15 +304,15 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
                 }
                 const int row = b * 32 + lane;
                 const int li = (b - sb) * 32 + lane;           // row within the sub-segment
-                if (pr.nch > 1) {
+                if (pi.z > 1) {
                     const float v = (c == 0) ? acc : part[li] + acc;
-                    if (c + 1 < pr.nch) {
+                    if (c + 1 < pi.z) {
                         part[li] = v;
                         continue;
                     }
                     acc = v;
                 }
-                if (row < pr.N) {
+                if (row < pi.w) {
                     if (pr.y_bf16) reinterpret_cast<uint16_t*>(pr.y)[row] = f32_to_bf16_bits(acc);
                     else reinterpret_cast<float*>(pr.y)[row] = acc;
                 }
@@ -327,37 +386,66 @@ bool encode_prob(GProb& g, const bit1_gemv_problem& pb) {
     return true;
 }
 
-// Cost-balanced contiguous block ranges (cost of a block ~ its bytes ~ K),
-// then the shared memory layout; false if some segment that needs a
-// cross-chunk partial buffer would not fit.
+// Contiguous block ranges, one per CTA, balanced on an estimate of each
+// CTA's time: a block costs K (its bytes are proportional to K) and every
+// table build (first block of a problem in the CTA, and every kGSegBlocks-th
+// block of a problem with several K chunks) costs kGBuildCost per chunk.  A
+// greedy pass packs blocks in order under a per-CTA budget; a binary search
+// finds the smallest budget that fits in nctas CTAs.  Then the shared memory
+// layout; false if it does not fit.
+constexpr double kGBuildCost = 6.0 * 4096;    // one chunk build ~ six 4096-wide blocks (measured)
+
+int partition(const std::vector<GProb>& probs, double T, std::vector<GRange>* out) {
+    const int n = (int)probs.size();
+    int ctas = 1;
+    double cur = 0.0;
+    GRange r{0, 0, 0, 0};
+    for (int p = 0; p < n; ++p) {
+        int taken = 0;
+        const double c = (double)probs[p].K;
+        const double build = kGBuildCost * probs[p].nch;
+        for (int b = 0; b < probs[p].RB; ++b) {
+            double add = c;
+            if (taken == 0 || (probs[p].nch > 1 && taken % kGSegBlocks == 0)) add += build;
+            if (cur > 0.0 && cur + add > T) {
+                if (out) { r.p1 = p; r.b1 = b; out->push_back(r); }
+                r = GRange{p, b, p, b};
+                ++ctas;
+                cur = 0.0;
+                taken = 0;
+                add = c + build;
+            }
+            cur += add;
+            ++taken;
+        }
+    }
+    if (out) { r.p1 = n - 1; r.b1 = probs[n - 1].RB; out->push_back(r); }
+    return ctas;
+}
+
 bool plan_layout(const std::vector<GProb>& probs, int nctas, GHeader& h, std::vector<GRange>& ranges) {
     const int n = (int)probs.size();
-    std::vector<double> cum(n + 1, 0.0);
-    for (int i = 0; i < n; ++i) cum[i + 1] = cum[i] + (double)probs[i].RB * probs[i].K;
-    const double total = cum[n];
-    auto locate = [&](double c, int& p, int& b) {   // first block whose start cost >= c
-        if (c >= total) { p = n - 1; b = probs[n - 1].RB; return; }
-        p = (int)(std::upper_bound(cum.begin(), cum.end(), c) - cum.begin()) - 1;
-        if (p < 0) p = 0;
-        const double per = (double)probs[p].K;
-        b = (int)((c - cum[p] + per - 1e-9) / per);
-        if (b > probs[p].RB) b = probs[p].RB;
-        if (b == probs[p].RB && p + 1 < n) { ++p; b = 0; }
-    };
-    ranges.resize(nctas);
+    double total = 0.0;
+    for (int p = 0; p < n; ++p) total += (double)probs[p].RB * probs[p].K + kGBuildCost * probs[p].nch;
+    double lo = total / nctas, hi = total + kGBuildCost * 8;
+    for (int it = 0; it < 60 && hi - lo > 1e-4 * lo; ++it) {
+        const double mid = 0.5 * (lo + hi);
+        if (partition(probs, mid, nullptr) <= nctas) hi = mid;
+        else lo = mid;
+    }
+    ranges.clear();
+    partition(probs, hi, &ranges);
+    while ((int)ranges.size() < nctas)            // CTAs without work
+        ranges.push_back(GRange{n - 1, probs[n - 1].RB, n - 1, probs[n - 1].RB});
+    for (const GRange& r : ranges)
+        if (r.p1 - r.p0 + 1 > kGMaxProbsPerCta) return false;
     int part_rows = 0;
-    for (int i = 0; i < nctas; ++i) {
-        GRange r;
-        locate(total * i / nctas, r.p0, r.b0);
-        locate(total * (i + 1) / nctas, r.p1, r.b1);
-        if (i == nctas - 1) { r.p1 = n - 1; r.b1 = probs[n - 1].RB; }
-        ranges[i] = r;
+    for (const GRange& r : ranges)
         for (int p = r.p0; p <= r.p1 && p < n; ++p) {
             if (probs[p].nch <= 1) continue;
             const int bs = p == r.p0 ? r.b0 : 0, be = p == r.p1 ? r.b1 : probs[p].RB;
             if (be > bs) part_rows = std::max(part_rows, std::min(be - bs, kGSegBlocks) * 32);
         }
-    }
     h.count = n;
     h.nctas = nctas;
     h.part_rows = part_rows;
@@ -370,9 +458,11 @@ bool plan_layout(const std::vector<GProb>& probs, int nctas, GHeader& h, std::ve
             const uint32_t off_tables = off;  off += tables;
             const uint32_t off_x = off;       off += xbytes;
             const uint32_t off_fac = off;     off += kGChunkGroups * 4;
+            const uint32_t off_xraw = off;    off += kGChunkGroups * 128 * 2;
+            const uint32_t off_pinfo = off;   off += kGMaxProbsPerCta * 16;
             const uint32_t off_part = off;    off += (uint32_t)part_rows * 4;
             off = (off + 7u) & ~7u;
-            const uint32_t off_bars = off;    off += W * S * 8;
+            const uint32_t off_bars = off;    off += W * S * 8 + 8;
             const size_t smem = 1024 + (size_t)off;
             if (smem <= (size_t)kGMaxSmem) {
                 h.W = W;
@@ -380,6 +470,8 @@ bool plan_layout(const std::vector<GProb>& probs, int nctas, GHeader& h, std::ve
                 h.off_tables = off_tables;
                 h.off_x = off_x;
                 h.off_fac = off_fac;
+                h.off_xraw = off_xraw;
+                h.off_pinfo = off_pinfo;
                 h.off_part = off_part;
                 h.off_bars = off_bars;
                 h.smem_bytes = (int)smem;

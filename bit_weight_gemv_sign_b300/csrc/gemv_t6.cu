@@ -126,9 +126,9 @@ k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
     }
     __syncthreads();
     uint8_t* tabs = sm + p.off_tables;
-    for (int t = threadIdx.x; t < Gc * kT6Fields * 8; t += blockDim.x) {
-        const int tt = t >> 3, g = tt / kT6Fields, f = tt - g * kT6Fields;
-        t6_build_chunk(tabs + g * kT6GroupBytes + f * kT6TableBytes, xs + g * 128, f, t & 7);
+    for (int t = threadIdx.x; t < Gc * kT6Fields * 4; t += blockDim.x) {
+        const int tt = t >> 2, g = tt / kT6Fields, f = tt - g * kT6Fields;
+        t6_build_pair(tabs + g * kT6GroupBytes + f * kT6TableBytes, xs + g * 128, f, t & 3, tt & 1);
     }
     __syncthreads();
     pdl_launch_dependents();

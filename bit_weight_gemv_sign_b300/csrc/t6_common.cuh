@@ -37,6 +37,12 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int
     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
                  ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar) : "memory");
 }
+// 1-D bulk copy global -> shared, completion on an mbarrier (sizes and both
+// addresses multiples of 16 bytes).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
@@ -54,30 +60,36 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t ra
 }
 
 // ---------------------------------------------------------------- tables
-// Chunk c (16 bytes: entries 8c..8c+7) of the table of field f of one group,
-// from the group's 128 prescaled activations x' (fp32, shared memory): six of
-// them (f < 21) or the last two (f = 21, an 8-byte table written by c = 0).
-// Entry e sits at byte 2e; complementary indices hold exact negatives (every
-// sum is formed symmetrically).  Eight threads build one table, so the eight
-// threads of a quarter warp store 128 contiguous bytes (no bank conflicts).
-__device__ __forceinline__ void t6_build_chunk(uint8_t* tab, const float* xg, int f, int c) {
+// Two 16-byte chunks (entries 8c..8c+7 for c = h and c = h+4) of the table of
+// field f of one group, from the group's 128 prescaled activations x' (fp32,
+// shared memory): six of them (f < 21) or the last two (f = 21: an 8-byte
+// table, written by h = 0).  Entry e sits at byte 2e; complementary indices
+// hold exact negatives (every sum is formed symmetrically).  Four threads
+// build one table; the thread with odd `flip` writes its upper chunk first,
+// so the eight threads of a quarter warp (two tables) store to eight
+// different bank quads at each store (no conflicts).
+__device__ __forceinline__ void t6_build_pair(uint8_t* tab, const float* xg, int f, int h, int flip) {
     if (f < 21) {
         const float* xs = xg + 6 * f;
         const float v0 = xs[0], v1 = xs[1], v2 = xs[2], v3 = xs[3], v4 = xs[4], v5 = xs[5];
         const float a = v0 + v1, b = v0 - v1;
         const float lo[8] = {-a - v2, b - v2, -b - v2, a - v2, -a + v2, b + v2, -b + v2, a + v2};
-        // hi part of entries 8c..8c+7: bits (3,4,5) of e = bits of c
-        const float s3 = (c & 1) ? v3 : -v3, s4 = (c & 2) ? v4 : -v4, s5 = (c & 4) ? v5 : -v5;
-        const float hc = (s3 + s4) + s5;
-        // the same value as the full-table form hi[c]: +-v3 +-v4 first, then +-v5
-        uint32_t wd[4];
+        const float s3 = (h & 1) ? v3 : -v3, s4 = (h & 2) ? v4 : -v4;
+        const float h34 = s3 + s4;                   // +-v3 +-v4 of chunk h (and of h+4)
+        const float hc0 = h34 - v5, hc1 = h34 + v5;  // chunk h (bit 5 clear) and h+4 (set)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const __half2 h = __floats2half2_rn(lo[2 * j] + hc, lo[2 * j + 1] + hc);
-            wd[j] = *reinterpret_cast<const uint32_t*>(&h);
+        for (int r = 0; r < 2; ++r) {
+            const int which = r ^ flip;              // 0: chunk h, 1: chunk h+4
+            const float hc = which ? hc1 : hc0;
+            uint32_t wd[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const __half2 q = __floats2half2_rn(lo[2 * j] + hc, lo[2 * j + 1] + hc);
+                wd[j] = *reinterpret_cast<const uint32_t*>(&q);
+            }
+            reinterpret_cast<uint4*>(tab)[h + 4 * which] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
         }
-        reinterpret_cast<uint4*>(tab)[c] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-    } else if (c == 0) {
+    } else if (h == 0) {
         const float v0 = xg[126], v1 = xg[127];
         const __half2 h0 = __floats2half2_rn(-v0 - v1, v0 - v1);
         const __half2 h1 = __floats2half2_rn(-v0 + v1, v0 + v1);

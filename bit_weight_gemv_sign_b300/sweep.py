@@ -62,16 +62,18 @@ class Sweep:
         o = self.sc_off[i] // 2
         return self.scales[o: o + m.N * (m.K // 128)].view(m.N, m.K // 128)
 
-    def x_of(self, i):
+    def x_of(self, i, xbuf=None):
         m = self.mats[i]
         o = self.x_off[i] // 2
-        return self.x[o: o + self.B * m.K].view(self.B, m.K)
+        xb = self.x if xbuf is None else xbuf
+        return xb[o: o + self.B * m.K].view(self.B, m.K)
 
-    def y_of(self, i):
+    def y_of(self, i, ybuf=None):
         m = self.mats[i]
+        yb = self.y if ybuf is None else ybuf
         if self.y_dtype == BF16:
-            return self.y[self.y_off[i]: self.y_off[i] + 2 * self.B * m.N].view(torch.bfloat16).view(self.B, m.N)
-        return self.y[self.y_off[i]: self.y_off[i] + 4 * self.B * m.N].view(torch.float32).view(self.B, m.N)
+            return yb[self.y_off[i]: self.y_off[i] + 2 * self.B * m.N].view(torch.bfloat16).view(self.B, m.N)
+        return yb[self.y_off[i]: self.y_off[i] + 4 * self.B * m.N].view(torch.float32).view(self.B, m.N)
 
     # ---- data ------------------------------------------------------------
     def host_matrix(self, i):
@@ -116,10 +118,12 @@ class Sweep:
     def replay(self):
         self.graph.replay()
 
-    def group_plan(self):
+    def group_plan(self, x=None, y=None):
         """One grouped launch over every matrix of the sweep (each with its own
-        input): the plan is built once; run() is one kernel launch."""
-        probs = [(self.bits_of(i), self.scales_of(i), self.x_of(i), self.y_of(i))
+        input): the plan is built once; run() is one kernel launch.  ``x`` and
+        ``y`` replace the activation / output arenas (same layout), e.g. for a
+        second I/O slot over the same resident weights."""
+        probs = [(self.bits_of(i), self.scales_of(i), self.x_of(i, x), self.y_of(i, y))
                  for i in range(len(self.mats))]
         return GroupPlan(probs, device=self.device)
 
