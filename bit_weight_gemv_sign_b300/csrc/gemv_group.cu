@@ -38,7 +38,7 @@ __device__ unsigned int g_group_wait_timeouts = 0;
 constexpr int kGChunkGroups = 32;            // K chunk: 32 groups = 4096 inputs
 constexpr int kGStageBytes = 5120;           // 4 KB bits box + 512 B scales box, 1 KB aligned
 constexpr int kGMaxCtas = 160;
-constexpr int kGWarps = 16;
+constexpr int kGWarps = 20;
 constexpr int kGMaxSmem = 227 * 1024;
 constexpr int kGSegBlocks = 128;             // sub-segment cap: 4096 rows of partials
 constexpr int kGMaxProbsPerCta = 64;         // problems one CTA's range may touch
@@ -74,6 +74,7 @@ struct GSingle {            // whole plan of a one-problem call, passed by value
 // ---------------------------------------------------------------- device
 struct GIter {               // position in one warp's sequence of stages
     int p, sb, c, b, j;      // problem, sub-segment start block, chunk, block, slice
+    int nsl;                 // slices of chunk c of problem p
 };
 
 // A CTA's work: for each problem p of its range, the blocks [bs(p), be(p)),
@@ -100,7 +101,10 @@ struct GCtx {
     // Move to the first valid stage at or after `it` (a block of this warp).
     __device__ __forceinline__ void settle(GIter& it) const {
         while (it.p <= R.p1) {
-            if (it.sb < be(it.p) && it.b < se(it.p, it.sb)) return;
+            if (it.sb < be(it.p) && it.b < se(it.p, it.sb)) {
+                it.nsl = slices(it.p, it.c);
+                return;
+            }
             if (it.sb < be(it.p) && ++it.c < nch(it.p)) {
                 it.b = it.sb + w;              // next chunk, same sub-segment
             } else if (it.sb < be(it.p) && (it.sb += mb(it.p)) < be(it.p)) {
@@ -137,12 +141,12 @@ struct GCtx {
         return false;
     }
     __device__ __forceinline__ GIter first() const {
-        GIter it{R.p0, bs(R.p0), 0, bs(R.p0) + w, 0};
+        GIter it{R.p0, bs(R.p0), 0, bs(R.p0) + w, 0, 0};
         settle(it);
         return it;
     }
     __device__ __forceinline__ void next(GIter& it) const {
-        if (++it.j < slices(it.p, it.c)) return;
+        if (++it.j < it.nsl) return;
         it.j = 0;
         it.b += W;
         settle(it);
@@ -217,7 +221,6 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
     int xphase = 0;
     const uint16_t* xr = reinterpret_cast<const uint16_t*>(sm + H->off_xraw);
     float* fac = reinterpret_cast<float*>(sm + H->off_fac);
-    float* xs = reinterpret_cast<float*>(sm + H->off_x);
     float* part = reinterpret_cast<float*>(sm + H->off_part);
     uint8_t* tabs = sm + H->off_tables;
     const uint32_t tb = base + H->off_tables;
@@ -252,21 +255,22 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
                     const int e = (int)((__float_as_uint(m) >> 23) & 0xffu) - 127;
                     mg = min(max(e - 11, -126), 127);          // max|x'| < 2^12
                 }
-                const float finv = __uint_as_float((uint32_t)(127 - mg) << 23);
-                *reinterpret_cast<float4*>(xs + g * 128 + 4 * lane) =
-                    make_float4(x0 * finv, x1 * finv, x2 * finv, x3 * finv);
-                if (lane == 0) fac[g] = __uint_as_float((uint32_t)(mg + 127) << 23);
+                if (lane == 0) {
+                    fac[g] = __uint_as_float((uint32_t)(mg + 127) << 23);
+                    fac[kGChunkGroups + g] = __uint_as_float((uint32_t)(127 - mg) << 23);
+                }
+            }
+            __syncthreads();
+            for (int t = threadIdx.x; t < cg * kT6Fields * 4; t += blockDim.x) {
+                const int tt = t >> 2, g = tt / kT6Fields, f = tt - g * kT6Fields;
+                t6_build_pair(tabs + g * kT6GroupBytes + f * kT6TableBytes, xr + g * 128,
+                              fac[kGChunkGroups + g], f, t & 3, tt & 1);
             }
             __syncthreads();
             if (threadIdx.x == 0) {                            // raw x consumed: fetch the next phase's
                 int np = p, nsb = sb, nc = c;
                 if (cx.next_phase(np, nsb, nc)) prefetch_x(np, nc);
             }
-            for (int t = threadIdx.x; t < cg * kT6Fields * 4; t += blockDim.x) {
-                const int tt = t >> 2, g = tt / kT6Fields, f = tt - g * kT6Fields;
-                t6_build_pair(tabs + g * kT6GroupBytes + f * kT6TableBytes, xs + g * 128, f, t & 3, tt & 1);
-            }
-            __syncthreads();
             if (p == cx.R.p0 && sb == cx.bs(p) && c == 0) pdl_launch_dependents();
 
             // --- this warp's blocks of the sub-segment, for chunk c
@@ -451,13 +455,14 @@ bool plan_layout(const std::vector<GProb>& probs, int nctas, GHeader& h, std::ve
     h.part_rows = part_rows;
     h.seg_blocks = kGSegBlocks;
     const int tables = kGChunkGroups * kT6GroupBytes;
-    const int xbytes = kGChunkGroups * 128 * 4;
-    for (int W : {kGWarps, kGWarps / 2}) {
-        for (int S = 3; S >= 1; --S) {
+    // (warps, stages per warp) in order of preference; the first that fits wins
+    static const int kCfg[][2] = {{20, 1}, {16, 1}, {12, 1}, {8, 2}, {8, 1}};
+    for (const auto& cf : kCfg) {
+        const int W = cf[0], S = cf[1];
+        {
             uint32_t off = (uint32_t)(W * S * kGStageBytes);
             const uint32_t off_tables = off;  off += tables;
-            const uint32_t off_x = off;       off += xbytes;
-            const uint32_t off_fac = off;     off += kGChunkGroups * 4;
+            const uint32_t off_fac = off;     off += kGChunkGroups * 8;   // 2^m_g and 2^-m_g
             const uint32_t off_xraw = off;    off += kGChunkGroups * 128 * 2;
             const uint32_t off_pinfo = off;   off += kGMaxProbsPerCta * 16;
             const uint32_t off_part = off;    off += (uint32_t)part_rows * 4;
@@ -468,7 +473,6 @@ bool plan_layout(const std::vector<GProb>& probs, int nctas, GHeader& h, std::ve
                 h.W = W;
                 h.S = S;
                 h.off_tables = off_tables;
-                h.off_x = off_x;
                 h.off_fac = off_fac;
                 h.off_xraw = off_xraw;
                 h.off_pinfo = off_pinfo;

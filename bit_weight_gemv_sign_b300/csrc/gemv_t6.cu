@@ -99,19 +99,16 @@ k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
 
     // Activations come from the preceding kernel of a decode step.
     pdl_wait();
-    float* fac = reinterpret_cast<float*>(sm + p.off_factors);   // [Gc] 2^m_g
-    float* xs = reinterpret_cast<float*>(sm + p.off_x);           // [Gc*128] x, then x'
+    float* fac = reinterpret_cast<float*>(sm + p.off_factors);   // [Gc] 2^m_g, [Gc] 2^-m_g
+    uint16_t* xs = reinterpret_cast<uint16_t*>(sm + p.off_x);     // [Gc*128] bf16 activations
     const uint16_t* xc = p.x + (size_t)g0 * 128;
-    for (int i = threadIdx.x; i < Gc * 32; i += blockDim.x) {     // 4 activations per thread
-        const uint2 xv = *reinterpret_cast<const uint2*>(xc + 4 * i);
-        *reinterpret_cast<float4*>(xs + 4 * i) =
-            make_float4(bf16_bits_to_f32(xv.x & 0xffffu), bf16_bits_to_f32(xv.x >> 16),
-                        bf16_bits_to_f32(xv.y & 0xffffu), bf16_bits_to_f32(xv.y >> 16));
-    }
+    for (int i = threadIdx.x; i < Gc * 16; i += blockDim.x)        // 8 activations per thread
+        reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(xc)[i];
     __syncthreads();
     for (int g = warp; g < Gc; g += W) {
-        const float4 xv = *reinterpret_cast<const float4*>(xs + g * 128 + 4 * lane);
-        float m = fmaxf(fmaxf(fabsf(xv.x), fabsf(xv.y)), fmaxf(fabsf(xv.z), fabsf(xv.w)));
+        const uint2 xv = *reinterpret_cast<const uint2*>(xs + g * 128 + 4 * lane);
+        float m = fmaxf(fmaxf(fabsf(bf16_bits_to_f32(xv.x & 0xffffu)), fabsf(bf16_bits_to_f32(xv.x >> 16))),
+                        fmaxf(fabsf(bf16_bits_to_f32(xv.y & 0xffffu)), fabsf(bf16_bits_to_f32(xv.y >> 16))));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         int mg = 0;
@@ -119,16 +116,16 @@ k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
             const int e = (int)((__float_as_uint(m) >> 23) & 0xffu) - 127;  // floor(log2 m), normal m
             mg = min(max(e - 11, -126), 127);                                // max|x'| < 2^12
         }
-        const float finv = __uint_as_float((uint32_t)(127 - mg) << 23);      // exact power of two
-        *reinterpret_cast<float4*>(xs + g * 128 + 4 * lane) =
-            make_float4(xv.x * finv, xv.y * finv, xv.z * finv, xv.w * finv);
-        if (lane == 0) fac[g] = __uint_as_float((uint32_t)(mg + 127) << 23);
+        if (lane == 0) {
+            fac[g] = __uint_as_float((uint32_t)(mg + 127) << 23);
+            fac[Gc + g] = __uint_as_float((uint32_t)(127 - mg) << 23);
+        }
     }
     __syncthreads();
     uint8_t* tabs = sm + p.off_tables;
     for (int t = threadIdx.x; t < Gc * kT6Fields * 4; t += blockDim.x) {
         const int tt = t >> 2, g = tt / kT6Fields, f = tt - g * kT6Fields;
-        t6_build_pair(tabs + g * kT6GroupBytes + f * kT6TableBytes, xs + g * 128, f, t & 3, tt & 1);
+        t6_build_pair(tabs + g * kT6GroupBytes + f * kT6TableBytes, xs + g * 128, fac[Gc + g], f, t & 3, tt & 1);
     }
     __syncthreads();
     pdl_launch_dependents();
@@ -266,8 +263,8 @@ bool plan_t6_q(int64_t N, int64_t K, int Q, T6Plan& pl) {
     pl.Gc = (int)(G / Q);
     pl.stage_bytes = (32 * pl.Gc * 18 + 1023) & ~1023;
     const int tables = pl.Gc * kT6GroupBytes;
-    const int factors = pl.Gc * 4;
-    const int xbytes = pl.Gc * 128 * 4;
+    const int factors = pl.Gc * 8;
+    const int xbytes = pl.Gc * 128 * 2;
     const int64_t RB = (N + 31) / 32;
     auto total = [&](int W, int S, int bpc) {
         return (size_t)1024 + (size_t)W * S * pl.stage_bytes + tables + factors + xbytes +

@@ -61,17 +61,23 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t ra
 
 // ---------------------------------------------------------------- tables
 // Two 16-byte chunks (entries 8c..8c+7 for c = h and c = h+4) of the table of
-// field f of one group, from the group's 128 prescaled activations x' (fp32,
-// shared memory): six of them (f < 21) or the last two (f = 21: an 8-byte
-// table, written by h = 0).  Entry e sits at byte 2e; complementary indices
+// field f of one group, from the group's 128 activations (bf16, shared memory)
+// times the group's power-of-two prescale finv (exact): six of them (f < 21)
+// or the last two (f = 21: an 8-byte table, written by h = 0).  Entry e sits at byte 2e; complementary indices
 // hold exact negatives (every sum is formed symmetrically).  Four threads
 // build one table; the thread with odd `flip` writes its upper chunk first,
 // so the eight threads of a quarter warp (two tables) store to eight
 // different bank quads at each store (no conflicts).
-__device__ __forceinline__ void t6_build_pair(uint8_t* tab, const float* xg, int f, int h, int flip) {
+__device__ __forceinline__ void t6_build_pair(uint8_t* tab, const uint16_t* xg, float finv, int f, int h,
+                                              int flip) {
     if (f < 21) {
-        const float* xs = xg + 6 * f;
-        const float v0 = xs[0], v1 = xs[1], v2 = xs[2], v3 = xs[3], v4 = xs[4], v5 = xs[5];
+        const uint16_t* xs = xg + 6 * f;   // bf16, 4-byte aligned (6f elements)
+        const uint32_t p01 = *reinterpret_cast<const uint32_t*>(xs);
+        const uint32_t p23 = *reinterpret_cast<const uint32_t*>(xs + 2);
+        const uint32_t p45 = *reinterpret_cast<const uint32_t*>(xs + 4);
+        const float v0 = bf16_bits_to_f32(p01 & 0xffffu) * finv, v1 = bf16_bits_to_f32(p01 >> 16) * finv;
+        const float v2 = bf16_bits_to_f32(p23 & 0xffffu) * finv, v3 = bf16_bits_to_f32(p23 >> 16) * finv;
+        const float v4 = bf16_bits_to_f32(p45 & 0xffffu) * finv, v5 = bf16_bits_to_f32(p45 >> 16) * finv;
         const float a = v0 + v1, b = v0 - v1;
         const float lo[8] = {-a - v2, b - v2, -b - v2, a - v2, -a + v2, b + v2, -b + v2, a + v2};
         const float s3 = (h & 1) ? v3 : -v3, s4 = (h & 2) ? v4 : -v4;
@@ -90,7 +96,8 @@ __device__ __forceinline__ void t6_build_pair(uint8_t* tab, const float* xg, int
             reinterpret_cast<uint4*>(tab)[h + 4 * which] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
         }
     } else if (h == 0) {
-        const float v0 = xg[126], v1 = xg[127];
+        const uint32_t p = *reinterpret_cast<const uint32_t*>(xg + 126);
+        const float v0 = bf16_bits_to_f32(p & 0xffffu) * finv, v1 = bf16_bits_to_f32(p >> 16) * finv;
         const __half2 h0 = __floats2half2_rn(-v0 - v1, v0 - v1);
         const __half2 h1 = __floats2half2_rn(-v0 + v1, v0 + v1);
         *reinterpret_cast<uint2*>(tab) = make_uint2(*reinterpret_cast<const uint32_t*>(&h0),
