@@ -53,9 +53,11 @@ bool shape_ok(int64_t B, int64_t N, int64_t K) {
 
 bit1_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BIT1_OK : BIT1_ECUDA; }
 
+// Batch 1: the 6-bit-table kernel; batch 2..8: the nibble-table kernel;
+// batch >= 16 with enough scratch: the tensor-core kernel; else one warp per row.
 int pick_variant(int64_t B, int64_t N, int64_t K, size_t ws_bytes) {
-    (void)ws_bytes;
     if (t6_supported(B, N, K)) return BIT1_GEMV_LUT6;
+    if (B >= 16 && tc_supported(B, N, K) && ws_bytes >= tc_workspace_bytes(B, N, K)) return BIT1_GEMV_TC;
     if (lut_supported(B, N, K)) return BIT1_GEMV_LUT;
     return BIT1_GEMV_SIMPLE;
 }
@@ -109,8 +111,11 @@ bit1_status bit1_gemv_ex(const uint8_t* bits, const uint16_t* scales, const uint
         case BIT1_GEMV_STREAM:
             if (!group1_supported(B, N, K)) return BIT1_ESHAPE;
             return from_cuda(launch_gemv_group1(a));
-        case BIT1_GEMV_SPLITK:
         case BIT1_GEMV_TC:
+            if (!tc_supported(B, N, K)) return BIT1_ESHAPE;
+            if (ws_bytes < tc_workspace_bytes(B, N, K)) return BIT1_EINVAL;
+            return from_cuda(launch_gemv_tc(a));
+        case BIT1_GEMV_SPLITK:
             return BIT1_ESHAPE;  // not available for any shape in this build
         default:
             return BIT1_EINVAL;
@@ -126,6 +131,7 @@ bit1_status bit1_gemv(const uint8_t* bits, const uint16_t* scales, const uint16_
 
 size_t bit1_gemv_workspace_bytes(int64_t B, int64_t N, int64_t K) {
     if (!shape_ok(B, N, K)) return 0;
+    if (B >= 16 && tc_supported(B, N, K)) return tc_workspace_bytes(B, N, K);
     return 0;
 }
 
@@ -136,12 +142,13 @@ int bit1_gemv_pick(int64_t B, int64_t N, int64_t K, size_t ws_bytes) {
 
 int bit1_gemv_launches(int64_t B, int64_t N, int64_t K, int variant) {
     if (!shape_ok(B, N, K)) return 0;
-    if (variant == BIT1_GEMV_AUTO) variant = pick_variant(B, N, K, 0);
+    if (variant == BIT1_GEMV_AUTO) variant = pick_variant(B, N, K, bit1_gemv_workspace_bytes(B, N, K));
     switch (variant) {
         case BIT1_GEMV_SIMPLE: return 1;
         case BIT1_GEMV_LUT: return lut_supported(B, N, K) ? 1 : 0;
         case BIT1_GEMV_LUT6: return t6_supported(B, N, K) ? 1 : 0;
         case BIT1_GEMV_STREAM: return group1_supported(B, N, K) ? 1 : 0;
+        case BIT1_GEMV_TC: return tc_launch_count(B, N, K);
         default: return 0;
     }
 }
@@ -172,9 +179,9 @@ const char* bit1_status_str(bit1_status s) {
 const char* bit1_version(void) { return "bit1 0.2 (sm_103a)"; }
 
 unsigned int bit1_device_wait_timeouts(void) {
-    const unsigned int a = t6_take_timeouts(), b = group_take_timeouts();
-    if (a == 0xffffffffu || b == 0xffffffffu) return 0xffffffffu;
-    return a + b;
+    const unsigned int a = t6_take_timeouts(), b = group_take_timeouts(), c = tc_take_timeouts();
+    if (a == 0xffffffffu || b == 0xffffffffu || c == 0xffffffffu) return 0xffffffffu;
+    return a + b + c;
 }
 
 size_t bit1_group_plan_bytes(int count) { return group_plan_bytes(count); }
