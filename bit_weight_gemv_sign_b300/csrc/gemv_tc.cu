@@ -11,27 +11,40 @@
 // Design (one CTA = 256 weight rows x one K range):
 //  * A (weights): two M = 128 operands per K step, held in tensor memory.
 //    Thread t of warps 0-7 owns one row: per 128-input step it reads the row's
-//    16 sign bytes from a TMA-filled shared-memory ring, forms +-s exactly in
-//    fp16 and writes the 64 fp16x2 words with tcgen05.st.  Inside every
+//    16 sign bytes from a shared-memory ring (TMA boxes of 64 bytes x 256 rows,
+//    four steps, 64-byte swizzle), forms +-s exactly in fp16 and writes the 64
+//    fp16x2 words with tcgen05.st.  Inside every
 //    32-bit sign word, inputs k and k+16 share one fp16x2 register (sign bits
 //    15 and 31), so one shift and one LOP3 produce two weights; the
 //    activations are stored in the same permuted K order, so the contraction
 //    is unchanged.  No dense weight tile ever exists in shared memory or HBM.
 //  * B (activations): a prep kernel converts x (bf16) to fp16 with an exact
 //    per-batch-row power-of-two prescale (a bf16 significand fits fp16's),
-//    permuted as above, into the workspace; TMA stages 64-wide K boxes with
-//    128-byte swizzle (the canonical K-major operand layout).
-//  * fp32 accumulators in tensor memory (N = batch rounded up to 16; two
-//    accumulators, one per 128-row half), read back with tcgen05.ld; the
-//    prescale is undone in the epilogue.
-//  * Warps 0-7 unpack and run the epilogue, warp 8 streams sign bits, warp 9
-//    streams activations, warp 10 issues the MMAs; every mbarrier wait is
-//    bounded.  When the row tiles alone cannot fill the SMs, K is split over
-//    CTAs and a second kernel sums the fp32 partials in a fixed order.
+//    permuted as above, into the workspace; one 3-D TMA box per step stages
+//    two 64-wide K slabs with 128-byte swizzle (the canonical K-major layout).
+//  * fp32 accumulators in tensor memory (N = batch rounded up to 16; four
+//    accumulators: two per 128-row half, for the even and the odd 16-input
+//    slices of each step, summed in that order in the epilogue), read back
+//    with tcgen05.ld; the prescale is undone in the epilogue.
+//  * Warps 0-7 unpack and run the epilogue, warp 8 streams sign bits (one
+//    issuing lane per ring slot), warp 9 streams activations (one lane per
+//    stage), warps 10-13 issue the MMAs, one warp per accumulator (one thread
+//    issues a tcgen05.mma about every 54 cycles, so a single issuer would
+//    bound the kernel at small batch); every mbarrier wait is bounded.
+//  * Sign bits and scales do not depend on the preceding kernel (the prep
+//    kernel lets this one start only after its own wait on its predecessor),
+//    so they stream and unpack before griddepcontrol.wait; only the
+//    activation loads, the MMAs and the epilogue wait.
+//  * When the row tiles alone cannot fill the SMs, K is split over the Ks CTAs
+//    of a thread-block cluster in whole 4-step chunks.  Each CTA stages its
+//    fp32 accumulators in its own shared memory; after a cluster barrier, CTA
+//    j sums rows [64j/Ks, 64(j+1)/Ks) x 4 of every CTA's tile through
+//    distributed shared memory in rank order (deterministic) and writes y.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
 
 #include "common.cuh"
@@ -44,19 +57,23 @@ __device__ unsigned int g_tc_wait_timeouts = 0;
 
 constexpr int kTcRows = 256;              // weight rows per CTA (two M = 128 MMAs)
 constexpr int kTcStepK = 128;             // inputs per pipeline step (one scale group)
-constexpr int kTcStages = 3;              // A (tensor memory) / B (shared memory) stages
-constexpr int kTcWSlots = 8;              // sign-bit ring slots (4 KB each)
+constexpr int kTcStages = 3;              // max A (tensor memory) / B (shared memory) stages
+constexpr int kTcChunkSteps = 4;          // sign-bit box: 64 bytes of each row = 4 steps
+constexpr int kTcWSlots = 4;              // sign-bit ring slots
+constexpr uint32_t kTcWSlotBytes = kTcRows * 16 * kTcChunkSteps;   // 16 KB
 constexpr int kTcMaxB = 64;               // batch rows per launch (accumulators: 2 x 64 columns)
 constexpr int kTcUnpackWarps = 8;
-constexpr int kTcThreads = 32 * (kTcUnpackWarps + 3);
-constexpr uint32_t kTcWSlotBytes = kTcRows * 16;
+constexpr int kTcMmaWarps = 4;
+constexpr int kTcThreads = 32 * (kTcUnpackWarps + 2 + kTcMmaWarps);
+constexpr int kTcPrepThreads = 512;
+constexpr int kTcPrepUnits = 8;           // 16-byte units of x per prep thread held in registers
 
 struct TcParams {
     const uint16_t* scales;
     const float* xscale;      // [Bp] 2^m_b (undo the prescale)
-    float* partial;           // [Ks][Bp][N] fp32 when Ks > 1, else null
     void* y;                  // [B][N]
-    int N, K, B, Bp, Ks, steps, y_bf16;
+    int N, K, B, Bp, Ks, chunks, y_bf16;
+    int stages;               // A/B stages: 3 when the accumulators fit 128 columns (Bp <= 32), else 2
 };
 
 // ---------------------------------------------------------------- helpers
@@ -77,34 +94,81 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
     asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
 }
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t remote_addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote_addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t map_rank(uint32_t local_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void store_y(const TcParams& p, int b, int row, float v) {
+    if (p.y_bf16) reinterpret_cast<uint16_t*>(p.y)[(int64_t)b * p.N + row] = f32_to_bf16_bits(v);
+    else reinterpret_cast<float*>(p.y)[(int64_t)b * p.N + row] = v;
+}
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, uint32_t bar) {
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+                 ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar) : "memory");
+}
+__device__ __forceinline__ uint32_t bf16_mag(uint32_t v) {   // |x| bits; NaN -> 0 (does not set the scale)
+    v &= 0x7fffu;
+    return v > 0x7f80u ? 0u : v;
+}
+__device__ __forceinline__ uint32_t bf16x2_max_mag(uint32_t w) { return max(bf16_mag(w & 0xffffu), bf16_mag(w >> 16)); }
+__device__ __forceinline__ uint32_t pack_h2(uint32_t lo_bf16, uint32_t hi_bf16, float finv) {
+    const __half2 h = __floats2half2_rn(bf16_bits_to_f32(lo_bf16) * finv, bf16_bits_to_f32(hi_bf16) * finv);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
 
 // ---------------------------------------------------------------- prep
 // One CTA per padded batch row b: xp[b][32q + 2j + h] = fp16(x[b][32q + j + 16h]
 // * 2^-m_b) and xscale[b] = 2^m_b, with m_b chosen so that max|x * 2^-m_b| lies
 // in [2^14, 2^15) (exact: bf16 keeps 8 significant bits, fp16 11).  Rows b >= B
 // are zero.
-__global__ void __launch_bounds__(256) k_tc_prep(const uint16_t* __restrict__ x, int B, int K,
-                                                 uint16_t* __restrict__ xp, float* __restrict__ xscale) {
+// Thread layout: 16-byte unit u = 8 consecutive inputs; the four units of a
+// 32-input block sit in four consecutive lanes, and lanes p and p^2 exchange
+// their units to form the (j, j+16) pairs.
+__global__ void __launch_bounds__(kTcPrepThreads) k_tc_prep(const uint16_t* __restrict__ x, int B, int K,
+                                                            uint16_t* __restrict__ xp, float* __restrict__ xscale) {
     pdl_wait();
+    pdl_launch_dependents();   // the main kernel may start: everything before this one has completed
     const int b = blockIdx.x;
-    __shared__ uint32_t red[8];
-    uint16_t* out = xp + (size_t)b * K;
+    __shared__ uint32_t red[kTcPrepThreads / 32];
+    uint4* out = reinterpret_cast<uint4*>(xp + (size_t)b * K);
+    const int units = K / 8;
     if (b >= B) {
-        for (int i = threadIdx.x; i < K / 8; i += blockDim.x) reinterpret_cast<uint4*>(out)[i] = make_uint4(0, 0, 0, 0);
+        for (int i = threadIdx.x; i < units; i += blockDim.x) out[i] = make_uint4(0, 0, 0, 0);
         if (threadIdx.x == 0) xscale[b] = 1.f;
         return;
     }
-    const uint16_t* in = x + (size_t)b * K;
-    uint32_t m = 0;                                   // max |x| as bf16 magnitude bits (monotone)
-    for (int i = threadIdx.x; i < K; i += blockDim.x) {
-        const uint32_t v = in[i] & 0x7fffu;
-        m = max(m, v > 0x7f80u ? 0u : v);             // NaN does not set the scale
+    const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)b * K);
+    const bool resident = units <= kTcPrepThreads * kTcPrepUnits;
+    uint4 v[kTcPrepUnits];
+    uint32_t m = 0;
+    if (resident) {
+#pragma unroll
+        for (int i = 0; i < kTcPrepUnits; ++i) {
+            const int u = threadIdx.x + i * kTcPrepThreads;
+            v[i] = u < units ? in[u] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < kTcPrepUnits; ++i)
+            m = max(m, max(max(bf16x2_max_mag(v[i].x), bf16x2_max_mag(v[i].y)),
+                           max(bf16x2_max_mag(v[i].z), bf16x2_max_mag(v[i].w))));
+    } else {
+        for (int u = threadIdx.x; u < units; u += blockDim.x) {
+            const uint4 t = in[u];
+            m = max(m, max(max(bf16x2_max_mag(t.x), bf16x2_max_mag(t.y)), max(bf16x2_max_mag(t.z), bf16x2_max_mag(t.w))));
+        }
     }
     m = __reduce_max_sync(0xffffffffu, m);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
     __syncthreads();
     m = red[0];
-    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) m = max(m, red[i]);
+#pragma unroll
+    for (int i = 1; i < kTcPrepThreads / 32; ++i) m = max(m, red[i]);
     int mb = 0;
     if (m != 0) {
         const int e = (int)(m >> 7) - 127;            // exponent of max|x| (subnormal -> -127)
@@ -112,32 +176,41 @@ __global__ void __launch_bounds__(256) k_tc_prep(const uint16_t* __restrict__ x,
     }
     const float finv = __uint_as_float((uint32_t)(127 - mb) << 23);
     if (threadIdx.x == 0) xscale[b] = __uint_as_float((uint32_t)(mb + 127) << 23);
-    for (int i = threadIdx.x; i < K / 2; i += blockDim.x) {   // output pair i = (32q + 2j, 32q + 2j + 1)
-        const int q = i >> 4, j = i & 15;
-        const float lo = bf16_bits_to_f32(in[32 * q + j]) * finv;
-        const float hi = bf16_bits_to_f32(in[32 * q + j + 16]) * finv;
-        const __half2 h = __floats2half2_rn(lo, hi);
-        reinterpret_cast<uint32_t*>(out)[i] = *reinterpret_cast<const uint32_t*>(&h);
+    const int p = threadIdx.x & 3;                     // unit position within its 32-input block
+    auto emit = [&](int u, uint4 own) {
+        uint4 oth;
+        oth.x = __shfl_xor_sync(0xffffffffu, own.x, 2);
+        oth.y = __shfl_xor_sync(0xffffffffu, own.y, 2);
+        oth.z = __shfl_xor_sync(0xffffffffu, own.z, 2);
+        oth.w = __shfl_xor_sync(0xffffffffu, own.w, 2);
+        // p = 0/1: inputs 8p..8p+7 (low of the pair) with 16+8p.. (high): pairs 8p..8p+3
+        // p = 2/3: partner's low with own high: pairs 8(p-2)+4..+7
+        const uint4 lo = (p < 2) ? own : oth, hi = (p < 2) ? oth : own;
+        const uint32_t l0 = (p < 2) ? lo.x : lo.z, l1 = (p < 2) ? lo.y : lo.w;
+        const uint32_t h0 = (p < 2) ? hi.x : hi.z, h1 = (p < 2) ? hi.y : hi.w;
+        uint4 r;
+        r.x = pack_h2(l0 & 0xffffu, h0 & 0xffffu, finv);
+        r.y = pack_h2(l0 >> 16, h0 >> 16, finv);
+        r.z = pack_h2(l1 & 0xffffu, h1 & 0xffffu, finv);
+        r.w = pack_h2(l1 >> 16, h1 >> 16, finv);
+        const int q = u >> 2;
+        const int slot = (p == 0) ? 0 : (p == 2) ? 1 : (p == 1) ? 2 : 3;   // 16-byte slot in the block's 64 output bytes
+        if (u < units) out[4 * q + slot] = r;
+    };
+    if (resident) {
+#pragma unroll
+        for (int i = 0; i < kTcPrepUnits; ++i) {
+            const int u = threadIdx.x + i * kTcPrepThreads;
+            if (i * kTcPrepThreads < units) emit(u, v[i]);   // warp-uniform (units is a multiple of 128)
+        }
+    } else {
+        for (int u = threadIdx.x; u < units; u += blockDim.x) emit(u, in[u]);
     }
 }
 
-// ---------------------------------------------------------------- reduce
-// y[b][n] = xscale[b] * sum over s = 0 .. Ks-1 (in order) of partial[s][b][n].
-__global__ void __launch_bounds__(256) k_tc_reduce(const float* __restrict__ partial, const float* __restrict__ xscale,
-                                                   int Ks, int B, int Bp, int N, void* __restrict__ y, int y_bf16) {
-    pdl_wait();
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= (int64_t)B * N) return;
-    const int b = (int)(i / N), n = (int)(i - (int64_t)b * N);
-    float v = 0.f;
-    for (int s = 0; s < Ks; ++s) v += partial[((int64_t)s * Bp + b) * N + n];
-    v *= xscale[b];
-    if (y_bf16) reinterpret_cast<uint16_t*>(y)[i] = f32_to_bf16_bits(v);
-    else reinterpret_cast<float*>(y)[i] = v;
-}
-
 // ---------------------------------------------------------------- main kernel
-// Grid: (row tiles) x Ks.  Shared memory: [sign-bit ring 8 x 4 KB][B ring 3 x
+// Grid: Ks x (row tiles), clusters of Ks along x.  Shared memory: [sign-bit
+// ring 4 x 16 KB, reused as the fp32 accumulator staging [Bp][256]][B ring 3 x
 // Bp*256 B][mbarriers][tensor-memory slot].
 __global__ void __launch_bounds__(kTcThreads, 1)
 k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ CUtensorMap tm_x,
@@ -147,11 +220,10 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
     const uint32_t base = (raw + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int Mt = (p.N + kTcRows - 1) / kTcRows;
-    const int mt = blockIdx.x % Mt, ks = blockIdx.x / Mt;
-    const int s0 = (int)((int64_t)p.steps * ks / p.Ks), s1 = (int)((int64_t)p.steps * (ks + 1) / p.Ks);
-    const int nst = s1 - s0;
-    const uint32_t btile = (uint32_t)p.Bp * 128u;          // one 64-wide K box of B
+    const int mt = blockIdx.x / p.Ks, ks = blockIdx.x % p.Ks;   // ks = rank in the cluster
+    const int c0 = (int)((int64_t)p.chunks * ks / p.Ks), c1 = (int)((int64_t)p.chunks * (ks + 1) / p.Ks);
+    const int nch = c1 - c0, s0 = c0 * kTcChunkSteps, nst = nch * kTcChunkSteps;
+    const uint32_t btile = (uint32_t)p.Bp * 128u;          // one 64-wide K slab of B
     const uint32_t bstage = 2u * btile;                     // one step (128 K)
     const uint32_t wring = base;
     const uint32_t bring = base + kTcWSlots * kTcWSlotBytes;
@@ -170,9 +242,9 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
         for (int s = 0; s < kTcStages; ++s) {
             mbar_init(afull + 8 * s, kTcUnpackWarps);
             mbar_init(bfull + 8 * s, 1);
-            mbar_init(freed + 8 * s, 1);
+            mbar_init(freed + 8 * s, kTcMmaWarps);    // one commit per MMA issuer
         }
-        mbar_init(d_done, 1);
+        mbar_init(d_done, kTcMmaWarps);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -182,10 +254,12 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
     asm volatile("tcgen05.fence::before_thread_sync;");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;");
-    // Tensor memory: D half h at columns [h*Bp, h*Bp + Bp); A stage st, half h
-    // at columns 128 + 128*st + 64*h (64 columns = 128 fp16 inputs).
+    // Tensor memory: accumulator (half h, slice parity q) at columns
+    // (2h + q)*Bp; A stage st, half h at columns abase + 128*st + 64*h (64
+    // columns = 128 fp16 inputs), abase = 4*Bp rounded up to 128.
     const uint32_t tmem = *tslot;
-    pdl_wait();
+    const int nstg = p.stages;
+    const uint32_t abase = (uint32_t)((4 * p.Bp + 127) / 128 * 128);
 
     if (warp < kTcUnpackWarps) {
         const int quad = warp & 3, h = warp >> 2;
@@ -195,6 +269,7 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
         const int G = p.K / 128;
         const uint16_t* rs = p.scales + (size_t)(live ? row : 0) * G;
         const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+        const uint32_t rsw = (uint32_t)(r >> 1) & 3u;      // 64-byte swizzle of this row
         bool ok = true;
         // fp16 scales of this row, 8 groups (16 bytes) per window, one window ahead
         uint4 sc_cur = make_uint4(0, 0, 0, 0), sc_nxt = sc_cur;
@@ -208,23 +283,31 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
                 sc_cur = sc_nxt;
                 if (live && (step >> 3) + 1 < G / 8) sc_nxt = ldg_nc_v4(rs + step + 8);
             }
-            const int st = s % kTcStages, ws = s % kTcWSlots;
-            if (s >= kTcStages && !warp_wait(freed + 8 * st, (uint32_t)(s / kTcStages - 1) & 1u)) { ok = false; break; }
-            if (!warp_wait(wfull + 8 * ws, (uint32_t)(s / kTcWSlots) & 1u)) { ok = false; break; }
+            const int st = s % nstg, c = s >> 2, i = s & 3, ws = c % kTcWSlots;
+            if (s >= nstg && !warp_wait(freed + 8 * st, (uint32_t)(s / nstg - 1) & 1u)) { ok = false; break; }
+            if (i == 0 && !warp_wait(wfull + 8 * ws, (uint32_t)(c / kTcWSlots) & 1u)) { ok = false; break; }
             asm volatile("tcgen05.fence::after_thread_sync;");
-            const uint4 w = lds128(wring + ws * kTcWSlotBytes + 16u * r);
-            __syncwarp();
-            if (lane == 0) tc_arrive(wempty + 8 * ws);
+            const uint4 w = lds128(wring + ws * kTcWSlotBytes + 64u * r + 16u * ((uint32_t)i ^ rsw));
+            if (i == kTcChunkSteps - 1) {
+                __syncwarp();
+                if (lane == 0) tc_arrive(wempty + 8 * ws);
+            }
             const uint32_t wsel = (step & 4) ? ((step & 2) ? sc_cur.w : sc_cur.z) : ((step & 2) ? sc_cur.y : sc_cur.x);
             const uint32_t s16 = (step & 1) ? (wsel >> 16) : (wsel & 0xffffu);
             const uint32_t s2 = live ? (s16 | (s16 << 16)) : 0u;
             const uint32_t words[4] = {~w.x, ~w.y, ~w.z, ~w.w};
-            const uint32_t col0 = 128u + 128u * st + 64u * h;
+            const uint32_t col0 = abase + 128u * st + 64u * h;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint32_t v[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = ((words[q] << (15 - j)) & 0x80008000u) | s2;  // bit 1 -> +s
+                for (int j = 0; j < 16; ++j) {
+                    // bits j and j+16 to the fp16 sign positions 15 and 31 (bit 1 -> +s); the
+                    // shift is written as a multiply so that it can issue on the FMA pipe
+                    uint32_t t;
+                    asm("mul.lo.u32 %0, %1, %2;" : "=r"(t) : "r"(words[q]), "r"(1u << (15 - j)));
+                    v[j] = (t & 0x80008000u) | s2;
+                }
                 asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
                              ::"r"(tmem + lane_base + col0 + 16u * q), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]),
                                "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]),
@@ -235,101 +318,98 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
             __syncwarp();
             if (lane == 0) tc_arrive(afull + 8 * st);
         }
-        // ---- epilogue: accumulator half h, row r
+        // ---- epilogue: accumulators of half h, row r
+        pdl_wait();
         if (ok) ok = warp_wait(d_done, 0);
         if (!ok) {
             if (lane == 0) atomicOr(&g_tc_wait_timeouts, 1u);
-        } else if (nst > 0) {
+        } else {
             asm volatile("tcgen05.fence::after_thread_sync;");
-            for (int c0 = 0; c0 < p.Bp; c0 += 16) {
-                uint32_t d[16];
+            for (int cb = 0; cb < p.Bp; cb += 16) {
+                uint32_t d[16], e[16];
                 asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
                              : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]), "=r"(d[4]), "=r"(d[5]), "=r"(d[6]),
                                "=r"(d[7]), "=r"(d[8]), "=r"(d[9]), "=r"(d[10]), "=r"(d[11]), "=r"(d[12]), "=r"(d[13]),
                                "=r"(d[14]), "=r"(d[15])
-                             : "r"(tmem + lane_base + (uint32_t)(h * p.Bp + c0)) : "memory");
+                             : "r"(tmem + lane_base + (uint32_t)(2 * h * p.Bp + cb)) : "memory");
+                asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                             : "=r"(e[0]), "=r"(e[1]), "=r"(e[2]), "=r"(e[3]), "=r"(e[4]), "=r"(e[5]), "=r"(e[6]),
+                               "=r"(e[7]), "=r"(e[8]), "=r"(e[9]), "=r"(e[10]), "=r"(e[11]), "=r"(e[12]), "=r"(e[13]),
+                               "=r"(e[14]), "=r"(e[15])
+                             : "r"(tmem + lane_base + (uint32_t)((2 * h + 1) * p.Bp + cb)) : "memory");
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                if (live) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int b = c0 + i;
-                        const float v = __uint_as_float(d[i]);
-                        if (p.partial) {
-                            p.partial[((int64_t)ks * p.Bp + b) * p.N + row] = v;
-                        } else if (b < p.B) {
-                            const float yv = v * p.xscale[b];
-                            if (p.y_bf16) reinterpret_cast<uint16_t*>(p.y)[(int64_t)b * p.N + row] = f32_to_bf16_bits(yv);
-                            else reinterpret_cast<float*>(p.y)[(int64_t)b * p.N + row] = yv;
-                        }
-                    }
+                for (int k = 0; k < 16; ++k) d[k] = __float_as_uint(__uint_as_float(d[k]) + __uint_as_float(e[k]));
+                if (p.Ks > 1) {
+                    // stage [b][r] in the (drained) sign-bit ring for the cluster reduction
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        asm volatile("st.shared.u32 [%0], %1;" ::"r"(wring + 4u * (uint32_t)((cb + k) * kTcRows + r)), "r"(d[k]) : "memory");
+                } else if (live) {
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        if (cb + k < p.B) store_y(p, cb + k, row, __uint_as_float(d[k]) * p.xscale[cb + k]);
                 }
             }
         }
     } else if (warp == kTcUnpackWarps) {
-        // ---- sign-bit producer: one 256-row x 16-byte box per step
-        if (lane == 0) {
+        // ---- sign-bit producer: lane L owns ring slot L (chunks L, L+4, ...)
+        if (lane < kTcWSlots) {
+            const uint32_t full = wfull + 8 * lane, empty = wempty + 8 * lane, dst = wring + lane * kTcWSlotBytes;
             int issued = 0;
-            for (int s = 0; s < nst; ++s) {
-                const int ws = s % kTcWSlots;
-                if (s >= kTcWSlots && !mbar_wait(wempty + 8 * ws, (uint32_t)(s / kTcWSlots - 1) & 1u)) {
+            for (int c = lane; c < nch; c += kTcWSlots, ++issued) {
+                if (issued > 0 && !mbar_wait(empty, (uint32_t)(issued - 1) & 1u)) {
                     atomicOr(&g_tc_wait_timeouts, 2u);
                     break;
                 }
-                mbar_expect_tx(wfull + 8 * ws, kTcWSlotBytes);
-                tma_2d(wring + ws * kTcWSlotBytes, &tm_bits, 16 * (s0 + s), mt * kTcRows, wfull + 8 * ws);
-                ++issued;
+                mbar_expect_tx(full, kTcWSlotBytes);
+                tma_2d(dst, &tm_bits, 16 * (s0 + kTcChunkSteps * c), mt * kTcRows, full);
             }
-            // every issued copy has landed before the CTA may exit
-            for (int s = std::max(0, issued - kTcWSlots); s < issued; ++s)
-                if (!mbar_wait(wfull + 8 * (s % kTcWSlots), (uint32_t)(s / kTcWSlots) & 1u)) atomicOr(&g_tc_wait_timeouts, 2u);
+            // the last issued copy has landed before the CTA may exit
+            if (issued > 0 && !mbar_wait(full, (uint32_t)(issued - 1) & 1u)) atomicOr(&g_tc_wait_timeouts, 2u);
         }
     } else if (warp == kTcUnpackWarps + 1) {
-        // ---- activation producer: two 64-input boxes per step
-        if (lane == 0) {
+        // ---- activation producer: lane st owns stage st (steps st, st+nstg, ...)
+        pdl_wait();
+        if (lane < nstg) {
+            const uint32_t full = bfull + 8 * lane, dst = bring + lane * bstage;
             int issued = 0;
-            for (int s = 0; s < nst; ++s) {
-                const int st = s % kTcStages;
-                if (s >= kTcStages && !mbar_wait(freed + 8 * st, (uint32_t)(s / kTcStages - 1) & 1u)) {
+            for (int s = lane; s < nst; s += nstg, ++issued) {
+                if (issued > 0 && !mbar_wait(freed + 8 * lane, (uint32_t)(issued - 1) & 1u)) {
                     atomicOr(&g_tc_wait_timeouts, 4u);
                     break;
                 }
-                const uint32_t dst = bring + st * bstage;
-                mbar_expect_tx(bfull + 8 * st, bstage);
-                const int k = (s0 + s) * kTcStepK;
-                tma_2d(dst, &tm_x, k, 0, bfull + 8 * st);
-                tma_2d(dst + btile, &tm_x, k + 64, 0, bfull + 8 * st);
-                ++issued;
+                mbar_expect_tx(full, bstage);
+                tma_3d(dst, &tm_x, 0, 0, 2 * (s0 + s), full);
             }
-            for (int s = std::max(0, issued - kTcStages); s < issued; ++s)
-                if (!mbar_wait(bfull + 8 * (s % kTcStages), (uint32_t)(s / kTcStages) & 1u)) atomicOr(&g_tc_wait_timeouts, 4u);
+            if (issued > 0 && !mbar_wait(full, (uint32_t)(issued - 1) & 1u)) atomicOr(&g_tc_wait_timeouts, 4u);
         }
     } else {
-        // ---- MMA issuer
+        // ---- MMA issuers: warp 10 + 2h + q accumulates half h, 16-input slices of parity q
+        const int mw = warp - (kTcUnpackWarps + 2), h = mw >> 1, q = mw & 1;
+        pdl_wait();
         if (lane == 0) {
             const uint32_t idesc = (1u << 4)                         // D: fp32
                                    | (0u << 7) | (0u << 10)          // A, B: fp16
                                    | ((uint32_t)(p.Bp >> 3) << 17)   // N
                                    | ((uint32_t)(128 >> 4) << 24);   // M
+            const uint32_t d_addr = tmem + (uint32_t)((2 * h + q) * p.Bp);
             for (int s = 0; s < nst; ++s) {
-                const int st = s % kTcStages;
-                const uint32_t par = (uint32_t)(s / kTcStages) & 1u;
+                const int st = s % nstg;
+                const uint32_t par = (uint32_t)(s / nstg) & 1u;
                 if (!mbar_wait(afull + 8 * st, par) || !mbar_wait(bfull + 8 * st, par)) {
                     atomicOr(&g_tc_wait_timeouts, 8u);
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;");
                 const uint32_t bst = bring + st * bstage;
+                const uint32_t a0 = tmem + abase + 128u * st + 64u * h;
 #pragma unroll
-                for (int kk = 0; kk < kTcStepK / 16; ++kk) {
+                for (int kk = q; kk < kTcStepK / 16; kk += 2) {
                     const uint64_t bdesc = tc_desc_sw128(bst + (kk >> 2) * btile + (kk & 3) * 32);
-                    const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t a_addr = tmem + 128u + 128u * st + 64u * h + 8u * kk;
-                        const uint32_t d_addr = tmem + (uint32_t)(h * p.Bp);
-                        asm volatile("{.reg .pred pa; setp.ne.b32 pa, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;}"
-                                     ::"r"(d_addr), "r"(a_addr), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
-                    }
+                    const uint32_t acc = (s > 0 || kk > q) ? 1u : 0u;
+                    asm volatile("{.reg .pred pa; setp.ne.b32 pa, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;}"
+                                 ::"r"(d_addr), "r"(a0 + 8u * kk), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
                 }
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                              ::"r"(freed + 8 * st) : "memory");
@@ -339,6 +419,32 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
             // no MMA may still be running when the tensor memory is released
             if (!mbar_wait(d_done, 0)) atomicOr(&g_tc_wait_timeouts, 8u);
         }
+    }
+    if (p.Ks > 1) {
+        // ---- split-K: sum the cluster's staged tiles in rank order (all threads
+        // take part in both cluster barriers; the second keeps every CTA's
+        // shared memory alive until all remote reads are done)
+        cluster_sync();
+        if (warp < kTcUnpackWarps) {
+            const int q0 = 64 * ks / p.Ks, q1 = 64 * (ks + 1) / p.Ks, nq = q1 - q0;
+            for (int it = threadIdx.x; it < nq * p.B; it += kTcUnpackWarps * 32) {
+                const int b = it / nq, r0 = 4 * (q0 + it % nq);
+                const uint32_t off = wring + 4u * (uint32_t)(b * kTcRows + r0);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+                for (int k = 0; k < p.Ks; ++k) {
+                    const float4 v = ld_cluster_v4(map_rank(off, (uint32_t)k));
+                    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+                }
+                const float xs = p.xscale[b];
+                const int row = mt * kTcRows + r0;
+                if (row + 0 < p.N) store_y(p, b, row + 0, acc.x * xs);
+                if (row + 1 < p.N) store_y(p, b, row + 1, acc.y * xs);
+                if (row + 2 < p.N) store_y(p, b, row + 2, acc.z * xs);
+                if (row + 3 < p.N) store_y(p, b, row + 3, acc.w * xs);
+            }
+        }
+        cluster_sync();
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
     __syncthreads();
@@ -362,32 +468,82 @@ PFN_cuTensorMapEncodeTiled_v12000 tc_encode() {
 }
 
 struct TcPlan {
-    int Bp, Mt, Ks, steps;
-    size_t smem, ws_xp, ws_scale, ws_part, ws_total, off_part;
+    int Bp, Mt, Ks, chunks;
+    size_t smem, off_scale, ws_total;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+size_t tc_smem(int Bp) {
+    const size_t need = 1024 + (size_t)kTcWSlots * kTcWSlotBytes + (size_t)kTcStages * 2 * 128 * Bp +
+                        8 * (2 * kTcWSlots + 3 * kTcStages + 1) + 16;
+    return std::max<size_t>(need, 120 * 1024);      // keeps a second CTA off the SM
+}
+
+void tc_set_attrs_once(cudaError_t* err) {
+    static std::once_flag once;
+    static cudaError_t e = cudaSuccess;
+    std::call_once(once, [] {
+        e = cudaFuncSetAttribute((const void*)k_gemv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute((const void*)k_gemv_tc, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    });
+    *err = e;
+}
+
+// Co-resident clusters of size ks for this kernel (0 when the query fails).
+int tc_max_clusters(int ks, size_t smem) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(ks * 256));
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void*)k_gemv_tc, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+// K split: the cluster size that minimises (waves of clusters) x (chunks per
+// CTA + one chunk of fixed cost); every CTA keeps at least two chunks.
+int tc_pick_ks(int Mt, int chunks, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::pair<int, int>, int> memo;   // (Mt, chunks) per smem class
+    const int key_smem = (int)(smem >> 10);
+    std::lock_guard<std::mutex> lk(mu);
+    auto key = std::make_pair(Mt * 4096 + key_smem, chunks);
+    auto it = memo.find(key);
+    if (it != memo.end()) return it->second;
+    const int sms = sm_count();
+    int best = 1;
+    double best_cost = (double)((Mt + sms - 1) / sms) * (chunks + 1);
+    for (int ks = 2; ks <= 16 && chunks / ks >= 2; ++ks) {
+        const int mc = tc_max_clusters(ks, smem);
+        if (mc <= 0) continue;
+        const double cost = (double)((Mt + mc - 1) / mc) * ((chunks + ks - 1) / ks + 1);
+        if (cost < best_cost - 1e-9) { best_cost = cost; best = ks; }
+    }
+    memo[key] = best;
+    return best;
+}
 
 TcPlan tc_plan(int64_t B, int64_t N, int64_t K) {
     TcPlan pl{};
     const int64_t Bc = std::min<int64_t>(B, kTcMaxB);
     pl.Bp = (int)((Bc + 15) / 16 * 16);
     pl.Mt = (int)((N + kTcRows - 1) / kTcRows);
-    pl.steps = (int)(K / kTcStepK);
-    // Split K until the CTAs fill the SMs once (one CTA per SM: it holds all
-    // 512 tensor-memory columns); every slice keeps at least 8 steps.
-    const int sms = sm_count();
-    int ks = 1;
-    while (pl.Mt * (ks + 1) <= sms && pl.steps / (ks + 1) >= 8) ++ks;
-    pl.Ks = ks;
-    const size_t need = 1024 + (size_t)kTcWSlots * kTcWSlotBytes + (size_t)kTcStages * 2 * 128 * pl.Bp +
-                        8 * (2 * kTcWSlots + 3 * kTcStages + 1) + 16;
-    pl.smem = std::max<size_t>(need, 120 * 1024);   // keeps a second CTA off the SM
-    pl.ws_xp = align256((size_t)pl.Bp * K * 2);
-    pl.ws_scale = 256;
-    pl.off_part = pl.ws_xp + pl.ws_scale;
-    pl.ws_part = pl.Ks > 1 ? align256((size_t)pl.Ks * pl.Bp * N * 4) : 0;
-    pl.ws_total = pl.off_part + pl.ws_part;
+    pl.chunks = (int)(K / (kTcStepK * kTcChunkSteps));
+    pl.smem = tc_smem(pl.Bp);
+    pl.Ks = 1;
+    pl.off_scale = align256((size_t)pl.Bp * K * 2);
+    pl.ws_total = pl.off_scale + 256;
     return pl;
 }
 
@@ -405,36 +561,55 @@ size_t tc_workspace_bytes(int64_t B, int64_t N, int64_t K) {
 
 int tc_launch_count(int64_t B, int64_t N, int64_t K) {
     if (!tc_supported(B, N, K)) return 0;
-    const TcPlan pl = tc_plan(B, N, K);
-    const int64_t chunks = (B + kTcMaxB - 1) / kTcMaxB;
-    return (int)(chunks * (2 + (pl.Ks > 1 ? 1 : 0)));
+    return (int)(2 * ((B + kTcMaxB - 1) / kTcMaxB));
 }
+
+namespace {
+
+cudaError_t launch_tc_main(const CUtensorMap& tm_bits, const CUtensorMap& tm_x, const TcParams& prm, int Mt,
+                           size_t smem, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(Mt * prm.Ks));
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)prm.Ks;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    void* args[] = {(void*)&tm_bits, (void*)&tm_x, (void*)&prm};
+    return cudaLaunchKernelExC(&cfg, (const void*)k_gemv_tc, args);
+}
+
+}  // namespace
 
 cudaError_t launch_gemv_tc(const GemvArgs& a) {
     if (!tc_supported(a.B, a.N, a.K)) return cudaErrorNotSupported;
-    const TcPlan pl = tc_plan(a.B, a.N, a.K);
+    TcPlan pl = tc_plan(a.B, a.N, a.K);
     if (!a.workspace || a.ws_bytes < pl.ws_total) return cudaErrorInvalidValue;
     auto enc = tc_encode();
     if (!enc) return cudaErrorNotSupported;
+    cudaError_t e;
+    tc_set_attrs_once(&e);
+    if (e != cudaSuccess) return e;
+    pl.Ks = tc_pick_ks(pl.Mt, pl.chunks, pl.smem);
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     uint16_t* xp = reinterpret_cast<uint16_t*>(ws);
-    float* xscale = reinterpret_cast<float*>(ws + pl.ws_xp);
-    float* partial = pl.Ks > 1 ? reinterpret_cast<float*>(ws + pl.off_part) : nullptr;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute((const void*)k_gemv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    float* xscale = reinterpret_cast<float*>(ws + pl.off_scale);
 
     CUtensorMap tm_bits;
     {
         const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 8), (cuuint64_t)a.N};
         const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 8)};
-        const cuuint32_t box[2] = {16, (cuuint32_t)kTcRows};
+        const cuuint32_t box[2] = {16 * kTcChunkSteps, (cuuint32_t)kTcRows};
         const cuuint32_t es[2] = {1, 1};
         if (enc(&tm_bits, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void*)a.bits, dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
@@ -445,16 +620,17 @@ cudaError_t launch_gemv_tc(const GemvArgs& a) {
         const uint16_t* xin = a.x + b0 * a.K;
         int Bci = Bc, Ki = (int)a.K;
         void* prep_args[] = {(void*)&xin, (void*)&Bci, (void*)&Ki, (void*)&xp, (void*)&xscale};
-        cudaError_t e = launch((const void*)k_tc_prep, dim3((unsigned)Bp), dim3(256), 0, a.stream, a.pdl || b0 > 0,
-                               prep_args);
+        e = launch((const void*)k_tc_prep, dim3((unsigned)Bp), dim3(kTcPrepThreads), 0, a.stream, a.pdl || b0 > 0,
+                   prep_args);
         if (e != cudaSuccess) return e;
+        // activations: [K/64 slabs][Bp rows][64 inputs], one box = 2 slabs x Bp rows
         CUtensorMap tm_x;
         {
-            const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)Bp};
-            const cuuint64_t strides[1] = {(cuuint64_t)(a.K * 2)};
-            const cuuint32_t box[2] = {64, (cuuint32_t)Bp};
-            const cuuint32_t es[2] = {1, 1};
-            if (enc(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (void*)xp, dims, strides, box, es,
+            const cuuint64_t dims[3] = {64, (cuuint64_t)Bp, (cuuint64_t)(a.K / 64)};
+            const cuuint64_t strides[2] = {(cuuint64_t)(a.K * 2), 128};
+            const cuuint32_t box[3] = {64, (cuuint32_t)Bp, 2};
+            const cuuint32_t es[3] = {1, 1, 1};
+            if (enc(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, (void*)xp, dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
                 return cudaErrorInvalidValue;
@@ -462,29 +638,17 @@ cudaError_t launch_gemv_tc(const GemvArgs& a) {
         TcParams prm;
         prm.scales = a.scales;
         prm.xscale = xscale;
-        prm.partial = partial;
         prm.y = static_cast<uint8_t*>(a.y) + b0 * a.N * ysz;
         prm.N = (int)a.N;
         prm.K = (int)a.K;
         prm.B = Bc;
         prm.Bp = Bp;
         prm.Ks = pl.Ks;
-        prm.steps = pl.steps;
+        prm.chunks = pl.chunks;
         prm.y_bf16 = a.y_bf16;
-        void* args[] = {(void*)&tm_bits, (void*)&tm_x, (void*)&prm};
-        e = launch((const void*)k_gemv_tc, dim3((unsigned)(pl.Mt * pl.Ks)), dim3(kTcThreads), pl.smem, a.stream, true,
-                   args);
+        prm.stages = 4 * Bp <= 128 ? 3 : 2;
+        e = launch_tc_main(tm_bits, tm_x, prm, pl.Mt, pl.smem, a.stream);
         if (e != cudaSuccess) return e;
-        if (pl.Ks > 1) {
-            const int64_t total = (int64_t)Bc * a.N;
-            const float* pc = partial;
-            const float* xs = xscale;
-            int Ksi = pl.Ks, Bpi = Bp, Ni = (int)a.N, yb = a.y_bf16;
-            void* yp = prm.y;
-            void* rargs[] = {(void*)&pc, (void*)&xs, (void*)&Ksi, (void*)&Bci, (void*)&Bpi, (void*)&Ni, (void*)&yp, (void*)&yb};
-            e = launch((const void*)k_tc_reduce, dim3((unsigned)((total + 255) / 256)), dim3(256), 0, a.stream, true, rargs);
-            if (e != cudaSuccess) return e;
-        }
     }
     return cudaSuccess;
 }

@@ -55,6 +55,21 @@ def test_tc_matches_oracle(orc, N, K, B):
     assert b1.bit1_device_wait_timeouts() == 0
 
 
+@pytest.mark.parametrize("N,K,B", [(20000, 8192, 16), (40000, 2048, 32)])
+def test_tc_long_rings_and_two_waves(orc, N, K, B):
+    """Row tiles alone fill the SMs (no K split): each CTA streams all of K
+    through its sign-bit ring several times over; 40000 rows need a second
+    wave of CTAs.  Sampled rows against the oracle."""
+    bits, scales, x = _problem(N, K, B, 7050 + N)
+    y = _run_tc(bits, scales, x, N, K, B)
+    rows = np.unique(np.concatenate([np.random.default_rng(N).choice(N, 384, replace=False),
+                                     [0, 255, 256, N - 1]]))
+    ref = orc.gemv_select(bits, scales, x, B, N, K, rows)
+    assert_gemv_close(y[:, torch.from_numpy(rows).cuda()], ref, abs_bound(scales[rows], x, K),
+                      f"tc N={N} K={K} B={B}")
+    assert b1.bit1_device_wait_timeouts() == 0
+
+
 def test_tc_bf16_output(orc):
     N, K, B = 700, 4096, 24
     bits, scales, x = _problem(N, K, B, 7101)
