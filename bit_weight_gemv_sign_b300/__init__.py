@@ -19,7 +19,7 @@ __all__ = [
     "bit1_gemv_workspace_bytes", "bit1_gemv_pick", "bit1_gemv_launches",
     "bit1_xor_patch", "bit1_status_str", "bit1_version", "bit1_device_wait_timeouts",
     "bit1_group_plan_bytes", "bit1_group_plan", "bit1_gemv_group", "GroupPlan",
-    "library_path", "load",
+    "library_path", "load", "bit1_gemv_tc_noalloc",
 ]
 
 OK, EINVAL, ESHAPE, ERANGE, ECUDA, ENAN = 0, 1, 2, 3, 4, 5
@@ -89,6 +89,8 @@ def load():
         lib.bit1_group_plan.restype = i32
         lib.bit1_gemv_group.argtypes = [p, p, ctypes.c_uint, p]
         lib.bit1_gemv_group.restype = i32
+        lib.bit1_gemv_tc_noalloc.argtypes = [p, p, p, i64, i64, i64, p, i32, ctypes.c_uint, p]
+        lib.bit1_gemv_tc_noalloc.restype = i32
         _lib = lib
         return lib
 
@@ -192,6 +194,26 @@ def bit1_gemv_ex(bits, scales, x, y=None, y_dtype=None, workspace=None, variant=
 def bit1_gemv(bits, scales, x, y=None, y_dtype=None, workspace=None, stream=None):
     return bit1_gemv_ex(bits, scales, x, y=y, y_dtype=y_dtype, workspace=workspace,
                         variant=AUTO, flags=0, stream=stream)
+
+
+def bit1_gemv_tc_noalloc(bits, scales, x, y=None, y_dtype=None, flags=0, stream=None, N=None, K=None):
+    """The tensor-core product without a workspace: its scratch is a static
+    device array shared by every call on the device (calls must not overlap
+    on the GPU; the first call on a device must precede any stream capture)."""
+    import torch
+    B = x.shape[0] if x.dim() == 2 else 1
+    K = x.shape[-1] if K is None else K
+    N = bits.shape[0] if N is None else N
+    if y is None:
+        yt = torch.bfloat16 if y_dtype == BF16 else torch.float32
+        y = torch.empty((B, N), dtype=yt, device=x.device)
+    if y.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("y must be float32 or bfloat16")
+    ydt = BF16 if y.dtype == torch.bfloat16 else F32
+    st = load().bit1_gemv_tc_noalloc(_dptr(bits, "bits"), _dptr(scales, "scales"), _dptr(x, "x"),
+                                     B, N, K, _dptr(y, "y"), ydt, int(flags), _stream(stream))
+    _check(st, "bit1_gemv_tc_noalloc")
+    return y
 
 
 def bit1_gemv_workspace_bytes(B: int, N: int, K: int) -> int:

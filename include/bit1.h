@@ -204,6 +204,37 @@ bit1_status bit1_xor_patch(uint8_t *bits, int64_t N, int64_t K,
  * count could not be read. */
 unsigned int bit1_device_wait_timeouts(void);
 
+/* ------------------------------------------------------------------------
+ * bit1_gemv_tc_noalloc -- the tensor-core batched product (bit1_gemv_ex with
+ * variant BIT1_GEMV_TC) without a caller workspace.  The pages have no
+ * counterpart of this call; it exists for callers that cannot allocate
+ * device memory around the product: code that runs while a CUDA graph is
+ * being captured (cudaMalloc is not permitted during capture), real-time
+ * paths that must not enter an allocator, and plain C hosts that have no
+ * device allocator of their own to size a workspace with.
+ *   Scratch: one file-scope device array of BIT1_NOALLOC_SCRATCH_BYTES per
+ *   device (the kernel stages at most 64 batch rows of K fp16 activations
+ *   plus 256 bytes per launch, so any B with K <= 32768 fits).  Its address
+ *   is taken with cudaGetSymbolAddress once per device, on the first call
+ *   on that device: make that first call before any stream capture.
+ *   Races: every call on a device uses the same scratch, so two calls whose
+ *   kernels overlap on the GPU (different streams, or different host threads
+ *   without ordering) corrupt each other's results; keep such calls ordered,
+ *   e.g. on one stream.
+ * Arguments as bit1_gemv_ex (flags: BIT1_FLAG_PDL).  Returns BIT1_ESHAPE if
+ * the shape is outside the tensor-core kernel's limits (K a multiple of 1024)
+ * or needs more scratch than BIT1_NOALLOC_SCRATCH_BYTES (only possible for
+ * K > 32768: the need is 2 * min(B, 64) rounded up to 16 * K + 256 bytes,
+ * each part rounded up to 256), checked
+ * before any CUDA call; BIT1_ECUDA if the scratch address cannot be
+ * obtained; otherwise as bit1_gemv_ex.  Allocates nothing.
+ */
+#define BIT1_NOALLOC_SCRATCH_BYTES ((size_t)4 * 1024 * 1024 + 4096)
+bit1_status bit1_gemv_tc_noalloc(const uint8_t *bits, const uint16_t *scales,
+                                 const uint16_t *x, int64_t B, int64_t N, int64_t K,
+                                 void *y, int y_dtype, unsigned flags,
+                                 bit1_stream_t stream);
+
 /* Static description of a status code. */
 const char *bit1_status_str(bit1_status status);
 
