@@ -53,11 +53,12 @@ bool shape_ok(int64_t B, int64_t N, int64_t K) {
 
 bit1_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BIT1_OK : BIT1_ECUDA; }
 
-// Batch 1: the 6-bit-table kernel; batch 2..8: the nibble-table kernel;
-// batch >= 16 with enough scratch: the tensor-core kernel; else one warp per row.
+// Batch >= 16 with enough scratch: the tensor-core kernel; otherwise the
+// 6-bit-table CUDA-core kernel (up to 8 batch rows per launch); shapes it
+// cannot take: the nibble-table kernel (batch 1), else one warp per row.
 int pick_variant(int64_t B, int64_t N, int64_t K, size_t ws_bytes) {
-    if (t6_supported(B, N, K)) return BIT1_GEMV_LUT6;
     if (B >= 16 && tc_supported(B, N, K) && ws_bytes >= tc_workspace_bytes(B, N, K)) return BIT1_GEMV_TC;
+    if (t6_supported(B, N, K)) return BIT1_GEMV_LUT6;
     if (lut_supported(B, N, K)) return BIT1_GEMV_LUT;
     return BIT1_GEMV_SIMPLE;
 }
@@ -146,7 +147,7 @@ int bit1_gemv_launches(int64_t B, int64_t N, int64_t K, int variant) {
     switch (variant) {
         case BIT1_GEMV_SIMPLE: return 1;
         case BIT1_GEMV_LUT: return lut_supported(B, N, K) ? 1 : 0;
-        case BIT1_GEMV_LUT6: return t6_supported(B, N, K) ? 1 : 0;
+        case BIT1_GEMV_LUT6: return t6_launch_count(B, N, K);
         case BIT1_GEMV_STREAM: return group1_supported(B, N, K) ? 1 : 0;
         case BIT1_GEMV_TC: return tc_launch_count(B, N, K);
         default: return 0;

@@ -1,8 +1,8 @@
-// Batch-1 GEMV over packed sign bits with 6-bit fp16 lookup tables, one row
-// per lane, TMA-staged weights and split-K over a thread-block cluster
-// (CUDA cores, sm_103a).
+// GEMV / skinny GEMM over packed sign bits with 6-bit fp16 lookup tables, one
+// row per lane, TMA-staged weights and split-K over a thread-block cluster
+// (CUDA cores, sm_103a); NB = 1..8 batch rows per launch.
 //
-// What it computes: y[n] = sum_g s[n][g] * sum_{k in g} (bit(n,k) ? x[k] : -x[k])
+// What it computes: y[b][n] = sum_g s[n][g] * sum_{k in g} (bit(n,k) ? x[b][k] : -x[b][k])
 // (web page "Bonsai 27B: 노트북과 폰에서 실행되는 27B급 이진 및 삼진 저비트 LLM",
 // section "이진(Binary) 가중치 형식"), the fp16 group scale applied inside the
 // product and fp32 accumulation (section "하이브리드 어텐션을 위한 저비트 커널").
@@ -19,6 +19,9 @@
 //    whose lanes pick any 32 entries of the same table is conflict-free.
 //  * Lane l of a warp owns row 32*b + l; all lanes walk the same fields in
 //    lockstep, so one shared table serves the whole warp and every CTA.
+//  * Batch rows: every batch row has its own tables; a lane reads its 16
+//    bytes of sign bits once per group and looks them up in each batch row's
+//    tables (the lookups, not the weight reads, grow with the batch).
 //  * x' = x * 2^-m_g per group (exact power-of-two prescale) keeps every entry
 //    within fp16 range; the entry rounding error is <= 2^-12 of the sum of the
 //    six |x'|, i.e. a relative 2.4e-4 of sum|s x| at most, inside the 1e-3
@@ -38,6 +41,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -54,14 +58,17 @@ constexpr int kT6MaxSmem = 227 * 1024;
 __device__ unsigned int g_bit1_wait_timeouts = 0;
 
 struct T6Params {
-    const uint16_t* x;
-    void* y;
+    const uint16_t* x;        // [NB][K] bf16
+    void* y;                  // [NB][N]
     int N, K, Gc, Q, S, stage_bytes, y_bf16;
+    int prow;                 // rows per batch row in the partials area (32 x blocks per cluster)
     uint32_t off_tables, off_factors, off_x, off_partials, off_bars;
 };
 
 // ---------------------------------------------------------------- kernel
-__global__ void __launch_bounds__(kT6MaxWarps * 32)
+// One CTA per SM (its shared memory sees to that), so all registers are usable.
+template <int NB>
+__global__ void __launch_bounds__(kT6MaxWarps * 32, 1)
 k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ CUtensorMap tm_sc,
           const __grid_constant__ T6Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -99,14 +106,16 @@ k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
 
     // Activations come from the preceding kernel of a decode step.
     pdl_wait();
-    float* fac = reinterpret_cast<float*>(sm + p.off_factors);   // [Gc] 2^m_g, [Gc] 2^-m_g
-    uint16_t* xs = reinterpret_cast<uint16_t*>(sm + p.off_x);     // [Gc*128] bf16 activations
-    const uint16_t* xc = p.x + (size_t)g0 * 128;
-    for (int i = threadIdx.x; i < Gc * 16; i += blockDim.x)        // 8 activations per thread
-        reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(xc)[i];
+    float* fac = reinterpret_cast<float*>(sm + p.off_factors);   // [NB][2*Gc]: 2^m_g, then 2^-m_g
+    uint16_t* xs = reinterpret_cast<uint16_t*>(sm + p.off_x);     // [NB][Gc*128] bf16 activations
+    for (int i = threadIdx.x; i < NB * Gc * 16; i += blockDim.x) { // 8 activations per thread
+        const int b = i / (Gc * 16), j = i - b * (Gc * 16);
+        reinterpret_cast<uint4*>(xs)[i] = reinterpret_cast<const uint4*>(p.x + (size_t)b * p.K + (size_t)g0 * 128)[j];
+    }
     __syncthreads();
-    for (int g = warp; g < Gc; g += W) {
-        const uint2 xv = *reinterpret_cast<const uint2*>(xs + g * 128 + 4 * lane);
+    for (int bg = warp; bg < NB * Gc; bg += W) {
+        const int b = bg / Gc, g = bg - b * Gc;
+        const uint2 xv = *reinterpret_cast<const uint2*>(xs + bg * 128 + 4 * lane);
         float m = fmaxf(fmaxf(fabsf(bf16_bits_to_f32(xv.x & 0xffffu)), fabsf(bf16_bits_to_f32(xv.x >> 16))),
                         fmaxf(fabsf(bf16_bits_to_f32(xv.y & 0xffffu)), fabsf(bf16_bits_to_f32(xv.y >> 16))));
 #pragma unroll
@@ -117,22 +126,23 @@ k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
             mg = min(max(e - 11, -126), 127);                                // max|x'| < 2^12
         }
         if (lane == 0) {
-            fac[g] = __uint_as_float((uint32_t)(mg + 127) << 23);
-            fac[Gc + g] = __uint_as_float((uint32_t)(127 - mg) << 23);
+            fac[b * 2 * Gc + g] = __uint_as_float((uint32_t)(mg + 127) << 23);
+            fac[b * 2 * Gc + Gc + g] = __uint_as_float((uint32_t)(127 - mg) << 23);
         }
     }
     __syncthreads();
-    uint8_t* tabs = sm + p.off_tables;
-    for (int t = threadIdx.x; t < Gc * kT6Fields * 4; t += blockDim.x) {
-        const int tt = t >> 2, g = tt / kT6Fields, f = tt - g * kT6Fields;
-        t6_build_pair(tabs + g * kT6GroupBytes + f * kT6TableBytes, xs + g * 128, fac[Gc + g], f, t & 3, tt & 1);
+    uint8_t* tabs = sm + p.off_tables;   // [NB][Gc][22 tables]
+    for (int t = threadIdx.x; t < NB * Gc * kT6Fields * 4; t += blockDim.x) {
+        const int tt = t >> 2, bg = tt / kT6Fields, f = tt - bg * kT6Fields;
+        const int b = bg / Gc, g = bg - b * Gc;
+        t6_build_pair(tabs + bg * kT6GroupBytes + f * kT6TableBytes, xs + bg * 128, fac[b * 2 * Gc + Gc + g], f,
+                      t & 3, tt & 1);
     }
     __syncthreads();
     pdl_launch_dependents();
 
     float* partials = reinterpret_cast<float*>(sm + p.off_partials);
     const uint32_t tb = base + p.off_tables;
-    const uint32_t fac_s = base + p.off_factors;
     bool ok = true;
     int k = 0;
     for (;; ++k) {
@@ -146,12 +156,12 @@ k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
         }
         const uint32_t st = base + (uint32_t)(warp * S + s) * p.stage_bytes;
         const uint32_t sts = st + bits_tile + (uint32_t)lane * Gc * 2u;
-        float acc = 0.f;
+        float acc[NB];
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb) acc[bb] = 0.f;
         for (int g8 = 0; g8 < Gc; g8 += 8) {
             const uint4 sv = lds128(sts + 2u * g8);
-            const uint4 fa = lds128(fac_s + 4u * g8), fb = lds128(fac_s + 4u * g8 + 16u);
             const uint32_t svw[4] = {sv.x, sv.y, sv.z, sv.w};
-            const uint32_t fw[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int g = g8 + j;
@@ -160,12 +170,17 @@ k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
                                    ((uint32_t)(j ^ (lane & 7)) << 4);
                 const uint4 wv = lds128(st + L);
                 const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
-                const float part = t6_group(w, tb + (uint32_t)g * kT6GroupBytes, std::make_index_sequence<kT6Fields>{});
                 const float sc = f16_bits_to_f32((uint16_t)(svw[j >> 1] >> (16 * (j & 1))));
-                acc = fmaf(part * sc, __uint_as_float(fw[j]), acc);
+#pragma unroll
+                for (int bb = 0; bb < NB; ++bb) {
+                    const float part = t6_group(w, tb + (uint32_t)((bb * Gc + g) * kT6GroupBytes),
+                                                std::make_index_sequence<kT6Fields>{});
+                    acc[bb] = fmaf(part * sc, fac[bb * 2 * Gc + g], acc[bb]);
+                }
             }
         }
-        partials[(b - rb0) * 32 + lane] = acc;
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb) partials[bb * p.prow + (b - rb0) * 32 + lane] = acc[bb];
         __syncwarp();
         if (lane == 0) issue(k + S);
     }
@@ -181,13 +196,14 @@ k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
     const int R = (rb1 - rb0) * 32;
     const int lo = (int)((int64_t)R * q / p.Q), hi = (int)((int64_t)R * (q + 1) / p.Q);
     const uint32_t part_s = base + p.off_partials;
+    for (int b = 0; b < NB; ++b)
     for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
         float v = 0.f;
-        for (int r = 0; r < p.Q; ++r) v += ld_cluster_f32(part_s + 4u * i, (uint32_t)r);
+        for (int r = 0; r < p.Q; ++r) v += ld_cluster_f32(part_s + 4u * (uint32_t)(b * p.prow + i), (uint32_t)r);
         const int row = rb0 * 32 + i;
         if (row < p.N) {
-            if (p.y_bf16) reinterpret_cast<uint16_t*>(p.y)[row] = f32_to_bf16_bits(v);
-            else reinterpret_cast<float*>(p.y)[row] = v;
+            if (p.y_bf16) reinterpret_cast<uint16_t*>(p.y)[(int64_t)b * p.N + row] = f32_to_bf16_bits(v);
+            else reinterpret_cast<float*>(p.y)[(int64_t)b * p.N + row] = v;
         }
     }
     cluster_sync();
@@ -215,26 +231,43 @@ struct T6Plan {
     T6Params p{};
 };
 
+constexpr int kT6MaxNB = 8;
+
+const void* t6_kernel(int nb) {
+    switch (nb) {
+        case 1: return (const void*)k_gemv_t6<1>;
+        case 2: return (const void*)k_gemv_t6<2>;
+        case 3: return (const void*)k_gemv_t6<3>;
+        case 4: return (const void*)k_gemv_t6<4>;
+        case 5: return (const void*)k_gemv_t6<5>;
+        case 6: return (const void*)k_gemv_t6<6>;
+        case 7: return (const void*)k_gemv_t6<7>;
+        case 8: return (const void*)k_gemv_t6<8>;
+        default: return nullptr;
+    }
+}
+
 // Cluster sizes that split G into slices of a multiple of 8 groups whose
-// tables fit comfortably in shared memory, most preferred first.
-int q_candidates(int64_t G, int* out) {
+// tables (NB batch rows) fit comfortably in shared memory, most preferred first.
+int q_candidates(int64_t G, int nb, int* out) {
     int n = 0;
     if (G % 8 != 0) return 0;
     const int64_t u = G / 8;  // units of 8 groups
     for (int q : {4, 2, 1, 5, 3, 7, 6, 8})
-        if (u % q == 0 && (G / q) * kT6GroupBytes <= 120 * 1024) out[n++] = q;
+        if (u % q == 0 && (G / q) * kT6GroupBytes * nb <= 150 * 1024) out[n++] = q;
     return n;
 }
 
-// Clusters of size Q that can be resident at once with this block size and
-// shared memory (clusters must fit inside one GPC, so this can be less than
-// SMs / Q); cached per configuration.
-int active_clusters(int Q, int threads, size_t smem) {
+// Clusters of size Q that can be resident at once with this kernel, block
+// size and shared memory (clusters must fit inside one GPC, so this can be
+// less than SMs / Q); cached per configuration.
+int active_clusters(const void* fn, int Q, int threads, size_t smem) {
+    struct Key { const void* fn; int Q, threads; size_t smem; int n; };
     static std::mutex mu;
-    static std::vector<std::pair<std::pair<int, int>, std::pair<size_t, int>>> cache;
+    static std::vector<Key> cache;
     std::lock_guard<std::mutex> lk(mu);
     for (auto& c : cache)
-        if (c.first.first == Q && c.first.second == threads && c.second.first == smem) return c.second.second;
+        if (c.fn == fn && c.Q == Q && c.threads == threads && c.smem == smem) return c.n;
     int n = 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(Q * (sm_count() / Q)));
@@ -247,28 +280,27 @@ int active_clusters(int Q, int threads, size_t smem) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaFuncSetAttribute((const void*)k_gemv_t6, cudaFuncAttributeMaxDynamicSharedMemorySize, kT6MaxSmem) !=
-            cudaSuccess ||
-        cudaOccupancyMaxActiveClusters(&n, (const void*)k_gemv_t6, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kT6MaxSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n <= 0) {
         cudaGetLastError();
         n = sm_count() / Q;  // no device (host-only checks): assume every SM
     }
-    cache.push_back({{Q, threads}, {smem, n}});
+    cache.push_back({fn, Q, threads, smem, n});
     return n;
 }
 
-bool plan_t6_q(int64_t N, int64_t K, int Q, T6Plan& pl) {
+bool plan_t6_q(int64_t N, int64_t K, int Q, int nb, T6Plan& pl) {
     const int64_t G = K / 128;
     pl.Q = Q;
     pl.Gc = (int)(G / Q);
     pl.stage_bytes = (32 * pl.Gc * 18 + 1023) & ~1023;
-    const int tables = pl.Gc * kT6GroupBytes;
-    const int factors = pl.Gc * 8;
-    const int xbytes = pl.Gc * 128 * 2;
+    const int tables = nb * pl.Gc * kT6GroupBytes;
+    const int factors = nb * pl.Gc * 8;
+    const int xbytes = nb * pl.Gc * 128 * 2;
     const int64_t RB = (N + 31) / 32;
     auto total = [&](int W, int S, int bpc) {
         return (size_t)1024 + (size_t)W * S * pl.stage_bytes + tables + factors + xbytes +
-               (size_t)bpc * 128 + (size_t)W * S * 8 + 64;
+               (size_t)nb * bpc * 128 + (size_t)W * S * 8 + 64;
     };
     // first guess with every SM, then shrink to the clusters that fit at once
     int ncl = sm_count() / Q;
@@ -283,7 +315,7 @@ bool plan_t6_q(int64_t N, int64_t K, int Q, T6Plan& pl) {
         while (total(W, S, bpc) > kT6MaxSmem && S > 1) --S;
         while (total(W, S, bpc) > kT6MaxSmem && W > 4) --W;
         if (total(W, S, bpc) > kT6MaxSmem) return false;
-        const int act = active_clusters(Q, W * 32, total(W, S, bpc));
+        const int act = active_clusters(t6_kernel(nb), Q, W * 32, total(W, S, bpc));
         if (act >= ncl) break;
         ncl = act < 1 ? 1 : act;
     }
@@ -296,7 +328,7 @@ bool plan_t6_q(int64_t N, int64_t K, int Q, T6Plan& pl) {
     pl.p.off_factors = off;       off += factors;          // 16-byte aligned (tables multiple of 128)
     off = (off + 15u) & ~15u;
     pl.p.off_x = off;             off += xbytes;
-    pl.p.off_partials = off;      off += bpc * 128;
+    pl.p.off_partials = off;      off += nb * bpc * 128;
     off = (off + 7u) & ~7u;
     pl.p.off_bars = off;
     pl.p.N = (int)N;
@@ -305,18 +337,19 @@ bool plan_t6_q(int64_t N, int64_t K, int Q, T6Plan& pl) {
     pl.p.Q = Q;
     pl.p.S = S;
     pl.p.stage_bytes = pl.stage_bytes;
+    pl.p.prow = bpc * 32;
     return true;
 }
 
 // Among the usable cluster sizes, take the plan that keeps the most SMs busy.
-bool plan_t6(int64_t N, int64_t K, T6Plan& best) {
-    if (N < 1 || N > (1LL << 30)) return false;
+bool plan_t6(int64_t N, int64_t K, int nb, T6Plan& best) {
+    if (N < 1 || N > (1LL << 30) || nb < 1 || nb > kT6MaxNB) return false;
     int qs[8];
-    const int nq = q_candidates(K / 128, qs);
+    const int nq = q_candidates(K / 128, nb, qs);
     bool found = false;
     for (int i = 0; i < nq; ++i) {
         T6Plan pl;
-        if (!plan_t6_q(N, K, qs[i], pl)) continue;
+        if (!plan_t6_q(N, K, qs[i], nb, pl)) continue;
         if (!found || pl.ncl * pl.Q > best.ncl * best.Q) {
             best = pl;
             found = true;
@@ -325,17 +358,18 @@ bool plan_t6(int64_t N, int64_t K, T6Plan& best) {
     return found;
 }
 
-}  // namespace
-
-bool t6_supported(int64_t B, int64_t N, int64_t K) {
-    int qs[8];
-    return B == 1 && K % 1024 == 0 && K <= (1LL << 20) && q_candidates(K / 128, qs) > 0 && N >= 1 &&
-           N <= (1LL << 30);
+// Batch rows per launch: the largest NB <= min(B, 8) that has a plan.
+int t6_chunk(int64_t B, int64_t N, int64_t K) {
+    for (int nb = (int)std::min<int64_t>(B, kT6MaxNB); nb >= 1; --nb) {
+        T6Plan pl;
+        if (plan_t6(N, K, nb, pl)) return nb;
+    }
+    return 0;
 }
 
-cudaError_t launch_gemv_t6(const GemvArgs& a) {
+cudaError_t launch_t6_chunk(const GemvArgs& a, int nb, const uint16_t* x, void* y, bool pdl) {
     T6Plan pl;
-    if (a.B != 1 || !plan_t6(a.N, a.K, pl)) return cudaErrorNotSupported;
+    if (!plan_t6(a.N, a.K, nb, pl)) return cudaErrorNotSupported;
     auto enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const int64_t G = a.K / 128;
@@ -360,15 +394,14 @@ cudaError_t launch_gemv_t6(const GemvArgs& a) {
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
+    const void* fn = t6_kernel(nb);
     {
-        const cudaError_t e = cudaFuncSetAttribute((const void*)k_gemv_t6,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kT6MaxSmem);
+        const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kT6MaxSmem);
         if (e != cudaSuccess) return e;
     }
-
     T6Params prm = pl.p;
-    prm.x = a.x;
-    prm.y = a.y;
+    prm.x = x;
+    prm.y = y;
     prm.y_bf16 = a.y_bf16;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(pl.ncl * pl.Q));
@@ -381,7 +414,7 @@ cudaError_t launch_gemv_t6(const GemvArgs& a) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     int na = 1;
-    if (a.pdl) {
+    if (pdl) {
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         na = 2;
@@ -389,7 +422,35 @@ cudaError_t launch_gemv_t6(const GemvArgs& a) {
     cfg.attrs = attr;
     cfg.numAttrs = na;
     void* args[] = {(void*)&tm_bits, (void*)&tm_sc, (void*)&prm};
-    return cudaLaunchKernelExC(&cfg, (const void*)k_gemv_t6, args);
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace
+
+bool t6_supported(int64_t B, int64_t N, int64_t K) {
+    int qs[8];
+    return B >= 1 && K % 1024 == 0 && K <= (1LL << 20) && q_candidates(K / 128, 1, qs) > 0 && N >= 1 &&
+           N <= (1LL << 30);
+}
+
+int t6_launch_count(int64_t B, int64_t N, int64_t K) {
+    if (!t6_supported(B, N, K)) return 0;
+    const int nb = t6_chunk(B, N, K);
+    return nb > 0 ? (int)((B + nb - 1) / nb) : 0;
+}
+
+cudaError_t launch_gemv_t6(const GemvArgs& a) {
+    if (!t6_supported(a.B, a.N, a.K)) return cudaErrorNotSupported;
+    const int nb = t6_chunk(a.B, a.N, a.K);
+    if (nb < 1) return cudaErrorNotSupported;
+    const size_t ysz = a.y_bf16 ? 2 : 4;
+    for (int64_t b0 = 0; b0 < a.B; b0 += nb) {
+        const int n = (int)std::min<int64_t>(nb, a.B - b0);
+        const cudaError_t e = launch_t6_chunk(a, n, a.x + b0 * a.K, static_cast<uint8_t*>(a.y) + b0 * a.N * ysz,
+                                              a.pdl || b0 > 0);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 unsigned int t6_take_timeouts() {

@@ -39,9 +39,11 @@ cudaError_t launch_gemv_simple(const GemvArgs& a);
 bool lut_supported(int64_t B, int64_t N, int64_t K);
 cudaError_t launch_gemv_lut(const GemvArgs& a);
 
-// Row-per-lane 6-bit-table batch-1 kernel with TMA staging and cluster
-// split-K (needs K a multiple of 1024 with a usable cluster split).
+// Row-per-lane 6-bit-table kernel with TMA staging and cluster split-K
+// (needs K a multiple of 1024 with a usable cluster split); up to 8 batch
+// rows per launch, larger batches in several launches (t6_launch_count).
 bool t6_supported(int64_t B, int64_t N, int64_t K);
+int t6_launch_count(int64_t B, int64_t N, int64_t K);
 cudaError_t launch_gemv_t6(const GemvArgs& a);
 // Number of bounded device waits that gave up since the last call (and reset).
 unsigned int t6_take_timeouts();

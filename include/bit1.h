@@ -71,9 +71,10 @@ enum bit1_gemv_variant {
     BIT1_GEMV_LUT = 2,     /* batch 1..8: CUDA-core table-lookup kernel */
     BIT1_GEMV_SPLITK = 3,  /* batch 1..8, short N: K split over CTAs, workspace reduction */
     BIT1_GEMV_TC = 4,      /* batch >= 16: tcgen05 tensor-core kernel */
-    BIT1_GEMV_LUT6 = 5,    /* batch 1, K a multiple of 1024: one row per lane,
-                              6-bit fp16 tables, TMA-staged weights, K split over
-                              a thread-block cluster */
+    BIT1_GEMV_LUT6 = 5,    /* K a multiple of 1024: one row per lane, 6-bit fp16
+                              tables per batch row, TMA-staged weights, K split
+                              over a thread-block cluster; up to 8 batch rows
+                              per launch (larger batches: several launches) */
     BIT1_GEMV_STREAM = 6   /* batch 1, K a multiple of 1024: the grouped kernel
                               below with one problem (one CTA per SM streaming a
                               contiguous row range, full-K tables, no clusters) */

@@ -93,6 +93,15 @@ def test_pick_and_launch_counts(lib):
     assert b1.bit1_gemv_launches(1, 4096, 4096, b1.AUTO) == 1
     assert b1.bit1_gemv_launches(1, 4096, 100, b1.AUTO) == 0
     assert b1.bit1_gemv_workspace_bytes(1, 4096, 100) == 0
+    # batched: the table kernel without scratch, the tensor cores from 16 rows with it
+    assert b1.bit1_gemv_pick(4, 12288, 4096) == b1.LUT6
+    assert b1.bit1_gemv_pick(16, 12288, 4096) == b1.LUT6
+    ws = b1.bit1_gemv_workspace_bytes(16, 12288, 4096)
+    assert ws > 0 and b1.bit1_gemv_pick(16, 12288, 4096, ws) == b1.TC
+    assert b1.bit1_gemv_pick(8, 12288, 4096, 1 << 30) == b1.LUT6
+    assert b1.bit1_gemv_launches(4, 12288, 4096, b1.LUT6) == 1
+    assert b1.bit1_gemv_launches(16, 12288, 4096, b1.LUT6) >= 2
+    assert b1.bit1_gemv_launches(16, 12288, 4096, b1.TC) == 2
 
 
 def test_pack_rejects_on_host(lib):

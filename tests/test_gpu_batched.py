@@ -1,0 +1,82 @@
+"""GPU parity of the CUDA-core batched path (BIT1_GEMV_LUT6 with B > 1: 6-bit
+tables per batch row, up to 8 rows per launch) against the CPU oracle on the
+same seeded inputs, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import bit_weight_gemv_sign_b300 as b1
+from bit_weight_gemv_sign_b300 import synth
+from tests.helpers import abs_bound, assert_gemv_close, dev_bf16, dev_u8, dev_u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    b1.load()
+
+
+def _problem(N, K, B, seed):
+    bits, scales = synth.matrix(N, K, seed)
+    x = synth.x_for(B, K, seed)
+    return bits, scales, x
+
+
+def _run(bits, scales, x, N, K, B, variant=b1.LUT6, y_dtype=b1.F32, flags=0):
+    y = b1.bit1_gemv_ex(dev_u8(bits), dev_u16(scales), dev_bf16(x).view(B, K), y_dtype=y_dtype,
+                        variant=variant, flags=flags, N=N, K=K)
+    torch.cuda.synchronize()
+    return y
+
+
+# one launch (B <= 8 when the tables fit), several launches (B = 9, 16), ragged
+# row blocks, long K with deep cluster splits
+BATCHED = [(256, 1024, 2), (300, 2048, 3), (1000, 4096, 4), (777, 4096, 5), (4100, 4096, 8),
+           (513, 12288, 6), (129, 5120, 7), (3000, 4096, 16), (64, 16384, 4), (5000, 12288, 9)]
+
+
+@pytest.mark.parametrize("N,K,B", BATCHED)
+def test_batched_tables_match_oracle(orc, N, K, B):
+    bits, scales, x = _problem(N, K, B, 8000 + N + K + B)
+    ref = orc.gemv(bits, scales, x, B, N, K)
+    y = _run(bits, scales, x, N, K, B)
+    assert_gemv_close(y, ref, abs_bound(scales, x, K), f"lut6 N={N} K={K} B={B}")
+    assert b1.bit1_device_wait_timeouts() == 0
+
+
+def test_batched_auto_bf16_and_pdl(orc):
+    N, K, B = 2000, 4096, 4
+    bits, scales, x = _problem(N, K, B, 8101)
+    assert b1.bit1_gemv_pick(B, N, K) == b1.LUT6
+    ref = orc.gemv(bits, scales, x, B, N, K)
+    y = _run(bits, scales, x, N, K, B, variant=b1.AUTO, y_dtype=b1.BF16)
+    assert y.dtype == torch.bfloat16
+    assert_gemv_close(y, ref, abs_bound(scales, x, K), "lut6 batched bf16")
+    a = _run(bits, scales, x, N, K, B)
+    c = _run(bits, scales, x, N, K, B, flags=b1.FLAG_PDL)
+    assert torch.equal(a, c)
+
+
+def test_batched_rows_independent_of_batch_size():
+    """A batch row's result does not depend on the other rows of the batch
+    (tables and prescales are per batch row; the row walk is the same)."""
+    N, K = 1500, 4096
+    bits, scales, x = _problem(N, K, 5, 8102)
+    y5 = _run(bits, scales, x, N, K, 5)
+    for b in range(5):
+        y1 = _run(bits, scales, x[b:b + 1], N, K, 1)
+        assert torch.equal(y1[0], y5[b]), f"batch row {b}"
+
+
+def test_batched_row_flip_negates_exactly():
+    N, K, B = 700, 4096, 4
+    bits, scales, x = _problem(N, K, B, 8103)
+    y = _run(bits, scales, x, N, K, B)
+    flipped = bits.copy()
+    flipped[[0, 31, 32, 699]] ^= 0xFF
+    y2 = _run(flipped, scales, x, N, K, B)
+    rows = torch.tensor([0, 31, 32, 699], device="cuda")
+    assert torch.equal(y2[:, rows], -y[:, rows])
