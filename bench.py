@@ -181,14 +181,15 @@ def time_oracle(sample, threads: int):
     return wbytes, secs
 
 
-def cpu_baseline(frac_den: int = 8):
+def cpu_baseline(frac_den: int = 1):
     threads = os.cpu_count() or 1
     sample = oracle_sample(frac_den)
     wbytes, secs = time_oracle(sample, threads)
+    what = ("all rows of the 253 sweep matrices (one full decode step" if frac_den == 1 else
+            f"first 1/{frac_den} of the rows of each of the 253 sweep matrices (")
     return {"value": wbytes / secs / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "seconds": secs, "sample": f"first 1/{frac_den} of the rows of each of the 253 sweep "
-                                        f"matrices ({wbytes} weight bytes), scalar fp64 oracle, "
-                                        f"{threads} threads"}
+            "seconds": secs, "tok_s_equiv": wbytes / secs / 1064263680,
+            "sample": f"{what}, {wbytes} weight bytes), scalar fp64 oracle, {threads} threads"}
 
 
 def run_reference(args):
@@ -221,6 +222,155 @@ def run_reference(args):
            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out))
     return 0
+
+
+# ---------------------------------------------------------------- extras
+# The other configurations of the workload family, measured on the same GPU
+# after the headline: each shape timed as a CUDA-graph replay of REPS calls
+# that rotate over enough distinct weight copies to exceed 3x the L2, so every
+# call streams its weights from HBM.
+
+L2_BYTES = 126 * 2**20
+
+
+def _weight_bytes(N, K):
+    return N * K // 8 + 2 * N * (K // 128)
+
+
+def _time_calls(torch, b1, N, K, B, variant, reps=30, ws_bytes=None):
+    """Microseconds per bit1_gemv_ex call (graph replay, L2 rotated), or None
+    when the variant does not take the shape."""
+    if b1.bit1_gemv_launches(B, N, K, variant) == 0:
+        return None
+    wb = _weight_bytes(N, K)
+    copies = max(2, (3 * L2_BYTES) // wb + 1)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(N * 131 + K * 7 + B)
+    bits = torch.randint(0, 256, (copies, N, K // 8), dtype=torch.uint8, device="cuda", generator=g)
+    sc = (torch.randn((copies, N, K // 128), device="cuda", generator=g).abs_() * 0.02).half().view(torch.int16)
+    x = torch.randn((B, K), device="cuda", generator=g).bfloat16()
+    y = torch.empty((B, N), device="cuda")
+    if ws_bytes is None:
+        ws_bytes = b1.bit1_gemv_workspace_bytes(max(B, 16), N, K) if variant == b1.TC else 0
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for i in range(3):
+            b1.bit1_gemv_ex(bits[i % copies], sc[i % copies], x, y=y, workspace=ws, variant=variant,
+                            flags=b1.FLAG_PDL, stream=s)
+        s.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            for i in range(reps):
+                b1.bit1_gemv_ex(bits[i % copies], sc[i % copies], x, y=y, workspace=ws, variant=variant,
+                                flags=b1.FLAG_PDL, stream=s)
+        graph.replay()
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        graph.replay()
+        e1.record(s)
+        e1.synchronize()
+    us = e0.elapsed_time(e1) / reps * 1e3
+    del bits, sc, graph
+    torch.cuda.empty_cache()
+    return us
+
+
+def _shape_entry(N, K, B, us):
+    if us is None:
+        return None
+    return {"us": round(us, 3), "weight_gbs": round(_weight_bytes(N, K) / (us * 1e-6) / 1e9, 1),
+            "tflops": round(2.0 * B * N * K / (us * 1e-6) / 1e12, 2)}
+
+
+def extra_c1_tiny(torch, b1):
+    """Tiny 256x1024 batch-1 GEMV and an 8-row XOR patch applied and removed."""
+    from bit_weight_gemv_sign_b300 import synth
+    N, K = synth.TINY.N, synth.TINY.K
+    us = _time_calls(torch, b1, N, K, 1, b1.AUTO, reps=50)
+    bits = torch.randint(0, 256, (N, K // 8), dtype=torch.uint8, device="cuda")
+    rows = [int(r) for r in synth.distinct_rows(N, 8, 0)]
+    b1.bit1_xor_patch(bits, rows)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(50):
+        b1.bit1_xor_patch(bits, rows)
+    e1.record()
+    e1.synchronize()
+    return {"shape": [N, K], "gemv": _shape_entry(N, K, 1, us),
+            "xor_patch_8_rows_us": round(e0.elapsed_time(e1) / 50 * 1e3, 3),
+            "note": "latency-bound sizes (36 KB of weights); reported, not a roofline case"}
+
+
+def extra_c2_projections(torch, b1):
+    from bit_weight_gemv_sign_b300 import synth
+    out = {}
+    for m in synth.PROJ_8B:
+        out[m.name] = {"shape": [m.N, m.K]}
+        for name, v in (("lut6", b1.LUT6), ("lut", b1.LUT), ("stream", b1.STREAM)):
+            out[m.name][name] = _shape_entry(m.N, m.K, 1, _time_calls(torch, b1, m.N, m.K, 1, v))
+    out["note"] = ("one bit1_gemv_ex call per projection, graph replay with PDL, L2 rotated; a 0.6-7 MB "
+                   "matrix is 0.1-1.1 us of HBM time, so a single call is bound by launch and ramp latency")
+    return out
+
+
+def extra_c4_crossover(torch, b1):
+    """CUDA-core path (6-bit tables, up to 8 batch rows per launch) vs the
+    tcgen05 path on the 8B MLP shapes."""
+    out = {}
+    for N, K, name in ((12288, 4096, "up_gate"), (4096, 12288, "down")):
+        rows = {}
+        cross = None
+        for B in (1, 4, 16, 32, 64):
+            cc = _time_calls(torch, b1, N, K, B, b1.LUT6)
+            tc = _time_calls(torch, b1, N, K, B, b1.TC)
+            rows[str(B)] = {"cuda_core": _shape_entry(N, K, B, cc), "tcgen05": _shape_entry(N, K, B, tc)}
+            if cross is None and cc is not None and tc is not None and tc < cc:
+                cross = B
+        out[name] = {"shape": [N, K], "by_batch": rows, "tcgen05_faster_from_batch": cross}
+    return out
+
+
+def extra_c5_sweep_27b(torch, b1, steps=20):
+    """27B-class sweep (448 matrices, 2.97 GB) as one grouped launch per step,
+    and the 100-entry patch applied and removed (timed on the host clock)."""
+    from bit_weight_gemv_sign_b300 import synth
+    from bit_weight_gemv_sign_b300.sweep import Sweep
+    sw = Sweep(synth.sweep_27b(), seed0=0, batch=1, y_dtype=b1.BF16).fill_device(27)
+    plan = sw.group_plan()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            plan.run(stream=s)
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            plan.run(stream=s)
+        e1.record(s)
+        e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    entries = synth.patch_entries_27b(100, 0)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    sw.apply_patch(entries)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    sw.apply_patch(entries)
+    torch.cuda.synchronize()
+    t2 = time.perf_counter()
+    hbm, _ = _peaks()
+    gbs = sw.weight_bytes / (ms * 1e-3) / 1e9
+    out = {"weight_bytes": sw.weight_bytes, "ms_per_step": ms, "weight_gbs": gbs, "hbm_frac": gbs / hbm,
+           "tok_s_equiv": 1e3 / ms, "patch_entries": len(entries),
+           "patch_apply_ms": (t1 - t0) * 1e3, "patch_remove_ms": (t2 - t1) * 1e3,
+           "note": "one grouped launch per step; patch parity and bit-identical restore are "
+                   "checked in tests/test_gpu_sweeps.py"}
+    del sw, plan
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_mine(args):
@@ -360,10 +510,15 @@ def run_mine(args):
         "device_wait_timeouts": timeouts,
         "clocks": clk.summary(),
     }
+    if rank == 0 and not args.no_extras:
+        out["extras"] = {"c1_tiny": extra_c1_tiny(torch, b1),
+                         "c2_projections_b1": extra_c2_projections(torch, b1),
+                         "c4_mlp_crossover": extra_c4_crossover(torch, b1),
+                         "c5_sweep_27b": extra_c5_sweep_27b(torch, b1)}
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
-        out["cpu_baseline"] = cpu_baseline(frac_den=8)
+        out["cpu_baseline"] = cpu_baseline(frac_den=1)
     if rank == 0:
         print(json.dumps(out))
     if dist:
@@ -378,6 +533,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other configurations (tiny, projections, crossover, 27B sweep)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

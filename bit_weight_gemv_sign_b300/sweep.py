@@ -93,6 +93,21 @@ class Sweep:
         torch.cuda.synchronize()
         return self
 
+    def fill_device(self, seed: int = 0):
+        """The same distributions generated on the device from one seeded
+        generator (sign bytes uniform, scales |N(0, 0.02)| in fp16, x N(0, 1) in
+        bf16): for timing runs that need no host copy of the weights."""
+        g = torch.Generator(device=self.device)
+        g.manual_seed(seed)
+        for i, m in enumerate(self.mats):
+            self.bits_of(i).copy_(torch.randint(0, 256, (m.N, m.K // 8), dtype=torch.uint8,
+                                                device=self.device, generator=g))
+            sc = torch.randn((m.N, m.K // 128), device=self.device, generator=g).abs_().mul_(0.02)
+            self.scales_of(i).copy_(sc.half().view(torch.int16))
+            self.x_of(i).copy_(torch.randn((self.B, m.K), device=self.device, generator=g).bfloat16())
+        torch.cuda.synchronize()
+        return self
+
     # ---- execution ---------------------------------------------------------
     def launches_per_step(self) -> int:
         return sum(bit1_gemv_launches(self.B, m.N, m.K, self.variant) for m in self.mats)

@@ -1,0 +1,95 @@
+"""Full-size decode sweeps in the launch configuration the benchmark times (one
+grouped persistent launch per step, bf16 output), checked against the CPU
+oracle on sampled rows of every matrix, and the 27B-class sweep with a
+100-entry row patch: applied, verified against the oracle on the patched
+weights, then removed and checked bit-identical to the original weights."""
+import numpy as np
+import pytest
+import torch
+
+import bit_weight_gemv_sign_b300 as b1
+from bit_weight_gemv_sign_b300 import synth
+from bit_weight_gemv_sign_b300.sweep import Sweep
+from tests.helpers import abs_bound, assert_gemv_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    b1.load()
+
+
+def _sample_rows(N, count, seed, extra=()):
+    rows = np.random.default_rng(seed).choice(N, min(count, N), replace=False)
+    return np.unique(np.concatenate([rows, [0, N - 1], np.asarray(extra, dtype=np.int64)])).astype(np.int64)
+
+
+def _check_matrix(orc, sw, i, y, rows, bits=None, what=""):
+    m = sw.mats[i]
+    hb, hs, hx = sw.host_matrix(i)
+    if bits is not None:
+        hb = bits
+    ref = orc.gemv_select(hb, hs, hx, 1, m.N, m.K, rows)
+    got = y[:, torch.from_numpy(rows).cuda()]
+    assert_gemv_close(got, ref, abs_bound(hs[rows], hx, m.K), f"{what} matrix {i} ({m.name})")
+
+
+def test_sweep_8b_grouped_launch_sampled_parity(orc):
+    sw = Sweep(synth.sweep_8b(), seed0=0, batch=1, y_dtype=b1.BF16).fill()
+    plan = sw.group_plan()
+    plan.run()
+    torch.cuda.synchronize()
+    assert b1.bit1_device_wait_timeouts() == 0
+    for i in range(len(sw.mats)):
+        rows = _sample_rows(sw.mats[i].N, 24, 1000 + i)
+        _check_matrix(orc, sw, i, sw.y_of(i), rows, what="8B sweep")
+    # a second step over the same plan gives the same bits
+    first = sw.y.clone()
+    plan.run()
+    torch.cuda.synchronize()
+    assert torch.equal(first, sw.y)
+
+
+def test_sweep_27b_patch_apply_verify_remove(orc):
+    sw = Sweep(synth.sweep_27b(), seed0=0, batch=1, y_dtype=b1.BF16).fill()
+    plan = sw.group_plan()
+    plan.run()
+    torch.cuda.synchronize()
+    y_before = sw.y.clone()
+
+    entries = synth.patch_entries_27b(100, 0)
+    by_mat = sw.apply_patch(entries)
+    torch.cuda.synchronize()
+    patch_bytes = sum(sw.mats[i].K // 8 * len(rows) for i, rows in by_mat.items())
+    assert len(entries) == 100 and patch_bytes > 0
+
+    plan.run()
+    torch.cuda.synchronize()
+    assert b1.bit1_device_wait_timeouts() == 0
+    for i, rows in sorted(by_mat.items()):
+        m = sw.mats[i]
+        hb, _, _ = sw.host_matrix(i)
+        patched = orc.xor_patch(hb, m.N, m.K, rows)
+        # the device weights equal the oracle's patched bytes, bit for bit
+        assert np.array_equal(sw.bits_of(i).cpu().numpy(), patched), f"patched bytes of matrix {i}"
+        sample = _sample_rows(m.N, 16, 2000 + i, extra=rows)
+        _check_matrix(orc, sw, i, sw.y_of(i), sample, bits=patched, what="27B patched")
+        # a flipped row is the exact negation of its unpatched output
+        r = torch.tensor(sorted(set(rows)), device="cuda")
+        assert torch.equal(sw.y_of(i)[:, r], -sw.y_of(i, y_before)[:, r])
+    # unpatched matrices: unchanged outputs
+    for i in range(len(sw.mats)):
+        if i not in by_mat:
+            assert torch.equal(sw.y_of(i), sw.y_of(i, y_before)), f"matrix {i} changed"
+
+    sw.apply_patch(entries)           # the same XOR removes the patch
+    torch.cuda.synchronize()
+    for i in sorted(by_mat):
+        hb, _, _ = sw.host_matrix(i)
+        assert np.array_equal(sw.bits_of(i).cpu().numpy(), hb), f"restore of matrix {i}"
+    plan.run()
+    torch.cuda.synchronize()
+    assert torch.equal(sw.y, y_before)
