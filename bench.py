@@ -39,6 +39,17 @@ def _peaks():
     return 6400.0, "fallback"
 
 
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """The largest of every rank's ``value`` (the step time a multi-GPU run
+    reports: the slowest replica); the value itself without a process group."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -411,11 +422,7 @@ def run_mine(args):
         e1.record(s)
         e1.synchronize()
     barrier()
-    ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, "cuda")
     ms_step = ms / args.steps
     gbs = ws * sw.weight_bytes / (ms_step * 1e-3) / 1e9
     timeouts = b1.bit1_device_wait_timeouts()
@@ -460,7 +467,7 @@ def run_mine(args):
     down.wait_stream(up)
     f1.record(down)
     f1.synchronize()
-    e2e_ms = f0.elapsed_time(f1) / args.steps
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), dist, "cuda") / args.steps
     e2e_gbs = ws * sw.weight_bytes / (e2e_ms * 1e-3) / 1e9
     hy = hy[0]
 
@@ -479,7 +486,7 @@ def run_mine(args):
             sw.replay()
         c1.record(sw.stream)
         c1.synchronize()
-    chain_ms = c0.elapsed_time(c1) / chain_steps
+    chain_ms = max_over_ranks(c0.elapsed_time(c1), dist, "cuda") / chain_steps
 
     hbm, src = _peaks()
     grp_src = os.path.join(ROOT, "bit_weight_gemv_sign_b300", "csrc", "gemv_group.cu")
