@@ -248,14 +248,23 @@ const void* t6_kernel(int nb) {
 }
 
 // Cluster sizes that split G into slices of a multiple of 8 groups whose
-// tables (NB batch rows) fit comfortably in shared memory, most preferred first.
+// tables (NB batch rows) fit comfortably in shared memory, most preferred
+// first.  Sizes above 8 are non-portable clusters (allowed on this part up to
+// 16): they let several batch rows' tables fit for long K (K = 12288 at four
+// rows needs slices of 8 groups, a cluster of 12).
 int q_candidates(int64_t G, int nb, int* out) {
     int n = 0;
     if (G % 8 != 0) return 0;
     const int64_t u = G / 8;  // units of 8 groups
-    for (int q : {4, 2, 1, 5, 3, 7, 6, 8})
+    for (int q : {4, 2, 1, 5, 3, 7, 6, 8, 12, 10, 16})
         if (u % q == 0 && (G / q) * kT6GroupBytes * nb <= 150 * 1024) out[n++] = q;
     return n;
+}
+
+cudaError_t t6_set_attrs(const void* fn) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kT6MaxSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    return e;
 }
 
 // Clusters of size Q that can be resident at once with this kernel, block
@@ -280,10 +289,12 @@ int active_clusters(const void* fn, int Q, int threads, size_t smem) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kT6MaxSmem) != cudaSuccess ||
-        cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n <= 0) {
+    if (t6_set_attrs(fn) != cudaSuccess || cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n <= 0) {
         cudaGetLastError();
-        n = sm_count() / Q;  // no device (host-only checks): assume every SM
+        int devices = 0;
+        const bool no_device = cudaGetDeviceCount(&devices) != cudaSuccess || devices == 0;
+        cudaGetLastError();
+        n = no_device ? sm_count() / Q : 0;  // host-only checks: assume every SM; on a GPU: unusable
     }
     cache.push_back({fn, Q, threads, smem, n});
     return n;
@@ -316,8 +327,9 @@ bool plan_t6_q(int64_t N, int64_t K, int Q, int nb, T6Plan& pl) {
         while (total(W, S, bpc) > kT6MaxSmem && W > 4) --W;
         if (total(W, S, bpc) > kT6MaxSmem) return false;
         const int act = active_clusters(t6_kernel(nb), Q, W * 32, total(W, S, bpc));
+        if (act < 1) return false;            // this cluster size cannot run here
         if (act >= ncl) break;
-        ncl = act < 1 ? 1 : act;
+        ncl = act;
     }
     pl.ncl = ncl;
     pl.W = W;
@@ -344,7 +356,7 @@ bool plan_t6_q(int64_t N, int64_t K, int Q, int nb, T6Plan& pl) {
 // Among the usable cluster sizes, take the plan that keeps the most SMs busy.
 bool plan_t6(int64_t N, int64_t K, int nb, T6Plan& best) {
     if (N < 1 || N > (1LL << 30) || nb < 1 || nb > kT6MaxNB) return false;
-    int qs[8];
+    int qs[16];
     const int nq = q_candidates(K / 128, nb, qs);
     bool found = false;
     for (int i = 0; i < nq; ++i) {
@@ -396,7 +408,7 @@ cudaError_t launch_t6_chunk(const GemvArgs& a, int nb, const uint16_t* x, void* 
     }
     const void* fn = t6_kernel(nb);
     {
-        const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kT6MaxSmem);
+        const cudaError_t e = t6_set_attrs(fn);
         if (e != cudaSuccess) return e;
     }
     T6Params prm = pl.p;
@@ -428,7 +440,7 @@ cudaError_t launch_t6_chunk(const GemvArgs& a, int nb, const uint16_t* x, void* 
 }  // namespace
 
 bool t6_supported(int64_t B, int64_t N, int64_t K) {
-    int qs[8];
+    int qs[16];
     return B >= 1 && K % 1024 == 0 && K <= (1LL << 20) && q_candidates(K / 128, 1, qs) > 0 && N >= 1 &&
            N <= (1LL << 30);
 }
