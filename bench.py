@@ -344,6 +344,16 @@ def extra_c4_crossover(torch, b1):
     return out
 
 
+def extra_pp512(torch, b1):
+    """Prompt processing: a 512-row batch through the tensor-core path on the
+    8B up/gate shape (eight 64-row launches per call)."""
+    N, K, B = 12288, 4096, 512
+    us = _time_calls(torch, b1, N, K, B, b1.TC, reps=10, ws_bytes=b1.bit1_gemv_workspace_bytes(B, N, K))
+    e = _shape_entry(N, K, B, us)
+    hbm, _ = _peaks()
+    return {"shape": [N, K], "batch": B, **e}
+
+
 def extra_c5_sweep_27b(torch, b1, steps=20):
     """27B-class sweep (448 matrices, 2.97 GB) as one grouped launch per step,
     and the 100-entry patch applied and removed (timed on the host clock)."""
@@ -521,6 +531,7 @@ def run_mine(args):
         out["extras"] = {"c1_tiny": extra_c1_tiny(torch, b1),
                          "c2_projections_b1": extra_c2_projections(torch, b1),
                          "c4_mlp_crossover": extra_c4_crossover(torch, b1),
+                         "pp512_tcgen05": extra_pp512(torch, b1),
                          "c5_sweep_27b": extra_c5_sweep_27b(torch, b1)}
     if rank == 0 and not args.no_cpu_baseline:
         import oracle

@@ -53,11 +53,14 @@ bool shape_ok(int64_t B, int64_t N, int64_t K) {
 
 bit1_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BIT1_OK : BIT1_ECUDA; }
 
-// Batch >= 16 with enough scratch: the tensor-core kernel; otherwise the
-// 6-bit-table CUDA-core kernel (up to 8 batch rows per launch); shapes it
-// cannot take: the nibble-table kernel (batch 1), else one warp per row.
+// Batch >= 16 with enough scratch: the tensor-core kernel.  Batch 1 below
+// 65536 rows: the nibble-table kernel (one launch of it is the shortest for
+// the projection sizes of 8B-27B models: less set-up than the cluster
+// kernel); larger or batched: the 6-bit-table kernel (up to 8 batch rows per
+// launch); what none of them takes: one warp per row.
 int pick_variant(int64_t B, int64_t N, int64_t K, size_t ws_bytes) {
     if (B >= 16 && tc_supported(B, N, K) && ws_bytes >= tc_workspace_bytes(B, N, K)) return BIT1_GEMV_TC;
+    if (B == 1 && N < 65536 && lut_supported(B, N, K)) return BIT1_GEMV_LUT;
     if (t6_supported(B, N, K)) return BIT1_GEMV_LUT6;
     if (lut_supported(B, N, K)) return BIT1_GEMV_LUT;
     return BIT1_GEMV_SIMPLE;

@@ -84,10 +84,12 @@ def test_gemv_variant_limits_on_host(lib):
 
 
 def test_pick_and_launch_counts(lib):
-    assert b1.bit1_gemv_pick(1, 4096, 4096) == b1.LUT6
-    assert b1.bit1_gemv_pick(1, 151936, 4096) == b1.LUT6
-    assert b1.bit1_gemv_pick(1, 4096, 12288) == b1.LUT6
-    assert b1.bit1_gemv_pick(1, 4096, 13312) == b1.LUT     # 6-bit tables would not fit
+    assert b1.bit1_gemv_pick(1, 4096, 4096) == b1.LUT       # one projection: nibble tables
+    assert b1.bit1_gemv_pick(1, 151936, 4096) == b1.LUT6    # very tall: 6-bit tables
+    assert b1.bit1_gemv_pick(1, 4096, 12288) == b1.LUT
+    assert b1.bit1_gemv_pick(1, 70000, 12288) == b1.LUT6
+    assert b1.bit1_gemv_pick(1, 4096, 13312) == b1.LUT
+    assert b1.bit1_gemv_pick(1, 5120, 17408) == b1.SIMPLE   # no table kernel takes K = 17 x 1024
     assert b1.bit1_gemv_pick(1, 4096, 1152) == b1.SIMPLE
     assert b1.bit1_gemv_pick(0, 4096, 4096) == 0
     assert b1.bit1_gemv_launches(1, 4096, 4096, b1.AUTO) == 1

@@ -97,6 +97,17 @@ def test_tc_mlp_shapes_full_size(orc, N, K, B):
     assert torch.isfinite(y).all()
 
 
+def test_tc_prompt_batch_512(orc):
+    """A 512-row prompt batch (eight 64-row launches over the same weights):
+    sampled rows of every batch row against the oracle."""
+    N, K, B = 2048, 4096, 512
+    bits, scales, x = _problem(N, K, B, 7250)
+    y = _run_tc(bits, scales, x, N, K, B, y_dtype=b1.BF16)
+    rows = np.unique(np.concatenate([np.random.default_rng(512).choice(N, 96, replace=False), [0, N - 1]]))
+    ref = orc.gemv_select(bits, scales, x, B, N, K, rows)
+    assert_gemv_close(y[:, torch.from_numpy(rows).cuda()], ref, abs_bound(scales[rows], x, K), "tc B=512")
+
+
 def test_tc_row_flip_negates_exactly():
     """Negated weights flow through the same products and the same fixed
     accumulation order, so a flipped row gives the exact negation."""
