@@ -10,7 +10,9 @@ synthetic tensors with the same format stand in for them):
   * sign bits  : i.i.d. uniform bytes, i.e. i.i.d. Bernoulli(0.5) bits;
   * scales     : |N(0, 0.02)| drawn in fp32, rounded to fp16 (RNE), plus an
                  optional offset (1e-3 for the tiny case);
-  * activations: N(0, 1) drawn in fp32, rounded to bf16 (RNE).
+  * activations: N(0, 1) drawn in fp32, rounded to bf16 (RNE);
+  * ternary    : codes -1/0/+1 with 0 at probability 1/3 (a BitNet-like
+                 share of zeros), or two independent uniform sign planes.
 Every matrix has its own Philox stream keyed by ``seed``; activations use a
 separate key space so that a matrix and its input never share a stream.
 """
@@ -59,6 +61,24 @@ def matrix(N: int, K: int, seed: int, scale_offset: float = 0.0):
     bits = sign_bits(N, K, g)
     scales = group_scales(N, K, g, offset=scale_offset)
     return bits, scales
+
+
+def ternary_codes(N: int, K: int, gen: np.random.Generator, p_zero: float = 1.0 / 3.0) -> np.ndarray:
+    """Ternary codes [N, K] int8: 0 with probability ``p_zero``, otherwise -1
+    or +1 with equal probability."""
+    p = (1.0 - p_zero) / 2.0
+    return gen.choice(np.array([-1, 0, 1], dtype=np.int8), size=(N, K), p=[p, p_zero, p])
+
+
+def ternary_matrix(N: int, K: int, seed: int):
+    """(a, b, scales) of one synthetic ternary matrix given directly as two
+    independent uniform sign planes (every pair of bits is a valid code, so
+    this draws 0 with probability 1/2 and -1, +1 with 1/4 each)."""
+    g = rng(seed)
+    a = sign_bits(N, K, g)
+    b = sign_bits(N, K, g)
+    scales = group_scales(N, K, g)
+    return a, b, scales
 
 
 def x_for(B: int, K: int, seed: int) -> np.ndarray:

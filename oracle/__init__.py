@@ -57,6 +57,14 @@ def configure(lib):
     lib.orc_gemv.restype = ctypes.c_int
     lib.orc_gemv_select.argtypes = [p, p, p, i64, i64, i64, p, i64, p]
     lib.orc_gemv_select.restype = ctypes.c_int
+    lib.orc_gemv_ternary.argtypes = [p, p, p, p, i64, i64, i64, p]
+    lib.orc_gemv_ternary.restype = ctypes.c_int
+    lib.orc_gemv_ternary_select.argtypes = [p, p, p, p, i64, i64, i64, p, i64, p]
+    lib.orc_gemv_ternary_select.restype = ctypes.c_int
+    lib.orc_ternary_planes.argtypes = [p, i64, i64, p, p]
+    lib.orc_ternary_planes.restype = ctypes.c_int
+    lib.orc_ternary_footprint_bytes.argtypes = [i64, i64]
+    lib.orc_ternary_footprint_bytes.restype = i64
     lib.orc_gemv_threads.argtypes = [p, p, p, i64, i64, i64, p, ctypes.c_int]
     lib.orc_gemv_threads.restype = ctypes.c_int
     lib.orc_xor_patch.argtypes = [p, i64, i64, p, i64]
@@ -155,6 +163,42 @@ def gemv_select(bits, scales, x, B: int, N: int, K: int, rows) -> np.ndarray:
     if st != OK:
         raise OracleError(st, "gemv_select")
     return y
+
+
+def gemv_ternary(a, b, scales, x, B: int, N: int, K: int) -> np.ndarray:
+    """Ternary product from the two sign planes a, b (t = (a + b) / 2), [B, N]."""
+    a, b, scales, x = _u8(a), _u8(b), _u16(scales), _u16(x)
+    y = np.zeros((B, N), dtype=np.float64)
+    st = _load().orc_gemv_ternary(_ptr(a), _ptr(b), _ptr(scales), _ptr(x), B, N, K, _ptr(y))
+    if st != OK:
+        raise OracleError(st, "gemv_ternary")
+    return y
+
+
+def gemv_ternary_select(a, b, scales, x, B: int, N: int, K: int, rows) -> np.ndarray:
+    a, b, scales, x = _u8(a), _u8(b), _u16(scales), _u16(x)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    y = np.zeros((B, rows.size), dtype=np.float64)
+    st = _load().orc_gemv_ternary_select(_ptr(a), _ptr(b), _ptr(scales), _ptr(x), B, N, K,
+                                         _ptr(rows), rows.size, _ptr(y))
+    if st != OK:
+        raise OracleError(st, "gemv_ternary_select")
+    return y
+
+
+def ternary_planes(t, N: int, K: int):
+    """Codes [N, K] (int8 in {-1, 0, 1}) -> (a, b) planes [N, K/8] each."""
+    t = np.ascontiguousarray(np.asarray(t, dtype=np.int8)).reshape(-1)
+    a = np.zeros(N * K // 8, dtype=np.uint8)
+    b = np.zeros(N * K // 8, dtype=np.uint8)
+    st = _load().orc_ternary_planes(_ptr(t), N, K, _ptr(a), _ptr(b))
+    if st != OK:
+        raise OracleError(st, "ternary_planes")
+    return a.reshape(N, K // 8), b.reshape(N, K // 8)
+
+
+def ternary_footprint_bytes(N: int, K: int) -> int:
+    return int(_load().orc_ternary_footprint_bytes(N, K))
 
 
 def gemv_threads(bits, scales, x, B: int, N: int, K: int, nthreads: int) -> np.ndarray:

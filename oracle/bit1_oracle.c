@@ -16,8 +16,13 @@
  *  [27B-kern] same page, section "하이브리드 어텐션을 위한 저비트 커널":
  *             packed sign codes are decoded and the group FP16 scale is applied
  *             inside the fused matmul; accumulation stays in high precision.
+ *  [27B-ter]  same page, section "삼진(Ternary) 가중치 형식" (ternary weight
+ *             format): w_i = s_g * t_i, t_i in {-1, 0, +1}, one FP16 scale per
+ *             group of 128, b_eff ~ log2(3) + 16/128 ~ 1.71 bits/weight.
  *  [27B-store] same page, section "저장 공간과 실제 배포 크기": binary weights
- *             are deployed in the native 1-bit layout.
+ *             are deployed in the native 1-bit layout; today's kernels keep
+ *             each ternary value in a 2-bit slot (deployed ~7.2 GB against
+ *             the ~5.9 GB minimum).
  *  [Bankai]   "LocalLLaMA, true 1-bit LLM용 XOR patch 방식 \"Bankai\" 실험에 주목",
  *             section "LocalLLaMA가 본 핵심 포인트": a patch is a list of
  *             (layer, projection, row) entries whose binary weights are
@@ -39,6 +44,12 @@
  *  - K must be a positive multiple of 128.
  *  - a patch entry flips all K bits of its row; scales are untouched;
  *    duplicate rows flip once per occurrence.
+ *
+ * Ternary ([27B-ter], [27B-store]).  Reading of the 2-bit slot, which the
+ * pages do not lay out: two bit planes a and b, each in the binary layout
+ * above, with t = (a + b) / 2 when a bit is read as +-1 (bit 1 -> +1):
+ * (1,1) -> +1, (0,0) -> -1, (1,0) and (0,1) -> 0.  Codes to planes:
+ * a = (t >= 0), b = (t > 0).  Both planes share the one scale array.
  */
 #include <math.h>
 #include <pthread.h>
@@ -252,6 +263,113 @@ int orc_gemv_select(const uint8_t *bits, const uint16_t *scales,
     }
     free(tmp);
     return ORC_OK;
+}
+
+/* ---- ternary linear layer ------------------------------------------------
+ * y[b,n] = sum_g s[n,g] * sum_{k in group g} t(n,k) * x[b,k] ([27B-ter]);
+ * t read from the two planes one weight at a time; fp64 accumulation, the
+ * group partial first, then one multiply by the scale.  Rows [n0, n1). */
+static int orc_trit(const uint8_t *pa, const uint8_t *pb, int64_t K, int64_t n, int64_t k)
+{
+    int va = orc_bit(pa, K, n, k) ? 1 : -1;
+    int vb = orc_bit(pb, K, n, k) ? 1 : -1;
+    return (va + vb) / 2;
+}
+
+static void orc_gemv_ternary_rows(const uint8_t *pa, const uint8_t *pb, const uint16_t *scales,
+                                  const uint16_t *x, int64_t B, int64_t N, int64_t K,
+                                  int64_t n0, int64_t n1, double *y)
+{
+    int64_t G = K / 128;
+    for (int64_t b = 0; b < B; b++) {
+        for (int64_t n = n0; n < n1; n++) {
+            double acc = 0.0;
+            for (int64_t g = 0; g < G; g++) {
+                double s = orc_half_to_double(scales[n * G + g]);
+                double part = 0.0;
+                for (int64_t k = 128 * g; k < 128 * g + 128; k++) {
+                    int t = orc_trit(pa, pb, K, n, k);
+                    double xv = orc_bf16_to_double(x[b * K + k]);
+                    if (t > 0)
+                        part += xv;
+                    else if (t < 0)
+                        part -= xv;
+                }
+                acc += s * part;
+            }
+            y[b * N + n] = acc;
+        }
+    }
+}
+
+int orc_gemv_ternary(const uint8_t *pa, const uint8_t *pb, const uint16_t *scales,
+                     const uint16_t *x, int64_t B, int64_t N, int64_t K, double *y)
+{
+    int st = orc_check_shape(B, N, K);
+    if (st != ORC_OK)
+        return st;
+    if (!pa || !pb || !scales || !x || !y)
+        return ORC_EINVAL;
+    orc_gemv_ternary_rows(pa, pb, scales, x, B, N, K, 0, N, y);
+    return ORC_OK;
+}
+
+int orc_gemv_ternary_select(const uint8_t *pa, const uint8_t *pb, const uint16_t *scales,
+                            const uint16_t *x, int64_t B, int64_t N, int64_t K,
+                            const int64_t *rows, int64_t n_sel, double *y)
+{
+    int st = orc_check_shape(B, N, K);
+    double *tmp;
+    if (st != ORC_OK)
+        return st;
+    if (!pa || !pb || !scales || !x || !y || (n_sel > 0 && !rows))
+        return ORC_EINVAL;
+    for (int64_t i = 0; i < n_sel; i++)
+        if (rows[i] < 0 || rows[i] >= N)
+            return ORC_ERANGE;
+    tmp = (double *)malloc(sizeof(double) * (size_t)B * (size_t)N);
+    if (!tmp)
+        return ORC_EINVAL;
+    for (int64_t i = 0; i < n_sel; i++) {
+        int64_t n = rows[i];
+        orc_gemv_ternary_rows(pa, pb, scales, x, B, N, K, n, n + 1, tmp);
+        for (int64_t b = 0; b < B; b++)
+            y[b * n_sel + i] = tmp[b * N + n];
+    }
+    free(tmp);
+    return ORC_OK;
+}
+
+/* Ternary codes [N][K] (int8, each -1, 0 or +1) to the two planes, one
+ * weight at a time; ERANGE (planes untouched) if any code is another value. */
+int orc_ternary_planes(const int8_t *t, int64_t N, int64_t K, uint8_t *pa, uint8_t *pb)
+{
+    int st = orc_check_shape(1, N, K);
+    if (st != ORC_OK)
+        return st;
+    if (!t || !pa || !pb)
+        return ORC_EINVAL;
+    for (int64_t i = 0; i < N * K; i++)
+        if (t[i] < -1 || t[i] > 1)
+            return ORC_ERANGE;
+    memset(pa, 0, (size_t)(N * K / 8));
+    memset(pb, 0, (size_t)(N * K / 8));
+    for (int64_t n = 0; n < N; n++) {
+        for (int64_t k = 0; k < K; k++) {
+            int8_t v = t[n * K + k];
+            if (v >= 0)
+                pa[n * (K / 8) + k / 8] |= (uint8_t)(1u << (k % 8));
+            if (v > 0)
+                pb[n * (K / 8) + k / 8] |= (uint8_t)(1u << (k % 8));
+        }
+    }
+    return ORC_OK;
+}
+
+/* Bytes of a ternary matrix in 2-bit slots: two sign planes plus the scales. */
+int64_t orc_ternary_footprint_bytes(int64_t N, int64_t K)
+{
+    return 2 * (N * K / 8) + 2 * N * (K / 128);
 }
 
 /* Same function, rows split over `nthreads` POSIX threads: parallel dispatch

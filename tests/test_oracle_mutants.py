@@ -12,6 +12,15 @@ from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "bit1_oracle.c")
 
+# The binary and ternary row loops share their outer lines; these tails make
+# each mutation site unique.
+_BIN = "\n                double part = 0.0;\n                for (int64_t k = 128 * g; k < 128 * g + 128; k++) {\n                    double xv"
+_TER = "\n                double part = 0.0;\n                for (int64_t k = 128 * g; k < 128 * g + 128; k++) {\n                    int t"
+_SCALE = "double s = orc_half_to_double(scales[n * G + g]);"
+_SCALE_T = "double s = orc_half_to_double(scales[g * N + n]);"
+_XB = "double xv = orc_bf16_to_double(x[b * K + k]);\n                    if (orc_bit"
+_XT = "double xv = orc_bf16_to_double(x[b * K + k]);\n                    if (t > 0)"
+
 # (name, text in the source, replacement, pins expected to catch it)
 MUTANTS = [
     ("msb_first_bit_order", "return (bits[n * (K / 8) + k / 8] >> (k % 8)) & 1;",
@@ -21,14 +30,12 @@ MUTANTS = [
     ("sign_polarity", "if (orc_bit(bits, K, n, k))", "if (!orc_bit(bits, K, n, k))",
      [lambda o: pins.test_gemv_brute_force_matches_dense(o, 8, 256, 1, 0),
       lambda o: pins.test_closed_form_all_bits_set_and_clear(o)]),
-    ("scale_index_transposed", "double s = orc_half_to_double(scales[n * G + g]);",
-     "double s = orc_half_to_double(scales[g * N + n]);",
+    ("scale_index_transposed", _SCALE + _BIN, _SCALE_T + _BIN,
      [lambda o: pins.test_gemv_scales_are_per_row_and_group(o)]),
-    ("last_group_dropped", "for (int64_t g = 0; g < G; g++) {\n                double s",
-     "for (int64_t g = 0; g < G - 1; g++) {\n                double s",
+    ("last_group_dropped", "for (int64_t g = 0; g < G; g++) {\n                " + _SCALE + _BIN,
+     "for (int64_t g = 0; g < G - 1; g++) {\n                " + _SCALE + _BIN,
      [lambda o: pins.test_gemv_brute_force_matches_dense(o, 5, 256, 3, 1)]),
-    ("batch_row_ignored", "double xv = orc_bf16_to_double(x[b * K + k]);",
-     "double xv = orc_bf16_to_double(x[k]);",
+    ("batch_row_ignored", _XB, _XB.replace("x[b * K + k]", "x[k]"),
      [lambda o: pins.test_gemv_brute_force_matches_dense(o, 5, 256, 3, 1)]),
     ("half_exponent_bias", "v = ldexp((double)(m + 1024), e - 25);",
      "v = ldexp((double)(m + 1024), e - 24);",
@@ -49,6 +56,24 @@ MUTANTS = [
      [lambda o: pins.test_pack_bits_are_sign_test_little_endian(o)]),
     ("footprint_scale_bytes", "return N * K / 8 + 2 * N * (K / 128);", "return N * K / 8 + N * (K / 128);",
      [lambda o: pins.test_footprint_is_1_125_bits_per_weight(o)]),
+    ("ternary_scale_index_transposed", _SCALE + _TER, _SCALE_T + _TER,
+     [lambda o: pins.test_ternary_brute_force_matches_dense(o, 5, 256, 3, 0)]),
+    ("ternary_batch_row_ignored", _XT, _XT.replace("x[b * K + k]", "x[k]"),
+     [lambda o: pins.test_ternary_brute_force_matches_dense(o, 5, 256, 3, 0)]),
+    ("ternary_reads_one_plane", "return (va + vb) / 2;", "return va;",
+     [lambda o: pins.test_ternary_brute_force_matches_dense(o, 5, 256, 3, 0),
+      lambda o: pins.test_ternary_all_zero_codes_give_exact_zero(o)]),
+    ("ternary_zero_subtracts", "else if (t < 0)\n                        part -= xv;",
+     "else if (t <= 0)\n                        part -= xv;",
+     [lambda o: pins.test_ternary_brute_force_matches_dense(o, 5, 256, 3, 0),
+      lambda o: pins.test_ternary_single_code_closed_form(o)]),
+    ("ternary_planes_threshold", "if (v >= 0)\n                pa", "if (v > 0)\n                pa",
+     [lambda o: pins.test_ternary_planes_match_numpy(o)]),
+    ("ternary_codes_unchecked", "if (t[i] < -1 || t[i] > 1)", "if (t[i] < -2 || t[i] > 2)",
+     [lambda o: pins.test_ternary_planes_reject_other_codes(o, 2)]),
+    ("ternary_footprint_one_plane", "return 2 * (N * K / 8) + 2 * N * (K / 128);",
+     "return (N * K / 8) + 2 * N * (K / 128);",
+     [lambda o: pins.test_ternary_footprint_and_printed_sizes(o)]),
 ]
 
 
@@ -68,7 +93,7 @@ def test_mutant_is_caught(tmp_path, name, old, new, checks):
         for chk in checks:
             try:
                 chk(oracle)
-            except (AssertionError, oracle.OracleError):
+            except (AssertionError, oracle.OracleError, pytest.fail.Exception):
                 caught += 1
     finally:
         oracle._lib = saved

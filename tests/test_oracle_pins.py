@@ -390,3 +390,148 @@ def test_patch_list_size_is_kilobyte_scale():
     assert len(set(entries)) == 100
     payload = len(entries) * (2 + 1 + 4)
     assert fig["min"] / 2 <= payload <= fig["max"]
+
+
+# ---------------------------------------------------------------- ternary
+
+def _np_planes(t):
+    """Independent encoding route: numpy's little-endian packbits of the two
+    threshold masks a = (t >= 0), b = (t > 0)."""
+    a = np.packbits((t >= 0).astype(np.uint8), axis=1, bitorder="little")
+    b = np.packbits((t > 0).astype(np.uint8), axis=1, bitorder="little")
+    return a, b
+
+
+def _dense_ternary(t, scales, x, N, K):
+    s = scales.reshape(N, K // 128).view(np.float16).astype(np.float64)
+    W = t.astype(np.float64) * np.repeat(s, 128, axis=1)
+    X = torch.from_numpy(x.reshape(-1, K).view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    return X @ W.T, W, X
+
+
+def test_ternary_planes_match_numpy(orc):
+    N, K = 6, 384
+    t = synth.ternary_codes(N, K, synth.rng(700))
+    a, b = orc.ternary_planes(t, N, K)
+    na, nb = _np_planes(t)
+    assert np.array_equal(a, na) and np.array_equal(b, nb)
+    # decoding the planes with numpy gives the codes back
+    ua = np.unpackbits(a, axis=1, bitorder="little").astype(np.int64) * 2 - 1
+    ub = np.unpackbits(b, axis=1, bitorder="little").astype(np.int64) * 2 - 1
+    assert np.array_equal((ua + ub) // 2, t.astype(np.int64))
+
+
+@pytest.mark.parametrize("bad", [2, -2, 127, -128])
+def test_ternary_planes_reject_other_codes(orc, bad):
+    import oracle
+    N, K = 2, 128
+    t = np.zeros((N, K), dtype=np.int8)
+    t[1, 77] = bad
+    with pytest.raises(oracle.OracleError) as e:
+        orc.ternary_planes(t, N, K)
+    assert e.value.status == 3
+
+
+@pytest.mark.parametrize("N,K,B", [(1, 128, 1), (3, 128, 2), (5, 256, 3), (7, 384, 2)])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_ternary_brute_force_matches_dense(orc, N, K, B, seed):
+    """The product through the planes equals a dense fp64 matmul of the codes
+    times the group scales (the ternary weight definition), with planes made
+    by numpy, not by the oracle."""
+    g = synth.rng(710 + seed)
+    t = synth.ternary_codes(N, K, g)
+    scales = synth.group_scales(N, K, g, offset=1e-3)
+    x = synth.activations(B, K, g)
+    a, b = _np_planes(t)
+    y = orc.gemv_ternary(a, b, scales, x, B, N, K)
+    ref, W, X = _dense_ternary(t, scales, x, N, K)
+    tol = 1e-12 * (np.abs(X) @ np.abs(W).T) + 1e-300
+    assert np.all(np.abs(y - ref) <= tol)
+
+
+def test_ternary_without_zeros_is_the_binary_product(orc):
+    """a == b means every code is +-1: the ternary layer is then the binary
+    layer with those bits (same summation order, so bit-identical)."""
+    N, K, B = 9, 512, 3
+    bits, scales = synth.matrix(N, K, 720)
+    x = synth.x_for(B, K, 720)
+    assert np.array_equal(orc.gemv_ternary(bits, bits, scales, x, B, N, K),
+                          orc.gemv(bits, scales, x, B, N, K))
+
+
+def test_ternary_all_zero_codes_give_exact_zero(orc):
+    N, K, B = 4, 256, 2
+    a, _, scales = synth.ternary_matrix(N, K, 721)
+    x = synth.x_for(B, K, 721)
+    y = orc.gemv_ternary(a, ~a, scales, x, B, N, K)
+    assert np.all(y == 0.0)
+
+
+def test_ternary_single_code_closed_form(orc):
+    """One +1 and one -1 in an otherwise zero row: y = s_g1 x_k1 - s_g2 x_k2."""
+    N, K = 2, 384
+    t = np.zeros((N, K), dtype=np.int8)
+    t[1, 5] = 1
+    t[1, 300] = -1
+    scales = np.array([0x3C00, 0x3C00, 0x3C00, 0x4000, 0x3800, 0x4400], dtype=np.uint16)  # 1,1,1 / 2,0.5,4
+    x = synth.activations(1, K, synth.rng(722))
+    xv = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).double().numpy().reshape(K)
+    a, b = _np_planes(t)
+    y = orc.gemv_ternary(a, b, scales, x, 1, N, K)
+    assert y[0, 0] == 0.0
+    assert y[0, 1] == 2.0 * xv[5] - 4.0 * xv[300]
+
+
+def test_ternary_flipping_both_planes_negates_exactly(orc):
+    """XOR of a row in both planes maps +1 <-> -1 and keeps 0 (1,0 <-> 0,1):
+    that output row is negated exactly, the others are unchanged."""
+    N, K, B = 6, 256, 2
+    a, b, scales = synth.ternary_matrix(N, K, 723)
+    x = synth.x_for(B, K, 723)
+    y0 = orc.gemv_ternary(a, b, scales, x, B, N, K)
+    rows = [1, 4]
+    a1, b1 = orc.xor_patch(a, N, K, rows), orc.xor_patch(b, N, K, rows)
+    y1 = orc.gemv_ternary(a1, b1, scales, x, B, N, K)
+    for n in range(N):
+        assert np.array_equal(y1[:, n], -y0[:, n] if n in rows else y0[:, n])
+
+
+def test_ternary_select_matches_full(orc):
+    N, K, B = 10, 256, 3
+    a, b, scales = synth.ternary_matrix(N, K, 724)
+    x = synth.x_for(B, K, 724)
+    full = orc.gemv_ternary(a, b, scales, x, B, N, K)
+    rows = [9, 0, 3, 3]
+    assert np.array_equal(orc.gemv_ternary_select(a, b, scales, x, B, N, K, rows), full[:, rows])
+
+
+def test_ternary_rejects_bad_shapes(orc):
+    import oracle
+    a, b, scales = synth.ternary_matrix(2, 128, 725)
+    x = synth.x_for(1, 128, 725)
+    for B, N, K in [(1, 2, 100), (0, 2, 128), (1, 0, 128)]:
+        with pytest.raises(oracle.OracleError):
+            orc.gemv_ternary(a, b, scales, x, B, N, K)
+    with pytest.raises(oracle.OracleError):
+        orc.gemv_ternary_select(a, b, scales, x, 1, 2, 128, [2])
+
+
+def test_ternary_footprint_and_printed_sizes(orc):
+    """2-bit slots with one fp16 scale per 128 inputs are 2.125 bits/weight;
+    the pages' ideal ternary cost log2(3) + 16/128 prints as 1.71 bits and
+    9.4x against fp16; over the 27B parameter split it gives the printed
+    5.9 GB, and the 2-bit slots give 7.37 GB, the pages' 'about 7.2 GB'."""
+    fig = json.load(open(GOLDEN))
+    N, K = 5120, 17408
+    assert orc.ternary_footprint_bytes(N, K) * 8 == 2.125 * N * K
+    assert orc.ternary_footprint_bytes(N, K) == 2 * orc.footprint_bytes(N, K) - 2 * N * (K // 128)
+    ideal = np.log2(3.0) + 16.0 / 128.0
+    assert round(ideal, 2) == fig["b_eff_ternary_bits_per_weight"]["value"]
+    assert round(16.0 / fig["b_eff_ternary_bits_per_weight"]["value"], 1) == fig["compression_ternary_vs_fp16"]["value"]
+    sp = fig["bonsai_27b_parameter_split"]
+    total = sp["language_model"] + sp["vision_tower"] + sp["embedding_and_lm_head"]
+    assert round(total * fig["b_eff_ternary_bits_per_weight"]["value"] / 8 / 1e9, 1) == \
+        fig["bonsai_27b_ternary_gigabytes"]["value"]
+    slot_bpw = orc.ternary_footprint_bytes(128, 128) * 8 / (128 * 128)
+    deployed = total * slot_bpw / 8 / 1e9
+    assert deployed == pytest.approx(fig["bonsai_27b_ternary_deployed_gigabytes"]["value"], rel=0.03)
