@@ -394,6 +394,39 @@ def extra_c5_sweep_27b(torch, b1, steps=20):
     return out
 
 
+def extra_ternary_sweep_8b(torch, b1, steps=20):
+    """Ternary 8B-class sweep in 2-bit slots (two sign planes per matrix,
+    2.1 GB with the scales): one grouped launch over both planes of all 253
+    matrices plus one combine launch per step."""
+    from bit_weight_gemv_sign_b300 import synth
+    from bit_weight_gemv_sign_b300.sweep import TernarySweep
+    sw = TernarySweep(synth.sweep_8b(), seed0=0, y_dtype=b1.BF16).fill_device(38)
+    plan = sw.group_plan()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            plan.run(stream=s)
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            plan.run(stream=s)
+        e1.record(s)
+        e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    hbm, _ = _peaks()
+    gbs = sw.weight_bytes / (ms * 1e-3) / 1e9
+    params = sum(m.N * m.K for m in sw.mats)
+    out = {"weight_bytes": sw.weight_bytes, "bits_per_weight": 8.0 * sw.weight_bytes / params,
+           "ms_per_step": ms, "weight_gbs": gbs, "hbm_frac": gbs / hbm, "tok_s_equiv": 1e3 / ms,
+           "launches_per_step": sw.launches_per_step(),
+           "note": "algorithmic bytes count the shared scales once; the two binary passes read "
+                   "them twice (2.25 bits/weight of traffic)"}
+    del sw, plan
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_mine(args):
     import torch
     import bit_weight_gemv_sign_b300 as b1
@@ -532,7 +565,8 @@ def run_mine(args):
                          "c2_projections_b1": extra_c2_projections(torch, b1),
                          "c4_mlp_crossover": extra_c4_crossover(torch, b1),
                          "pp512_tcgen05": extra_pp512(torch, b1),
-                         "c5_sweep_27b": extra_c5_sweep_27b(torch, b1)}
+                         "c5_sweep_27b": extra_c5_sweep_27b(torch, b1),
+                         "ternary_sweep_8b": extra_ternary_sweep_8b(torch, b1)}
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
         oracle.build()

@@ -20,6 +20,8 @@ __all__ = [
     "bit1_xor_patch", "bit1_status_str", "bit1_version", "bit1_device_wait_timeouts",
     "bit1_group_plan_bytes", "bit1_group_plan", "bit1_gemv_group", "GroupPlan",
     "library_path", "load", "bit1_gemv_tc_noalloc",
+    "bit1_ternary_planes", "bit1_gemv_ternary", "bit1_gemv_ternary_workspace_bytes",
+    "bit1_gemv_ternary_launches", "bit1_ternary_combine",
 ]
 
 OK, EINVAL, ESHAPE, ERANGE, ECUDA, ENAN = 0, 1, 2, 3, 4, 5
@@ -91,6 +93,16 @@ def load():
         lib.bit1_gemv_group.restype = i32
         lib.bit1_gemv_tc_noalloc.argtypes = [p, p, p, i64, i64, i64, p, i32, ctypes.c_uint, p]
         lib.bit1_gemv_tc_noalloc.restype = i32
+        lib.bit1_ternary_planes.argtypes = [p, i64, i64, p, p, p, p]
+        lib.bit1_ternary_planes.restype = i32
+        lib.bit1_gemv_ternary_workspace_bytes.argtypes = [i64, i64, i64]
+        lib.bit1_gemv_ternary_workspace_bytes.restype = sz
+        lib.bit1_gemv_ternary.argtypes = [p, p, p, p, i64, i64, i64, p, i32, p, sz, i32, ctypes.c_uint, p]
+        lib.bit1_gemv_ternary.restype = i32
+        lib.bit1_gemv_ternary_launches.argtypes = [i64, i64, i64, i32]
+        lib.bit1_gemv_ternary_launches.restype = i32
+        lib.bit1_ternary_combine.argtypes = [p, p, i64, p, i32, p]
+        lib.bit1_ternary_combine.restype = i32
         _lib = lib
         return lib
 
@@ -286,3 +298,67 @@ class GroupPlan:
 
     def run(self, flags: int = 0, stream=None) -> None:
         bit1_gemv_group(self.dev.data_ptr(), self.host.ctypes.data, flags, stream)
+
+
+# ---------------------------------------------------------------- ternary (2-bit slots)
+
+def bit1_ternary_planes(codes, a=None, b=None, flags=None, stream=None):
+    """Ternary codes int8 [N, K] (CUDA, each -1/0/+1) -> sign planes (a, b),
+    uint8 [N, K/8] each, with t = (a + b) / 2.  ``flags`` (int32 [1] CUDA
+    tensor) receives the code-range flag (``bit1_pack_flags_status``)."""
+    import torch
+    N, K = codes.shape
+    if a is None:
+        a = torch.empty((N, K // 8), dtype=torch.uint8, device=codes.device)
+    if b is None:
+        b = torch.empty((N, K // 8), dtype=torch.uint8, device=codes.device)
+    st = load().bit1_ternary_planes(_dptr(codes, "codes", (torch.int8,)), N, K, _dptr(a, "a"),
+                                    _dptr(b, "b"), _dptr(flags, "flags"), _stream(stream))
+    _check(st, "bit1_ternary_planes")
+    return a, b
+
+
+def bit1_gemv_ternary_workspace_bytes(B: int, N: int, K: int) -> int:
+    return int(load().bit1_gemv_ternary_workspace_bytes(B, N, K))
+
+
+def bit1_gemv_ternary_launches(B: int, N: int, K: int, variant: int = AUTO) -> int:
+    return int(load().bit1_gemv_ternary_launches(B, N, K, int(variant)))
+
+
+def bit1_gemv_ternary(a, b, scales, x, y=None, y_dtype=None, workspace=None, variant=AUTO, flags=0,
+                      stream=None, N=None, K=None):
+    """y[B, N] = x[B, K] (bf16) times the ternary matrix given by its planes
+    a, b (uint8 [N, K/8]) and scales [N, K/128].  ``workspace`` defaults to
+    a fresh buffer of bit1_gemv_ternary_workspace_bytes bytes."""
+    import torch
+    B = x.shape[0] if x.dim() == 2 else 1
+    K = x.shape[-1] if K is None else K
+    N = a.shape[0] if N is None else N
+    if y is None:
+        yt = torch.bfloat16 if y_dtype == BF16 else torch.float32
+        y = torch.empty((B, N), dtype=yt, device=x.device)
+    if y.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("y must be float32 or bfloat16")
+    ydt = BF16 if y.dtype == torch.bfloat16 else F32
+    if workspace is None:
+        workspace = torch.empty(max(bit1_gemv_ternary_workspace_bytes(B, N, K), 256),
+                                dtype=torch.uint8, device=x.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = load().bit1_gemv_ternary(_dptr(a, "a"), _dptr(b, "b"), _dptr(scales, "scales"), _dptr(x, "x"),
+                                  B, N, K, _dptr(y, "y"), ydt, _dptr(workspace, "workspace"), ws_bytes,
+                                  int(variant), int(flags), _stream(stream))
+    _check(st, "bit1_gemv_ternary")
+    return y
+
+
+def bit1_ternary_combine(ya, yb, y, stream=None) -> None:
+    """y = (ya + yb) / 2 elementwise; ya, yb fp32, y fp32 or bf16, same length."""
+    import torch
+    n = ya.numel()
+    if yb.numel() != n or y.numel() != n:
+        raise ValueError("ya, yb and y must have the same number of elements")
+    ydt = BF16 if y.dtype == torch.bfloat16 else F32
+    st = load().bit1_ternary_combine(_dptr(ya, "ya", (torch.float32,)), _dptr(yb, "yb", (torch.float32,)),
+                                     n, _dptr(y, "y", (torch.float32, torch.bfloat16)), ydt, _stream(stream))
+    _check(st, "bit1_ternary_combine")

@@ -82,48 +82,76 @@ bit1_status bit1_pack(const void* w, int w_dtype, int64_t N, int64_t K, uint8_t*
 
 bit1_status bit1_pack_flags_status(uint32_t flags) {
     if (flags & 1u) return BIT1_ENAN;
-    if (flags & 2u) return BIT1_ERANGE;
+    if (flags & 6u) return BIT1_ERANGE;
     return BIT1_OK;
 }
 
-bit1_status bit1_gemv_ex(const uint8_t* bits, const uint16_t* scales, const uint16_t* x,
-                         int64_t B, int64_t N, int64_t K, void* y, int y_dtype, void* workspace,
-                         size_t ws_bytes, int variant, unsigned flags, bit1_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Everything bit1_gemv_ex checks before launching: the status it would
+// return, with `variant` resolved (AUTO -> the pick for this shape).
+bit1_status gemv_check(const uint8_t* bits, const uint16_t* scales, const uint16_t* x, int64_t B,
+                       int64_t N, int64_t K, const void* y, int y_dtype, const void* workspace,
+                       size_t ws_bytes, int* variant, unsigned flags) {
     if (!shape_ok(B, N, K)) return BIT1_ESHAPE;
     if (!bits || !scales || !x || !y) return BIT1_EINVAL;
     if (!aligned16(bits) || !aligned16(scales) || !aligned16(x) || !aligned16(y)) return BIT1_EINVAL;
     if (y_dtype != BIT1_F32 && y_dtype != BIT1_BF16) return BIT1_EINVAL;
     if (ws_bytes > 0 && (!workspace || !aligned16(workspace))) return BIT1_EINVAL;
     if (flags & ~BIT1_FLAG_PDL) return BIT1_EINVAL;
-    if (variant == BIT1_GEMV_AUTO) variant = pick_variant(B, N, K, ws_bytes);
+    if (*variant == BIT1_GEMV_AUTO) *variant = pick_variant(B, N, K, ws_bytes);
+    switch (*variant) {
+        case BIT1_GEMV_SIMPLE: return BIT1_OK;
+        case BIT1_GEMV_LUT: return lut_supported(B, N, K) ? BIT1_OK : BIT1_ESHAPE;
+        case BIT1_GEMV_LUT6: return t6_supported(B, N, K) ? BIT1_OK : BIT1_ESHAPE;
+        case BIT1_GEMV_STREAM: return group1_supported(B, N, K) ? BIT1_OK : BIT1_ESHAPE;
+        case BIT1_GEMV_TC:
+            if (!tc_supported(B, N, K)) return BIT1_ESHAPE;
+            return ws_bytes < tc_workspace_bytes(B, N, K) ? BIT1_EINVAL : BIT1_OK;
+        case BIT1_GEMV_SPLITK: return BIT1_ESHAPE;  // not available for any shape in this build
+        default: return BIT1_EINVAL;
+    }
+}
+
+// Launch a checked call (variant already resolved).
+bit1_status gemv_run(const uint8_t* bits, const uint16_t* scales, const uint16_t* x, int64_t B,
+                     int64_t N, int64_t K, void* y, int y_dtype, void* workspace, size_t ws_bytes,
+                     int variant, unsigned flags, cudaStream_t stream) {
     GemvArgs a;
     a.bits = bits; a.scales = scales; a.x = x;
     a.B = B; a.N = N; a.K = K;
     a.y = y; a.y_bf16 = (y_dtype == BIT1_BF16);
     a.workspace = workspace; a.ws_bytes = ws_bytes;
     a.pdl = (flags & BIT1_FLAG_PDL) != 0;
-    a.stream = (cudaStream_t)stream;
+    a.stream = stream;
     switch (variant) {
-        case BIT1_GEMV_SIMPLE:
-            return from_cuda(launch_gemv_simple(a));
-        case BIT1_GEMV_LUT:
-            if (!lut_supported(B, N, K)) return BIT1_ESHAPE;
-            return from_cuda(launch_gemv_lut(a));
-        case BIT1_GEMV_LUT6:
-            if (!t6_supported(B, N, K)) return BIT1_ESHAPE;
-            return from_cuda(launch_gemv_t6(a));
-        case BIT1_GEMV_STREAM:
-            if (!group1_supported(B, N, K)) return BIT1_ESHAPE;
-            return from_cuda(launch_gemv_group1(a));
-        case BIT1_GEMV_TC:
-            if (!tc_supported(B, N, K)) return BIT1_ESHAPE;
-            if (ws_bytes < tc_workspace_bytes(B, N, K)) return BIT1_EINVAL;
-            return from_cuda(launch_gemv_tc(a));
-        case BIT1_GEMV_SPLITK:
-            return BIT1_ESHAPE;  // not available for any shape in this build
-        default:
-            return BIT1_EINVAL;
+        case BIT1_GEMV_SIMPLE: return from_cuda(launch_gemv_simple(a));
+        case BIT1_GEMV_LUT: return from_cuda(launch_gemv_lut(a));
+        case BIT1_GEMV_LUT6: return from_cuda(launch_gemv_t6(a));
+        case BIT1_GEMV_STREAM: return from_cuda(launch_gemv_group1(a));
+        case BIT1_GEMV_TC: return from_cuda(launch_gemv_tc(a));
+        default: return BIT1_EINVAL;
     }
+}
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// fp32 scratch of one half of a ternary product.
+size_t ternary_half_bytes(int64_t B, int64_t N) { return align256((size_t)B * (size_t)N * sizeof(float)); }
+
+}  // namespace
+
+extern "C" {
+
+bit1_status bit1_gemv_ex(const uint8_t* bits, const uint16_t* scales, const uint16_t* x,
+                         int64_t B, int64_t N, int64_t K, void* y, int y_dtype, void* workspace,
+                         size_t ws_bytes, int variant, unsigned flags, bit1_stream_t stream) {
+    bit1_status st = gemv_check(bits, scales, x, B, N, K, y, y_dtype, workspace, ws_bytes, &variant, flags);
+    if (st != BIT1_OK) return st;
+    return gemv_run(bits, scales, x, B, N, K, y, y_dtype, workspace, ws_bytes, variant, flags,
+                    (cudaStream_t)stream);
 }
 
 bit1_status bit1_gemv(const uint8_t* bits, const uint16_t* scales, const uint16_t* x, int64_t B,
@@ -193,6 +221,62 @@ size_t bit1_group_plan_bytes(int count) { return group_plan_bytes(count); }
 bit1_status bit1_group_plan(const bit1_gemv_problem* problems, int count, void* host_plan,
                             size_t plan_bytes) {
     return group_plan(problems, count, host_plan, plan_bytes);
+}
+
+bit1_status bit1_ternary_planes(const int8_t* codes, int64_t N, int64_t K, uint8_t* a, uint8_t* b,
+                                uint32_t* d_flags, bit1_stream_t stream) {
+    if (!shape_ok(1, N, K)) return BIT1_ESHAPE;
+    if (!codes || !a || !b) return BIT1_EINVAL;
+    if (!aligned16(codes) || !aligned16(a) || !aligned16(b)) return BIT1_EINVAL;
+    if (d_flags && ((uintptr_t)d_flags & 3u)) return BIT1_EINVAL;
+    return from_cuda(launch_ternary_planes(codes, N, K, a, b, d_flags, (cudaStream_t)stream));
+}
+
+size_t bit1_gemv_ternary_workspace_bytes(int64_t B, int64_t N, int64_t K) {
+    if (!shape_ok(B, N, K)) return 0;
+    return 2 * ternary_half_bytes(B, N) + bit1_gemv_workspace_bytes(B, N, K);
+}
+
+bit1_status bit1_gemv_ternary(const uint8_t* a, const uint8_t* b, const uint16_t* scales,
+                              const uint16_t* x, int64_t B, int64_t N, int64_t K, void* y,
+                              int y_dtype, void* workspace, size_t ws_bytes, int variant,
+                              unsigned flags, bit1_stream_t stream) {
+    if (!shape_ok(B, N, K)) return BIT1_ESHAPE;
+    if (!a || !b || !aligned16(a) || !aligned16(b)) return BIT1_EINVAL;
+    if (!workspace || !aligned16(workspace)) return BIT1_EINVAL;
+    const size_t half = ternary_half_bytes(B, N);
+    if (ws_bytes < 2 * half) return BIT1_EINVAL;
+    float* ya = reinterpret_cast<float*>(workspace);
+    float* yb = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + half);
+    void* rest = static_cast<uint8_t*>(workspace) + 2 * half;
+    const size_t rest_bytes = ws_bytes - 2 * half;
+    if (!y || !aligned16(y) || (y_dtype != BIT1_F32 && y_dtype != BIT1_BF16)) return BIT1_EINVAL;
+    // Both halves take the same checks (only the bits pointer differs).
+    bit1_status st = gemv_check(a, scales, x, B, N, K, ya, BIT1_F32, rest_bytes ? rest : nullptr,
+                                rest_bytes, &variant, flags);
+    if (st != BIT1_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    st = gemv_run(a, scales, x, B, N, K, ya, BIT1_F32, rest, rest_bytes, variant, flags, s);
+    if (st != BIT1_OK) return st;
+    st = gemv_run(b, scales, x, B, N, K, yb, BIT1_F32, rest, rest_bytes, variant, flags, s);
+    if (st != BIT1_OK) return st;
+    return from_cuda(launch_ternary_combine(ya, yb, B * N, y, y_dtype == BIT1_BF16, s));
+}
+
+int bit1_gemv_ternary_launches(int64_t B, int64_t N, int64_t K, int variant) {
+    if (!shape_ok(B, N, K)) return 0;
+    if (variant == BIT1_GEMV_AUTO)
+        variant = pick_variant(B, N, K, bit1_gemv_workspace_bytes(B, N, K));
+    const int one = bit1_gemv_launches(B, N, K, variant);
+    return one ? 2 * one + 1 : 0;
+}
+
+bit1_status bit1_ternary_combine(const float* ya, const float* yb, int64_t n, void* y, int y_dtype,
+                                 bit1_stream_t stream) {
+    if (n < 1) return BIT1_ESHAPE;
+    if (!ya || !yb || !y || !aligned16(ya) || !aligned16(yb) || !aligned16(y)) return BIT1_EINVAL;
+    if (y_dtype != BIT1_F32 && y_dtype != BIT1_BF16) return BIT1_EINVAL;
+    return from_cuda(launch_ternary_combine(ya, yb, n, y, y_dtype == BIT1_BF16, (cudaStream_t)stream));
 }
 
 bit1_status bit1_gemv_group(const void* device_plan, const void* host_plan, unsigned flags,

@@ -64,6 +64,12 @@ int tc_launch_count(int64_t B, int64_t N, int64_t K);
 cudaError_t launch_gemv_tc(const GemvArgs& a);
 unsigned int tc_take_timeouts();
 
+// Ternary weights in 2-bit slots (ternary.cu).
+cudaError_t launch_ternary_planes(const int8_t* codes, int64_t N, int64_t K, uint8_t* a, uint8_t* b,
+                                  uint32_t* flags, cudaStream_t stream);
+cudaError_t launch_ternary_combine(const float* ya, const float* yb, int64_t n, void* y, bool y_bf16,
+                                   cudaStream_t stream);
+
 int sm_count();
 
 }  // namespace bit1

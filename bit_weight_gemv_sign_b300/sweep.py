@@ -19,7 +19,7 @@ import torch
 
 from . import synth
 from . import (BF16, F32, FLAG_PDL, AUTO, GroupPlan, bit1_gemv_ex, bit1_gemv_launches,
-               bit1_xor_patch)
+               bit1_ternary_combine, bit1_xor_patch)
 
 
 def _align(n: int, a: int = 256) -> int:
@@ -152,3 +152,88 @@ class Sweep:
             m = self.mats[i]
             bit1_xor_patch(self.bits_of(i), rows, N=m.N, K=m.K)
         return by_mat
+
+
+class TernaryPlan:
+    """A grouped launch over both sign planes of every ternary matrix (two
+    problems per matrix, fp32 halves into one contiguous arena each) and one
+    combine launch that forms y = (ya + yb) / 2 over the whole arena."""
+
+    def __init__(self, sweep: "TernarySweep"):
+        sw = sweep
+        probs = []
+        for i in range(len(sw.mats)):
+            probs.append((sw.bits_of(i), sw.scales_of(i), sw.x_of(i), sw.half_of(sw.ya, i)))
+            probs.append((sw.bits_b_of(i), sw.scales_of(i), sw.x_of(i), sw.half_of(sw.yb, i)))
+        self.sweep = sw
+        self.group = GroupPlan(probs, device=sw.device)
+
+    def run(self, flags: int = 0, stream=None) -> None:
+        self.group.run(flags=flags, stream=stream)
+        sw = self.sweep
+        bit1_ternary_combine(sw.ya, sw.yb, sw.yt, stream=stream)
+
+
+class TernarySweep(Sweep):
+    """The same decode sweep with ternary weights in 2-bit slots: two sign
+    planes per matrix (t = (a + b) / 2) sharing one scale array; batch 1.
+    Outputs are laid out contiguously (row offsets rounded up to 64) so that
+    one combine launch serves every matrix."""
+
+    def __init__(self, mats, seed0: int = 0, y_dtype: int = BF16, device: str = "cuda"):
+        super().__init__(mats, seed0=seed0, batch=1, y_dtype=y_dtype, device=device)
+        self.bits_b = torch.empty_like(self.bits)
+        self.row_off = []
+        nr = 0
+        for m in self.mats:
+            self.row_off.append(nr)
+            nr += _align(m.N, 64)
+        self.rows_total = nr
+        self.ya = torch.empty(nr, dtype=torch.float32, device=device)
+        self.yb = torch.empty(nr, dtype=torch.float32, device=device)
+        self.yt = torch.empty(nr, dtype=torch.bfloat16 if y_dtype == BF16 else torch.float32, device=device)
+        self.weight_bytes = sum(2 * (m.N * m.K // 8) + 2 * m.N * (m.K // 128) for m in self.mats)
+
+    def bits_b_of(self, i):
+        m = self.mats[i]
+        return self.bits_b[self.bits_off[i]: self.bits_off[i] + m.N * m.K // 8].view(m.N, m.K // 8)
+
+    def half_of(self, arena, i):
+        return arena[self.row_off[i]: self.row_off[i] + self.mats[i].N].view(1, self.mats[i].N)
+
+    def y_of(self, i, ybuf=None):
+        return self.half_of(self.yt if ybuf is None else ybuf, i)
+
+    def host_matrix(self, i):
+        """(a, b, scales, x) of ternary matrix i, seeded."""
+        m = self.mats[i]
+        a, b, scales = synth.ternary_matrix(m.N, m.K, self.seed0 + i)
+        x = synth.x_for(1, m.K, self.seed0 + i)
+        return a, b, scales, x
+
+    def fill(self):
+        for i in range(len(self.mats)):
+            a, b, scales, x = self.host_matrix(i)
+            self.bits_of(i).copy_(torch.from_numpy(a))
+            self.bits_b_of(i).copy_(torch.from_numpy(b))
+            self.scales_of(i).copy_(torch.from_numpy(scales.view(np.int16)))
+            self.x_of(i).copy_(torch.from_numpy(x.view(np.int16)).view(torch.bfloat16))
+        torch.cuda.synchronize()
+        return self
+
+    def fill_device(self, seed: int = 0):
+        super().fill_device(seed)
+        g = torch.Generator(device=self.device)
+        g.manual_seed(seed + 1)
+        self.bits_b.copy_(torch.randint(0, 256, self.bits_b.shape, dtype=torch.uint8, device=self.device,
+                                        generator=g))
+        torch.cuda.synchronize()
+        return self
+
+    def launches_per_step(self) -> int:
+        return 2
+
+    def group_plan(self, x=None, y=None):
+        if x is not None or y is not None:
+            raise ValueError("a ternary sweep has one I/O slot")
+        return TernaryPlan(self)

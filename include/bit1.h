@@ -51,7 +51,7 @@ typedef enum bit1_status {
     BIT1_OK = 0,
     BIT1_EINVAL = 1, /* null or misaligned pointer, unknown dtype/variant, bad count */
     BIT1_ESHAPE = 2, /* B, N < 1; K not a positive multiple of 128; shape beyond a variant's limits */
-    BIT1_ERANGE = 3, /* patch row outside [0, N); packed scale not finite */
+    BIT1_ERANGE = 3, /* patch row outside [0, N); packed scale not finite; ternary code not -1/0/+1 */
     BIT1_ECUDA = 4,  /* a CUDA runtime call or kernel launch failed */
     BIT1_ENAN = 5    /* NaN among the weights given to bit1_pack */
 } bit1_status;
@@ -106,7 +106,8 @@ bit1_status bit1_pack(const void *w, int w_dtype, int64_t N, int64_t K,
                       uint8_t *bits, uint16_t *scales, uint32_t *d_flags,
                       bit1_stream_t stream);
 
-/* BIT1_ENAN if bit 0 is set, else BIT1_ERANGE if bit 1 is set, else BIT1_OK. */
+/* BIT1_ENAN if bit 0 is set, else BIT1_ERANGE if bit 1 (bit1_pack) or bit 2
+ * (bit1_ternary_planes) is set, else BIT1_OK. */
 bit1_status bit1_pack_flags_status(uint32_t flags);
 
 /* ------------------------------------------------------------------------
@@ -235,6 +236,66 @@ bit1_status bit1_gemv_tc_noalloc(const uint8_t *bits, const uint16_t *scales,
                                  const uint16_t *x, int64_t B, int64_t N, int64_t K,
                                  void *y, int y_dtype, unsigned flags,
                                  bit1_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Ternary weights in 2-bit slots (page "Bonsai 27B: ...", section
+ * "삼진(Ternary) 가중치 형식": w = s_g * t with t in {-1, 0, +1} and one FP16
+ * scale per 128 inputs; section "저장 공간과 실제 배포 크기": the current
+ * kernels keep each ternary value in a 2-bit slot, 2.125 bits/weight with the
+ * scales, against the log2(3) + 16/128 ~ 1.71 bits of the ideal code).
+ * This library's reading of the slot (the pages do not lay it out): two sign
+ * planes a and b, each [N][K/8] in the binary layout above, with
+ *     t = (a + b) / 2   (a bit read as +-1):  (1,1) -> +1, (0,0) -> -1,
+ *                                             (1,0) and (0,1) -> 0,
+ * and one fp16 scale array [N][K/128] shared by both planes.  Flipping a row
+ * in both planes with bit1_xor_patch negates that row (0 stays 0); the
+ * Bankai page notes that XOR patching does not carry over to ternary codes
+ * in general, and this library offers no ternary patch call.
+ *
+ * bit1_ternary_planes -- codes -> planes: a = (t >= 0), b = (t > 0).
+ *   codes   : device, int8 [N][K], each -1, 0 or +1
+ *   a, b    : device, N*K/8 bytes each (written)
+ *   d_flags : device pointer to one uint32, or NULL.  The call zeroes it on
+ *             `stream`; the kernel sets bit 2 if any code is outside
+ *             {-1, 0, +1} (the planes are then unspecified).  After
+ *             synchronising, bit1_pack_flags_status() maps bit 2 to
+ *             BIT1_ERANGE.
+ * Returns BIT1_ESHAPE / BIT1_EINVAL on bad arguments (nothing launched),
+ * BIT1_ECUDA on launch failure, else BIT1_OK.
+ */
+bit1_status bit1_ternary_planes(const int8_t *codes, int64_t N, int64_t K,
+                                uint8_t *a, uint8_t *b, uint32_t *d_flags,
+                                bit1_stream_t stream);
+
+/* bit1_gemv_ternary -- y[b][n] = sum_g s[n][g] * sum_{k in g} t(n,k) x[b][k]
+ * for the planes above, computed as the mean of the two binary products
+ * (one bit1_gemv_ex pass per plane into fp32 scratch, then one combine
+ * kernel).  Result within 1e-3 * sum_k |s*x_k| + 1e-6 of the exact value
+ * (plus the bf16 output rounding for y_dtype = BIT1_BF16).
+ *   a, b, scales, x, B, N, K, y, y_dtype, variant, flags : as bit1_gemv_ex
+ *                  (the variant and flags apply to both binary passes)
+ *   workspace    : REQUIRED device scratch of ws_bytes bytes, 16-byte
+ *                  aligned: at least the two fp32 halves, 2 * (B*N*4 rounded
+ *                  up to 256) bytes, else BIT1_EINVAL; the fastest kernels
+ *                  want bit1_gemv_ternary_workspace_bytes(B, N, K).
+ * Checks every argument of both passes before launching anything.
+ */
+size_t bit1_gemv_ternary_workspace_bytes(int64_t B, int64_t N, int64_t K);
+bit1_status bit1_gemv_ternary(const uint8_t *a, const uint8_t *b,
+                              const uint16_t *scales, const uint16_t *x,
+                              int64_t B, int64_t N, int64_t K, void *y,
+                              int y_dtype, void *workspace, size_t ws_bytes,
+                              int variant, unsigned flags, bit1_stream_t stream);
+/* Kernel launches of one bit1_gemv_ternary call (0 on bad arguments). */
+int bit1_gemv_ternary_launches(int64_t B, int64_t N, int64_t K, int variant);
+
+/* bit1_ternary_combine -- y[i] = (ya[i] + yb[i]) / 2 for i < n, fp32 sum,
+ * output fp32 or bf16 (round to nearest even).  The second step of
+ * bit1_gemv_ternary, exposed so that many ternary matrices run as one
+ * bit1_gemv_group launch (two problems per matrix, fp32 outputs laid out
+ * contiguously) plus one combine.  All pointers device, 16-byte aligned. */
+bit1_status bit1_ternary_combine(const float *ya, const float *yb, int64_t n,
+                                 void *y, int y_dtype, bit1_stream_t stream);
 
 /* Static description of a status code. */
 const char *bit1_status_str(bit1_status status);

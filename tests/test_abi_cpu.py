@@ -30,7 +30,8 @@ def _declared_functions():
 def test_header_declares_the_abi():
     names = _declared_functions()
     for want in ("bit1_pack", "bit1_gemv", "bit1_gemv_ex", "bit1_xor_patch",
-                 "bit1_gemv_workspace_bytes", "bit1_status_str"):
+                 "bit1_gemv_workspace_bytes", "bit1_status_str", "bit1_ternary_planes",
+                 "bit1_gemv_ternary", "bit1_ternary_combine"):
         assert want in names
 
 
@@ -52,6 +53,7 @@ def test_pack_flags_mapping(lib):
     assert b1.bit1_pack_flags_status(1) == b1.ENAN
     assert b1.bit1_pack_flags_status(2) == b1.ERANGE
     assert b1.bit1_pack_flags_status(3) == b1.ENAN
+    assert b1.bit1_pack_flags_status(4) == b1.ERANGE      # ternary code out of range
 
 
 FAKE = 1 << 20  # aligned non-null address: never dereferenced by the checks below
@@ -131,3 +133,35 @@ def test_binding_fails_loudly_without_cuda_tensors(lib):
     x = torch.zeros(1, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         b1.bit1_gemv(torch.zeros(8, 16, dtype=torch.uint8), torch.zeros(8, 1, dtype=torch.int16), x)
+
+
+def test_ternary_rejects_on_host(lib):
+    f = lib.bit1_ternary_planes
+    assert f(FAKE, 8, 100, FAKE, FAKE, None, None) == b1.ESHAPE
+    assert f(None, 8, 128, FAKE, FAKE, None, None) == b1.EINVAL
+    assert f(FAKE, 8, 128, FAKE + 4, FAKE, None, None) == b1.EINVAL
+    assert f(FAKE, 8, 128, FAKE, FAKE, FAKE + 2, None) == b1.EINVAL
+    g = lib.bit1_gemv_ternary
+    half = 256                                        # 1 x 8 fp32, rounded up to 256
+    assert g(FAKE, FAKE, FAKE, FAKE, 1, 8, 100, FAKE, b1.F32, FAKE, 2 * half, 0, 0, None) == b1.ESHAPE
+    assert g(FAKE, None, FAKE, FAKE, 1, 8, 128, FAKE, b1.F32, FAKE, 2 * half, 0, 0, None) == b1.EINVAL
+    assert g(FAKE, FAKE, FAKE, FAKE, 1, 8, 128, FAKE, b1.F32, None, 0, 0, 0, None) == b1.EINVAL
+    assert g(FAKE, FAKE, FAKE, FAKE, 1, 8, 128, FAKE, b1.F32, FAKE, 2 * half - 1, 0, 0, None) == b1.EINVAL
+    assert g(FAKE, FAKE, FAKE, FAKE, 1, 8, 128, FAKE, b1.F16, FAKE, 2 * half, 0, 0, None) == b1.EINVAL
+    assert g(FAKE, FAKE, FAKE, FAKE, 2, 8, 1024, FAKE, b1.F32, FAKE, 2 * half, b1.LUT, 0, None) == b1.ESHAPE
+    assert g(FAKE, FAKE, FAKE, FAKE, 1, 8, 128, FAKE, b1.F32, FAKE, 2 * half, 0, 0x80, None) == b1.EINVAL
+    c = lib.bit1_ternary_combine
+    assert c(FAKE, FAKE, 0, FAKE, b1.F32, None) == b1.ESHAPE
+    assert c(FAKE, FAKE + 4, 8, FAKE, b1.F32, None) == b1.EINVAL
+    assert c(FAKE, FAKE, 8, FAKE, b1.F16, None) == b1.EINVAL
+
+
+def test_ternary_workspace_and_launch_counts(lib):
+    assert b1.bit1_gemv_ternary_workspace_bytes(1, 4096, 4096) == 2 * 16384
+    assert b1.bit1_gemv_ternary_workspace_bytes(3, 10, 128) == 2 * 256
+    ws16 = b1.bit1_gemv_ternary_workspace_bytes(16, 12288, 4096)
+    assert ws16 == 2 * 16 * 12288 * 4 + b1.bit1_gemv_workspace_bytes(16, 12288, 4096)
+    assert b1.bit1_gemv_ternary_workspace_bytes(1, 8, 100) == 0
+    assert b1.bit1_gemv_ternary_launches(1, 4096, 4096) == 3
+    assert b1.bit1_gemv_ternary_launches(16, 12288, 4096, b1.TC) == 5
+    assert b1.bit1_gemv_ternary_launches(1, 8, 100) == 0
