@@ -65,6 +65,14 @@ def configure(lib):
     lib.orc_ternary_planes.restype = ctypes.c_int
     lib.orc_ternary_footprint_bytes.argtypes = [i64, i64]
     lib.orc_ternary_footprint_bytes.restype = i64
+    lib.orc_t5_pack.argtypes = [p, i64, i64, p]
+    lib.orc_t5_pack.restype = ctypes.c_int
+    lib.orc_t5_unpack.argtypes = [p, i64, i64, p]
+    lib.orc_t5_unpack.restype = ctypes.c_int
+    lib.orc_gemv_t5.argtypes = [p, p, p, i64, i64, i64, p]
+    lib.orc_gemv_t5.restype = ctypes.c_int
+    lib.orc_t5_footprint_bytes.argtypes = [i64, i64]
+    lib.orc_t5_footprint_bytes.restype = i64
     lib.orc_gemv_threads.argtypes = [p, p, p, i64, i64, i64, p, ctypes.c_int]
     lib.orc_gemv_threads.restype = ctypes.c_int
     lib.orc_xor_patch.argtypes = [p, i64, i64, p, i64]
@@ -199,6 +207,39 @@ def ternary_planes(t, N: int, K: int):
 
 def ternary_footprint_bytes(N: int, K: int) -> int:
     return int(_load().orc_ternary_footprint_bytes(N, K))
+
+
+def t5_pack(t, N: int, K: int) -> np.ndarray:
+    """Codes [N, K] (int8 in {-1, 0, 1}) -> five-per-byte packing [N, K/128*26]."""
+    t = np.ascontiguousarray(np.asarray(t, dtype=np.int8)).reshape(-1)
+    out = np.zeros(N * (K // 128) * 26, dtype=np.uint8)
+    st = _load().orc_t5_pack(_ptr(t), N, K, _ptr(out))
+    if st != OK:
+        raise OracleError(st, "t5_pack")
+    return out.reshape(N, (K // 128) * 26)
+
+
+def t5_unpack(p, N: int, K: int) -> np.ndarray:
+    p = _u8(p)
+    t = np.zeros(N * K, dtype=np.int8)
+    st = _load().orc_t5_unpack(_ptr(p), N, K, _ptr(t))
+    if st != OK:
+        raise OracleError(st, "t5_unpack")
+    return t.reshape(N, K)
+
+
+def gemv_t5(p, scales, x, B: int, N: int, K: int) -> np.ndarray:
+    """Ternary product straight from the five-per-byte packing, [B, N]."""
+    p, scales, x = _u8(p), _u16(scales), _u16(x)
+    y = np.zeros((B, N), dtype=np.float64)
+    st = _load().orc_gemv_t5(_ptr(p), _ptr(scales), _ptr(x), B, N, K, _ptr(y))
+    if st != OK:
+        raise OracleError(st, "gemv_t5")
+    return y
+
+
+def t5_footprint_bytes(N: int, K: int) -> int:
+    return int(_load().orc_t5_footprint_bytes(N, K))
 
 
 def gemv_threads(bits, scales, x, B: int, N: int, K: int, nthreads: int) -> np.ndarray:

@@ -372,6 +372,123 @@ int64_t orc_ternary_footprint_bytes(int64_t N, int64_t K)
     return 2 * (N * K / 8) + 2 * N * (K / 128);
 }
 
+/* ---- ternary, five codes per byte ----------------------------------------
+ * The native packing closer to log2(3) bits ([27B-ter]; [27B-store] says the
+ * deployed 2-bit slots exceed the information-theoretic minimum until native
+ * ternary kernels exist).  Reading (the pages give no layout): each group of
+ * 128 codes of a row is 26 bytes; byte j < 25 holds codes 5j .. 5j+4 and byte
+ * 25 holds codes 125 .. 127, each byte the base-3 number
+ *     v = sum_i (t_i + 1) * 3^i   (i = 0 for the lowest k),
+ * so a 5-code byte is 0 .. 242 and the last byte 0 .. 26.  Row n, group g
+ * starts at byte (n * (K/128) + g) * 26.  With the scales: 1.75 bits/weight. */
+static int orc_t5_digits(int64_t j)
+{
+    return j < 25 ? 5 : 3;
+}
+
+int orc_t5_pack(const int8_t *t, int64_t N, int64_t K, uint8_t *out)
+{
+    int st = orc_check_shape(1, N, K);
+    int64_t G = K / 128;
+    if (st != ORC_OK)
+        return st;
+    if (!t || !out)
+        return ORC_EINVAL;
+    for (int64_t i = 0; i < N * K; i++)
+        if (t[i] < -1 || t[i] > 1)
+            return ORC_ERANGE;
+    for (int64_t n = 0; n < N; n++) {
+        for (int64_t g = 0; g < G; g++) {
+            uint8_t *grp = out + (n * G + g) * 26;
+            int64_t k = 128 * g;
+            for (int64_t j = 0; j < 26; j++) {
+                int v = 0, p = 1;
+                for (int i = 0; i < orc_t5_digits(j); i++) {
+                    v += (t[n * K + k] + 1) * p;
+                    p *= 3;
+                    k++;
+                }
+                grp[j] = (uint8_t)v;
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* Code t(n, k) of a packed matrix, or 2 if its byte is out of range. */
+static int orc_t5_code(const uint8_t *p, int64_t K, int64_t n, int64_t k)
+{
+    int64_t G = K / 128, g = k / 128, r = k % 128;
+    int64_t j = r / 5;
+    int i = (int)(r % 5), v = p[(n * G + g) * 26 + j];
+    if (v > (j < 25 ? 242 : 26))
+        return 2;
+    while (i-- > 0)
+        v /= 3;
+    return v % 3 - 1;
+}
+
+int orc_t5_unpack(const uint8_t *p, int64_t N, int64_t K, int8_t *t)
+{
+    int st = orc_check_shape(1, N, K);
+    if (st != ORC_OK)
+        return st;
+    if (!p || !t)
+        return ORC_EINVAL;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t k = 0; k < K; k++) {
+            int c = orc_t5_code(p, K, n, k);
+            if (c == 2)
+                return ORC_ERANGE;
+            t[n * K + k] = (int8_t)c;
+        }
+    return ORC_OK;
+}
+
+/* y[b,n] = sum_g s[n,g] * sum_{k in g} t(n,k) x[b,k], codes read one at a
+ * time from the packed bytes; fp64, group partial first.  ERANGE (y
+ * untouched) if any byte is out of range. */
+int orc_gemv_t5(const uint8_t *p, const uint16_t *scales, const uint16_t *x,
+                int64_t B, int64_t N, int64_t K, double *y)
+{
+    int st = orc_check_shape(B, N, K);
+    int64_t G = K / 128;
+    if (st != ORC_OK)
+        return st;
+    if (!p || !scales || !x || !y)
+        return ORC_EINVAL;
+    for (int64_t n = 0; n < N; n++)
+        for (int64_t k = 0; k < K; k++)
+            if (orc_t5_code(p, K, n, k) == 2)
+                return ORC_ERANGE;
+    for (int64_t b = 0; b < B; b++) {
+        for (int64_t n = 0; n < N; n++) {
+            double acc = 0.0;
+            for (int64_t g = 0; g < G; g++) {
+                double s = orc_half_to_double(scales[n * G + g]);
+                double part = 0.0;
+                for (int64_t k = 128 * g; k < 128 * g + 128; k++) {
+                    int c = orc_t5_code(p, K, n, k);
+                    double xv = orc_bf16_to_double(x[b * K + k]);
+                    if (c > 0)
+                        part += xv;
+                    else if (c < 0)
+                        part -= xv;
+                }
+                acc += s * part;
+            }
+            y[b * N + n] = acc;
+        }
+    }
+    return ORC_OK;
+}
+
+/* Bytes of a matrix packed five codes per byte: 26 per group plus the scale. */
+int64_t orc_t5_footprint_bytes(int64_t N, int64_t K)
+{
+    return N * (K / 128) * 26 + 2 * N * (K / 128);
+}
+
 /* Same function, rows split over `nthreads` POSIX threads: parallel dispatch
  * of the scalar loop above, nothing else (used only to time the oracle on
  * all host cores). */

@@ -69,11 +69,29 @@ MUTANTS = [
       lambda o: pins.test_ternary_single_code_closed_form(o)]),
     ("ternary_planes_threshold", "if (v >= 0)\n                pa", "if (v > 0)\n                pa",
      [lambda o: pins.test_ternary_planes_match_numpy(o)]),
-    ("ternary_codes_unchecked", "if (t[i] < -1 || t[i] > 1)", "if (t[i] < -2 || t[i] > 2)",
+    ("ternary_codes_unchecked", "if (t[i] < -1 || t[i] > 1)\n            return ORC_ERANGE;\n    memset",
+     "if (t[i] < -2 || t[i] > 2)\n            return ORC_ERANGE;\n    memset",
      [lambda o: pins.test_ternary_planes_reject_other_codes(o, 2)]),
     ("ternary_footprint_one_plane", "return 2 * (N * K / 8) + 2 * N * (K / 128);",
      "return (N * K / 8) + 2 * N * (K / 128);",
      [lambda o: pins.test_ternary_footprint_and_printed_sizes(o)]),
+    ("t5_digit_order_reversed", "    while (i-- > 0)\n        v /= 3;",
+     "    i = (j < 25 ? 4 : 2) - i;\n    while (i-- > 0)\n        v /= 3;",
+     [lambda o: pins.test_t5_pack_matches_numpy(o),
+      lambda o: pins.test_t5_every_byte_value_decodes_to_its_base3_digits(o)]),
+    ("t5_codes_unchecked", "if (t[i] < -1 || t[i] > 1)\n            return ORC_ERANGE;\n    for (int64_t n",
+     "if (t[i] < -1 || t[i] > 3)\n            return ORC_ERANGE;\n    for (int64_t n",
+     [lambda o: pins.test_t5_rejects_out_of_range(o)]),
+    ("t5_group_stride", "int i = (int)(r % 5), v = p[(n * G + g) * 26 + j];",
+     "int i = (int)(r % 5), v = p[(n * G + g) * 25 + j];",
+     [lambda o: pins.test_t5_pack_matches_numpy(o)]),
+    ("t5_last_byte_unchecked", "if (v > (j < 25 ? 242 : 26))", "if (v > 242)",
+     [lambda o: pins.test_t5_rejects_out_of_range(o)]),
+    ("t5_code_offset", "    return v % 3 - 1;", "    return 1 - v % 3;",
+     [lambda o: pins.test_t5_gemv_matches_dense_and_planes(o, 4, 256, 2)]),
+    ("t5_footprint_padded", "return N * (K / 128) * 26 + 2 * N * (K / 128);",
+     "return N * (K / 128) * 32 + 2 * N * (K / 128);",
+     [lambda o: pins.test_t5_footprint_between_ideal_and_slots(o)]),
 ]
 
 

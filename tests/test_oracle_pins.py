@@ -535,3 +535,94 @@ def test_ternary_footprint_and_printed_sizes(orc):
     slot_bpw = orc.ternary_footprint_bytes(128, 128) * 8 / (128 * 128)
     deployed = total * slot_bpw / 8 / 1e9
     assert deployed == pytest.approx(fig["bonsai_27b_ternary_deployed_gigabytes"]["value"], rel=0.03)
+
+
+# ---------------------------------------------------------------- ternary, five codes per byte
+
+def _np_t5(t):
+    """Independent packing route: numpy dot products of (t + 1) with the
+    powers of three, per group: 25 five-code bytes, then one three-code byte."""
+    N, K = t.shape
+    d = (t.astype(np.int64) + 1).reshape(N, K // 128, 128)
+    five = d[:, :, :125].reshape(N, K // 128, 25, 5) @ np.array([1, 3, 9, 27, 81])
+    three = d[:, :, 125:] @ np.array([1, 3, 9])
+    return np.concatenate([five, three[:, :, None]], axis=2).reshape(N, -1).astype(np.uint8)
+
+
+def test_t5_pack_matches_numpy(orc):
+    N, K = 5, 384
+    t = synth.ternary_codes(N, K, synth.rng(900))
+    p = orc.t5_pack(t, N, K)
+    assert p.shape == (N, 3 * 26)
+    assert np.array_equal(p, _np_t5(t))
+    assert np.array_equal(orc.t5_unpack(p, N, K), t)
+
+
+def test_t5_every_byte_value_decodes_to_its_base3_digits(orc):
+    """Brute force over all 243 five-code bytes and all 27 three-code bytes,
+    against Python's own base-3 digits."""
+    N, K = 243, 128
+    p = np.empty((N, 26), dtype=np.uint8)
+    p[:, :25] = 121                     # five codes 0 (digit 1)
+    p[:, 25] = 13                       # three codes 0
+    p[:, 7] = np.arange(243)
+    p[:27, 25] = np.arange(27)
+    t = orc.t5_unpack(p, N, K)
+    for v in range(243):
+        digits = [int(c) for c in np.base_repr(v, 3).zfill(5)[::-1]]
+        assert list(t[v, 35:40]) == [d - 1 for d in digits]
+        assert not np.any(np.delete(t[v], list(range(35, 40)) + ([125, 126, 127] if v < 27 else [])))
+    for v in range(27):
+        digits = [int(c) for c in np.base_repr(v, 3).zfill(3)[::-1]]
+        assert list(t[v, 125:128]) == [d - 1 for d in digits]
+
+
+def test_t5_rejects_out_of_range(orc):
+    import oracle
+    N, K = 2, 256
+    t = np.zeros((N, K), dtype=np.int8)
+    t[1, 200] = 3
+    with pytest.raises(oracle.OracleError):
+        orc.t5_pack(t, N, K)
+    p = orc.t5_pack(np.zeros((N, K), dtype=np.int8), N, K)
+    x = synth.x_for(1, K, 901)
+    scales = synth.group_scales(N, K, synth.rng(901))
+    for pos, val in ((3, 243), (25, 27), (51, 27)):
+        q = p.copy()
+        q[1, pos] = val
+        with pytest.raises(oracle.OracleError):
+            orc.t5_unpack(q, N, K)
+        with pytest.raises(oracle.OracleError):
+            orc.gemv_t5(q, scales, x, 1, N, K)
+    q = p.copy()
+    q[1, 24] = 242                      # largest valid five-code byte
+    q[1, 25] = 26                       # largest valid three-code byte
+    orc.t5_unpack(q, N, K)
+
+
+@pytest.mark.parametrize("N,K,B", [(1, 128, 1), (4, 256, 2), (7, 384, 3)])
+def test_t5_gemv_matches_dense_and_planes(orc, N, K, B):
+    g = synth.rng(910 + N)
+    t = synth.ternary_codes(N, K, g)
+    scales = synth.group_scales(N, K, g, offset=1e-3)
+    x = synth.activations(B, K, g)
+    y = orc.gemv_t5(_np_t5(t), scales, x, B, N, K)
+    ref, W, X = _dense_ternary(t, scales, x, N, K)
+    assert np.all(np.abs(y - ref) <= 1e-12 * (np.abs(X) @ np.abs(W).T) + 1e-300)
+    a, b = _np_planes(t)
+    assert np.array_equal(y, orc.gemv_ternary(a, b, scales, x, B, N, K))
+
+
+def test_t5_footprint_between_ideal_and_slots(orc):
+    """26 bytes per 128 codes plus the fp16 scale are 1.75 bits/weight: over
+    the 27B parameter split that is 6.07 GB, between the pages' ideal 5.9 GB
+    and their 2-bit-slot 'about 7.2 GB'; 8/5 bits per code is above log2(3)."""
+    fig = json.load(open(GOLDEN))
+    N, K = 5120, 17408
+    assert orc.t5_footprint_bytes(N, K) * 8 == 1.75 * N * K
+    assert 8 / 5 >= np.log2(3.0)
+    sp = fig["bonsai_27b_parameter_split"]
+    total = sp["language_model"] + sp["vision_tower"] + sp["embedding_and_lm_head"]
+    gb = total * 1.75 / 8 / 1e9
+    assert fig["bonsai_27b_ternary_gigabytes"]["value"] < gb < fig["bonsai_27b_ternary_deployed_gigabytes"]["value"]
+    assert orc.t5_footprint_bytes(N, K) < orc.ternary_footprint_bytes(N, K)
