@@ -427,6 +427,66 @@ def extra_ternary_sweep_8b(torch, b1, steps=20):
     return out
 
 
+def extra_t5(torch, b1, reps=20):
+    """Ternary codes packed five per byte (1.75 bits/weight): the direct
+    product on the 8B-class projection shapes at batch 1 (graph replay over
+    copies rotated past L2), and the device transcode to the 2-bit-slot planes
+    on the LM-head shape."""
+    out = {}
+    for (N, K) in ((4096, 4096), (12288, 4096), (4096, 12288)):
+        pb = N * (K // 128) * 26
+        wb = pb + 2 * N * (K // 128)
+        copies = max(2, (3 * L2_BYTES) // wb + 1)
+        g = torch.Generator(device="cuda")
+        g.manual_seed(N + K)
+        packed = torch.randint(0, 243, (copies, N, (K // 128) * 26), dtype=torch.uint8, device="cuda", generator=g)
+        sc = (torch.randn((copies, N, K // 128), device="cuda", generator=g).abs_() * 0.02).half().view(torch.int16)
+        x = torch.randn((1, K), device="cuda", generator=g).bfloat16()
+        y = torch.empty((1, N), device="cuda")
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            for i in range(3):
+                b1.bit1_gemv_t5(packed[i % copies], sc[i % copies], x, y=y, stream=s, N=N)
+            s.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=s):
+                for i in range(reps):
+                    b1.bit1_gemv_t5(packed[i % copies], sc[i % copies], x, y=y, stream=s, N=N)
+            graph.replay()
+            s.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            graph.replay()
+            e1.record(s)
+            e1.synchronize()
+        us = e0.elapsed_time(e1) / reps * 1e3
+        out[f"gemv_{N}x{K}_b1"] = {"us": round(us, 3), "weight_gbs": round(wb / (us * 1e-6) / 1e9, 1),
+                                   "gweights_s": round(N * K / (us * 1e-6) / 1e9, 1)}
+        del packed, sc, graph
+        torch.cuda.empty_cache()
+    N, K = 151936, 4096
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    packed = torch.randint(0, 243, (N, (K // 128) * 26), dtype=torch.uint8, device="cuda", generator=g)
+    a = torch.empty((N, K // 8), dtype=torch.uint8, device="cuda")
+    b = torch.empty_like(a)
+    for _ in range(3):
+        b1.bit1_t5_to_planes(packed, K, a=a, b=b)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        b1.bit1_t5_to_planes(packed, K, a=a, b=b)
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / 5
+    moved = packed.numel() + a.numel() + b.numel()
+    out["to_planes_151936x4096"] = {"ms": round(ms, 4), "gbs_in_plus_out": round(moved / (ms * 1e-3) / 1e9, 1)}
+    del packed, a, b
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_mine(args):
     import torch
     import bit_weight_gemv_sign_b300 as b1
@@ -566,7 +626,8 @@ def run_mine(args):
                          "c4_mlp_crossover": extra_c4_crossover(torch, b1),
                          "pp512_tcgen05": extra_pp512(torch, b1),
                          "c5_sweep_27b": extra_c5_sweep_27b(torch, b1),
-                         "ternary_sweep_8b": extra_ternary_sweep_8b(torch, b1)}
+                         "ternary_sweep_8b": extra_ternary_sweep_8b(torch, b1),
+                         "ternary_t5": extra_t5(torch, b1)}
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
         oracle.build()

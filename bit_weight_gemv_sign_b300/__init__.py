@@ -22,6 +22,7 @@ __all__ = [
     "library_path", "load", "bit1_gemv_tc_noalloc",
     "bit1_ternary_planes", "bit1_gemv_ternary", "bit1_gemv_ternary_workspace_bytes",
     "bit1_gemv_ternary_launches", "bit1_ternary_combine",
+    "bit1_t5_pack", "bit1_t5_to_planes", "bit1_gemv_t5", "bit1_gemv_t5_launches",
 ]
 
 OK, EINVAL, ESHAPE, ERANGE, ECUDA, ENAN = 0, 1, 2, 3, 4, 5
@@ -103,6 +104,14 @@ def load():
         lib.bit1_gemv_ternary_launches.restype = i32
         lib.bit1_ternary_combine.argtypes = [p, p, i64, p, i32, p]
         lib.bit1_ternary_combine.restype = i32
+        lib.bit1_t5_pack.argtypes = [p, i64, i64, p, p, p]
+        lib.bit1_t5_pack.restype = i32
+        lib.bit1_t5_to_planes.argtypes = [p, i64, i64, p, p, p, p]
+        lib.bit1_t5_to_planes.restype = i32
+        lib.bit1_gemv_t5.argtypes = [p, p, p, i64, i64, i64, p, i32, p]
+        lib.bit1_gemv_t5.restype = i32
+        lib.bit1_gemv_t5_launches.argtypes = [i64, i64, i64]
+        lib.bit1_gemv_t5_launches.restype = i32
         _lib = lib
         return lib
 
@@ -362,3 +371,53 @@ def bit1_ternary_combine(ya, yb, y, stream=None) -> None:
     st = load().bit1_ternary_combine(_dptr(ya, "ya", (torch.float32,)), _dptr(yb, "yb", (torch.float32,)),
                                      n, _dptr(y, "y", (torch.float32, torch.bfloat16)), ydt, _stream(stream))
     _check(st, "bit1_ternary_combine")
+
+
+# ---------------------------------------------------------------- ternary (five codes per byte)
+
+def bit1_t5_pack(codes, packed=None, flags=None, stream=None):
+    """Codes int8 [N, K] (CUDA) -> packed uint8 [N, K/128*26]."""
+    import torch
+    N, K = codes.shape
+    if packed is None:
+        packed = torch.empty((N, (K // 128) * 26), dtype=torch.uint8, device=codes.device)
+    st = load().bit1_t5_pack(_dptr(codes, "codes", (torch.int8,)), N, K, _dptr(packed, "packed"),
+                             _dptr(flags, "flags"), _stream(stream))
+    _check(st, "bit1_t5_pack")
+    return packed
+
+
+def bit1_t5_to_planes(packed, K, a=None, b=None, flags=None, stream=None):
+    """Packed bytes [N, K/128*26] -> the 2-bit-slot planes (a, b), uint8 [N, K/8] each."""
+    import torch
+    N = packed.shape[0]
+    if a is None:
+        a = torch.empty((N, K // 8), dtype=torch.uint8, device=packed.device)
+    if b is None:
+        b = torch.empty((N, K // 8), dtype=torch.uint8, device=packed.device)
+    st = load().bit1_t5_to_planes(_dptr(packed, "packed"), N, K, _dptr(a, "a"), _dptr(b, "b"),
+                                  _dptr(flags, "flags"), _stream(stream))
+    _check(st, "bit1_t5_to_planes")
+    return a, b
+
+
+def bit1_gemv_t5_launches(B: int, N: int, K: int) -> int:
+    return int(load().bit1_gemv_t5_launches(B, N, K))
+
+
+def bit1_gemv_t5(packed, scales, x, y=None, y_dtype=None, stream=None, N=None, K=None):
+    """y[B, N] = x[B, K] (bf16) times the ternary matrix packed five codes per byte."""
+    import torch
+    B = x.shape[0] if x.dim() == 2 else 1
+    K = x.shape[-1] if K is None else K
+    N = packed.shape[0] if N is None else N
+    if y is None:
+        yt = torch.bfloat16 if y_dtype == BF16 else torch.float32
+        y = torch.empty((B, N), dtype=yt, device=x.device)
+    if y.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("y must be float32 or bfloat16")
+    ydt = BF16 if y.dtype == torch.bfloat16 else F32
+    st = load().bit1_gemv_t5(_dptr(packed, "packed"), _dptr(scales, "scales"), _dptr(x, "x"), B, N, K,
+                             _dptr(y, "y"), ydt, _stream(stream))
+    _check(st, "bit1_gemv_t5")
+    return y

@@ -82,7 +82,7 @@ bit1_status bit1_pack(const void* w, int w_dtype, int64_t N, int64_t K, uint8_t*
 
 bit1_status bit1_pack_flags_status(uint32_t flags) {
     if (flags & 1u) return BIT1_ENAN;
-    if (flags & 6u) return BIT1_ERANGE;
+    if (flags & 14u) return BIT1_ERANGE;
     return BIT1_OK;
 }
 
@@ -277,6 +277,35 @@ bit1_status bit1_ternary_combine(const float* ya, const float* yb, int64_t n, vo
     if (!ya || !yb || !y || !aligned16(ya) || !aligned16(yb) || !aligned16(y)) return BIT1_EINVAL;
     if (y_dtype != BIT1_F32 && y_dtype != BIT1_BF16) return BIT1_EINVAL;
     return from_cuda(launch_ternary_combine(ya, yb, n, y, y_dtype == BIT1_BF16, (cudaStream_t)stream));
+}
+
+bit1_status bit1_t5_pack(const int8_t* codes, int64_t N, int64_t K, uint8_t* packed, uint32_t* d_flags,
+                         bit1_stream_t stream) {
+    if (!shape_ok(1, N, K)) return BIT1_ESHAPE;
+    if (!codes || !packed || !aligned16(codes) || !aligned16(packed)) return BIT1_EINVAL;
+    if (d_flags && ((uintptr_t)d_flags & 3u)) return BIT1_EINVAL;
+    return from_cuda(launch_t5_pack(codes, N, K, packed, d_flags, (cudaStream_t)stream));
+}
+
+bit1_status bit1_t5_to_planes(const uint8_t* packed, int64_t N, int64_t K, uint8_t* a, uint8_t* b,
+                              uint32_t* d_flags, bit1_stream_t stream) {
+    if (!shape_ok(1, N, K)) return BIT1_ESHAPE;
+    if (!packed || !a || !b || !aligned16(packed) || !aligned16(a) || !aligned16(b)) return BIT1_EINVAL;
+    if (d_flags && ((uintptr_t)d_flags & 3u)) return BIT1_EINVAL;
+    return from_cuda(launch_t5_planes(packed, N, K, a, b, d_flags, (cudaStream_t)stream));
+}
+
+bit1_status bit1_gemv_t5(const uint8_t* packed, const uint16_t* scales, const uint16_t* x, int64_t B,
+                         int64_t N, int64_t K, void* y, int y_dtype, bit1_stream_t stream) {
+    if (!shape_ok(B, N, K)) return BIT1_ESHAPE;
+    if (!packed || !scales || !x || !y) return BIT1_EINVAL;
+    if (!aligned16(packed) || !aligned16(scales) || !aligned16(x) || !aligned16(y)) return BIT1_EINVAL;
+    if (y_dtype != BIT1_F32 && y_dtype != BIT1_BF16) return BIT1_EINVAL;
+    return from_cuda(launch_gemv_t5(packed, scales, x, B, N, K, y, y_dtype == BIT1_BF16, (cudaStream_t)stream));
+}
+
+int bit1_gemv_t5_launches(int64_t B, int64_t N, int64_t K) {
+    return shape_ok(B, N, K) ? t5_launch_count(B) : 0;
 }
 
 bit1_status bit1_gemv_group(const void* device_plan, const void* host_plan, unsigned flags,

@@ -70,6 +70,15 @@ cudaError_t launch_ternary_planes(const int8_t* codes, int64_t N, int64_t K, uin
 cudaError_t launch_ternary_combine(const float* ya, const float* yb, int64_t n, void* y, bool y_bf16,
                                    cudaStream_t stream);
 
+// Ternary codes packed five per byte (t5.cu).
+cudaError_t launch_t5_pack(const int8_t* codes, int64_t N, int64_t K, uint8_t* out, uint32_t* flags,
+                           cudaStream_t stream);
+cudaError_t launch_t5_planes(const uint8_t* packed, int64_t N, int64_t K, uint8_t* a, uint8_t* b,
+                             uint32_t* flags, cudaStream_t stream);
+cudaError_t launch_gemv_t5(const uint8_t* packed, const uint16_t* scales, const uint16_t* x, int64_t B,
+                           int64_t N, int64_t K, void* y, bool y_bf16, cudaStream_t stream);
+int t5_launch_count(int64_t B);
+
 int sm_count();
 
 }  // namespace bit1

@@ -106,8 +106,9 @@ bit1_status bit1_pack(const void *w, int w_dtype, int64_t N, int64_t K,
                       uint8_t *bits, uint16_t *scales, uint32_t *d_flags,
                       bit1_stream_t stream);
 
-/* BIT1_ENAN if bit 0 is set, else BIT1_ERANGE if bit 1 (bit1_pack) or bit 2
- * (bit1_ternary_planes) is set, else BIT1_OK. */
+/* BIT1_ENAN if bit 0 is set, else BIT1_ERANGE if bit 1 (bit1_pack), bit 2
+ * (a ternary code out of range) or bit 3 (a packed ternary byte out of
+ * range) is set, else BIT1_OK. */
 bit1_status bit1_pack_flags_status(uint32_t flags);
 
 /* ------------------------------------------------------------------------
@@ -296,6 +297,41 @@ int bit1_gemv_ternary_launches(int64_t B, int64_t N, int64_t K, int variant);
  * contiguously) plus one combine.  All pointers device, 16-byte aligned. */
 bit1_status bit1_ternary_combine(const float *ya, const float *yb, int64_t n,
                                  void *y, int y_dtype, bit1_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Ternary codes packed five per byte: a storage closer to the ideal
+ * log2(3) bits (same page and sections as above; the pages give no layout).
+ * This library's packing: row-major [N][K/128 * 26] bytes; the 128 codes of
+ * group g of row n are the 26 bytes at (n * K/128 + g) * 26: byte j < 25
+ * holds codes 5j .. 5j+4 and byte 25 holds codes 125 .. 127, each byte the
+ * base-3 number v = sum_i (t_i + 1) * 3^i with i = 0 for the lowest k
+ * (0 .. 242; the last byte 0 .. 26).  With the fp16 scales [N][K/128] (the
+ * same array as the other layouts) this is 1.75 bits/weight, against 2.125
+ * for the 2-bit slots.  Flag bits (read with bit1_pack_flags_status, which
+ * maps them to BIT1_ERANGE): bit 2 a code outside {-1, 0, +1}, bit 3 a byte
+ * outside its range.  d_flags as in bit1_pack: optional, zeroed by the call.
+ *
+ * bit1_t5_pack      -- codes int8 [N][K] -> packed bytes.
+ * bit1_t5_to_planes -- packed bytes -> the two planes of the 2-bit-slot
+ *                      layout (N*K/8 bytes each), so a matrix stored in this
+ *                      compact form runs on bit1_gemv_ternary's kernels.
+ * bit1_gemv_t5      -- y[B][N] straight from the packed bytes: one warp per
+ *                      row, fp32 accumulation, up to 8 batch rows per launch
+ *                      (bit1_gemv_t5_launches); within the bit1_gemv
+ *                      tolerance.  A byte out of range gives an unspecified
+ *                      (but in-bounds) result for its row.
+ * All pointers device, 16-byte aligned; BIT1_ESHAPE / BIT1_EINVAL on bad
+ * arguments with nothing launched.
+ */
+bit1_status bit1_t5_pack(const int8_t *codes, int64_t N, int64_t K,
+                         uint8_t *packed, uint32_t *d_flags, bit1_stream_t stream);
+bit1_status bit1_t5_to_planes(const uint8_t *packed, int64_t N, int64_t K,
+                              uint8_t *a, uint8_t *b, uint32_t *d_flags,
+                              bit1_stream_t stream);
+bit1_status bit1_gemv_t5(const uint8_t *packed, const uint16_t *scales,
+                         const uint16_t *x, int64_t B, int64_t N, int64_t K,
+                         void *y, int y_dtype, bit1_stream_t stream);
+int bit1_gemv_t5_launches(int64_t B, int64_t N, int64_t K);
 
 /* Static description of a status code. */
 const char *bit1_status_str(bit1_status status);

@@ -54,6 +54,7 @@ def test_pack_flags_mapping(lib):
     assert b1.bit1_pack_flags_status(2) == b1.ERANGE
     assert b1.bit1_pack_flags_status(3) == b1.ENAN
     assert b1.bit1_pack_flags_status(4) == b1.ERANGE      # ternary code out of range
+    assert b1.bit1_pack_flags_status(8) == b1.ERANGE      # packed ternary byte out of range
 
 
 FAKE = 1 << 20  # aligned non-null address: never dereferenced by the checks below
@@ -165,3 +166,17 @@ def test_ternary_workspace_and_launch_counts(lib):
     assert b1.bit1_gemv_ternary_launches(1, 4096, 4096) == 3
     assert b1.bit1_gemv_ternary_launches(16, 12288, 4096, b1.TC) == 5
     assert b1.bit1_gemv_ternary_launches(1, 8, 100) == 0
+
+
+def test_t5_rejects_on_host(lib):
+    assert lib.bit1_t5_pack(FAKE, 8, 100, FAKE, None, None) == b1.ESHAPE
+    assert lib.bit1_t5_pack(FAKE, 8, 128, FAKE + 1, None, None) == b1.EINVAL
+    assert lib.bit1_t5_to_planes(FAKE, 8, 128, FAKE, None, None, None) == b1.EINVAL
+    assert lib.bit1_t5_to_planes(FAKE, 0, 128, FAKE, FAKE, None, None) == b1.ESHAPE
+    g = lib.bit1_gemv_t5
+    assert g(FAKE, FAKE, FAKE, 1, 8, 100, FAKE, b1.F32, None) == b1.ESHAPE
+    assert g(FAKE, FAKE, None, 1, 8, 128, FAKE, b1.F32, None) == b1.EINVAL
+    assert g(FAKE, FAKE, FAKE, 1, 8, 128, FAKE, b1.F16, None) == b1.EINVAL
+    assert b1.bit1_gemv_t5_launches(1, 8, 128) == 1
+    assert b1.bit1_gemv_t5_launches(17, 8, 128) == 3
+    assert b1.bit1_gemv_t5_launches(1, 8, 100) == 0

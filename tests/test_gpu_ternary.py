@@ -177,3 +177,91 @@ def test_ternary_sweep_8b_grouped_sampled_parity(orc):
     plan.run()
     torch.cuda.synchronize()
     assert torch.equal(first, sw.yt)
+
+
+# ---------------------------------------------------------------- five codes per byte
+
+@pytest.mark.parametrize("N,K", [(1, 128), (37, 1152), (300, 4096)])
+def test_t5_pack_and_planes_bit_exact(orc, N, K):
+    t = synth.ternary_codes(N, K, synth.rng(850 + N))
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    p = b1.bit1_t5_pack(torch.from_numpy(t).cuda(), flags=flags)
+    torch.cuda.synchronize()
+    assert b1.bit1_pack_flags_status(int(flags.item())) == b1.OK
+    ep = orc.t5_pack(t, N, K)
+    assert np.array_equal(p.cpu().numpy(), ep)
+    a, b = b1.bit1_t5_to_planes(p, K, flags=flags)
+    torch.cuda.synchronize()
+    assert b1.bit1_pack_flags_status(int(flags.item())) == b1.OK
+    ea, eb = orc.ternary_planes(orc.t5_unpack(ep, N, K), N, K)
+    assert np.array_equal(a.cpu().numpy(), ea) and np.array_equal(b.cpu().numpy(), eb)
+
+
+def test_t5_every_byte_value_through_the_planes(orc):
+    """All 243 five-code bytes and all 27 three-code bytes, decoded by the
+    device transcode, against the oracle's base-3 decoding."""
+    N, K = 243, 128
+    p = np.empty((N, 26), dtype=np.uint8)
+    p[:, :25] = 121
+    p[:, 25] = 13
+    p[:, 7] = np.arange(243)
+    p[:27, 25] = np.arange(27)
+    a, b = b1.bit1_t5_to_planes(torch.from_numpy(p).cuda(), K)
+    torch.cuda.synchronize()
+    ea, eb = orc.ternary_planes(orc.t5_unpack(p, N, K), N, K)
+    assert np.array_equal(a.cpu().numpy(), ea) and np.array_equal(b.cpu().numpy(), eb)
+
+
+def test_t5_flags_bad_codes_and_bytes():
+    N, K = 2, 256
+    t = np.zeros((N, K), dtype=np.int8)
+    t[1, 130] = -3
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    b1.bit1_t5_pack(torch.from_numpy(t).cuda(), flags=flags)
+    torch.cuda.synchronize()
+    assert b1.bit1_pack_flags_status(int(flags.item())) == b1.ERANGE
+    for pos, val in ((3, 243), (25, 27), (51, 200)):
+        p = np.full((N, 52), 121, dtype=np.uint8)
+        p[:, 25] = p[:, 51] = 13
+        p[1, pos] = val
+        b1.bit1_t5_to_planes(torch.from_numpy(p).cuda(), K, flags=flags)
+        torch.cuda.synchronize()
+        assert b1.bit1_pack_flags_status(int(flags.item())) == b1.ERANGE, (pos, val)
+
+
+@pytest.mark.parametrize("B,N,K", [(1, 1000, 4096), (3, 129, 1152), (8, 257, 2048), (11, 64, 1024)])
+def test_gemv_t5_parity(orc, B, N, K):
+    g = synth.rng(860 + B)
+    t = synth.ternary_codes(N, K, g)
+    scales = synth.group_scales(N, K, g)
+    x = synth.activations(B, K, g)
+    p = orc.t5_pack(t, N, K)
+    ref = orc.gemv_t5(p, scales, x, B, N, K)
+    bound = abs_bound(scales, x, K)
+    for ydt in (b1.F32, b1.BF16):
+        y = b1.bit1_gemv_t5(dev_u8(p), dev_u16(scales), dev_bf16(x).view(B, K), y_dtype=ydt, N=N)
+        torch.cuda.synchronize()
+        assert_gemv_close(y, ref, bound, f"t5 B={B} N={N} K={K} y={ydt}")
+
+
+def test_t5_stored_then_run_on_the_slot_kernels(orc):
+    """The compact packing, expanded on the device, multiplied by the 2-bit
+    slot path: the same result (within tolerance) as the direct product."""
+    N, K, B = 4096, 4096, 1
+    g = synth.rng(870)
+    t = synth.ternary_codes(N, K, g)
+    scales = synth.group_scales(N, K, g)
+    x = synth.activations(B, K, g)
+    p = dev_u8(orc.t5_pack(t, N, K))
+    a, b = b1.bit1_t5_to_planes(p, K)
+    ds, dx = dev_u16(scales), dev_bf16(x).view(B, K)
+    y1 = b1.bit1_gemv_ternary(a, b, ds, dx)
+    y2 = b1.bit1_gemv_t5(p, ds, dx, N=N)
+    torch.cuda.synchronize()
+    rows = np.arange(0, N, 37)
+    ea, eb = orc.ternary_planes(t, N, K)
+    ref = orc.gemv_ternary_select(ea, eb, scales, x, B, N, K, rows)
+    bd = abs_bound(scales[rows], x, K)
+    idx = torch.from_numpy(rows).cuda()
+    assert_gemv_close(y1[:, idx], ref, bd, "t5 -> planes -> slot kernels")
+    assert_gemv_close(y2[:, idx], ref, bd, "t5 direct")
