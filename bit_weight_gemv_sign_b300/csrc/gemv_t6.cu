@@ -353,24 +353,41 @@ bool plan_t6_q(int64_t N, int64_t K, int Q, int nb, T6Plan& pl) {
     return true;
 }
 
-// Among the usable cluster sizes, take the plan that keeps the most SMs busy.
+// Relative time of a plan, in units of one warp's work on one 32-row block of
+// one group: a warp runs ceil(bpc / W) blocks of Gc groups back to back (its
+// dependent chain), an SM issues about eight warps' worth at once, and the
+// table build (about 0.75 units per group, spread over the W warps) comes
+// first.  More SMs with fewer warps each can lose: half the warps per CTA and
+// twice the K per CTA doubles every warp's chain.
+double t6_estimate(const T6Plan& pl) {
+    const int bpc = pl.p.prow / 32;
+    const double chain = (double)((bpc + pl.W - 1) / pl.W);
+    return pl.Gc * std::max(chain, bpc / 8.0) + 0.75 * pl.Gc / pl.W;
+}
+
+// Among the usable cluster sizes, take the plan with the smallest estimate
+// (ties: more SMs busy).
 bool plan_t6(int64_t N, int64_t K, int nb, T6Plan& best) {
     if (N < 1 || N > (1LL << 30) || nb < 1 || nb > kT6MaxNB) return false;
     int qs[16];
     const int nq = q_candidates(K / 128, nb, qs);
     bool found = false;
+    double best_est = 0.0;
     for (int i = 0; i < nq; ++i) {
         T6Plan pl;
         if (!plan_t6_q(N, K, qs[i], nb, pl)) continue;
-        if (!found || pl.ncl * pl.Q > best.ncl * best.Q) {
+        const double est = t6_estimate(pl);
+        if (!found || est < best_est - 1e-9 ||
+            (est < best_est + 1e-9 && pl.ncl * pl.Q > best.ncl * best.Q)) {
             best = pl;
+            best_est = est;
             found = true;
         }
     }
     return found;
 }
 
-// Batch rows per launch: the largest NB <= min(B, 8) that has a plan.
+// Largest batch rows per launch: the largest NB <= min(B, 8) that has a plan.
 int t6_chunk(int64_t B, int64_t N, int64_t K) {
     for (int nb = (int)std::min<int64_t>(B, kT6MaxNB); nb >= 1; --nb) {
         T6Plan pl;
@@ -456,11 +473,15 @@ cudaError_t launch_gemv_t6(const GemvArgs& a) {
     const int nb = t6_chunk(a.B, a.N, a.K);
     if (nb < 1) return cudaErrorNotSupported;
     const size_t ysz = a.y_bf16 ? 2 : 4;
-    for (int64_t b0 = 0; b0 < a.B; b0 += nb) {
-        const int n = (int)std::min<int64_t>(nb, a.B - b0);
+    // ceil(B / nb) launches with balanced batch chunks (8 rows at nb = 6 run
+    // as 4 + 4, not 6 + 2).
+    const int64_t chunks = (a.B + nb - 1) / nb;
+    for (int64_t i = 0, b0 = 0; i < chunks; ++i) {
+        const int n = (int)(a.B / chunks + (i < a.B % chunks ? 1 : 0));
         const cudaError_t e = launch_t6_chunk(a, n, a.x + b0 * a.K, static_cast<uint8_t*>(a.y) + b0 * a.N * ysz,
                                               a.pdl || b0 > 0);
         if (e != cudaSuccess) return e;
+        b0 += n;
     }
     return cudaSuccess;
 }

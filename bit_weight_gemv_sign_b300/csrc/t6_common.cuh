@@ -124,10 +124,10 @@ __device__ __forceinline__ unsigned short t6_ld(const uint32_t (&w)[4], uint32_t
     return t;
 }
 
-// acc + (fp32) t, the fp16 -> fp32 widening exact, in one mixed-precision FMA.
+// acc + (fp32) t, the fp16 -> fp32 widening exact, in one mixed-precision add
+// (one rounding, in fp32).
 __device__ __forceinline__ float t6_add(unsigned short t, float acc) {
-    const unsigned short one = 0x3C00;
-    asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc) : "h"(t), "h"(one));
+    asm("add.rn.f32.f16 %0, %1, %0;" : "+f"(acc) : "h"(t));
     return acc;
 }
 
