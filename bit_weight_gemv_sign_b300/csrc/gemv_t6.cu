@@ -34,7 +34,9 @@
 //  * K is split over the Q CTAs of a cluster: each builds only its K/Q slice of
 //    tables; the per-row partials are summed in a fixed order through
 //    distributed shared memory (deterministic, so a flipped row negates
-//    exactly).
+//    exactly).  When a CTA has few row blocks (short N), each block is shared
+//    by KW warps that take disjoint group ranges of its slice, so the CTA
+//    still runs up to 16 warps; their partials join the same fixed-order sum.
 //  * The weight stream of the first stages is issued before
 //    griddepcontrol.wait (programmatic dependent launch): only x depends on
 //    the preceding kernel.
@@ -62,12 +64,13 @@ struct T6Params {
     void* y;                  // [NB][N]
     int N, K, Gc, Q, S, stage_bytes, y_bf16;
     int prow;                 // rows per batch row in the partials area (32 x blocks per cluster)
+    int KW;                   // warps sharing one row block, each on Gc/KW of its groups (1: no split)
     uint32_t off_tables, off_factors, off_x, off_partials, off_bars;
 };
 
 // ---------------------------------------------------------------- kernel
 // One CTA per SM (its shared memory sees to that), so all registers are usable.
-template <int NB>
+template <int NB, bool SPLIT>
 __global__ void __launch_bounds__(kT6MaxWarps * 32, 1)
 k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ CUtensorMap tm_sc,
           const __grid_constant__ T6Params p) {
@@ -77,6 +80,10 @@ k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
     uint8_t* sm = smem_raw + (base - raw);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
+    // Warp = (row-block slot wb, K part kw).  With KW > 1 the planner gives
+    // every slot exactly one block, loaded once (no stage reuse), and the KW
+    // warps of a slot read disjoint group ranges of the same stage.
+    const int KW = SPLIT ? p.KW : 1, wb = SPLIT ? warp / KW : warp, kw = warp - wb * KW, WB = W / KW;
     uint32_t q;
     asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(q));
     const int ncl = gridDim.x / p.Q, cl = blockIdx.x / p.Q;
@@ -85,19 +92,19 @@ k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
     const int Gc = p.Gc, S = p.S;
     const int g0 = (int)q * Gc;
     const uint32_t bits_tile = 32u * Gc * 16u, sc_tile = 32u * Gc * 2u;
-    const uint32_t bars = base + p.off_bars + (uint32_t)(warp * S) * 8u;
+    const uint32_t bars = base + p.off_bars + (uint32_t)(wb * S) * 8u;
 
-    auto issue = [&](int k) {  // lane 0: block rb0 + warp + k*W -> stage k % S
-        const int b = rb0 + warp + k * W;
+    auto issue = [&](int k) {  // lane 0 of K part 0: block rb0 + wb + k*WB -> stage k % S
+        const int b = rb0 + wb + k * WB;
         if (b >= rb1) return;
-        const uint32_t st = base + (uint32_t)(warp * S + (k % S)) * p.stage_bytes;
+        const uint32_t st = base + (uint32_t)(wb * S + (k % S)) * p.stage_bytes;
         const uint32_t bar = bars + 8u * (k % S);
         mbar_expect_tx(bar, bits_tile + sc_tile);
         for (int j = 0; j < Gc / 8; ++j)   // 128-byte column j of the slice: groups g0+8j .. g0+8j+7
             tma_2d(st + 4096u * j, &tm_bits, (g0 + 8 * j) * 16, b * 32, bar);
         tma_2d(st + bits_tile, &tm_sc, g0, b * 32, bar);
     };
-    if (lane == 0) {
+    if (lane == 0 && kw == 0) {
         for (int s = 0; s < S; ++s) mbar_init(bars + 8u * s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         for (int k = 0; k < S; ++k) issue(k);
@@ -145,7 +152,8 @@ k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
     const uint32_t tb = base + p.off_tables;
     bool ok = true;
     int k = 0;
-    for (;; ++k) {
+    if constexpr (!SPLIT) {
+      for (;; ++k) {
         const int b = rb0 + warp + k * W;
         if (b >= rb1) break;
         const int s = k % S;
@@ -183,11 +191,48 @@ k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
         for (int bb = 0; bb < NB; ++bb) partials[bb * p.prow + (b - rb0) * 32 + lane] = acc[bb];
         __syncwarp();
         if (lane == 0) issue(k + S);
+      }
+    } else {
+        // K split inside the CTA: this warp's block (one per slot, loaded once
+        // into stage 0 of the slot), groups [g_lo, g_hi) of the slice.
+        const int b = rb0 + wb;
+        const int g_lo = kw * (Gc / KW), g_hi = g_lo + Gc / KW;
+        if (b < rb1) {
+            if (!mbar_wait(bars, 0u)) {
+                if (lane == 0) atomicOr(&g_bit1_wait_timeouts, 1u);
+                ok = false;
+            } else {
+                const uint32_t st = base + (uint32_t)(wb * S) * p.stage_bytes;
+                const uint32_t sts = st + bits_tile + (uint32_t)lane * Gc * 2u;
+                float acc[NB];
+#pragma unroll
+                for (int bb = 0; bb < NB; ++bb) acc[bb] = 0.f;
+                for (int g = g_lo; g < g_hi; ++g) {
+                    const uint32_t L = ((uint32_t)(g & ~7) << 9) + (uint32_t)lane * 128u +
+                                       ((uint32_t)((g & 7) ^ (lane & 7)) << 4);
+                    const uint4 wv = lds128(st + L);
+                    const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+                    unsigned short sh;
+                    asm volatile("ld.shared.b16 %0, [%1];" : "=h"(sh) : "r"(sts + 2u * (uint32_t)g));
+                    const float sc = f16_bits_to_f32(sh);
+#pragma unroll
+                    for (int bb = 0; bb < NB; ++bb) {
+                        const float part = t6_group(w, tb + (uint32_t)((bb * Gc + g) * kT6GroupBytes),
+                                                    std::make_index_sequence<kT6Fields>{});
+                        acc[bb] = fmaf(part * sc, fac[bb * 2 * Gc + g], acc[bb]);
+                    }
+                }
+#pragma unroll
+                for (int bb = 0; bb < NB; ++bb)
+                    partials[(kw * NB + bb) * p.prow + (b - rb0) * 32 + lane] = acc[bb];
+            }
+        }
+        k = 1;
     }
     if (!ok && lane == 0) {
         // Give copies still in flight a bounded chance to land before exit.
         for (int kk = k + 1; kk < k + S; ++kk)
-            if (rb0 + warp + kk * W < rb1) (void)mbar_wait(bars + 8u * (kk % S), (uint32_t)(kk / S) & 1u);
+            if (rb0 + wb + kk * WB < rb1) (void)mbar_wait(bars + 8u * (kk % S), (uint32_t)(kk / S) & 1u);
     }
 
     // Sum the Q partials of every row in a fixed order.
@@ -199,7 +244,14 @@ k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
     for (int b = 0; b < NB; ++b)
     for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
         float v = 0.f;
-        for (int r = 0; r < p.Q; ++r) v += ld_cluster_f32(part_s + 4u * (uint32_t)(b * p.prow + i), (uint32_t)r);
+        for (int r = 0; r < p.Q; ++r) {
+            if constexpr (SPLIT) {
+                for (int j = 0; j < KW; ++j)
+                    v += ld_cluster_f32(part_s + 4u * (uint32_t)((j * NB + b) * p.prow + i), (uint32_t)r);
+            } else {
+                v += ld_cluster_f32(part_s + 4u * (uint32_t)(b * p.prow + i), (uint32_t)r);
+            }
+        }
         const int row = rb0 * 32 + i;
         if (row < p.N) {
             if (p.y_bf16) reinterpret_cast<uint16_t*>(p.y)[(int64_t)b * p.N + row] = f32_to_bf16_bits(v);
@@ -233,19 +285,23 @@ struct T6Plan {
 
 constexpr int kT6MaxNB = 8;
 
-const void* t6_kernel(int nb) {
+template <bool SPLIT>
+const void* t6_kernel_s(int nb) {
     switch (nb) {
-        case 1: return (const void*)k_gemv_t6<1>;
-        case 2: return (const void*)k_gemv_t6<2>;
-        case 3: return (const void*)k_gemv_t6<3>;
-        case 4: return (const void*)k_gemv_t6<4>;
-        case 5: return (const void*)k_gemv_t6<5>;
-        case 6: return (const void*)k_gemv_t6<6>;
-        case 7: return (const void*)k_gemv_t6<7>;
-        case 8: return (const void*)k_gemv_t6<8>;
+        case 1: return (const void*)k_gemv_t6<1, SPLIT>;
+        case 2: return (const void*)k_gemv_t6<2, SPLIT>;
+        case 3: return (const void*)k_gemv_t6<3, SPLIT>;
+        case 4: return (const void*)k_gemv_t6<4, SPLIT>;
+        case 5: return (const void*)k_gemv_t6<5, SPLIT>;
+        case 6: return (const void*)k_gemv_t6<6, SPLIT>;
+        case 7: return (const void*)k_gemv_t6<7, SPLIT>;
+        case 8: return (const void*)k_gemv_t6<8, SPLIT>;
         default: return nullptr;
     }
 }
+
+// The kernel for nb batch rows, with (kw > 1) or without the in-CTA K split.
+const void* t6_kernel(int nb, int kw) { return kw > 1 ? t6_kernel_s<true>(nb) : t6_kernel_s<false>(nb); }
 
 // Cluster sizes that split G into slices of a multiple of 8 groups whose
 // tables (NB batch rows) fit comfortably in shared memory, most preferred
@@ -309,24 +365,41 @@ bool plan_t6_q(int64_t N, int64_t K, int Q, int nb, T6Plan& pl) {
     const int factors = nb * pl.Gc * 8;
     const int xbytes = nb * pl.Gc * 128 * 2;
     const int64_t RB = (N + 31) / 32;
-    auto total = [&](int W, int S, int bpc) {
-        return (size_t)1024 + (size_t)W * S * pl.stage_bytes + tables + factors + xbytes +
-               (size_t)nb * bpc * 128 + (size_t)W * S * 8 + 64;
+    auto total = [&](int W, int S, int bpc, int KW) {
+        return (size_t)1024 + (size_t)(W / KW) * S * pl.stage_bytes + tables + factors + xbytes +
+               (size_t)nb * bpc * 128 * KW + (size_t)(W / KW) * S * 8 + 64;
     };
     // first guess with every SM, then shrink to the clusters that fit at once
     int ncl = sm_count() / Q;
     if (ncl < 1) return false;
-    int W = 0, S = 0, bpc = 0;
+    int W = 0, S = 0, bpc = 0, KW = 1;
     for (int iter = 0; iter < 3; ++iter) {
         bpc = (int)((RB + ncl - 1) / ncl);
-        W = bpc < kT6MaxWarps ? bpc : kT6MaxWarps;
-        if (W < 4) W = 4;  // at least 4 warps: they share the table build
-        S = (bpc + W - 1) / W;
-        if (S > 3) S = 3;
-        while (total(W, S, bpc) > kT6MaxSmem && S > 1) --S;
-        while (total(W, S, bpc) > kT6MaxSmem && W > 4) --W;
-        if (total(W, S, bpc) > kT6MaxSmem) return false;
-        const int act = active_clusters(t6_kernel(nb), Q, W * 32, total(W, S, bpc));
+        // Few row blocks per CTA: give each block KW warps, each on Gc/KW of
+        // its groups (whole 8-group boxes or fewer than 8 groups), so that
+        // the CTA still runs up to 16 warps.  Each block is then loaded once.
+        KW = 1;
+        for (int kw : {8, 4, 2}) {
+            const int gp = pl.Gc / kw;
+            if (bpc * kw <= kT6MaxWarps && pl.Gc % kw == 0 && (gp < 8 || gp % 8 == 0) &&
+                total(bpc * kw, 1, bpc, kw) <= kT6MaxSmem) {
+                KW = kw;
+                break;
+            }
+        }
+        if (KW > 1) {
+            W = bpc * KW;
+            S = 1;
+        } else {
+            W = bpc < kT6MaxWarps ? bpc : kT6MaxWarps;
+            if (W < 4) W = 4;  // at least 4 warps: they share the table build
+            S = (bpc + W - 1) / W;
+            if (S > 3) S = 3;
+            while (total(W, S, bpc, 1) > kT6MaxSmem && S > 1) --S;
+            while (total(W, S, bpc, 1) > kT6MaxSmem && W > 4) --W;
+            if (total(W, S, bpc, 1) > kT6MaxSmem) return false;
+        }
+        const int act = active_clusters(t6_kernel(nb, KW), Q, W * 32, total(W, S, bpc, KW));
         if (act < 1) return false;            // this cluster size cannot run here
         if (act >= ncl) break;
         ncl = act;
@@ -334,13 +407,13 @@ bool plan_t6_q(int64_t N, int64_t K, int Q, int nb, T6Plan& pl) {
     pl.ncl = ncl;
     pl.W = W;
     pl.S = S;
-    pl.smem = total(W, S, bpc);
-    uint32_t off = (uint32_t)(W * S * pl.stage_bytes);
+    pl.smem = total(W, S, bpc, KW);
+    uint32_t off = (uint32_t)((W / KW) * S * pl.stage_bytes);
     pl.p.off_tables = off;        off += tables;           // multiple of 128 (stages are 1 KB multiples)
     pl.p.off_factors = off;       off += factors;          // 16-byte aligned (tables multiple of 128)
     off = (off + 15u) & ~15u;
     pl.p.off_x = off;             off += xbytes;
-    pl.p.off_partials = off;      off += nb * bpc * 128;
+    pl.p.off_partials = off;      off += nb * bpc * 128 * KW;
     off = (off + 7u) & ~7u;
     pl.p.off_bars = off;
     pl.p.N = (int)N;
@@ -350,19 +423,20 @@ bool plan_t6_q(int64_t N, int64_t K, int Q, int nb, T6Plan& pl) {
     pl.p.S = S;
     pl.p.stage_bytes = pl.stage_bytes;
     pl.p.prow = bpc * 32;
+    pl.p.KW = KW;
     return true;
 }
 
 // Relative time of a plan, in units of one warp's work on one 32-row block of
-// one group: a warp runs ceil(bpc / W) blocks of Gc groups back to back (its
-// dependent chain), an SM issues about eight warps' worth at once, and the
+// one group: a warp runs ceil(bpc / WB) blocks of Gc / KW groups back to back
+// (its dependent chain), an SM issues about eight warps' worth at once, and the
 // table build (about 0.75 units per group, spread over the W warps) comes
 // first.  More SMs with fewer warps each can lose: half the warps per CTA and
 // twice the K per CTA doubles every warp's chain.
 double t6_estimate(const T6Plan& pl) {
-    const int bpc = pl.p.prow / 32;
-    const double chain = (double)((bpc + pl.W - 1) / pl.W);
-    return pl.Gc * std::max(chain, bpc / 8.0) + 0.75 * pl.Gc / pl.W;
+    const int bpc = pl.p.prow / 32, KW = pl.p.KW, WB = pl.W / KW;
+    const double chain = (double)((bpc + WB - 1) / WB) * pl.Gc / KW;
+    return std::max(chain, bpc * pl.Gc / 8.0) + 0.75 * pl.Gc / pl.W;
 }
 
 // Among the usable cluster sizes, take the plan with the smallest estimate
@@ -423,7 +497,7 @@ cudaError_t launch_t6_chunk(const GemvArgs& a, int nb, const uint16_t* x, void* 
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    const void* fn = t6_kernel(nb);
+    const void* fn = t6_kernel(nb, pl.p.KW);
     {
         const cudaError_t e = t6_set_attrs(fn);
         if (e != cudaSuccess) return e;

@@ -33,9 +33,12 @@ def _run(bits, scales, x, N, K, B, variant=b1.LUT6, y_dtype=b1.F32, flags=0):
 
 
 # one launch (B <= 8 when the tables fit), several launches (B = 9, 16), ragged
-# row blocks, long K with deep cluster splits
+# row blocks, long K with deep cluster splits; short N (few row blocks per
+# CTA) puts several warps on one block, each on part of its groups
 BATCHED = [(256, 1024, 2), (300, 2048, 3), (1000, 4096, 4), (777, 4096, 5), (4100, 4096, 8),
-           (513, 12288, 6), (129, 5120, 7), (3000, 4096, 16), (64, 16384, 4), (5000, 12288, 9)]
+           (513, 12288, 6), (129, 5120, 7), (3000, 4096, 16), (64, 16384, 4), (5000, 12288, 9),
+           (4096, 4096, 4), (1024, 4096, 5), (2048, 12288, 3), (1, 4096, 2), (33, 1024, 8),
+           (4096, 12288, 2)]
 
 
 @pytest.mark.parametrize("N,K,B", BATCHED)
