@@ -150,16 +150,32 @@ class ClockSampler:
                 "reasons": sorted(self.reasons - {"gpu_idle"})}
 
 
-def _traffic_for(kernel_src: str):
+# Every source the grouped kernel compiles from: a change to any of them
+# invalidates the committed DRAM counters.
+GROUP_KERNEL_SOURCES = ("bit_weight_gemv_sign_b300/csrc/gemv_group.cu",
+                        "bit_weight_gemv_sign_b300/csrc/t6_common.cuh",
+                        "bit_weight_gemv_sign_b300/csrc/common.cuh",
+                        "bit_weight_gemv_sign_b300/csrc/internal.h",
+                        "include/bit1.h")
+
+
+def kernel_sources_hash(paths=GROUP_KERNEL_SOURCES) -> str:
+    h = hashlib.sha256()
+    for rel in paths:
+        h.update(rel.encode())
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_for():
     """Per-launch DRAM bytes of the dominant kernel from the committed ncu
-    summary, or None when the kernel source changed since it was taken."""
+    summary, or None when any of its sources changed since it was taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
         d = json.load(open(p))
-        h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
-        if d.get("kernel_src_sha256_16") != h:
+        if d.get("kernel_sources_sha256_16") != kernel_sources_hash():
             return None
         return d.get("dram_bytes_per_launch_sweep_avg")
     except Exception:
@@ -592,8 +608,7 @@ def run_mine(args):
     chain_ms = max_over_ranks(c0.elapsed_time(c1), dist, "cuda") / chain_steps
 
     hbm, src = _peaks()
-    grp_src = os.path.join(ROOT, "bit_weight_gemv_sign_b300", "csrc", "gemv_group.cu")
-    traffic = _traffic_for(grp_src)
+    traffic = _traffic_for()
     out = {
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
