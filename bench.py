@@ -503,6 +503,50 @@ def extra_t5(torch, b1, reps=20):
     return out
 
 
+def extra_verify_sweep_8b(torch, b1, B=5, steps=20):
+    """A speculative-decoding verify pass on the 8B-class sweep: every matrix
+    multiplies B = 5 rows (four drafted tokens plus one) in one grouped launch,
+    against the same 253 products as per-matrix batched launches (graph + PDL)
+    and the batch-1 sweep."""
+    from bit_weight_gemv_sign_b300 import synth
+    from bit_weight_gemv_sign_b300.sweep import Sweep
+    sw = Sweep(synth.sweep_8b(), seed0=0, batch=B, y_dtype=b1.BF16).fill_device(55)
+    plan = sw.group_plan()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            plan.run(stream=s)
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            plan.run(stream=s)
+        e1.record(s)
+        e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    sw.capture(pdl=True)
+    with torch.cuda.stream(sw.stream):       # graph replays run on the current stream
+        for _ in range(2):
+            sw.replay()
+        sw.stream.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(sw.stream)
+        for _ in range(5):
+            sw.replay()
+        c1.record(sw.stream)
+        c1.synchronize()
+    ms_chain = c0.elapsed_time(c1) / 5
+    hbm, _ = _peaks()
+    gbs = sw.weight_bytes / (ms * 1e-3) / 1e9
+    out = {"batch_rows": B, "weight_bytes": sw.weight_bytes, "ms_per_verify_step": ms,
+           "ms_per_token_row": ms / B, "weight_gbs": gbs, "hbm_frac": gbs / hbm,
+           "ms_per_step_per_matrix_launches": ms_chain, "launches_per_step_per_matrix": sw.launches_per_step(),
+           "note": "one grouped launch per step; compare ms_per_token_row with the batch-1 sweep's ms_per_step"}
+    del sw, plan
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_mine(args):
     import torch
     import bit_weight_gemv_sign_b300 as b1
@@ -642,7 +686,8 @@ def run_mine(args):
                          "pp512_tcgen05": extra_pp512(torch, b1),
                          "c5_sweep_27b": extra_c5_sweep_27b(torch, b1),
                          "ternary_sweep_8b": extra_ternary_sweep_8b(torch, b1),
-                         "ternary_t5": extra_t5(torch, b1)}
+                         "ternary_t5": extra_t5(torch, b1),
+                         "verify_sweep_8b_b5": extra_verify_sweep_8b(torch, b1)}
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
         oracle.build()

@@ -90,6 +90,8 @@ def load():
         lib.bit1_group_plan_bytes.restype = sz
         lib.bit1_group_plan.argtypes = [ctypes.POINTER(_Problem), i32, p, sz]
         lib.bit1_group_plan.restype = i32
+        lib.bit1_group_plan_batched.argtypes = [ctypes.POINTER(_Problem), i32, i32, p, sz]
+        lib.bit1_group_plan_batched.restype = i32
         lib.bit1_gemv_group.argtypes = [p, p, ctypes.c_uint, p]
         lib.bit1_gemv_group.restype = i32
         lib.bit1_gemv_tc_noalloc.argtypes = [p, p, p, i64, i64, i64, p, i32, ctypes.c_uint, p]
@@ -268,8 +270,9 @@ def bit1_group_plan_bytes(count: int) -> int:
     return int(load().bit1_group_plan_bytes(int(count)))
 
 
-def bit1_group_plan(problems, host_plan_ptr: int, plan_bytes: int) -> None:
-    """problems: sequence of (bits, scales, x, y) CUDA tensors (batch 1)."""
+def bit1_group_plan(problems, host_plan_ptr: int, plan_bytes: int, B: int = 1) -> None:
+    """problems: sequence of (bits, scales, x, y) CUDA tensors; x is [B, K]
+    (or [K] at B = 1) bf16 and y [B, N].  B > 1 calls bit1_group_plan_batched."""
     import torch
     arr = (_Problem * len(problems))()
     for i, (bits, scales, x, y) in enumerate(problems):
@@ -277,7 +280,10 @@ def bit1_group_plan(problems, host_plan_ptr: int, plan_bytes: int) -> None:
             raise TypeError("y must be float32 or bfloat16")
         arr[i] = _Problem(_dptr(bits, "bits"), _dptr(scales, "scales"), _dptr(x, "x"), _dptr(y, "y"),
                           bits.shape[0], x.shape[-1], BF16 if y.dtype == torch.bfloat16 else F32)
-    st = load().bit1_group_plan(arr, len(problems), host_plan_ptr, plan_bytes)
+    if B == 1:
+        st = load().bit1_group_plan(arr, len(problems), host_plan_ptr, plan_bytes)
+    else:
+        st = load().bit1_group_plan_batched(arr, len(problems), int(B), host_plan_ptr, plan_bytes)
     _check(st, "bit1_group_plan")
 
 
@@ -291,15 +297,16 @@ class GroupPlan:
     128-byte aligned).  The tensors named in ``problems`` must stay alive and
     in place while the plan is used."""
 
-    def __init__(self, problems, device="cuda"):
+    def __init__(self, problems, device="cuda", B: int = 1):
         import numpy as np
         import torch
         self.problems = list(problems)
+        self.B = int(B)
         self.nbytes = bit1_group_plan_bytes(len(self.problems))
         self._host_raw = np.zeros(self.nbytes + 128, dtype=np.uint8)
         off = (-self._host_raw.ctypes.data) % 128
         self.host = self._host_raw[off: off + self.nbytes]
-        bit1_group_plan(self.problems, self.host.ctypes.data, self.nbytes)
+        bit1_group_plan(self.problems, self.host.ctypes.data, self.nbytes, self.B)
         self._dev_raw = torch.empty(self.nbytes + 128, dtype=torch.uint8, device=device)
         doff = (-self._dev_raw.data_ptr()) % 128
         self.dev = self._dev_raw[doff: doff + self.nbytes]

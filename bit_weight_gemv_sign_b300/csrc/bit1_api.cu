@@ -220,7 +220,12 @@ size_t bit1_group_plan_bytes(int count) { return group_plan_bytes(count); }
 
 bit1_status bit1_group_plan(const bit1_gemv_problem* problems, int count, void* host_plan,
                             size_t plan_bytes) {
-    return group_plan(problems, count, host_plan, plan_bytes);
+    return group_plan(problems, count, 1, host_plan, plan_bytes);
+}
+
+bit1_status bit1_group_plan_batched(const bit1_gemv_problem* problems, int count, int B, void* host_plan,
+                                    size_t plan_bytes) {
+    return group_plan(problems, count, B, host_plan, plan_bytes);
 }
 
 bit1_status bit1_ternary_planes(const int8_t* codes, int64_t N, int64_t K, uint8_t* a, uint8_t* b,

@@ -35,17 +35,27 @@ namespace bit1 {
 
 __device__ unsigned int g_group_wait_timeouts = 0;
 
-constexpr int kGChunkGroups = 32;            // K chunk: 32 groups = 4096 inputs
+constexpr int kGChunkGroups = 32;            // K chunk at batch 1: 32 groups = 4096 inputs
 constexpr int kGStageBytes = 5120;           // 4 KB bits box + 512 B scales box, 1 KB aligned
 constexpr int kGMaxCtas = 160;
 constexpr int kGWarps = 20;
 constexpr int kGMaxSmem = 227 * 1024;
 constexpr int kGSegBlocks = 128;             // sub-segment cap: 4096 rows of partials
 constexpr int kGMaxProbsPerCta = 64;         // problems one CTA's range may touch
+constexpr int kGMaxNB = 6;                   // batch rows per grouped launch
+
+// K chunk (groups) at nb batch rows: the tables of all rows, nb * CG * 2816
+// bytes, stay at about 90 KB.
+__host__ __device__ constexpr int g_chunk_groups(int nb) { return nb == 1 ? 32 : nb == 2 ? 16 : 8; }
+// Row blocks per sub-segment of a multi-chunk problem: nb * 32 * seg floats of
+// partials stay at about 16 KB.
+__host__ __device__ constexpr int g_seg_blocks(int nb) { return nb == 1 ? 128 : nb == 2 ? 64 : nb <= 4 ? 32 : 16; }
 
 struct GHeader {            // 64 bytes
     int count, nctas, W, S;
-    uint32_t off_tables, off_x, off_fac, off_part, off_bars;
+    uint32_t off_tables;
+    int nb;                 // batch rows: x is [nb][K], y is [nb][N] for every problem
+    uint32_t off_fac, off_part, off_bars;
     int part_rows, smem_bytes, ranges_off, probs_off;
     int seg_blocks;         // row blocks per sub-segment of a problem with K > 4096
     uint32_t off_xraw;      // raw bf16 activations of the next phase (bulk copy target)
@@ -82,6 +92,7 @@ struct GIter {               // position in one warp's sequence of stages
 // one K chunk are cut: their row partials live in shared memory between
 // chunks); per sub-segment, chunk by chunk; per chunk, this warp's blocks
 // (every W-th); per block, the chunk's 8-group slices.
+template <int CG>
 struct GCtx {
     const GProb* P;
     const int4* I;          // shared memory: {RB, G, nch, N} of problems R.p0.. (index p - R.p0)
@@ -94,7 +105,7 @@ struct GCtx {
     __device__ __forceinline__ int mb(int p) const { return nch(p) > 1 ? seg_blocks : 0x3fffffff; }
     __device__ __forceinline__ int se(int p, int sb) const { return min(be(p), sb + mb(p)); }
     __device__ __forceinline__ int slices(int p, int c) const {
-        const int cg = min(kGChunkGroups, info(p).y - kGChunkGroups * c);
+        const int cg = min(CG, info(p).y - CG * c);
         return cg >> 3;
     }
     __device__ __forceinline__ bool done(const GIter& it) const { return it.p > R.p1; }
@@ -153,14 +164,16 @@ struct GCtx {
     }
 };
 
+template <int CG>
 __device__ __forceinline__ void g_issue(const GProb* P, const GIter& it, uint32_t st, uint32_t bar) {
     const GProb& pr = P[it.p];
-    const int g = kGChunkGroups * it.c + 8 * it.j;
+    const int g = CG * it.c + 8 * it.j;
     mbar_expect_tx(bar, 4096u + 512u);
     tma_2d(st, &pr.tm_bits, g * 16, it.b * 32, bar);
     tma_2d(st + 4096u, &pr.tm_sc, g, it.b * 32, bar);
 }
 
+template <int NB, int CG>
 __device__ __forceinline__ void g_body(const uint8_t* plan) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
@@ -168,8 +181,8 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
     uint8_t* sm = smem_raw + (base - raw);
 
     const GHeader* H = reinterpret_cast<const GHeader*>(plan);
-    const int W = H->W, S = H->S;
-    GCtx cx;
+    const int W = H->W, S = H->S, prows = H->part_rows;
+    GCtx<CG> cx;
     cx.P = reinterpret_cast<const GProb*>(plan + H->probs_off);
     cx.R = reinterpret_cast<const GRange*>(plan + H->ranges_off)[blockIdx.x];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -193,7 +206,7 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
         for (int s = 0; s < S; ++s) mbar_init(bars + 8u * s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         for (int s = 0; s < S && !cx.done(prod); ++s) {
-            g_issue(P, prod, stages + (uint32_t)s * kGStageBytes, bars + 8u * s);
+            g_issue<CG>(P, prod, stages + (uint32_t)s * kGStageBytes, bars + 8u * s);
             cx.next(prod);
         }
     } else {
@@ -205,11 +218,13 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
     // phase ahead (mbarrier xbar, one completion per phase).
     const uint32_t xbar = base + H->off_bars + (uint32_t)(W * S) * 8u;
     const uint32_t xraw = base + H->off_xraw;
-    auto prefetch_x = [&](int p, int c) {
+    auto prefetch_x = [&](int p, int c) {   // chunk c of every batch row's x
         const GProb& q = P[p];
-        const int cg = min(kGChunkGroups, q.G - kGChunkGroups * c);
-        mbar_expect_tx(xbar, (uint32_t)cg * 256u);
-        bulk_g2s(xraw, q.x + (size_t)c * kGChunkGroups * 128, (uint32_t)cg * 256u, xbar);
+        const int cg = min(CG, q.G - CG * c);
+        mbar_expect_tx(xbar, (uint32_t)(NB * cg) * 256u);
+        for (int b = 0; b < NB; ++b)
+            bulk_g2s(xraw + (uint32_t)(b * CG) * 256u, q.x + (size_t)b * q.K + (size_t)c * CG * 128,
+                     (uint32_t)cg * 256u, xbar);
     };
     pdl_wait();   // inputs may come from the preceding kernel
     if (threadIdx.x == 0) {
@@ -235,7 +250,7 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
       for (int sb = cx.bs(p); sb < cx.be(p); sb += cx.mb(p)) {
         const int be = cx.se(p, sb);
         for (int c = 0; c < pi.z; ++c) {
-            const int cg = min(kGChunkGroups, pi.y - kGChunkGroups * c);
+            const int cg = min(CG, pi.y - CG * c);
             // --- tables for (problem p, chunk c): every thread of the CTA
             __syncthreads();                                   // old tables no longer read
             if (!mbar_wait(xbar, (uint32_t)(xphase & 1))) {     // this phase's activations
@@ -243,8 +258,9 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
                 ok = false;
             }
             ++xphase;
-            for (int g = warp; g < cg; g += W) {               // one group per warp pass
-                const uint2 xv = *reinterpret_cast<const uint2*>(xr + g * 128 + 4 * lane);
+            for (int bg = warp; bg < NB * cg; bg += W) {       // one (row, group) per warp pass
+                const int b = bg / cg, g = bg - b * cg;
+                const uint2 xv = *reinterpret_cast<const uint2*>(xr + (b * CG + g) * 128 + 4 * lane);
                 const float x0 = bf16_bits_to_f32(xv.x & 0xffffu), x1 = bf16_bits_to_f32(xv.x >> 16);
                 const float x2 = bf16_bits_to_f32(xv.y & 0xffffu), x3 = bf16_bits_to_f32(xv.y >> 16);
                 float m = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
@@ -256,15 +272,16 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
                     mg = min(max(e - 11, -126), 127);          // max|x'| < 2^12
                 }
                 if (lane == 0) {
-                    fac[g] = __uint_as_float((uint32_t)(mg + 127) << 23);
-                    fac[kGChunkGroups + g] = __uint_as_float((uint32_t)(127 - mg) << 23);
+                    fac[b * 2 * CG + g] = __uint_as_float((uint32_t)(mg + 127) << 23);
+                    fac[b * 2 * CG + CG + g] = __uint_as_float((uint32_t)(127 - mg) << 23);
                 }
             }
             __syncthreads();
-            for (int t = threadIdx.x; t < cg * kT6Fields * 4; t += blockDim.x) {
-                const int tt = t >> 2, g = tt / kT6Fields, f = tt - g * kT6Fields;
-                t6_build_pair(tabs + g * kT6GroupBytes + f * kT6TableBytes, xr + g * 128,
-                              fac[kGChunkGroups + g], f, t & 3, tt & 1);
+            for (int t = threadIdx.x; t < NB * cg * kT6Fields * 4; t += blockDim.x) {
+                const int tt = t >> 2, bg = tt / kT6Fields, f = tt - bg * kT6Fields;
+                const int b = bg / cg, g = bg - b * cg;
+                t6_build_pair(tabs + (b * CG + g) * kT6GroupBytes + f * kT6TableBytes, xr + (b * CG + g) * 128,
+                              fac[b * 2 * CG + CG + g], f, t & 3, tt & 1);
             }
             __syncthreads();
             if (threadIdx.x == 0) {                            // raw x consumed: fetch the next phase's
@@ -276,7 +293,9 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
             // --- this warp's blocks of the sub-segment, for chunk c
             const int nsl = cg >> 3;
             for (int b = sb + warp; b < be; b += W) {
-                float acc = 0.f;
+                float acc[NB];
+#pragma unroll
+                for (int bb = 0; bb < NB; ++bb) acc[bb] = 0.f;
                 for (int j = 0; j < nsl; ++j, ++k) {
                     const int s = k % S;
                     if (ok && !mbar_wait(bars + 8u * s, (uint32_t)(k / S) & 1u)) {
@@ -287,38 +306,62 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
                     if (ok) {
                         const uint32_t st = stages + (uint32_t)s * kGStageBytes;
                         const uint4 sv = lds128(st + 4096u + 16u * lane);       // 8 scales of row `lane`
-                        const uint4 fa = lds128(fac_s + 32u * j), fb = lds128(fac_s + 32u * j + 16u);
                         const uint32_t svw[4] = {sv.x, sv.y, sv.z, sv.w};
-                        const uint32_t fw[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+                        if constexpr (NB == 1) {
+                            const uint4 fa = lds128(fac_s + 32u * j), fb = lds128(fac_s + 32u * j + 16u);
+                            const uint32_t fw[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
 #pragma unroll
-                        for (int jj = 0; jj < 8; ++jj) {
-                            const uint32_t L = (uint32_t)lane * 128u + ((uint32_t)(jj ^ (lane & 7)) << 4);
-                            const uint4 wv = lds128(st + L);
-                            const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
-                            const float pt = t6_group(w4, tb + (uint32_t)(8 * j + jj) * kT6GroupBytes,
-                                                      std::make_index_sequence<kT6Fields>{});
-                            const float sc = f16_bits_to_f32((uint16_t)(svw[jj >> 1] >> (16 * (jj & 1))));
-                            acc = fmaf(pt * sc, __uint_as_float(fw[jj]), acc);
+                            for (int jj = 0; jj < 8; ++jj) {
+                                const uint32_t L = (uint32_t)lane * 128u + ((uint32_t)(jj ^ (lane & 7)) << 4);
+                                const uint4 wv = lds128(st + L);
+                                const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+                                const float pt = t6_group(w4, tb + (uint32_t)(8 * j + jj) * kT6GroupBytes,
+                                                          std::make_index_sequence<kT6Fields>{});
+                                const float sc = f16_bits_to_f32((uint16_t)(svw[jj >> 1] >> (16 * (jj & 1))));
+                                acc[0] = fmaf(pt * sc, __uint_as_float(fw[jj]), acc[0]);
+                            }
+                        } else {
+                            // Several batch rows: the 16 sign bytes of a group are read
+                            // once and looked up in every row's tables.
+#pragma unroll
+                            for (int jj = 0; jj < 8; ++jj) {
+                                const uint32_t L = (uint32_t)lane * 128u + ((uint32_t)(jj ^ (lane & 7)) << 4);
+                                const uint4 wv = lds128(st + L);
+                                const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+                                const float sc = f16_bits_to_f32((uint16_t)(svw[jj >> 1] >> (16 * (jj & 1))));
+#pragma unroll
+                                for (int bb = 0; bb < NB; ++bb) {
+                                    const int g = bb * CG + 8 * j + jj;
+                                    const float pt = t6_group(w4, tb + (uint32_t)g * kT6GroupBytes,
+                                                              std::make_index_sequence<kT6Fields>{});
+                                    acc[bb] = fmaf(pt * sc, fac[bb * 2 * CG + 8 * j + jj], acc[bb]);
+                                }
+                            }
                         }
                     }
                     __syncwarp();
                     if (lane == 0 && ok && !cx.done(prod))
-                        g_issue(P, prod, stages + (uint32_t)(k % S) * kGStageBytes, bars + 8u * (k % S));
+                        g_issue<CG>(P, prod, stages + (uint32_t)(k % S) * kGStageBytes, bars + 8u * (k % S));
                     if (!cx.done(prod)) cx.next(prod);
                 }
                 const int row = b * 32 + lane;
                 const int li = (b - sb) * 32 + lane;           // row within the sub-segment
                 if (pi.z > 1) {
-                    const float v = (c == 0) ? acc : part[li] + acc;
-                    if (c + 1 < pi.z) {
-                        part[li] = v;
-                        continue;
+#pragma unroll
+                    for (int bb = 0; bb < NB; ++bb) {
+                        const int pl = bb * prows + li;
+                        acc[bb] = (c == 0) ? acc[bb] : part[pl] + acc[bb];
+                        if (c + 1 < pi.z) part[pl] = acc[bb];
                     }
-                    acc = v;
+                    if (c + 1 < pi.z) continue;
                 }
                 if (row < pi.w) {
-                    if (pr.y_bf16) reinterpret_cast<uint16_t*>(pr.y)[row] = f32_to_bf16_bits(acc);
-                    else reinterpret_cast<float*>(pr.y)[row] = acc;
+#pragma unroll
+                    for (int bb = 0; bb < NB; ++bb) {
+                        const int64_t o = (int64_t)bb * pi.w + row;
+                        if (pr.y_bf16) reinterpret_cast<uint16_t*>(pr.y)[o] = f32_to_bf16_bits(acc[bb]);
+                        else reinterpret_cast<float*>(pr.y)[o] = acc[bb];
+                    }
                 }
             }
         }
@@ -332,11 +375,17 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
 }
 
 __global__ void __launch_bounds__(kGWarps * 32, 1) k_gemv_group(const uint8_t* __restrict__ plan) {
-    g_body(plan);
+    g_body<1, g_chunk_groups(1)>(plan);
+}
+
+// Several batch rows per problem: at most 16 warps, so 128 registers a thread.
+template <int NB>
+__global__ void __launch_bounds__(16 * 32, 1) k_gemv_group_b(const uint8_t* __restrict__ plan) {
+    g_body<NB, g_chunk_groups(NB)>(plan);
 }
 
 __global__ void __launch_bounds__(kGWarps * 32, 1) k_gemv_group1(const __grid_constant__ GSingle plan) {
-    g_body(reinterpret_cast<const uint8_t*>(&plan));
+    g_body<1, g_chunk_groups(1)>(reinterpret_cast<const uint8_t*>(&plan));
 }
 
 // ---------------------------------------------------------------- host
@@ -355,7 +404,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode() {
     return fn;
 }
 
-bool encode_prob(GProb& g, const bit1_gemv_problem& pb) {
+bool encode_prob(GProb& g, const bit1_gemv_problem& pb, int nb) {
     auto enc = g_encode();
     if (!enc) return false;
     const int64_t G = pb.K / 128;
@@ -386,31 +435,36 @@ bool encode_prob(GProb& g, const bit1_gemv_problem& pb) {
     g.G = (int)G;
     g.RB = (int)((pb.N + 31) / 32);
     g.y_bf16 = pb.y_dtype == BIT1_BF16;
-    g.nch = (int)((G + kGChunkGroups - 1) / kGChunkGroups);
+    const int cg = g_chunk_groups(nb);
+    g.nch = (int)((G + cg - 1) / cg);
     return true;
 }
 
 // Contiguous block ranges, one per CTA, balanced on an estimate of each
-// CTA's time: a block costs K (its bytes are proportional to K) and every
-// table build (first block of a problem in the CTA, and every kGSegBlocks-th
-// block of a problem with several K chunks) costs kGBuildCost per chunk.  A
+// CTA's time: a block costs K (its bytes are proportional to K; its lookups
+// to K times the batch rows) and every table build (first block of a problem
+// in the CTA, and every seg-th block of a problem with several K chunks)
+// costs kGBuildCost per chunk, scaled by the chunk's tables (nb * CG groups
+// against 32 at batch 1).  A
 // greedy pass packs blocks in order under a per-CTA budget; a binary search
 // finds the smallest budget that fits in nctas CTAs.  Then the shared memory
 // layout; false if it does not fit.
 constexpr double kGBuildCost = 6.0 * 4096;    // one chunk build ~ six 4096-wide blocks (measured)
 
-int partition(const std::vector<GProb>& probs, double T, std::vector<GRange>* out) {
+int partition(const std::vector<GProb>& probs, double T, std::vector<GRange>* out, int nb) {
     const int n = (int)probs.size();
+    const int seg = g_seg_blocks(nb);
+    const double rowf = 1.0 + 0.8 * (nb - 1);     // lookups grow with the batch, the weight reads do not
     int ctas = 1;
     double cur = 0.0;
     GRange r{0, 0, 0, 0};
     for (int p = 0; p < n; ++p) {
         int taken = 0;
-        const double c = (double)probs[p].K;
-        const double build = kGBuildCost * probs[p].nch;
+        const double c = (double)probs[p].K * rowf;
+        const double build = kGBuildCost * probs[p].nch * (nb * g_chunk_groups(nb) / 32.0);
         for (int b = 0; b < probs[p].RB; ++b) {
             double add = c;
-            if (taken == 0 || (probs[p].nch > 1 && taken % kGSegBlocks == 0)) add += build;
+            if (taken == 0 || (probs[p].nch > 1 && taken % seg == 0)) add += build;
             if (cur > 0.0 && cur + add > T) {
                 if (out) { r.p1 = p; r.b1 = b; out->push_back(r); }
                 r = GRange{p, b, p, b};
@@ -427,18 +481,21 @@ int partition(const std::vector<GProb>& probs, double T, std::vector<GRange>* ou
     return ctas;
 }
 
-bool plan_layout(const std::vector<GProb>& probs, int nctas, GHeader& h, std::vector<GRange>& ranges) {
+bool plan_layout(const std::vector<GProb>& probs, int nctas, int nb, GHeader& h, std::vector<GRange>& ranges) {
     const int n = (int)probs.size();
+    const int CG = g_chunk_groups(nb), seg = g_seg_blocks(nb);
+    const double rowf = 1.0 + 0.8 * (nb - 1);
     double total = 0.0;
-    for (int p = 0; p < n; ++p) total += (double)probs[p].RB * probs[p].K + kGBuildCost * probs[p].nch;
-    double lo = total / nctas, hi = total + kGBuildCost * 8;
+    for (int p = 0; p < n; ++p)
+        total += (double)probs[p].RB * probs[p].K * rowf + kGBuildCost * probs[p].nch * (nb * CG / 32.0);
+    double lo = total / nctas, hi = total + kGBuildCost * nb * 8;
     for (int it = 0; it < 60 && hi - lo > 1e-4 * lo; ++it) {
         const double mid = 0.5 * (lo + hi);
-        if (partition(probs, mid, nullptr) <= nctas) hi = mid;
+        if (partition(probs, mid, nullptr, nb) <= nctas) hi = mid;
         else lo = mid;
     }
     ranges.clear();
-    partition(probs, hi, &ranges);
+    partition(probs, hi, &ranges, nb);
     while ((int)ranges.size() < nctas)            // CTAs without work
         ranges.push_back(GRange{n - 1, probs[n - 1].RB, n - 1, probs[n - 1].RB});
     for (const GRange& r : ranges)
@@ -448,24 +505,27 @@ bool plan_layout(const std::vector<GProb>& probs, int nctas, GHeader& h, std::ve
         for (int p = r.p0; p <= r.p1 && p < n; ++p) {
             if (probs[p].nch <= 1) continue;
             const int bs = p == r.p0 ? r.b0 : 0, be = p == r.p1 ? r.b1 : probs[p].RB;
-            if (be > bs) part_rows = std::max(part_rows, std::min(be - bs, kGSegBlocks) * 32);
+            if (be > bs) part_rows = std::max(part_rows, std::min(be - bs, seg) * 32);
         }
     h.count = n;
     h.nctas = nctas;
+    h.nb = nb;
     h.part_rows = part_rows;
-    h.seg_blocks = kGSegBlocks;
-    const int tables = kGChunkGroups * kT6GroupBytes;
-    // (warps, stages per warp) in order of preference; the first that fits wins
+    h.seg_blocks = seg;
+    const int tables = nb * CG * kT6GroupBytes;
+    // (warps, stages per warp) in order of preference; the first that fits
+    // wins.  Several batch rows: at most 16 warps (the kernel's register cap).
     static const int kCfg[][2] = {{20, 1}, {16, 1}, {12, 1}, {8, 2}, {8, 1}};
     for (const auto& cf : kCfg) {
         const int W = cf[0], S = cf[1];
+        if (nb > 1 && W > 16) continue;
         {
             uint32_t off = (uint32_t)(W * S * kGStageBytes);
             const uint32_t off_tables = off;  off += tables;
-            const uint32_t off_fac = off;     off += kGChunkGroups * 8;   // 2^m_g and 2^-m_g
-            const uint32_t off_xraw = off;    off += kGChunkGroups * 128 * 2;
+            const uint32_t off_fac = off;     off += nb * CG * 8;      // 2^m_g and 2^-m_g per row
+            const uint32_t off_xraw = off;    off += nb * CG * 128 * 2;
             const uint32_t off_pinfo = off;   off += kGMaxProbsPerCta * 16;
-            const uint32_t off_part = off;    off += (uint32_t)part_rows * 4;
+            const uint32_t off_part = off;    off += (uint32_t)(part_rows * nb) * 4;
             off = (off + 7u) & ~7u;
             const uint32_t off_bars = off;    off += W * S * 8 + 8;
             const size_t smem = 1024 + (size_t)off;
@@ -506,18 +566,19 @@ size_t group_plan_bytes(int count) {
     return probs_off + (size_t)count * sizeof(GProb);
 }
 
-bit1_status group_plan(const bit1_gemv_problem* problems, int count, void* host_plan, size_t bytes) {
+bit1_status group_plan(const bit1_gemv_problem* problems, int count, int nb, void* host_plan, size_t bytes) {
     if (count < 1 || !problems || !host_plan) return BIT1_EINVAL;
+    if (nb < 1 || nb > kGMaxNB) return BIT1_ESHAPE;
     if (bytes < group_plan_bytes(count) || ((uintptr_t)host_plan & 127)) return BIT1_EINVAL;
     for (int i = 0; i < count; ++i)
         if (!problem_ok(problems[i])) return BIT1_ESHAPE;
     std::vector<GProb> probs(count);
     for (int i = 0; i < count; ++i)
-        if (!encode_prob(probs[i], problems[i])) return BIT1_ECUDA;
+        if (!encode_prob(probs[i], problems[i], nb)) return BIT1_ECUDA;
     GHeader h{};
     std::vector<GRange> ranges;
     const int nctas = std::min(sm_count(), kGMaxCtas);
-    if (!plan_layout(probs, nctas, h, ranges)) return BIT1_ESHAPE;
+    if (!plan_layout(probs, nctas, nb, h, ranges)) return BIT1_ESHAPE;
     const size_t r_off = 64;
     const size_t p_off = (r_off + (size_t)kGMaxCtas * sizeof(GRange) + 127) & ~(size_t)127;
     h.ranges_off = (int)r_off;
@@ -532,12 +593,22 @@ bit1_status group_plan(const bit1_gemv_problem* problems, int count, void* host_
 
 cudaError_t launch_group(const void* device_plan, const void* host_plan, bool pdl, cudaStream_t stream) {
     const GHeader* h = static_cast<const GHeader*>(host_plan);
-    cudaError_t e = set_smem_attr((const void*)k_gemv_group);
+    const void* fn = nullptr;
+    switch (h->nb) {
+        case 1: fn = (const void*)k_gemv_group; break;
+        case 2: fn = (const void*)k_gemv_group_b<2>; break;
+        case 3: fn = (const void*)k_gemv_group_b<3>; break;
+        case 4: fn = (const void*)k_gemv_group_b<4>; break;
+        case 5: fn = (const void*)k_gemv_group_b<5>; break;
+        case 6: fn = (const void*)k_gemv_group_b<6>; break;
+        default: return cudaErrorInvalidValue;
+    }
+    cudaError_t e = set_smem_attr(fn);
     if (e != cudaSuccess) return e;
     const uint8_t* dp = static_cast<const uint8_t*>(device_plan);
     void* args[] = {(void*)&dp};
-    return launch((const void*)k_gemv_group, dim3((unsigned)h->nctas), dim3((unsigned)(h->W * 32)),
-                  (size_t)h->smem_bytes, stream, pdl, args);
+    return launch(fn, dim3((unsigned)h->nctas), dim3((unsigned)(h->W * 32)), (size_t)h->smem_bytes, stream, pdl,
+                  args);
 }
 
 bool group1_supported(int64_t B, int64_t N, int64_t K) {
@@ -555,14 +626,14 @@ cudaError_t launch_gemv_group1(const GemvArgs& a) {
     pb.y_dtype = a.y_bf16 ? BIT1_BF16 : BIT1_F32;
     if (!problem_ok(pb)) return cudaErrorInvalidValue;
     std::vector<GProb> probs(1);
-    if (!encode_prob(probs[0], pb)) return cudaErrorInvalidValue;
+    if (!encode_prob(probs[0], pb, 1)) return cudaErrorInvalidValue;
     static GSingle single;  // large: keep off the stack; filled and copied into the launch
     static std::mutex mu;
     std::lock_guard<std::mutex> lk(mu);
     std::memset(&single, 0, sizeof(single));
     std::vector<GRange> ranges;
     const int nctas = std::min(sm_count(), kGMaxCtas);
-    if (!plan_layout(probs, nctas, single.h, ranges)) return cudaErrorInvalidValue;
+    if (!plan_layout(probs, nctas, 1, single.h, ranges)) return cudaErrorInvalidValue;
     single.h.ranges_off = (int)offsetof(GSingle, r);
     single.h.probs_off = (int)offsetof(GSingle, p);
     std::memcpy(single.r, ranges.data(), ranges.size() * sizeof(GRange));

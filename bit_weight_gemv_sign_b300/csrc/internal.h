@@ -50,7 +50,7 @@ unsigned int t6_take_timeouts();
 
 // Grouped persistent kernel (gemv_group.cu).
 size_t group_plan_bytes(int count);
-bit1_status group_plan(const bit1_gemv_problem* problems, int count, void* host_plan, size_t bytes);
+bit1_status group_plan(const bit1_gemv_problem* problems, int count, int nb, void* host_plan, size_t bytes);
 cudaError_t launch_group(const void* device_plan, const void* host_plan, bool pdl, cudaStream_t stream);
 bool group1_supported(int64_t B, int64_t N, int64_t K);
 cudaError_t launch_gemv_group1(const GemvArgs& a);

@@ -135,12 +135,13 @@ class Sweep:
 
     def group_plan(self, x=None, y=None):
         """One grouped launch over every matrix of the sweep (each with its own
-        input): the plan is built once; run() is one kernel launch.  ``x`` and
+        input, ``batch`` rows of it): the plan is built once; run() is one
+        kernel launch.  ``x`` and
         ``y`` replace the activation / output arenas (same layout), e.g. for a
         second I/O slot over the same resident weights."""
         probs = [(self.bits_of(i), self.scales_of(i), self.x_of(i, x), self.y_of(i, y))
                  for i in range(len(self.mats))]
-        return GroupPlan(probs, device=self.device)
+        return GroupPlan(probs, device=self.device, B=self.B)
 
     def apply_patch(self, entries, proj_count: int = 7):
         """Apply (or, applied again, remove) a list of (layer, projection, row)

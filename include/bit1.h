@@ -181,6 +181,17 @@ typedef struct bit1_gemv_problem {
 size_t bit1_group_plan_bytes(int count);
 bit1_status bit1_group_plan(const bit1_gemv_problem *problems, int count,
                             void *host_plan, size_t plan_bytes);
+
+/* The same with B batch rows per problem (1 <= B <= 6, else BIT1_ESHAPE):
+ * every problem's x is bf16 [B][K] and its y is [B][N] (row-major, y_dtype),
+ * all problems sharing B.  This is the batched verify pass of a speculative
+ * drafter (the Bonsai 27B page, section "DSpark: 추측 디코딩으로 한 번 더
+ * 가속": the target model checks the k drafted tokens in one multi-row pass).
+ * The whole weight set runs once for all B rows: the sign bits of a group are
+ * read once and looked up in every row's tables.  Same plan buffer size and
+ * the same bit1_gemv_group call. */
+bit1_status bit1_group_plan_batched(const bit1_gemv_problem *problems, int count,
+                                    int B, void *host_plan, size_t plan_bytes);
 /* flags: BIT1_FLAG_PDL or 0. */
 bit1_status bit1_gemv_group(const void *device_plan, const void *host_plan,
                             unsigned flags, bit1_stream_t stream);
