@@ -59,7 +59,7 @@ bit1_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BIT1_OK : BIT1_
 // kernel); larger or batched: the 6-bit-table kernel (up to 8 batch rows per
 // launch); what none of them takes: one warp per row.
 int pick_variant(int64_t B, int64_t N, int64_t K, size_t ws_bytes) {
-    if (B >= 16 && tc_supported(B, N, K) && ws_bytes >= tc_workspace_bytes(B, N, K)) return BIT1_GEMV_TC;
+    if (B >= 16 && tc_supported(B, N, K) && ws_bytes >= tc_min_workspace_bytes(B, N, K)) return BIT1_GEMV_TC;
     if (B == 1 && N < 65536 && lut_supported(B, N, K)) return BIT1_GEMV_LUT;
     if (t6_supported(B, N, K)) return BIT1_GEMV_LUT6;
     if (lut_supported(B, N, K)) return BIT1_GEMV_LUT;
@@ -109,7 +109,7 @@ bit1_status gemv_check(const uint8_t* bits, const uint16_t* scales, const uint16
         case BIT1_GEMV_STREAM: return group1_supported(B, N, K) ? BIT1_OK : BIT1_ESHAPE;
         case BIT1_GEMV_TC:
             if (!tc_supported(B, N, K)) return BIT1_ESHAPE;
-            return ws_bytes < tc_workspace_bytes(B, N, K) ? BIT1_EINVAL : BIT1_OK;
+            return ws_bytes < tc_min_workspace_bytes(B, N, K) ? BIT1_EINVAL : BIT1_OK;
         case BIT1_GEMV_SPLITK: return BIT1_ESHAPE;  // not available for any shape in this build
         default: return BIT1_EINVAL;
     }

@@ -72,7 +72,7 @@ struct TcParams {
     const uint16_t* scales;
     const float* xscale;      // [Bp] 2^m_b (undo the prescale)
     void* y;                  // [B][N]
-    int N, K, B, Bp, Ks, chunks, y_bf16;
+    int N, K, B, Bp, Ks, chunks, y_bf16;   // B: valid batch rows of all batch chunks of the launch
     int stages;               // A/B stages: 3 when the accumulators fit 128 columns (Bp <= 32), else 2
 };
 
@@ -221,6 +221,9 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const int mt = blockIdx.x / p.Ks, ks = blockIdx.x % p.Ks;   // ks = rank in the cluster
+    // Batch chunk: rows [cb0, cb0 + Bp) of x' and y (several chunks run as one
+    // launch along grid y when the workspace holds all of them).
+    const int cb0 = (int)blockIdx.y * p.Bp, bvalid = min(p.Bp, p.B - cb0);
     const int c0 = (int)((int64_t)p.chunks * ks / p.Ks), c1 = (int)((int64_t)p.chunks * (ks + 1) / p.Ks);
     const int nch = c1 - c0, s0 = c0 * kTcChunkSteps, nst = nch * kTcChunkSteps;
     const uint32_t btile = (uint32_t)p.Bp * 128u;          // one 64-wide K slab of B
@@ -348,7 +351,8 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
                 } else if (live) {
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
-                        if (cb + k < p.B) store_y(p, cb + k, row, __uint_as_float(d[k]) * p.xscale[cb + k]);
+                        if (cb + k < bvalid)
+                            store_y(p, cb0 + cb + k, row, __uint_as_float(d[k]) * p.xscale[cb0 + cb + k]);
                 }
             }
         }
@@ -380,7 +384,7 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
                     break;
                 }
                 mbar_expect_tx(full, bstage);
-                tma_3d(dst, &tm_x, 0, 0, 2 * (s0 + s), full);
+                tma_3d(dst, &tm_x, 0, cb0, 2 * (s0 + s), full);
             }
             if (issued > 0 && !mbar_wait(full, (uint32_t)(issued - 1) & 1u)) atomicOr(&g_tc_wait_timeouts, 4u);
         }
@@ -427,7 +431,7 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
         cluster_sync();
         if (warp < kTcUnpackWarps) {
             const int q0 = 64 * ks / p.Ks, q1 = 64 * (ks + 1) / p.Ks, nq = q1 - q0;
-            for (int it = threadIdx.x; it < nq * p.B; it += kTcUnpackWarps * 32) {
+            for (int it = threadIdx.x; it < nq * bvalid; it += kTcUnpackWarps * 32) {
                 const int b = it / nq, r0 = 4 * (q0 + it % nq);
                 const uint32_t off = wring + 4u * (uint32_t)(b * kTcRows + r0);
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -436,12 +440,12 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
                     const float4 v = ld_cluster_v4(map_rank(off, (uint32_t)k));
                     acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
                 }
-                const float xs = p.xscale[b];
+                const float xs = p.xscale[cb0 + b];
                 const int row = mt * kTcRows + r0;
-                if (row + 0 < p.N) store_y(p, b, row + 0, acc.x * xs);
-                if (row + 1 < p.N) store_y(p, b, row + 1, acc.y * xs);
-                if (row + 2 < p.N) store_y(p, b, row + 2, acc.z * xs);
-                if (row + 3 < p.N) store_y(p, b, row + 3, acc.w * xs);
+                if (row + 0 < p.N) store_y(p, cb0 + b, row + 0, acc.x * xs);
+                if (row + 1 < p.N) store_y(p, cb0 + b, row + 1, acc.y * xs);
+                if (row + 2 < p.N) store_y(p, cb0 + b, row + 2, acc.z * xs);
+                if (row + 3 < p.N) store_y(p, cb0 + b, row + 3, acc.w * xs);
             }
         }
         cluster_sync();
@@ -469,7 +473,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tc_encode() {
 
 struct TcPlan {
     int Bp, Mt, Ks, chunks;
-    size_t smem, off_scale, ws_total;
+    int nbc;                        // batch chunks of Bp rows
+    size_t smem, off_scale, ws_total;   // one chunk at a time (the minimum scratch)
+    size_t off_scale_all, ws_all;   // every chunk staged at once: one launch pair for the whole batch
 };
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -544,6 +550,9 @@ TcPlan tc_plan(int64_t B, int64_t N, int64_t K) {
     pl.Ks = 1;
     pl.off_scale = align256((size_t)pl.Bp * K * 2);
     pl.ws_total = pl.off_scale + 256;
+    pl.nbc = (int)((B + kTcMaxB - 1) / kTcMaxB);
+    pl.off_scale_all = align256((size_t)pl.nbc * pl.Bp * K * 2);
+    pl.ws_all = pl.off_scale_all + align256((size_t)pl.nbc * pl.Bp * 4);
     return pl;
 }
 
@@ -556,20 +565,25 @@ bool tc_supported(int64_t B, int64_t N, int64_t K) {
 
 size_t tc_workspace_bytes(int64_t B, int64_t N, int64_t K) {
     if (!tc_supported(B, N, K)) return 0;
+    return tc_plan(B, N, K).ws_all;
+}
+
+size_t tc_min_workspace_bytes(int64_t B, int64_t N, int64_t K) {
+    if (!tc_supported(B, N, K)) return 0;
     return tc_plan(B, N, K).ws_total;
 }
 
 int tc_launch_count(int64_t B, int64_t N, int64_t K) {
     if (!tc_supported(B, N, K)) return 0;
-    return (int)(2 * ((B + kTcMaxB - 1) / kTcMaxB));
+    return 2;   // with tc_workspace_bytes() of scratch; less scratch: two per 64-row chunk
 }
 
 namespace {
 
 cudaError_t launch_tc_main(const CUtensorMap& tm_bits, const CUtensorMap& tm_x, const TcParams& prm, int Mt,
-                           size_t smem, cudaStream_t stream) {
+                           int nbc, size_t smem, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(Mt * prm.Ks));
+    cfg.gridDim = dim3((unsigned)(Mt * prm.Ks), (unsigned)nbc);
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -597,7 +611,8 @@ cudaError_t launch_gemv_tc(const GemvArgs& a) {
     cudaError_t e;
     tc_set_attrs_once(&e);
     if (e != cudaSuccess) return e;
-    pl.Ks = tc_pick_ks(pl.Mt, pl.chunks, pl.smem);
+    const bool one = pl.nbc > 1 && a.ws_bytes >= pl.ws_all;   // all batch chunks in one launch pair
+    pl.Ks = tc_pick_ks(pl.Mt * (one ? pl.nbc : 1), pl.chunks, pl.smem);
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     uint16_t* xp = reinterpret_cast<uint16_t*>(ws);
     float* xscale = reinterpret_cast<float*>(ws + pl.off_scale);
@@ -614,19 +629,24 @@ cudaError_t launch_gemv_tc(const GemvArgs& a) {
             return cudaErrorInvalidValue;
     }
     const size_t ysz = a.y_bf16 ? 2 : 4;
-    for (int64_t b0 = 0; b0 < a.B; b0 += kTcMaxB) {
+    // All batch chunks in one prep + one main launch (grid y = chunk) when the
+    // scratch holds every chunk's activations; else one pair per 64-row chunk.
+    const int nbc_launch = one ? pl.nbc : 1;
+    if (one) xscale = reinterpret_cast<float*>(ws + pl.off_scale_all);
+    for (int64_t b0 = 0; b0 < a.B; b0 += (int64_t)kTcMaxB * nbc_launch) {
         const int Bc = (int)std::min<int64_t>(kTcMaxB, a.B - b0);
-        const int Bp = (Bc + 15) / 16 * 16;
+        const int Bp = one ? pl.Bp : (Bc + 15) / 16 * 16;
+        const int rows = Bp * nbc_launch;                  // x' rows this launch pair stages
         const uint16_t* xin = a.x + b0 * a.K;
-        int Bci = Bc, Ki = (int)a.K;
+        int Bci = (int)std::min<int64_t>(a.B - b0, (int64_t)rows), Ki = (int)a.K;
         void* prep_args[] = {(void*)&xin, (void*)&Bci, (void*)&Ki, (void*)&xp, (void*)&xscale};
-        e = launch((const void*)k_tc_prep, dim3((unsigned)Bp), dim3(kTcPrepThreads), 0, a.stream, a.pdl || b0 > 0,
+        e = launch((const void*)k_tc_prep, dim3((unsigned)rows), dim3(kTcPrepThreads), 0, a.stream, a.pdl || b0 > 0,
                    prep_args);
         if (e != cudaSuccess) return e;
-        // activations: [K/64 slabs][Bp rows][64 inputs], one box = 2 slabs x Bp rows
+        // activations: [K/64 slabs][rows][64 inputs], one box = 2 slabs x Bp rows
         CUtensorMap tm_x;
         {
-            const cuuint64_t dims[3] = {64, (cuuint64_t)Bp, (cuuint64_t)(a.K / 64)};
+            const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(a.K / 64)};
             const cuuint64_t strides[2] = {(cuuint64_t)(a.K * 2), 128};
             const cuuint32_t box[3] = {64, (cuuint32_t)Bp, 2};
             const cuuint32_t es[3] = {1, 1, 1};
@@ -641,13 +661,13 @@ cudaError_t launch_gemv_tc(const GemvArgs& a) {
         prm.y = static_cast<uint8_t*>(a.y) + b0 * a.N * ysz;
         prm.N = (int)a.N;
         prm.K = (int)a.K;
-        prm.B = Bc;
+        prm.B = Bci;
         prm.Bp = Bp;
         prm.Ks = pl.Ks;
         prm.chunks = pl.chunks;
         prm.y_bf16 = a.y_bf16;
         prm.stages = 4 * Bp <= 128 ? 3 : 2;
-        e = launch_tc_main(tm_bits, tm_x, prm, pl.Mt, pl.smem, a.stream);
+        e = launch_tc_main(tm_bits, tm_x, prm, pl.Mt, nbc_launch, pl.smem, a.stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

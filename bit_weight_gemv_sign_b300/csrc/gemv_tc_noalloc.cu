@@ -35,7 +35,7 @@ extern "C" bit1_status bit1_gemv_tc_noalloc(const uint8_t* bits, const uint16_t*
     if (B < 1 || N < 1 || K < 128 || K % 128 != 0 || B > 0x7fffffffLL || N > 0x7fffffffLL || K > (1LL << 24))
         return BIT1_ESHAPE;
     if (!tc_supported(B, N, K)) return BIT1_ESHAPE;
-    const size_t need = tc_workspace_bytes(B, N, K);
+    const size_t need = tc_min_workspace_bytes(B, N, K);
     if (need == 0 || need > kNoAllocScratchBytes) return BIT1_ESHAPE;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return BIT1_ECUDA;

@@ -59,7 +59,8 @@ unsigned int group_take_timeouts();
 // tcgen05 tensor-core batched kernel (gemv_tc.cu): K a multiple of 1024;
 // needs tc_workspace_bytes() of scratch; tc_launch_count() launches per call.
 bool tc_supported(int64_t B, int64_t N, int64_t K);
-size_t tc_workspace_bytes(int64_t B, int64_t N, int64_t K);
+size_t tc_workspace_bytes(int64_t B, int64_t N, int64_t K);      // all batch chunks at once (fastest)
+size_t tc_min_workspace_bytes(int64_t B, int64_t N, int64_t K);  // one 64-row chunk at a time
 int tc_launch_count(int64_t B, int64_t N, int64_t K);
 cudaError_t launch_gemv_tc(const GemvArgs& a);
 unsigned int tc_take_timeouts();

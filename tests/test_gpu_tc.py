@@ -98,7 +98,7 @@ def test_tc_mlp_shapes_full_size(orc, N, K, B):
 
 
 def test_tc_prompt_batch_512(orc):
-    """A 512-row prompt batch (eight 64-row launches over the same weights):
+    """A 512-row prompt batch (eight 64-row chunks, all in one launch pair):
     sampled rows of every batch row against the oracle."""
     N, K, B = 2048, 4096, 512
     bits, scales, x = _problem(N, K, B, 7250)
@@ -182,3 +182,24 @@ def test_tc_workspace_rules():
     assert b1.bit1_gemv_launches(B, 512, 1152, b1.TC) == 0
     # batch < 16: AUTO never picks the tensor cores
     assert b1.bit1_gemv_pick(8, N, K, 1 << 30) != b1.TC
+
+
+@pytest.mark.parametrize("B", [100, 200])
+def test_tc_batch_chunks_one_launch_and_sequential(orc, B):
+    """More than 64 batch rows: with bit1_gemv_workspace_bytes of scratch all
+    64-row chunks run as one launch pair (grid y = chunk, a ragged last
+    chunk); with only one chunk's scratch they run one pair per chunk.  Both
+    against the oracle, fp32 and bf16."""
+    N, K = 700, 2048
+    bits, scales, x = _problem(N, K, B, 7800 + B)
+    full = b1.bit1_gemv_workspace_bytes(B, N, K)
+    one_chunk = b1.bit1_gemv_workspace_bytes(64, N, K)
+    assert full > one_chunk
+    ref = orc.gemv(bits, scales, x, B, N, K)
+    bound = abs_bound(scales, x, K)
+    for ws_bytes in (full, one_chunk):
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        for ydt in (b1.F32, b1.BF16):
+            y = _run_tc(bits, scales, x, N, K, B, y_dtype=ydt, workspace=ws)
+            assert_gemv_close(y, ref, bound, f"tc B={B} ws={ws_bytes} y={ydt}")
+    assert b1.bit1_device_wait_timeouts() == 0
