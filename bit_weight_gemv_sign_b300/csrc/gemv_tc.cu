@@ -61,7 +61,8 @@ constexpr int kTcStages = 3;              // max A (tensor memory) / B (shared m
 constexpr int kTcChunkSteps = 4;          // sign-bit box: 64 bytes of each row = 4 steps
 constexpr int kTcWSlots = 4;              // sign-bit ring slots
 constexpr uint32_t kTcWSlotBytes = kTcRows * 16 * kTcChunkSteps;   // 16 KB
-constexpr int kTcMaxB = 64;               // batch rows per launch (accumulators: 2 x 64 columns)
+constexpr int kTcMaxB = 64;               // batch rows per chunk with two accumulators per half
+constexpr int kTcWideB = 128;             // rows per chunk with one accumulator per half (wide mode)
 constexpr int kTcUnpackWarps = 8;
 constexpr int kTcMmaWarps = 4;
 constexpr int kTcThreads = 32 * (kTcUnpackWarps + 2 + kTcMmaWarps);
@@ -74,6 +75,8 @@ struct TcParams {
     void* y;                  // [B][N]
     int N, K, B, Bp, Ks, chunks, y_bf16;   // B: valid batch rows of all batch chunks of the launch
     int stages;               // A/B stages: 3 when the accumulators fit 128 columns (Bp <= 32), else 2
+    // Wide mode (Bp > 64): one accumulator per 128-row half (columns h*Bp), two
+    // MMA issuers each issuing all eight 16-input slices of a step; Ks = 1.
 };
 
 // ---------------------------------------------------------------- helpers
@@ -245,9 +248,9 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
         for (int s = 0; s < kTcStages; ++s) {
             mbar_init(afull + 8 * s, kTcUnpackWarps);
             mbar_init(bfull + 8 * s, 1);
-            mbar_init(freed + 8 * s, kTcMmaWarps);    // one commit per MMA issuer
+            mbar_init(freed + 8 * s, p.Bp > kTcMaxB ? 2 : kTcMmaWarps);    // one commit per MMA issuer
         }
-        mbar_init(d_done, kTcMmaWarps);
+        mbar_init(d_done, p.Bp > kTcMaxB ? 2 : kTcMmaWarps);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -262,7 +265,8 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
     // columns = 128 fp16 inputs), abase = 4*Bp rounded up to 128.
     const uint32_t tmem = *tslot;
     const int nstg = p.stages;
-    const uint32_t abase = (uint32_t)((4 * p.Bp + 127) / 128 * 128);
+    const bool wide = p.Bp > kTcMaxB;
+    const uint32_t abase = (uint32_t)(((wide ? 2 : 4) * p.Bp + 127) / 128 * 128);
 
     if (warp < kTcUnpackWarps) {
         const int quad = warp & 3, h = warp >> 2;
@@ -334,15 +338,19 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
                              : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]), "=r"(d[4]), "=r"(d[5]), "=r"(d[6]),
                                "=r"(d[7]), "=r"(d[8]), "=r"(d[9]), "=r"(d[10]), "=r"(d[11]), "=r"(d[12]), "=r"(d[13]),
                                "=r"(d[14]), "=r"(d[15])
-                             : "r"(tmem + lane_base + (uint32_t)(2 * h * p.Bp + cb)) : "memory");
-                asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-                             : "=r"(e[0]), "=r"(e[1]), "=r"(e[2]), "=r"(e[3]), "=r"(e[4]), "=r"(e[5]), "=r"(e[6]),
-                               "=r"(e[7]), "=r"(e[8]), "=r"(e[9]), "=r"(e[10]), "=r"(e[11]), "=r"(e[12]), "=r"(e[13]),
-                               "=r"(e[14]), "=r"(e[15])
-                             : "r"(tmem + lane_base + (uint32_t)((2 * h + 1) * p.Bp + cb)) : "memory");
+                             : "r"(tmem + lane_base + (uint32_t)((wide ? h : 2 * h) * p.Bp + cb)) : "memory");
+                if (!wide) {
+                    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                                 : "=r"(e[0]), "=r"(e[1]), "=r"(e[2]), "=r"(e[3]), "=r"(e[4]), "=r"(e[5]), "=r"(e[6]),
+                                   "=r"(e[7]), "=r"(e[8]), "=r"(e[9]), "=r"(e[10]), "=r"(e[11]), "=r"(e[12]), "=r"(e[13]),
+                                   "=r"(e[14]), "=r"(e[15])
+                                 : "r"(tmem + lane_base + (uint32_t)((2 * h + 1) * p.Bp + cb)) : "memory");
+                }
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (!wide) {
 #pragma unroll
-                for (int k = 0; k < 16; ++k) d[k] = __float_as_uint(__uint_as_float(d[k]) + __uint_as_float(e[k]));
+                    for (int k = 0; k < 16; ++k) d[k] = __float_as_uint(__uint_as_float(d[k]) + __uint_as_float(e[k]));
+                }
                 if (p.Ks > 1) {
                     // stage [b][r] in the (drained) sign-bit ring for the cluster reduction
 #pragma unroll
@@ -392,12 +400,14 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
         // ---- MMA issuers: warp 10 + 2h + q accumulates half h, 16-input slices of parity q
         const int mw = warp - (kTcUnpackWarps + 2), h = mw >> 1, q = mw & 1;
         pdl_wait();
-        if (lane == 0) {
+        // wide mode: warp (h, 0) issues every slice into the one accumulator of half h
+        const int kk0 = wide ? 0 : q, kkd = wide ? 1 : 2;
+        if (lane == 0 && !(wide && q == 1)) {
             const uint32_t idesc = (1u << 4)                         // D: fp32
                                    | (0u << 7) | (0u << 10)          // A, B: fp16
                                    | ((uint32_t)(p.Bp >> 3) << 17)   // N
                                    | ((uint32_t)(128 >> 4) << 24);   // M
-            const uint32_t d_addr = tmem + (uint32_t)((2 * h + q) * p.Bp);
+            const uint32_t d_addr = tmem + (uint32_t)((wide ? h : 2 * h + q) * p.Bp);
             for (int s = 0; s < nst; ++s) {
                 const int st = s % nstg;
                 const uint32_t par = (uint32_t)(s / nstg) & 1u;
@@ -409,9 +419,9 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
                 const uint32_t bst = bring + st * bstage;
                 const uint32_t a0 = tmem + abase + 128u * st + 64u * h;
 #pragma unroll
-                for (int kk = q; kk < kTcStepK / 16; kk += 2) {
+                for (int kk = kk0; kk < kTcStepK / 16; kk += kkd) {
                     const uint64_t bdesc = tc_desc_sw128(bst + (kk >> 2) * btile + (kk & 3) * 32);
-                    const uint32_t acc = (s > 0 || kk > q) ? 1u : 0u;
+                    const uint32_t acc = (s > 0 || kk > kk0) ? 1u : 0u;
                     asm volatile("{.reg .pred pa; setp.ne.b32 pa, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;}"
                                  ::"r"(d_addr), "r"(a0 + 8u * kk), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
                 }
@@ -473,9 +483,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tc_encode() {
 
 struct TcPlan {
     int Bp, Mt, Ks, chunks;
-    int nbc;                        // batch chunks of Bp rows
-    size_t smem, off_scale, ws_total;   // one chunk at a time (the minimum scratch)
-    size_t off_scale_all, ws_all;   // every chunk staged at once: one launch pair for the whole batch
+    size_t smem, off_scale, ws_total;   // one chunk of <= 64 rows at a time (the minimum scratch)
+    // Every chunk staged at once, one launch pair for the whole batch: chunks
+    // of 64 rows (narrow) or of 128 (wide mode); the scratch covers both.
+    int nbc_n, Bp_n, nbc_w, Bp_w;
+    size_t ws_all;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -550,9 +562,12 @@ TcPlan tc_plan(int64_t B, int64_t N, int64_t K) {
     pl.Ks = 1;
     pl.off_scale = align256((size_t)pl.Bp * K * 2);
     pl.ws_total = pl.off_scale + 256;
-    pl.nbc = (int)((B + kTcMaxB - 1) / kTcMaxB);
-    pl.off_scale_all = align256((size_t)pl.nbc * pl.Bp * K * 2);
-    pl.ws_all = pl.off_scale_all + align256((size_t)pl.nbc * pl.Bp * 4);
+    pl.nbc_n = (int)((B + kTcMaxB - 1) / kTcMaxB);
+    pl.Bp_n = pl.nbc_n == 1 ? pl.Bp : kTcMaxB;
+    pl.nbc_w = (int)((B + kTcWideB - 1) / kTcWideB);
+    pl.Bp_w = B <= kTcMaxB ? pl.Bp_n : (pl.nbc_w == 1 ? (int)((B + 15) / 16 * 16) : kTcWideB);
+    const size_t rows = (size_t)std::max(pl.nbc_n * pl.Bp_n, pl.nbc_w * pl.Bp_w);
+    pl.ws_all = align256(rows * K * 2) + align256(rows * 4);
     return pl;
 }
 
@@ -611,8 +626,28 @@ cudaError_t launch_gemv_tc(const GemvArgs& a) {
     cudaError_t e;
     tc_set_attrs_once(&e);
     if (e != cudaSuccess) return e;
-    const bool one = pl.nbc > 1 && a.ws_bytes >= pl.ws_all;   // all batch chunks in one launch pair
-    pl.Ks = tc_pick_ks(pl.Mt * (one ? pl.nbc : 1), pl.chunks, pl.smem);
+    // All batch chunks in one launch pair when the scratch holds them.  Narrow
+    // (64-row chunks, K split over a cluster) or wide (128-row chunks: each
+    // weight tile unpacked once for 128 rows, but no K split, since the
+    // cluster reduction stages at most 64 rows): the smaller estimate of waves
+    // x chunks per CTA, a wide chunk step costing about 1.4 narrow ones
+    // (measured).
+    const bool one = a.B > kTcMaxB && a.ws_bytes >= pl.ws_all;
+    int nbc = 1;
+    if (one) {
+        const int sms = std::max(1, sm_count());
+        const int ks_n = tc_pick_ks(pl.Mt * pl.nbc_n, pl.chunks, tc_smem(pl.Bp_n));
+        const double cost_n = (double)((pl.Mt * pl.nbc_n * ks_n + sms - 1) / sms) *
+                              ((pl.chunks + ks_n - 1) / ks_n + 1);
+        const double cost_w = 1.4 * (double)((pl.Mt * pl.nbc_w + sms - 1) / sms) * (pl.chunks + 1);
+        const bool wide = cost_w < cost_n;
+        nbc = wide ? pl.nbc_w : pl.nbc_n;
+        pl.Bp = wide ? pl.Bp_w : pl.Bp_n;
+        pl.smem = tc_smem(pl.Bp);
+        pl.Ks = wide ? 1 : ks_n;
+    } else {
+        pl.Ks = tc_pick_ks(pl.Mt, pl.chunks, pl.smem);
+    }
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     uint16_t* xp = reinterpret_cast<uint16_t*>(ws);
     float* xscale = reinterpret_cast<float*>(ws + pl.off_scale);
@@ -631,9 +666,9 @@ cudaError_t launch_gemv_tc(const GemvArgs& a) {
     const size_t ysz = a.y_bf16 ? 2 : 4;
     // All batch chunks in one prep + one main launch (grid y = chunk) when the
     // scratch holds every chunk's activations; else one pair per 64-row chunk.
-    const int nbc_launch = one ? pl.nbc : 1;
-    if (one) xscale = reinterpret_cast<float*>(ws + pl.off_scale_all);
-    for (int64_t b0 = 0; b0 < a.B; b0 += (int64_t)kTcMaxB * nbc_launch) {
+    const int nbc_launch = nbc;
+    if (one) xscale = reinterpret_cast<float*>(ws + align256((size_t)nbc * pl.Bp * a.K * 2));
+    for (int64_t b0 = 0; b0 < a.B; b0 += one ? a.B : (int64_t)kTcMaxB) {
         const int Bc = (int)std::min<int64_t>(kTcMaxB, a.B - b0);
         const int Bp = one ? pl.Bp : (Bc + 15) / 16 * 16;
         const int rows = Bp * nbc_launch;                  // x' rows this launch pair stages
