@@ -203,3 +203,18 @@ def test_tc_batch_chunks_one_launch_and_sequential(orc, B):
             y = _run_tc(bits, scales, x, N, K, B, y_dtype=ydt, workspace=ws)
             assert_gemv_close(y, ref, bound, f"tc B={B} ws={ws_bytes} y={ydt}")
     assert b1.bit1_device_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("N,K,B", [(12288, 4096, 256), (12288, 4096, 200), (30000, 2048, 100)])
+def test_tc_wide_chunks(orc, N, K, B):
+    """Shapes whose cost estimate picks 128-row chunks with one accumulator per
+    half (many row tiles, B > 64; 200 rows leave a ragged last chunk, 100 rows
+    a single 112-row chunk): sampled rows of every batch row against the oracle."""
+    bits, scales, x = _problem(N, K, B, 7900 + B)
+    for ydt in (b1.F32, b1.BF16):
+        y = _run_tc(bits, scales, x, N, K, B, y_dtype=ydt)
+        rows = np.unique(np.concatenate([np.random.default_rng(N + B).choice(N, 40, replace=False), [0, N - 1]]))
+        ref = orc.gemv_select(bits, scales, x, B, N, K, rows)
+        assert_gemv_close(y[:, torch.from_numpy(rows).cuda()], ref, abs_bound(scales[rows], x, K),
+                          f"tc wide N={N} K={K} B={B} y={ydt}")
+    assert b1.bit1_device_wait_timeouts() == 0
