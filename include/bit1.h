@@ -142,11 +142,17 @@ bit1_status bit1_gemv_ex(const uint8_t *bits, const uint16_t *scales,
                          int variant, unsigned flags, bit1_stream_t stream);
 
 /* Scratch bytes that let bit1_gemv use its fastest kernel for this shape
- * (0 when no kernel needs scratch). */
+ * (0 when no kernel needs scratch).  On the tensor cores (B >= 16) this is
+ * the fp16 copy of every batch row's activations plus one float per row,
+ * so a batch beyond 64 rows runs as one launch pair; any workspace of at
+ * least one 64-row chunk's share (16 * ceil(min(B, 64) / 16) * K * 2 bytes
+ * rounded up to 256, plus 256) still selects the tensor cores and runs one
+ * launch pair per 64-row chunk. */
 size_t bit1_gemv_workspace_bytes(int64_t B, int64_t N, int64_t K);
 
 /* The variant bit1_gemv picks for this shape and workspace size, and the
- * number of kernel launches one call makes (0 on bad arguments). */
+ * number of kernel launches one call makes with bit1_gemv_workspace_bytes of
+ * scratch (0 on bad arguments). */
 int bit1_gemv_pick(int64_t B, int64_t N, int64_t K, size_t ws_bytes);
 int bit1_gemv_launches(int64_t B, int64_t N, int64_t K, int variant);
 
