@@ -23,6 +23,7 @@ __all__ = [
     "bit1_ternary_planes", "bit1_gemv_ternary", "bit1_gemv_ternary_workspace_bytes",
     "bit1_gemv_ternary_launches", "bit1_ternary_combine",
     "bit1_t5_pack", "bit1_t5_to_planes", "bit1_gemv_t5", "bit1_gemv_t5_launches",
+    "bit1_selftest_wait_timeout",
 ]
 
 OK, EINVAL, ESHAPE, ERANGE, ECUDA, ENAN = 0, 1, 2, 3, 4, 5
@@ -86,6 +87,8 @@ def load():
         lib.bit1_version.restype = ctypes.c_char_p
         lib.bit1_device_wait_timeouts.argtypes = []
         lib.bit1_device_wait_timeouts.restype = ctypes.c_uint
+        lib.bit1_selftest_wait_timeout.argtypes = [p, p]
+        lib.bit1_selftest_wait_timeout.restype = i32
         lib.bit1_group_plan_bytes.argtypes = [i32]
         lib.bit1_group_plan_bytes.restype = sz
         lib.bit1_group_plan.argtypes = [ctypes.POINTER(_Problem), i32, p, sz]
@@ -128,6 +131,14 @@ def bit1_version() -> str:
 
 def bit1_device_wait_timeouts() -> int:
     return int(load().bit1_device_wait_timeouts())
+
+
+def bit1_selftest_wait_timeout(done, stream=None) -> None:
+    """Run the bounded-wait self-test kernel (``done``: int32 [1] CUDA tensor,
+    set to 1 when the kernel exits)."""
+    import torch
+    st = load().bit1_selftest_wait_timeout(_dptr(done, "done", (torch.int32,)), _stream(stream))
+    _check(st, "bit1_selftest_wait_timeout")
 
 
 # ---------------------------------------------------------------- helpers

@@ -313,6 +313,11 @@ int bit1_gemv_t5_launches(int64_t B, int64_t N, int64_t K) {
     return shape_ok(B, N, K) ? t5_launch_count(B) : 0;
 }
 
+bit1_status bit1_selftest_wait_timeout(unsigned int* d_done, bit1_stream_t stream) {
+    if (!d_done || ((uintptr_t)d_done & 3u)) return BIT1_EINVAL;
+    return from_cuda(launch_wait_selftest(d_done, (cudaStream_t)stream));
+}
+
 bit1_status bit1_gemv_group(const void* device_plan, const void* host_plan, unsigned flags,
                             bit1_stream_t stream) {
     if (!device_plan || !host_plan || ((uintptr_t)device_plan & 127) || ((uintptr_t)host_plan & 127))

@@ -560,6 +560,26 @@ cudaError_t launch_gemv_t6(const GemvArgs& a) {
     return cudaSuccess;
 }
 
+// Self-test of the bounded wait: one thread waits on an mbarrier phase that
+// nothing completes.  The wait gives up after its iteration limit, records
+// the event in the timeout counter (bit 4) and the kernel returns normally:
+// the failure path of every bounded wait, exercised without a fault or hang.
+__global__ void __launch_bounds__(32, 1) k_wait_selftest(unsigned int* __restrict__ done) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = (uint32_t)__cvta_generic_to_shared(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (!mbar_wait(b, 0u)) atomicOr(&g_bit1_wait_timeouts, 16u);
+        *done = 1u;
+    }
+}
+
+cudaError_t launch_wait_selftest(unsigned int* d_done, cudaStream_t stream) {
+    k_wait_selftest<<<1, 32, 0, stream>>>(d_done);
+    return cudaGetLastError();
+}
+
 unsigned int t6_take_timeouts() {
     unsigned int v = 0, zero = 0;
     if (cudaMemcpyFromSymbol(&v, g_bit1_wait_timeouts, sizeof(v)) != cudaSuccess) return 0xffffffffu;

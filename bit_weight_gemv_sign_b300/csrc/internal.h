@@ -47,6 +47,8 @@ int t6_launch_count(int64_t B, int64_t N, int64_t K);
 cudaError_t launch_gemv_t6(const GemvArgs& a);
 // Number of bounded device waits that gave up since the last call (and reset).
 unsigned int t6_take_timeouts();
+// One kernel whose bounded wait runs out on purpose (sets *d_done = 1 on exit).
+cudaError_t launch_wait_selftest(unsigned int* d_done, cudaStream_t stream);
 
 // Grouped persistent kernel (gemv_group.cu).
 size_t group_plan_bytes(int count);

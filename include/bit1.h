@@ -224,6 +224,15 @@ bit1_status bit1_xor_patch(uint8_t *bits, int64_t N, int64_t K,
  * count could not be read. */
 unsigned int bit1_device_wait_timeouts(void);
 
+/* Self-test of that failure path: launches one kernel whose bounded wait is
+ * on a barrier that nothing completes.  The wait gives up after its limit
+ * (2^22 polls of a suspending try_wait: about 16 s on B300), the kernel
+ * records the event (the next bit1_device_wait_timeouts() is nonzero),
+ * writes 1 to the device uint32 *d_done and exits normally; the context
+ * stays usable.  No fault, trap or hang is involved.  BIT1_EINVAL on a null
+ * or misaligned d_done. */
+bit1_status bit1_selftest_wait_timeout(unsigned int *d_done, bit1_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * bit1_gemv_tc_noalloc -- the tensor-core batched product (bit1_gemv_ex with
  * variant BIT1_GEMV_TC) without a caller workspace.  The pages have no

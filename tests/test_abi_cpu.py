@@ -180,3 +180,8 @@ def test_t5_rejects_on_host(lib):
     assert b1.bit1_gemv_t5_launches(1, 8, 128) == 1
     assert b1.bit1_gemv_t5_launches(17, 8, 128) == 3
     assert b1.bit1_gemv_t5_launches(1, 8, 100) == 0
+
+
+def test_selftest_rejects_bad_pointer_on_host(lib):
+    assert lib.bit1_selftest_wait_timeout(None, None) == b1.EINVAL
+    assert lib.bit1_selftest_wait_timeout(FAKE + 2, None) == b1.EINVAL
