@@ -219,6 +219,91 @@ def cpu_baseline(frac_den: int = 1):
             "sample": f"{what}, {wbytes} weight bytes), scalar fp64 oracle, {threads} threads"}
 
 
+def _timed(fn):
+    t0 = time.perf_counter()
+    fn()
+    return time.perf_counter() - t0
+
+
+def oracle_beside_extras(extras: dict) -> None:
+    """The CPU oracle, as it stands, timed beside each extra row on a bounded
+    sample of that row's workload (a few seconds in all); added to each row
+    as "cpu_oracle".  Binary products use the oracle's row-threaded loop on
+    all host cores, the ternary ones its single-threaded loops."""
+    import numpy as np
+    import oracle
+    from bit_weight_gemv_sign_b300 import synth
+    threads = os.cpu_count() or 1
+
+    def binary(N, K, B, rows, seed):
+        bits, scales = synth.matrix(N, K, seed)
+        x = synth.x_for(B, K, seed)
+        b, sc = np.ascontiguousarray(bits[:rows]), np.ascontiguousarray(scales[:rows])
+        secs = _timed(lambda: oracle.gemv_threads(b, sc, x, B, rows, K, threads))
+        return secs * N / rows            # seconds for the whole matrix
+
+    def entry(value, unit, sample, thr):
+        return {"value": value, "unit": unit, "cores": thr, "kind": "oracle", "sample": sample}
+
+    if "c1_tiny" in extras:
+        secs = binary(256, 1024, 1, 256, 0)
+        extras["c1_tiny"]["cpu_oracle"] = entry(secs * 1e6, "us per GEMV", "the whole 256x1024 product", threads)
+    if "c2_projections_b1" in extras:
+        secs = binary(12288, 4096, 1, 768, 1)
+        wb = 12288 * 4096 // 8 + 2 * 12288 * 32
+        extras["c2_projections_b1"]["cpu_oracle"] = entry(wb / secs / 1e9, "GB/s",
+                                                          "768 of the 12288 rows of an up/gate projection", threads)
+    if "c4_mlp_crossover" in extras:
+        out = {}
+        for B in (16, 64):
+            secs = binary(12288, 4096, B, 96, 2)
+            out[f"B{B}_us_per_call"] = secs * 1e6
+            out[f"B{B}_tflops"] = 2.0 * B * 12288 * 4096 / secs / 1e12
+        extras["c4_mlp_crossover"]["cpu_oracle"] = {**entry(out["B16_us_per_call"], "us per call at B = 16",
+                                                            "96 of the 12288 rows of up/gate at B = 16 and 64",
+                                                            threads), **out}
+    if "pp512_tcgen05" in extras:
+        secs = binary(12288, 4096, 512, 8, 3)
+        extras["pp512_tcgen05"]["cpu_oracle"] = entry(2.0 * 512 * 12288 * 4096 / secs / 1e12, "TFLOP/s",
+                                                      "8 of the 12288 rows at B = 512", threads)
+    if "c5_sweep_27b" in extras:
+        wb = secs = 0.0
+        for i, m in enumerate(synth.sweep_27b()[:7]):          # one layer's seven matrices
+            rows = max(1, m.N // 64)
+            secs += binary(m.N, m.K, 1, rows, 100 + i) * rows / m.N
+            wb += rows * (m.K // 8 + 2 * (m.K // 128))
+        extras["c5_sweep_27b"]["cpu_oracle"] = entry(wb / secs / 1e9, "GB/s",
+                                                     "1/64 of the rows of one 27B-class layer's seven matrices",
+                                                     threads)
+    if "verify_sweep_8b_b5" in extras:
+        wb = secs = 0.0
+        for i, m in enumerate(synth.sweep_8b()[:7]):
+            rows = max(1, m.N // 64)
+            secs += binary(m.N, m.K, 5, rows, 200 + i) * rows / m.N
+            wb += rows * (m.K // 8 + 2 * (m.K // 128))
+        extras["verify_sweep_8b_b5"]["cpu_oracle"] = entry(wb / secs / 1e9, "GB/s (5 rows per weight read)",
+                                                           "1/64 of the rows of one 8B-class layer at B = 5",
+                                                           threads)
+    if "ternary_sweep_8b" in extras:
+        N, K, rows = 12288, 4096, 96
+        a, b, scales = synth.ternary_matrix(rows, K, 4)
+        x = synth.x_for(1, K, 4)
+        secs = _timed(lambda: oracle.gemv_ternary(a, b, scales, x, 1, rows, K))
+        wb = rows * (2 * K // 8 + 2 * (K // 128))
+        extras["ternary_sweep_8b"]["cpu_oracle"] = entry(wb / secs / 1e9, "GB/s",
+                                                         "96 rows of a 12288x4096 ternary matrix, 2-bit slots", 1)
+    if "ternary_t5" in extras:
+        K, rows = 4096, 96
+        t = synth.ternary_codes(rows, K, synth.rng(5))
+        packed = oracle.t5_pack(t, rows, K)
+        scales = synth.group_scales(rows, K, synth.rng(6))
+        x = synth.x_for(1, K, 5)
+        secs = _timed(lambda: oracle.gemv_t5(packed, scales, x, 1, rows, K))
+        wb = rows * (26 * K // 128 + 2 * (K // 128))
+        extras["ternary_t5"]["cpu_oracle"] = entry(wb / secs / 1e9, "GB/s",
+                                                   "96 rows x 4096, five codes per byte", 1)
+
+
 def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
@@ -692,6 +777,8 @@ def run_mine(args):
         import oracle
         oracle.build()
         out["cpu_baseline"] = cpu_baseline(frac_den=1)
+        if "extras" in out:
+            oracle_beside_extras(out["extras"])
     if rank == 0:
         print(json.dumps(out))
     if dist:
