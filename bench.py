@@ -159,11 +159,20 @@ GROUP_KERNEL_SOURCES = ("bit_weight_gemv_sign_b300/csrc/gemv_group.cu",
                         "include/bit1.h")
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments and blank-line or trailing-space noise:
+    a comment edit leaves the compiled kernel, and so its counters, unchanged."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_sources_hash(paths=GROUP_KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
     for rel in paths:
         h.update(rel.encode())
-        h.update(open(os.path.join(ROOT, rel), "rb").read())
+        h.update(_code_only(open(os.path.join(ROOT, rel), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

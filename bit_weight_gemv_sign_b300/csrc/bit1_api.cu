@@ -105,12 +105,12 @@ bit1_status gemv_check(const uint8_t* bits, const uint16_t* scales, const uint16
     switch (*variant) {
         case BIT1_GEMV_SIMPLE: return BIT1_OK;
         case BIT1_GEMV_LUT: return lut_supported(B, N, K) ? BIT1_OK : BIT1_ESHAPE;
-        case BIT1_GEMV_LUT6: return t6_supported(B, N, K) ? BIT1_OK : BIT1_ESHAPE;
         case BIT1_GEMV_STREAM: return group1_supported(B, N, K) ? BIT1_OK : BIT1_ESHAPE;
         case BIT1_GEMV_TC:
             if (!tc_supported(B, N, K)) return BIT1_ESHAPE;
             return ws_bytes < tc_min_workspace_bytes(B, N, K) ? BIT1_EINVAL : BIT1_OK;
-        case BIT1_GEMV_SPLITK: return BIT1_ESHAPE;  // not available for any shape in this build
+        case BIT1_GEMV_SPLITK:  // the cluster split-K table kernel, named explicitly
+        case BIT1_GEMV_LUT6: return t6_supported(B, N, K) ? BIT1_OK : BIT1_ESHAPE;
         default: return BIT1_EINVAL;
     }
 }
@@ -129,6 +129,7 @@ bit1_status gemv_run(const uint8_t* bits, const uint16_t* scales, const uint16_t
     switch (variant) {
         case BIT1_GEMV_SIMPLE: return from_cuda(launch_gemv_simple(a));
         case BIT1_GEMV_LUT: return from_cuda(launch_gemv_lut(a));
+        case BIT1_GEMV_SPLITK:
         case BIT1_GEMV_LUT6: return from_cuda(launch_gemv_t6(a));
         case BIT1_GEMV_STREAM: return from_cuda(launch_gemv_group1(a));
         case BIT1_GEMV_TC: return from_cuda(launch_gemv_tc(a));
@@ -178,6 +179,7 @@ int bit1_gemv_launches(int64_t B, int64_t N, int64_t K, int variant) {
     switch (variant) {
         case BIT1_GEMV_SIMPLE: return 1;
         case BIT1_GEMV_LUT: return lut_supported(B, N, K) ? 1 : 0;
+        case BIT1_GEMV_SPLITK:
         case BIT1_GEMV_LUT6: return t6_launch_count(B, N, K);
         case BIT1_GEMV_STREAM: return group1_supported(B, N, K) ? 1 : 0;
         case BIT1_GEMV_TC: return tc_launch_count(B, N, K);

@@ -69,7 +69,11 @@ enum bit1_gemv_variant {
     BIT1_GEMV_AUTO = 0,
     BIT1_GEMV_SIMPLE = 1,  /* any shape; one warp per row (reference-quality) */
     BIT1_GEMV_LUT = 2,     /* batch 1..8: CUDA-core table-lookup kernel */
-    BIT1_GEMV_SPLITK = 3,  /* batch 1..8, short N: K split over CTAs, workspace reduction */
+    BIT1_GEMV_SPLITK = 3,  /* the split-K kernel by name: the same kernel as
+                              BIT1_GEMV_LUT6, whose K split over a cluster
+                              (fixed-order DSMEM reduction, no workspace) and,
+                              for short N, over the warps of a CTA, is this
+                              library's split-K variant */
     BIT1_GEMV_TC = 4,      /* batch >= 16: tcgen05 tensor-core kernel */
     BIT1_GEMV_LUT6 = 5,    /* K a multiple of 1024: one row per lane, 6-bit fp16
                               tables per batch row, TMA-staged weights, K split

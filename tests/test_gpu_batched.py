@@ -83,3 +83,14 @@ def test_batched_row_flip_negates_exactly():
     y2 = _run(flipped, scales, x, N, K, B)
     rows = torch.tensor([0, 31, 32, 699], device="cuda")
     assert torch.equal(y2[:, rows], -y[:, rows])
+
+
+def test_splitk_names_the_cluster_split_kernel():
+    """BIT1_GEMV_SPLITK runs the cluster split-K table kernel: the same bits as
+    BIT1_GEMV_LUT6, and within the tolerance of the oracle."""
+    N, K, B = 300, 8192, 3
+    bits, scales, x = _problem(N, K, B, 8104)
+    a = _run(bits, scales, x, N, K, B, variant=b1.SPLITK)
+    b = _run(bits, scales, x, N, K, B, variant=b1.LUT6)
+    assert torch.equal(a, b)
+    assert b1.bit1_gemv_launches(B, N, K, b1.SPLITK) == b1.bit1_gemv_launches(B, N, K, b1.LUT6)
