@@ -223,9 +223,16 @@ def cpu_baseline(frac_den: int = 1):
     wbytes, secs = time_oracle(sample, threads)
     what = ("all rows of the 253 sweep matrices (one full decode step" if frac_den == 1 else
             f"first 1/{frac_den} of the rows of each of the 253 sweep matrices (")
+    # the same oracle on one core, over the first 1/64 of each matrix's rows
+    import numpy as np
+    sub = [(np.ascontiguousarray(b[:max(1, n // 64)]), np.ascontiguousarray(sc[:max(1, n // 64)]), x,
+            max(1, n // 64), K) for b, sc, x, n, K in sample]
+    wb1, secs1 = time_oracle(sub, 1)
     return {"value": wbytes / secs / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "seconds": secs, "tok_s_equiv": wbytes / secs / 1064263680,
-            "sample": f"{what}, {wbytes} weight bytes), scalar fp64 oracle, {threads} threads"}
+            "sample": f"{what}, {wbytes} weight bytes), scalar fp64 oracle, {threads} threads",
+            "single_thread": {"value": wb1 / secs1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"first 1/64 of the rows of each sweep matrix ({wb1} weight bytes)"}}
 
 
 def _timed(fn):
@@ -352,6 +359,7 @@ def run_reference(args):
 # call streams its weights from HBM.
 
 L2_BYTES = 126 * 2**20
+NOMINAL_HBM_GBS = 7700.0    # B300 HBM3e, nominal
 
 
 def _weight_bytes(N, K):
@@ -777,6 +785,7 @@ def run_mine(args):
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": gbs / ws, "peak": hbm, "unit": "GB/s",
                      "frac": gbs / ws / hbm, "peak_source": src, "traffic": traffic,
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": gbs / ws / NOMINAL_HBM_GBS,
                      "kernel": "k_gemv_group (one launch per step)"},
         "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": sw.x_bytes,
                 "d2h_bytes_per_step": hy.numel() * hy.element_size(), "ms_per_step": e2e_ms,
