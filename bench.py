@@ -223,16 +223,19 @@ def cpu_baseline(frac_den: int = 1):
     wbytes, secs = time_oracle(sample, threads)
     what = ("all rows of the 253 sweep matrices (one full decode step" if frac_den == 1 else
             f"first 1/{frac_den} of the rows of each of the 253 sweep matrices (")
-    # the same oracle on one core, over the first 1/64 of each matrix's rows
+    # the same oracle on one core over the first 1/256 of each matrix's rows,
+    # best of three (the host cores are shared)
     import numpy as np
-    sub = [(np.ascontiguousarray(b[:max(1, n // 64)]), np.ascontiguousarray(sc[:max(1, n // 64)]), x,
-            max(1, n // 64), K) for b, sc, x, n, K in sample]
-    wb1, secs1 = time_oracle(sub, 1)
+    sub = [(np.ascontiguousarray(b[:max(1, n // 256)]), np.ascontiguousarray(sc[:max(1, n // 256)]), x,
+            max(1, n // 256), K) for b, sc, x, n, K in sample]
+    runs = [time_oracle(sub, 1) for _ in range(3)]
+    wb1, secs1 = runs[0][0], min(r[1] for r in runs)
     return {"value": wbytes / secs / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "seconds": secs, "tok_s_equiv": wbytes / secs / 1064263680,
             "sample": f"{what}, {wbytes} weight bytes), scalar fp64 oracle, {threads} threads",
             "single_thread": {"value": wb1 / secs1 / 1e9, "unit": "GB/s", "cores": 1,
-                              "sample": f"first 1/64 of the rows of each sweep matrix ({wb1} weight bytes)"}}
+                              "sample": f"first 1/256 of the rows of each sweep matrix ({wb1} weight bytes), "
+                                        "best of three"}}
 
 
 def _timed(fn):
