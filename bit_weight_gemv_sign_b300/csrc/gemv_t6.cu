@@ -23,9 +23,10 @@
 //    bytes of sign bits once per group and looks them up in each batch row's
 //    tables (the lookups, not the weight reads, grow with the batch).
 //  * x' = x * 2^-m_g per group (exact power-of-two prescale) keeps every entry
-//    within fp16 range; the entry rounding error is <= 2^-12 of the sum of the
-//    six |x'|, i.e. a relative 2.4e-4 of sum|s x| at most, inside the 1e-3
-//    budget.  The group's fp32 partial is multiplied by s_g and 2^m_g.
+//    within fp16 range; the entry rounding error is <= 2^-11 of the sum of the
+//    six |x'| (round to nearest, 11 significant bits), i.e. a relative 4.9e-4
+//    of sum|s x| at most, inside the 1e-3 budget.  The group's fp32 partial
+//    is multiplied by s_g and 2^m_g.
 //  * Weights and scales of 32-row blocks are copied by TMA into per-warp
 //    rings (mbarrier completion, bounded waits).  Bits arrive as 2-D boxes of
 //    [32 rows][128 B] (8 groups) with 128-byte swizzle: row r's 16-byte chunk
