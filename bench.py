@@ -551,8 +551,9 @@ def extra_ternary_sweep_8b(torch, b1, steps=20):
 def extra_t5(torch, b1, reps=20):
     """Ternary codes packed five per byte (1.75 bits/weight): the direct
     product on the 8B-class projection shapes at batch 1 (graph replay over
-    copies rotated past L2), and the device transcode to the 2-bit-slot planes
-    on the LM-head shape."""
+    copies rotated past L2), beside the same shapes in 2-bit slots through
+    bit1_gemv_ternary, and the device transcode to the 2-bit-slot planes on the
+    LM-head shape."""
     out = {}
     for (N, K) in ((4096, 4096), (12288, 4096), (4096, 12288)):
         pb = N * (K // 128) * 26
@@ -581,9 +582,30 @@ def extra_t5(torch, b1, reps=20):
             e1.record(s)
             e1.synchronize()
         us = e0.elapsed_time(e1) / reps * 1e3
+        # the same shape in 2-bit slots: two binary passes and a combine per call
+        a = torch.randint(0, 256, (copies, N, K // 8), dtype=torch.uint8, device="cuda", generator=g)
+        bpl = torch.randint(0, 256, (copies, N, K // 8), dtype=torch.uint8, device="cuda", generator=g)
+        wst = torch.empty(max(b1.bit1_gemv_ternary_workspace_bytes(1, N, K), 256), dtype=torch.uint8, device="cuda")
+        with torch.cuda.stream(s):
+            for i in range(3):
+                b1.bit1_gemv_ternary(a[i % copies], bpl[i % copies], sc[i % copies], x, y=y, workspace=wst, stream=s)
+            s.synchronize()
+            gs = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gs, stream=s):
+                for i in range(reps):
+                    b1.bit1_gemv_ternary(a[i % copies], bpl[i % copies], sc[i % copies], x, y=y, workspace=wst,
+                                         stream=s)
+            gs.replay()
+            s.synchronize()
+            e0.record(s)
+            gs.replay()
+            e1.record(s)
+            e1.synchronize()
+        us_slot = e0.elapsed_time(e1) / reps * 1e3
         out[f"gemv_{N}x{K}_b1"] = {"us": round(us, 3), "weight_gbs": round(wb / (us * 1e-6) / 1e9, 1),
-                                   "gweights_s": round(N * K / (us * 1e-6) / 1e9, 1)}
-        del packed, sc, graph
+                                   "gweights_s": round(N * K / (us * 1e-6) / 1e9, 1),
+                                   "slot_path_us": round(us_slot, 3)}
+        del packed, sc, graph, a, bpl, gs
         torch.cuda.empty_cache()
     N, K = 151936, 4096
     g = torch.Generator(device="cuda")

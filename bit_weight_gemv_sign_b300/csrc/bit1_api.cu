@@ -308,11 +308,14 @@ bit1_status bit1_gemv_t5(const uint8_t* packed, const uint16_t* scales, const ui
     if (!packed || !scales || !x || !y) return BIT1_EINVAL;
     if (!aligned16(packed) || !aligned16(scales) || !aligned16(x) || !aligned16(y)) return BIT1_EINVAL;
     if (y_dtype != BIT1_F32 && y_dtype != BIT1_BF16) return BIT1_EINVAL;
+    if (t5lut_supported(B, N, K))   // batch 1: table-lookup kernel
+        return from_cuda(launch_gemv_t5lut(packed, scales, x, N, K, y, y_dtype == BIT1_BF16, (cudaStream_t)stream));
     return from_cuda(launch_gemv_t5(packed, scales, x, B, N, K, y, y_dtype == BIT1_BF16, (cudaStream_t)stream));
 }
 
 int bit1_gemv_t5_launches(int64_t B, int64_t N, int64_t K) {
-    return shape_ok(B, N, K) ? t5_launch_count(B) : 0;
+    if (!shape_ok(B, N, K)) return 0;
+    return t5lut_supported(B, N, K) ? 1 : t5_launch_count(B);
 }
 
 bit1_status bit1_selftest_wait_timeout(unsigned int* d_done, bit1_stream_t stream) {

@@ -81,6 +81,10 @@ cudaError_t launch_t5_planes(const uint8_t* packed, int64_t N, int64_t K, uint8_
 cudaError_t launch_gemv_t5(const uint8_t* packed, const uint16_t* scales, const uint16_t* x, int64_t B,
                            int64_t N, int64_t K, void* y, bool y_bf16, cudaStream_t stream);
 int t5_launch_count(int64_t B);
+// Batch-1 table-lookup product on the five-per-byte packing (t5lut.cu).
+bool t5lut_supported(int64_t B, int64_t N, int64_t K);
+cudaError_t launch_gemv_t5lut(const uint8_t* packed, const uint16_t* scales, const uint16_t* x, int64_t N,
+                              int64_t K, void* y, bool y_bf16, cudaStream_t stream);
 
 int sm_count();
 

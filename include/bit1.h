@@ -345,11 +345,15 @@ bit1_status bit1_ternary_combine(const float *ya, const float *yb, int64_t n,
  * bit1_t5_to_planes -- packed bytes -> the two planes of the 2-bit-slot
  *                      layout (N*K/8 bytes each), so a matrix stored in this
  *                      compact form runs on bit1_gemv_ternary's kernels.
- * bit1_gemv_t5      -- y[B][N] straight from the packed bytes: one warp per
- *                      row, fp32 accumulation, up to 8 batch rows per launch
- *                      (bit1_gemv_t5_launches); within the bit1_gemv
- *                      tolerance.  A byte out of range gives an unspecified
- *                      (but in-bounds) result for its row.
+ * bit1_gemv_t5      -- y[B][N] straight from the packed bytes, fp32
+ *                      accumulation, within the bit1_gemv tolerance.  At
+ *                      B = 1 with K a multiple of 1024: a table-lookup
+ *                      kernel (a byte splits into v mod 27 and v / 27, each
+ *                      looked up in a small table of activation partial
+ *                      sums; deterministic).  Otherwise one warp per row, up
+ *                      to 8 batch rows per launch (bit1_gemv_t5_launches).
+ *                      A byte out of range gives an unspecified (but
+ *                      in-bounds) result for its row.
  * All pointers device, 16-byte aligned; BIT1_ESHAPE / BIT1_EINVAL on bad
  * arguments with nothing launched.
  */

@@ -265,3 +265,32 @@ def test_t5_stored_then_run_on_the_slot_kernels(orc):
     idx = torch.from_numpy(rows).cuda()
     assert_gemv_close(y1[:, idx], ref, bd, "t5 -> planes -> slot kernels")
     assert_gemv_close(y2[:, idx], ref, bd, "t5 direct")
+
+
+@pytest.mark.parametrize("N,K", [(1, 1024), (33, 4096), (1000, 5120), (300, 12288), (5000, 2048), (64, 17408)])
+def test_gemv_t5_batch1_table_kernel(orc, N, K):
+    """Batch 1 with K a multiple of 1024 runs the table-lookup kernel (K in one
+    chunk, in several, and with a partial last chunk; ragged N): every output
+    against the oracle, fp32 and bf16, and the same result as the slot
+    kernels on the planes of the same codes (within the tolerance)."""
+    g = synth.rng(880 + N)
+    t = synth.ternary_codes(N, K, g)
+    scales = synth.group_scales(N, K, g)
+    x = synth.activations(1, K, g)
+    p = orc.t5_pack(t, N, K)
+    ref = orc.gemv_t5(p, scales, x, 1, N, K)
+    bound = abs_bound(scales, x, K)
+    dp, ds, dx = dev_u8(p), dev_u16(scales), dev_bf16(x).view(1, K)
+    for ydt in (b1.F32, b1.BF16):
+        y = b1.bit1_gemv_t5(dp, ds, dx, y_dtype=ydt, N=N)
+        torch.cuda.synchronize()
+        assert_gemv_close(y, ref, bound, f"t5 table kernel N={N} K={K} y={ydt}")
+    a, b = b1.bit1_t5_to_planes(dp, K)
+    ys = b1.bit1_gemv_ternary(a, b, ds, dx)
+    y = b1.bit1_gemv_t5(dp, ds, dx, N=N)
+    torch.cuda.synchronize()
+    assert_gemv_close(y, ys.double().cpu().numpy(), 2 * bound, "t5 table kernel vs slot kernels")
+    y2 = b1.bit1_gemv_t5(dp, ds, dx, N=N)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2)                      # deterministic
+    assert b1.bit1_gemv_t5_launches(1, N, K) == 1
