@@ -13,13 +13,11 @@
 //  * k_t5_planes    bytes -> the two sign planes of the 2-bit-slot layout
 //                   (a = t >= 0, b = t > 0), so that a matrix kept in the
 //                   compact packing runs on the slot kernels;
-//  * k_gemv_t5      the product straight from the bytes: one warp per row,
-//                   lanes over the row's bytes, a 256-entry shared table that
-//                   turns a byte into its five digits, fp32 accumulation.
-//                   Plain by design: a byte-indexed table of partial sums (the
-//                   6-bit trick of the binary kernels) has 243 live entries,
-//                   which a warp's 32 lookups hit with bank conflicts, and
-//                   building one costs ~50 entries per input.
+//  * k_gemv_t5      the product straight from the bytes for the shapes the
+//                   batch-1 table kernel (t5lut.cu) does not take: one warp
+//                   per row, lanes over the row's bytes, a 256-entry shared
+//                   table that turns a byte into its five digits, fp32
+//                   accumulation, up to 8 batch rows per launch.
 #include <algorithm>
 
 #include "common.cuh"
