@@ -57,6 +57,8 @@ def configure(lib):
     lib.orc_gemv.restype = ctypes.c_int
     lib.orc_gemv_select.argtypes = [p, p, p, i64, i64, i64, p, i64, p]
     lib.orc_gemv_select.restype = ctypes.c_int
+    lib.orc_gemv_swiglu.argtypes = [p, p, p, i64, i64, i64, p]
+    lib.orc_gemv_swiglu.restype = ctypes.c_int
     lib.orc_gemv_ternary.argtypes = [p, p, p, p, i64, i64, i64, p]
     lib.orc_gemv_ternary.restype = ctypes.c_int
     lib.orc_gemv_ternary_select.argtypes = [p, p, p, p, i64, i64, i64, p, i64, p]
@@ -171,6 +173,16 @@ def gemv_select(bits, scales, x, B: int, N: int, K: int, rows) -> np.ndarray:
     if st != OK:
         raise OracleError(st, "gemv_select")
     return y
+
+
+def gemv_swiglu(bits, scales, x, B: int, N2: int, K: int) -> np.ndarray:
+    """Interleaved gate/up rows (2n gate, 2n+1 up) -> silu(gate) * up, [B, N2/2]."""
+    bits, scales, x = _u8(bits), _u16(scales), _u16(x)
+    h = np.zeros((B, N2 // 2), dtype=np.float64)
+    st = _load().orc_gemv_swiglu(_ptr(bits), _ptr(scales), _ptr(x), B, N2, K, _ptr(h))
+    if st != OK:
+        raise OracleError(st, "gemv_swiglu")
+    return h
 
 
 def gemv_ternary(a, b, scales, x, B: int, N: int, K: int) -> np.ndarray:

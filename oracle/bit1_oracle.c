@@ -27,6 +27,9 @@
  *             section "LocalLLaMA가 본 핵심 포인트": a patch is a list of
  *             (layer, projection, row) entries whose binary weights are
  *             flipped; applying and removing are the same XOR.
+ *  [27B-arch] same page, section "Bonsai 27B의 표현 방식": the base model
+ *             keeps its architecture, whose MLP is SwiGLU; the MLP
+ *             projections are binary like every other matrix.
  *  [8B-what]  "PrismML Bonsai — 1.15GB짜리 8B 모델이 말이 되나?", section
  *             "1-bit이 뭔지부터": weights are {-1,+1}; multiplies become
  *             additions and subtractions.
@@ -262,6 +265,38 @@ int orc_gemv_select(const uint8_t *bits, const uint16_t *scales,
             y[b * n_sel + i] = tmp[b * N + n];
     }
     free(tmp);
+    return ORC_OK;
+}
+
+/* ---- gate/up pair with the SwiGLU activation ------------------------------
+ * [27B-arch]: the MLP is SwiGLU, h = silu(gate x) * (up x), fed to the down
+ * projection.  Reading of the layout, which the pages do not give: the gate
+ * and up matrices are stored as one matrix with interleaved rows, row 2n the
+ * gate and row 2n+1 the up projection of output n.  h[b,n] = silu(g) * u with
+ * the textbook silu(g) = g / (1 + exp(-g)), in fp64 on the exact GEMV
+ * results.  N2 (the interleaved row count) must be even. */
+int orc_gemv_swiglu(const uint8_t *bits, const uint16_t *scales, const uint16_t *x,
+                    int64_t B, int64_t N2, int64_t K, double *h)
+{
+    int st = orc_check_shape(B, N2, K);
+    double *y;
+    if (st != ORC_OK)
+        return st;
+    if (N2 % 2 != 0)
+        return ORC_ESHAPE;
+    if (!bits || !scales || !x || !h)
+        return ORC_EINVAL;
+    y = (double *)malloc(sizeof(double) * (size_t)B * (size_t)N2);
+    if (!y)
+        return ORC_EINVAL;
+    orc_gemv_rows(bits, scales, x, B, N2, K, 0, N2, y);
+    for (int64_t b = 0; b < B; b++) {
+        for (int64_t n = 0; n < N2 / 2; n++) {
+            double g = y[b * N2 + 2 * n], u = y[b * N2 + 2 * n + 1];
+            h[b * (N2 / 2) + n] = g / (1.0 + exp(-g)) * u;
+        }
+    }
+    free(y);
     return ORC_OK;
 }
 

@@ -92,6 +92,19 @@ MUTANTS = [
     ("t5_footprint_padded", "return N * (K / 128) * 26 + 2 * N * (K / 128);",
      "return N * (K / 128) * 32 + 2 * N * (K / 128);",
      [lambda o: pins.test_t5_footprint_between_ideal_and_slots(o)]),
+    ("swiglu_gate_up_swapped", "double g = y[b * N2 + 2 * n], u = y[b * N2 + 2 * n + 1];",
+     "double u = y[b * N2 + 2 * n], g = y[b * N2 + 2 * n + 1];",
+     [lambda o: pins.test_swiglu_matches_dense_and_library_silu(o, 6, 256, 2, 1),
+      lambda o: pins.test_swiglu_zero_gate_or_zero_up_gives_zero(o)]),
+    ("swiglu_sigmoid_sign", "g / (1.0 + exp(-g)) * u", "g / (1.0 + exp(g)) * u",
+     [lambda o: pins.test_swiglu_closed_form_saturation(o),
+      lambda o: pins.test_swiglu_matches_dense_and_library_silu(o, 6, 256, 2, 1)]),
+    ("swiglu_sigmoid_without_g", "g / (1.0 + exp(-g)) * u", "1.0 / (1.0 + exp(-g)) * u",
+     [lambda o: pins.test_swiglu_zero_gate_or_zero_up_gives_zero(o)]),
+    ("swiglu_batch_row_ignored", "h[b * (N2 / 2) + n] =", "h[n] =",
+     [lambda o: pins.test_swiglu_matches_dense_and_library_silu(o, 10, 384, 3, 2)]),
+    ("swiglu_odd_rows_accepted", "    if (N2 % 2 != 0)\n        return ORC_ESHAPE;\n", "",
+     [lambda o: pins.test_swiglu_rejects_odd_row_count(o)]),
 ]
 
 

@@ -203,6 +203,75 @@ def test_gemv_select_and_threads_agree(orc):
     assert np.array_equal(yt, y)
 
 
+# ---------------------------------------------------------------- SwiGLU pair
+
+def _silu_np(g):
+    """silu(g) = g * sigmoid(g), the sigmoid from scipy's expit (a library
+    routine, not the oracle's g / (1 + exp(-g)))."""
+    from scipy.special import expit
+    return g * expit(g)
+
+
+@pytest.mark.parametrize("N2,K,B,seed", [(2, 128, 1, 0), (6, 256, 2, 1), (10, 384, 3, 2)])
+def test_swiglu_matches_dense_and_library_silu(orc, N2, K, B, seed):
+    """Gate rows 2n, up rows 2n+1: dense fp64 matmul, then the library
+    sigmoid.  Tolerance: the GEMV rounding (1e-12 of sum |s x|) carried
+    through h = silu(g) u with |silu'| <= 1.1, plus the product's rounding."""
+    g = synth.rng(300 + seed)
+    bits = synth.sign_bits(N2, K, g)
+    scales = synth.group_scales(N2, K, g, offset=1e-3)
+    x = synth.activations(B, K, g)
+    h = orc.gemv_swiglu(bits, scales, x, B, N2, K)
+    y, W, X = _dense(bits, scales, x, N2, K)
+    bd = _bound(W, X)
+    gate, up = y[:, 0::2], y[:, 1::2]
+    want = _silu_np(gate) * up
+    tol = 1e-12 * (1.1 * bd[:, 0::2] * np.abs(up) + np.abs(gate) * bd[:, 1::2]) + 1e-14 * np.abs(want) + 1e-300
+    assert h.shape == (B, N2 // 2)
+    assert np.all(np.abs(h - want) <= tol)
+    # the pair is not symmetric: gate and up swapped gives another result
+    assert not np.allclose(h, _silu_np(up) * gate, rtol=1e-6, atol=0)
+
+
+def test_swiglu_zero_gate_or_zero_up_gives_zero(orc):
+    """silu(0) = 0 and u = 0 each force h = 0 exactly; the other outputs are
+    untouched by zeroing one pair's scales."""
+    N2, K, B = 8, 256, 2
+    bits, scales = synth.matrix(N2, K, 31, scale_offset=1e-3)
+    x = synth.x_for(B, K, 31)
+    h = orc.gemv_swiglu(bits, scales, x, B, N2, K)
+    s0 = scales.reshape(N2, K // 128).copy()
+    s0[2] = 0          # gate of output 1
+    s0[7] = 0          # up of output 3
+    hz = orc.gemv_swiglu(bits, s0, x, B, N2, K)
+    assert np.all(hz[:, [1, 3]] == 0.0)
+    assert np.array_equal(hz[:, [0, 2]], h[:, [0, 2]])
+
+
+def test_swiglu_closed_form_saturation(orc):
+    """All bits set and one scale value per row: g = s_g * sum x and
+    u = s_u * sum x in closed form; a large positive gate passes through
+    (silu(g) = g up to e^-g), a large negative one closes (h ~ g e^g u)."""
+    N2, K, B = 4, 128, 1
+    bits = np.full((N2, K // 8), 0xFF, dtype=np.uint8)
+    x = synth.to_bf16_bits(np.full((B, K), 0.25))      # sum x = 32 exactly
+    sv = np.array([1.25, 0.5, -1.25, 0.5], dtype=np.float16)   # g = +-40, u = 16
+    scales = sv.view(np.uint16).reshape(N2, 1)
+    h = orc.gemv_swiglu(bits, scales, x, B, N2, K)
+    assert abs(h[0, 0] - 40.0 * 16.0) <= 640.0 * 1e-15 + 640.0 * np.exp(-40.0)
+    want_neg = -40.0 * np.exp(-40.0) / (1.0 + np.exp(-40.0)) * 16.0
+    assert abs(h[0, 1] - want_neg) <= 1e-12 * abs(want_neg)
+
+
+def test_swiglu_rejects_odd_row_count(orc):
+    bits = np.zeros((3, 16), dtype=np.uint8)
+    scales = np.zeros((3, 1), dtype=np.uint16)
+    x = np.zeros((1, 128), dtype=np.uint16)
+    with pytest.raises(orc.OracleError) as e:
+        orc.gemv_swiglu(bits, scales, x, 1, 3, 128)
+    assert e.value.status == orc.ESHAPE
+
+
 def test_gemv_rejects_bad_shapes(orc):
     bits = np.zeros((2, 24), dtype=np.uint8)
     scales = np.zeros((2, 2), dtype=np.uint16)
