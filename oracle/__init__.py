@@ -59,6 +59,8 @@ def configure(lib):
     lib.orc_gemv_select.restype = ctypes.c_int
     lib.orc_gemv_swiglu.argtypes = [p, p, p, i64, i64, i64, p]
     lib.orc_gemv_swiglu.restype = ctypes.c_int
+    lib.orc_gemv_swiglu_select.argtypes = [p, p, p, i64, i64, i64, p, i64, p]
+    lib.orc_gemv_swiglu_select.restype = ctypes.c_int
     lib.orc_gemv_ternary.argtypes = [p, p, p, p, i64, i64, i64, p]
     lib.orc_gemv_ternary.restype = ctypes.c_int
     lib.orc_gemv_ternary_select.argtypes = [p, p, p, p, i64, i64, i64, p, i64, p]
@@ -182,6 +184,18 @@ def gemv_swiglu(bits, scales, x, B: int, N2: int, K: int) -> np.ndarray:
     st = _load().orc_gemv_swiglu(_ptr(bits), _ptr(scales), _ptr(x), B, N2, K, _ptr(h))
     if st != OK:
         raise OracleError(st, "gemv_swiglu")
+    return h
+
+
+def gemv_swiglu_select(bits, scales, x, B: int, N2: int, K: int, units) -> np.ndarray:
+    """h[B, len(units)] for the listed hidden units only (sampled checks)."""
+    bits, scales, x = _u8(bits), _u16(scales), _u16(x)
+    units = np.ascontiguousarray(np.asarray(units, dtype=np.int64))
+    h = np.zeros((B, units.size), dtype=np.float64)
+    st = _load().orc_gemv_swiglu_select(_ptr(bits), _ptr(scales), _ptr(x), B, N2, K,
+                                        _ptr(units), units.size, _ptr(h))
+    if st != OK:
+        raise OracleError(st, "gemv_swiglu_select")
     return h
 
 

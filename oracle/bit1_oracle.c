@@ -300,6 +300,39 @@ int orc_gemv_swiglu(const uint8_t *bits, const uint16_t *scales, const uint16_t 
     return ORC_OK;
 }
 
+/* Selected hidden units only: h[b * n_sel + i] = h[b, units[i]] of the
+ * interleaved pair above, from rows 2 units[i] and 2 units[i] + 1 alone.
+ * Used to check full-size problems on sampled outputs. */
+int orc_gemv_swiglu_select(const uint8_t *bits, const uint16_t *scales, const uint16_t *x,
+                           int64_t B, int64_t N2, int64_t K, const int64_t *units,
+                           int64_t n_sel, double *h)
+{
+    int st = orc_check_shape(B, N2, K);
+    double *y;
+    if (st != ORC_OK)
+        return st;
+    if (N2 % 2 != 0)
+        return ORC_ESHAPE;
+    if (!bits || !scales || !x || !h || (n_sel > 0 && !units))
+        return ORC_EINVAL;
+    for (int64_t i = 0; i < n_sel; i++)
+        if (units[i] < 0 || units[i] >= N2 / 2)
+            return ORC_ERANGE;
+    y = (double *)malloc(sizeof(double) * (size_t)B * (size_t)N2);
+    if (!y)
+        return ORC_EINVAL;
+    for (int64_t i = 0; i < n_sel; i++) {
+        int64_t n = units[i];
+        orc_gemv_rows(bits, scales, x, B, N2, K, 2 * n, 2 * n + 2, y);
+        for (int64_t b = 0; b < B; b++) {
+            double g = y[b * N2 + 2 * n], u = y[b * N2 + 2 * n + 1];
+            h[b * n_sel + i] = g / (1.0 + exp(-g)) * u;
+        }
+    }
+    free(y);
+    return ORC_OK;
+}
+
 /* ---- ternary linear layer ------------------------------------------------
  * y[b,n] = sum_g s[n,g] * sum_{k in group g} t(n,k) * x[b,k] ([27B-ter]);
  * t read from the two planes one weight at a time; fp64 accumulation, the

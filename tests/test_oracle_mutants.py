@@ -20,6 +20,10 @@ _SCALE = "double s = orc_half_to_double(scales[n * G + g]);"
 _SCALE_T = "double s = orc_half_to_double(scales[g * N + n]);"
 _XB = "double xv = orc_bf16_to_double(x[b * K + k]);\n                    if (orc_bit"
 _XT = "double xv = orc_bf16_to_double(x[b * K + k]);\n                    if (t > 0)"
+# The SwiGLU pair's full and selected forms share the gate/up line.
+_GU = "double g = y[b * N2 + 2 * n], u = y[b * N2 + 2 * n + 1];"
+_GU_SW = "double u = y[b * N2 + 2 * n], g = y[b * N2 + 2 * n + 1];"
+_HF = "\n            h[b * (N2 / 2) + n] ="
 
 # (name, text in the source, replacement, pins expected to catch it)
 MUTANTS = [
@@ -92,19 +96,24 @@ MUTANTS = [
     ("t5_footprint_padded", "return N * (K / 128) * 26 + 2 * N * (K / 128);",
      "return N * (K / 128) * 32 + 2 * N * (K / 128);",
      [lambda o: pins.test_t5_footprint_between_ideal_and_slots(o)]),
-    ("swiglu_gate_up_swapped", "double g = y[b * N2 + 2 * n], u = y[b * N2 + 2 * n + 1];",
-     "double u = y[b * N2 + 2 * n], g = y[b * N2 + 2 * n + 1];",
+    ("swiglu_gate_up_swapped", _GU + _HF, _GU_SW + _HF,
      [lambda o: pins.test_swiglu_matches_dense_and_library_silu(o, 6, 256, 2, 1),
       lambda o: pins.test_swiglu_zero_gate_or_zero_up_gives_zero(o)]),
-    ("swiglu_sigmoid_sign", "g / (1.0 + exp(-g)) * u", "g / (1.0 + exp(g)) * u",
+    ("swiglu_sigmoid_sign", _HF + " g / (1.0 + exp(-g)) * u", _HF + " g / (1.0 + exp(g)) * u",
      [lambda o: pins.test_swiglu_closed_form_saturation(o),
       lambda o: pins.test_swiglu_matches_dense_and_library_silu(o, 6, 256, 2, 1)]),
-    ("swiglu_sigmoid_without_g", "g / (1.0 + exp(-g)) * u", "1.0 / (1.0 + exp(-g)) * u",
+    ("swiglu_sigmoid_without_g", _HF + " g / (1.0 + exp(-g)) * u", _HF + " 1.0 / (1.0 + exp(-g)) * u",
      [lambda o: pins.test_swiglu_zero_gate_or_zero_up_gives_zero(o)]),
-    ("swiglu_batch_row_ignored", "h[b * (N2 / 2) + n] =", "h[n] =",
+    ("swiglu_batch_row_ignored", _HF, "\n            h[n] =",
      [lambda o: pins.test_swiglu_matches_dense_and_library_silu(o, 10, 384, 3, 2)]),
-    ("swiglu_odd_rows_accepted", "    if (N2 % 2 != 0)\n        return ORC_ESHAPE;\n", "",
+    ("swiglu_odd_rows_accepted", "    if (N2 % 2 != 0)\n        return ORC_ESHAPE;\n    if (!bits || !scales || !x || !h)\n",
+     "    if (!bits || !scales || !x || !h)\n",
      [lambda o: pins.test_swiglu_rejects_odd_row_count(o)]),
+    ("swiglu_select_batch_row_ignored", "h[b * n_sel + i] = g", "h[i] = g",
+     [lambda o: pins.test_swiglu_select_matches_full(o)]),
+    ("swiglu_select_gate_up_swapped", _GU + "\n            h[b * n_sel + i] =",
+     _GU_SW + "\n            h[b * n_sel + i] =",
+     [lambda o: pins.test_swiglu_select_matches_full(o)]),
 ]
 
 

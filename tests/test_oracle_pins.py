@@ -263,6 +263,19 @@ def test_swiglu_closed_form_saturation(orc):
     assert abs(h[0, 1] - want_neg) <= 1e-12 * abs(want_neg)
 
 
+def test_swiglu_select_matches_full(orc):
+    N2, K, B = 14, 384, 2
+    bits, scales = synth.matrix(N2, K, 33, scale_offset=1e-3)
+    x = synth.x_for(B, K, 33)
+    h = orc.gemv_swiglu(bits, scales, x, B, N2, K)
+    units = [6, 0, 3, 3]
+    hs = orc.gemv_swiglu_select(bits, scales, x, B, N2, K, units)
+    assert np.array_equal(hs, h[:, units])
+    with pytest.raises(orc.OracleError) as e:
+        orc.gemv_swiglu_select(bits, scales, x, B, N2, K, [7])
+    assert e.value.status == orc.ERANGE
+
+
 def test_swiglu_rejects_odd_row_count(orc):
     bits = np.zeros((3, 16), dtype=np.uint8)
     scales = np.zeros((3, 1), dtype=np.uint16)
