@@ -303,6 +303,14 @@ def oracle_beside_extras(extras: dict) -> None:
         extras["verify_sweep_8b_b5"]["cpu_oracle"] = entry(wb / secs / 1e9, "GB/s (5 rows per weight read)",
                                                            "1/64 of the rows of one 8B-class layer at B = 5",
                                                            threads)
+    if "fused_mlp_sweep_8b" in extras:
+        N2, K, rows = 24576, 4096, 192
+        bits, scales = synth.matrix(rows, K, 7)
+        x = synth.x_for(1, K, 7)
+        secs = _timed(lambda: oracle.gemv_swiglu(bits, scales, x, 1, rows, K))
+        wb = rows * (K // 8 + 2 * (K // 128))
+        extras["fused_mlp_sweep_8b"]["cpu_oracle"] = entry(wb / secs / 1e9, "GB/s",
+                                                           "192 rows (96 gate/up pairs) x 4096 with SwiGLU", 1)
     if "ternary_sweep_8b" in extras:
         N, K, rows = 12288, 4096, 96
         a, b, scales = synth.ternary_matrix(rows, K, 4)
@@ -674,6 +682,43 @@ def extra_verify_sweep_8b(torch, b1, B=5, steps=20):
     return out
 
 
+def extra_fused_mlp_sweep_8b(torch, b1, steps=20):
+    """The 8B-class sweep with each layer's gate and up projections in one
+    interleaved matrix whose epilogue applies SwiGLU (217 matrices, the same
+    weight bytes), against the plain 253-matrix sweep timed in the same way
+    on the same box: the fused activation should cost nothing measurable."""
+    from bit_weight_gemv_sign_b300 import synth
+    from bit_weight_gemv_sign_b300.sweep import Sweep
+
+    def timed(mats):
+        sw = Sweep(mats, seed0=0, batch=1, y_dtype=b1.BF16).fill_device(66)
+        plan = sw.group_plan()
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                plan.run(stream=s)
+            s.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(steps):
+                plan.run(stream=s)
+            e1.record(s)
+            e1.synchronize()
+        wb, yb = sw.weight_bytes, sum(2 * m.out for m in sw.mats)
+        del sw, plan
+        torch.cuda.empty_cache()
+        return e0.elapsed_time(e1) / steps, wb, yb
+
+    ms_f, wb, yb_f = timed(synth.sweep_8b_fused_mlp())
+    ms_p, wb_p, yb_p = timed(synth.sweep_8b())
+    hbm, _ = _peaks()
+    gf, gp = wb / (ms_f * 1e-3) / 1e9, wb_p / (ms_p * 1e-3) / 1e9
+    return {"matrices": 217, "weight_bytes": wb, "ms_per_step": ms_f, "weight_gbs": gf, "hbm_frac": gf / hbm,
+            "plain_sweep_ms_per_step": ms_p, "plain_sweep_weight_gbs": gp, "output_bytes": yb_f,
+            "plain_output_bytes": yb_p,
+            "note": "one grouped launch per step either way; h = silu(gate) * up is written instead of gate and up"}
+
+
 def run_mine(args):
     import torch
     import bit_weight_gemv_sign_b300 as b1
@@ -832,7 +877,8 @@ def run_mine(args):
                          "c5_sweep_27b": extra_c5_sweep_27b(torch, b1),
                          "ternary_sweep_8b": extra_ternary_sweep_8b(torch, b1),
                          "ternary_t5": extra_t5(torch, b1),
-                         "verify_sweep_8b_b5": extra_verify_sweep_8b(torch, b1)}
+                         "verify_sweep_8b_b5": extra_verify_sweep_8b(torch, b1),
+                         "fused_mlp_sweep_8b": extra_fused_mlp_sweep_8b(torch, b1)}
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
         oracle.build()

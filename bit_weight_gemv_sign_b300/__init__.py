@@ -30,11 +30,12 @@ OK, EINVAL, ESHAPE, ERANGE, ECUDA, ENAN = 0, 1, 2, 3, 4, 5
 F32, BF16, F16 = 0, 1, 2
 AUTO, SIMPLE, LUT, SPLITK, TC, LUT6, STREAM = 0, 1, 2, 3, 4, 5, 6
 FLAG_PDL = 1
+EPI_NONE, EPI_SWIGLU = 0, 1
 
 class _Problem(ctypes.Structure):
     _fields_ = [("bits", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("x", ctypes.c_void_p),
                 ("y", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
-                ("y_dtype", ctypes.c_int)]
+                ("y_dtype", ctypes.c_int), ("epilogue", ctypes.c_int)]
 
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -282,15 +283,19 @@ def bit1_group_plan_bytes(count: int) -> int:
 
 
 def bit1_group_plan(problems, host_plan_ptr: int, plan_bytes: int, B: int = 1) -> None:
-    """problems: sequence of (bits, scales, x, y) CUDA tensors; x is [B, K]
-    (or [K] at B = 1) bf16 and y [B, N].  B > 1 calls bit1_group_plan_batched."""
+    """problems: sequence of (bits, scales, x, y) or (bits, scales, x, y,
+    epilogue) CUDA tensors; x is [B, K] (or [K] at B = 1) bf16 and y [B, N]
+    ([B, N/2] with EPI_SWIGLU, the rows then interleaved gate/up pairs).
+    B > 1 calls bit1_group_plan_batched."""
     import torch
     arr = (_Problem * len(problems))()
-    for i, (bits, scales, x, y) in enumerate(problems):
+    for i, pr in enumerate(problems):
+        bits, scales, x, y = pr[:4]
+        epi = int(pr[4]) if len(pr) > 4 else EPI_NONE
         if y.dtype not in (torch.float32, torch.bfloat16):
             raise TypeError("y must be float32 or bfloat16")
         arr[i] = _Problem(_dptr(bits, "bits"), _dptr(scales, "scales"), _dptr(x, "x"), _dptr(y, "y"),
-                          bits.shape[0], x.shape[-1], BF16 if y.dtype == torch.bfloat16 else F32)
+                          bits.shape[0], x.shape[-1], BF16 if y.dtype == torch.bfloat16 else F32, epi)
     if B == 1:
         st = load().bit1_group_plan(arr, len(problems), host_plan_ptr, plan_bytes)
     else:

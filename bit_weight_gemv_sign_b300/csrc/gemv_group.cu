@@ -73,6 +73,7 @@ struct alignas(128) GProb {
     const uint16_t* x;
     void* y;
     int N, K, G, RB, y_bf16, nch;
+    int swiglu;             // rows are (gate, up) pairs; y is h = silu(gate) * up, [nb][N/2]
 };
 
 struct GSingle {            // whole plan of a one-problem call, passed by value
@@ -355,7 +356,21 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
                     }
                     if (c + 1 < pi.z) continue;
                 }
-                if (row < pi.w) {
+                if (pr.swiglu) {
+                    // Lane 2m holds the gate row and lane 2m+1 the up row of hidden
+                    // unit row/2 (N even: a pair is in range or out of it whole).
+#pragma unroll
+                    for (int bb = 0; bb < NB; ++bb) {
+                        const float u = __shfl_down_sync(0xffffffffu, acc[bb], 1);
+                        if (!(lane & 1) && row < pi.w) {
+                            const float gt = acc[bb];
+                            const float h = gt / (1.f + expf(-gt)) * u;
+                            const int64_t o = (int64_t)bb * (pi.w >> 1) + (row >> 1);
+                            if (pr.y_bf16) reinterpret_cast<uint16_t*>(pr.y)[o] = f32_to_bf16_bits(h);
+                            else reinterpret_cast<float*>(pr.y)[o] = h;
+                        }
+                    }
+                } else if (row < pi.w) {
 #pragma unroll
                     for (int bb = 0; bb < NB; ++bb) {
                         const int64_t o = (int64_t)bb * pi.w + row;
@@ -435,6 +450,7 @@ bool encode_prob(GProb& g, const bit1_gemv_problem& pb, int nb) {
     g.G = (int)G;
     g.RB = (int)((pb.N + 31) / 32);
     g.y_bf16 = pb.y_dtype == BIT1_BF16;
+    g.swiglu = pb.epilogue == BIT1_EPI_SWIGLU;
     const int cg = g_chunk_groups(nb);
     g.nch = (int)((G + cg - 1) / cg);
     return true;
@@ -550,7 +566,8 @@ bool problem_ok(const bit1_gemv_problem& pb) {
     return pb.bits && pb.scales && pb.x && pb.y && pb.N >= 1 && pb.N <= (1LL << 30) && pb.K >= 1024 &&
            pb.K % 1024 == 0 && pb.K <= (1LL << 20) && (pb.y_dtype == BIT1_F32 || pb.y_dtype == BIT1_BF16) &&
            ((uintptr_t)pb.bits & 15) == 0 && ((uintptr_t)pb.scales & 15) == 0 && ((uintptr_t)pb.x & 15) == 0 &&
-           ((uintptr_t)pb.y & 15) == 0;
+           ((uintptr_t)pb.y & 15) == 0 &&
+           (pb.epilogue == BIT1_EPI_NONE || (pb.epilogue == BIT1_EPI_SWIGLU && pb.N % 2 == 0));
 }
 
 cudaError_t set_smem_attr(const void* f) {
@@ -616,7 +633,7 @@ bool group1_supported(int64_t B, int64_t N, int64_t K) {
 }
 
 cudaError_t launch_gemv_group1(const GemvArgs& a) {
-    bit1_gemv_problem pb;
+    bit1_gemv_problem pb{};
     pb.bits = a.bits;
     pb.scales = a.scales;
     pb.x = a.x;

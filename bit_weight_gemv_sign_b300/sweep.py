@@ -18,8 +18,8 @@ import numpy as np
 import torch
 
 from . import synth
-from . import (BF16, F32, FLAG_PDL, AUTO, GroupPlan, bit1_gemv_ex, bit1_gemv_launches,
-               bit1_ternary_combine, bit1_xor_patch)
+from . import (BF16, F32, FLAG_PDL, AUTO, EPI_NONE, EPI_SWIGLU, GroupPlan, bit1_gemv_ex,
+               bit1_gemv_launches, bit1_ternary_combine, bit1_xor_patch)
 
 
 def _align(n: int, a: int = 256) -> int:
@@ -42,7 +42,7 @@ class Sweep:
             self.bits_off.append(nb); nb += _align(m.N * m.K // 8)
             self.sc_off.append(ns); ns += _align(m.N * (m.K // 128) * 2)
             self.x_off.append(nx); nx += _align(batch * m.K * 2)
-            self.y_off.append(ny); ny += _align(batch * m.N * ysz)
+            self.y_off.append(ny); ny += _align(batch * m.out * ysz)
         self.bits = torch.empty(nb, dtype=torch.uint8, device=device)
         self.scales = torch.empty(ns // 2, dtype=torch.int16, device=device)
         self.x = torch.empty(nx // 2, dtype=torch.bfloat16, device=device)
@@ -72,8 +72,8 @@ class Sweep:
         m = self.mats[i]
         yb = self.y if ybuf is None else ybuf
         if self.y_dtype == BF16:
-            return yb[self.y_off[i]: self.y_off[i] + 2 * self.B * m.N].view(torch.bfloat16).view(self.B, m.N)
-        return yb[self.y_off[i]: self.y_off[i] + 4 * self.B * m.N].view(torch.float32).view(self.B, m.N)
+            return yb[self.y_off[i]: self.y_off[i] + 2 * self.B * m.out].view(torch.bfloat16).view(self.B, m.out)
+        return yb[self.y_off[i]: self.y_off[i] + 4 * self.B * m.out].view(torch.float32).view(self.B, m.out)
 
     # ---- data ------------------------------------------------------------
     def host_matrix(self, i):
@@ -113,6 +113,8 @@ class Sweep:
         return sum(bit1_gemv_launches(self.B, m.N, m.K, self.variant) for m in self.mats)
 
     def run_eager(self, stream=None, pdl: bool = True):
+        if any(m.swiglu for m in self.mats):
+            raise ValueError("the SwiGLU epilogue runs in the grouped launch only (group_plan)")
         for i, m in enumerate(self.mats):
             bit1_gemv_ex(self.bits_of(i), self.scales_of(i), self.x_of(i), y=self.y_of(i),
                          variant=self.variant, flags=FLAG_PDL if pdl else 0, stream=stream,
@@ -139,8 +141,8 @@ class Sweep:
         kernel launch.  ``x`` and
         ``y`` replace the activation / output arenas (same layout), e.g. for a
         second I/O slot over the same resident weights."""
-        probs = [(self.bits_of(i), self.scales_of(i), self.x_of(i, x), self.y_of(i, y))
-                 for i in range(len(self.mats))]
+        probs = [(self.bits_of(i), self.scales_of(i), self.x_of(i, x), self.y_of(i, y),
+                  EPI_SWIGLU if m.swiglu else EPI_NONE) for i, m in enumerate(self.mats)]
         return GroupPlan(probs, device=self.device, B=self.B)
 
     def apply_patch(self, entries, proj_count: int = 7):

@@ -102,6 +102,11 @@ class Mat:
     name: str
     N: int   # outputs (rows)
     K: int   # inputs (columns, multiple of 128)
+    swiglu: bool = False   # rows are interleaved (gate, up) pairs; N / 2 outputs
+
+    @property
+    def out(self) -> int:
+        return self.N // 2 if self.swiglu else self.N
 
 
 TINY = Mat("tiny", 256, 1024)
@@ -120,6 +125,21 @@ def sweep_8b() -> list:
         out += [Mat(f"L{layer}.q", 4096, 4096), Mat(f"L{layer}.k", 1024, 4096),
                 Mat(f"L{layer}.v", 1024, 4096), Mat(f"L{layer}.o", 4096, 4096),
                 Mat(f"L{layer}.gate", 12288, 4096), Mat(f"L{layer}.up", 12288, 4096),
+                Mat(f"L{layer}.down", 4096, 12288)]
+    out.append(Mat("lm_head", 151936, 4096))
+    return out
+
+
+def sweep_8b_fused_mlp() -> list:
+    """The 8B-class sweep with each layer's gate and up projections stored as
+    one interleaved 24576 x 4096 matrix whose product ends in the SwiGLU
+    activation (36 x {q, k, v, o, gate_up, down} + the LM head, 217 matrices,
+    the same weights and bytes as ``sweep_8b``)."""
+    out = []
+    for layer in range(36):
+        out += [Mat(f"L{layer}.q", 4096, 4096), Mat(f"L{layer}.k", 1024, 4096),
+                Mat(f"L{layer}.v", 1024, 4096), Mat(f"L{layer}.o", 4096, 4096),
+                Mat(f"L{layer}.gate_up", 24576, 4096, swiglu=True),
                 Mat(f"L{layer}.down", 4096, 12288)]
     out.append(Mat("lm_head", 151936, 4096))
     return out

@@ -183,10 +183,25 @@ typedef struct bit1_gemv_problem {
     const uint8_t *bits;     /* [N][K/8] sign bits */
     const uint16_t *scales;  /* [N][K/128] fp16 scales */
     const uint16_t *x;       /* [K] bf16 activations */
-    void *y;                 /* [N] output of y_dtype */
+    void *y;                 /* [N] output of y_dtype ([N/2] with BIT1_EPI_SWIGLU) */
     int64_t N, K;
     int y_dtype;
+    int epilogue;            /* BIT1_EPI_NONE (0) or BIT1_EPI_SWIGLU; other values: BIT1_ESHAPE */
 } bit1_gemv_problem;
+
+/* Epilogue of a grouped problem.  BIT1_EPI_SWIGLU: the problem is the gate and
+ * up projections of a SwiGLU MLP (the Bonsai 27B page, section "Bonsai 27B의
+ * 표현 방식": the base model keeps its SwiGLU MLP, and the MLP projections are
+ * binary like the rest) stored as ONE matrix with interleaved rows -- row 2n
+ * the gate, row 2n+1 the up projection of hidden unit n; N (the interleaved
+ * row count) must be even, else BIT1_ESHAPE.  y then receives
+ *     h[b][n] = silu(g) * u,  silu(g) = g / (1 + exp(-g)),
+ * [B][N/2] of y_dtype, computed in fp32 from the fp32 gate and up results
+ * before the one output rounding; the gate and up values are not written.
+ * Error: the GEMV error of g and u carried through h (|silu'| <= 1.1) plus a
+ * few fp32 ulps of h. */
+#define BIT1_EPI_NONE   0
+#define BIT1_EPI_SWIGLU 1
 
 size_t bit1_group_plan_bytes(int count);
 bit1_status bit1_group_plan(const bit1_gemv_problem *problems, int count,

@@ -45,3 +45,25 @@ def assert_gemv_close(y_gpu: torch.Tensor, y_ref: np.ndarray, bound: np.ndarray,
         raise AssertionError(f"{what}: {bad.sum()} outputs out of tolerance; first at {tuple(i)}: "
                              f"gpu {yg[tuple(i)]!r} oracle {y_ref[tuple(i)]!r} tol {tol[tuple(i)]!r}")
     return float((err / tol).max()) if err.size else 0.0
+
+
+def assert_swiglu_close(h_gpu: torch.Tensor, h_ref: np.ndarray, g_ref: np.ndarray, u_ref: np.ndarray,
+                        bound_g: np.ndarray, bound_u: np.ndarray, what: str = ""):
+    """Tolerance of h = silu(g) u from the GEMV tolerance of g and u
+    (dg <= 1e-3 * bound_g + 1e-6, likewise du): |silu'| <= 1.1 and
+    |silu(g)| <= |g| give |dh| <= 1.1 dg (|u| + du) + |g| du; plus eight fp32
+    ulps of h for the activation and the product, and the bf16 output's own
+    rounding (2^-8 |h|) when h is bf16."""
+    hg = h_gpu.detach().float().cpu().numpy().astype(np.float64).reshape(h_ref.shape)
+    dg = 1e-3 * bound_g + 1e-6
+    du = 1e-3 * bound_u + 1e-6
+    tol = 1.1 * dg * (np.abs(u_ref) + du) + np.abs(g_ref) * du + 8 * 2.0 ** -24 * np.abs(h_ref) + 1e-30
+    if h_gpu.dtype == torch.bfloat16:
+        tol = tol + 2.0 ** -8 * np.abs(h_ref)
+    err = np.abs(hg - h_ref)
+    bad = err > tol
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} outputs out of tolerance; first at {tuple(i)}: "
+                             f"gpu {hg[tuple(i)]!r} oracle {h_ref[tuple(i)]!r} tol {tol[tuple(i)]!r}")
+    return float((err / tol).max()) if err.size else 0.0

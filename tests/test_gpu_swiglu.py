@@ -1,0 +1,133 @@
+"""The SwiGLU epilogue of the grouped launch: a problem whose rows are
+interleaved (gate, up) pairs writes h = silu(gate) * up instead of the two
+products (the Bonsai 27B page, section "Bonsai 27B의 표현 방식": the base
+model's MLP is SwiGLU).  Against the CPU oracle on mixed plans (SwiGLU and
+plain problems in one launch; one and several K chunks; ragged pair counts),
+batch rows 1 .. 6, fp32 and bf16 output; the full 8B-class sweep with fused
+gate/up matrices on sampled outputs of every matrix."""
+import numpy as np
+import pytest
+import torch
+
+import bit_weight_gemv_sign_b300 as b1
+from bit_weight_gemv_sign_b300 import synth
+from bit_weight_gemv_sign_b300.sweep import Sweep
+from tests.helpers import abs_bound, assert_gemv_close, assert_swiglu_close, dev_bf16, dev_u8, dev_u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    b1.load()
+
+
+# (N, K, SwiGLU): N is the interleaved row count of a SwiGLU problem
+SHAPES = [(2000, 4096, True), (300, 4096, False), (64, 1024, True), (2050, 5120, True),
+          (300, 12288, True), (2, 2048, True), (4096, 1024, False), (24576, 4096, True)]
+
+
+def _problems(B, seed, ydt, shapes=SHAPES):
+    host, probs = [], []
+    for i, (N, K, sw) in enumerate(shapes):
+        bits, scales = synth.matrix(N, K, seed + i)
+        x = synth.x_for(B, K, seed + i)
+        out = N // 2 if sw else N
+        y = torch.empty((B, out), dtype=torch.bfloat16 if ydt == b1.BF16 else torch.float32, device="cuda")
+        host.append((bits, scales, x))
+        xd = dev_bf16(x).view(B, K) if B > 1 else dev_bf16(x).view(K)
+        probs.append((dev_u8(bits), dev_u16(scales), xd, y, b1.EPI_SWIGLU if sw else b1.EPI_NONE))
+    return host, probs
+
+
+def _check(orc, shapes, host, probs, B, what):
+    for (N, K, sw), (bits, scales, x), pr in zip(shapes, host, probs):
+        y = pr[3]
+        bound = abs_bound(scales, x, K)
+        if not sw:
+            assert_gemv_close(y, orc.gemv(bits, scales, x, B, N, K), bound, f"{what} plain N={N} K={K}")
+            continue
+        yo = orc.gemv(bits, scales, x, B, N, K)
+        h = orc.gemv_swiglu(bits, scales, x, B, N, K)
+        assert_swiglu_close(y, h, yo[:, 0::2], yo[:, 1::2], bound[:, 0::2], bound[:, 1::2],
+                            f"{what} SwiGLU N={N} K={K}")
+
+
+@pytest.mark.parametrize("B", [1, 2, 3, 5, 6])
+@pytest.mark.parametrize("ydt", [b1.F32, b1.BF16])
+def test_swiglu_grouped_matches_oracle(orc, B, ydt):
+    shapes = SHAPES if B <= 2 else SHAPES[:-1]
+    host, probs = _problems(B, 9400 + 10 * B + ydt, ydt, shapes)
+    plan = b1.GroupPlan(probs, B=B)
+    plan.run()
+    torch.cuda.synchronize()
+    assert b1.bit1_device_wait_timeouts() == 0
+    _check(orc, shapes, host, probs, B, f"grouped B={B} y={ydt}")
+    first = [p[3].clone() for p in probs]
+    plan.run(flags=b1.FLAG_PDL)
+    torch.cuda.synchronize()
+    for a, p in zip(first, probs):
+        assert torch.equal(a, p[3])
+
+
+def test_swiglu_pairs_the_plain_products():
+    """The fused epilogue acts on the very accumulators the plain launch
+    writes: h agrees with silu(g) * u formed by torch in fp32 from the plain
+    fp32 results to a few ulps, pair by pair, in the interleaved order."""
+    shapes = [(2000, 4096, True), (300, 12288, True), (2050, 5120, True)]
+    for B in (1, 4):
+        host, probs = _problems(B, 9500 + B, b1.F32, shapes)
+        plain = [(p[0], p[1], p[2], torch.empty((B, s[0]), dtype=torch.float32, device="cuda"))
+                 for p, s in zip(probs, shapes)]
+        b1.GroupPlan(probs, B=B).run()
+        b1.GroupPlan(plain, B=B).run()
+        torch.cuda.synchronize()
+        for p, q in zip(probs, plain):
+            g, u = q[3][:, 0::2], q[3][:, 1::2]
+            want = torch.nn.functional.silu(g) * u
+            tol = 8 * 2.0 ** -24 * (g.abs() * u.abs()) + 1e-30
+            assert torch.all((p[3] - want).abs() <= tol)
+
+
+def test_swiglu_rejects_odd_rows_and_unknown_epilogue():
+    host, probs = _problems(1, 9600, b1.F32, [(64, 1024, True)])
+    bits, scales, x, _, _ = probs[0]
+    odd = (bits[:63], scales[:63], x, torch.empty(31, device="cuda"), b1.EPI_SWIGLU)
+    with pytest.raises(b1.Bit1Error) as e:
+        b1.GroupPlan([odd])
+    assert e.value.status == b1.ESHAPE
+    bad = (bits, scales, x, torch.empty(64, device="cuda"), 2)
+    with pytest.raises(b1.Bit1Error) as e:
+        b1.GroupPlan([bad])
+    assert e.value.status == b1.ESHAPE
+
+
+def _sample(n, count, seed):
+    r = np.random.default_rng(seed).choice(n, min(count, n), replace=False)
+    return np.unique(np.concatenate([r, [0, n - 1]])).astype(np.int64)
+
+
+def test_fused_mlp_sweep_8b_sampled_parity(orc):
+    """The 8B-class sweep with every layer's gate and up in one interleaved
+    24576 x 4096 matrix ending in SwiGLU: one grouped launch, bf16 output,
+    sampled outputs of all 217 matrices against the oracle."""
+    sw = Sweep(synth.sweep_8b_fused_mlp(), seed0=800, batch=1, y_dtype=b1.BF16).fill()
+    plan = sw.group_plan()
+    plan.run()
+    torch.cuda.synchronize()
+    assert b1.bit1_device_wait_timeouts() == 0
+    for i, m in enumerate(sw.mats):
+        hb, hs, hx = sw.host_matrix(i)
+        units = _sample(m.out, 8, 4000 + i)
+        got = sw.y_of(i)[:, torch.from_numpy(units).cuda()]
+        if not m.swiglu:
+            ref = orc.gemv_select(hb, hs, hx, 1, m.N, m.K, units)
+            assert_gemv_close(got, ref, abs_bound(hs[units], hx, m.K), f"fused sweep {m.name}")
+            continue
+        h = orc.gemv_swiglu_select(hb, hs, hx, 1, m.N, m.K, units)
+        gu = orc.gemv_select(hb, hs, hx, 1, m.N, m.K, np.stack([2 * units, 2 * units + 1], 1).ravel())
+        bd = abs_bound(hs.reshape(m.N, -1)[np.stack([2 * units, 2 * units + 1], 1).ravel()], hx, m.K)
+        assert_swiglu_close(got, h, gu[:, 0::2], gu[:, 1::2], bd[:, 0::2], bd[:, 1::2],
+                            f"fused sweep {m.name}")
