@@ -839,6 +839,27 @@ def run_mine(args):
         c1.synchronize()
     chain_ms = max_over_ranks(c0.elapsed_time(c1), dist, "cuda") / chain_steps
 
+    # secondary: the same weights as a fused dependent chain -- per layer q|k|v
+    # as one matrix, o, gate|up interleaved with the SwiGLU epilogue, and down
+    # reading that h -- 145 launches (graph + PDL)
+    fz = Sweep(synth.decode_chain_8b_fused(), seed0=0, batch=1, y_dtype=b1.BF16,
+               feed_swiglu=True).fill_device(77)
+    fz.capture(pdl=True)
+    with torch.cuda.stream(fz.stream):
+        for _ in range(3):
+            fz.replay()
+        fz.stream.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(fz.stream)
+        for _ in range(chain_steps):
+            fz.replay()
+        c1.record(fz.stream)
+        c1.synchronize()
+    fused_ms = max_over_ranks(c0.elapsed_time(c1), dist, "cuda") / chain_steps
+    fused_launches, fused_bytes = fz.launches_per_step(), fz.weight_bytes
+    del fz
+    torch.cuda.empty_cache()
+
     hbm, src = _peaks()
     traffic = _traffic_for()
     out = {
@@ -866,6 +887,11 @@ def run_mine(args):
                          "ms_per_step": chain_ms, "tok_s_equiv": 1e3 / chain_ms,
                          "launches_per_step": sw.launches_per_step(),
                          "what": "253 dependent launches (graph + PDL, each waits before reading x)"},
+        "decode_chain_fused": {"value": fused_bytes / (fused_ms * 1e-3) / 1e9, "unit": "GB/s",
+                               "ms_per_step": fused_ms, "tok_s_equiv": 1e3 / fused_ms,
+                               "launches_per_step": fused_launches,
+                               "what": "the same weights as 145 dependent launches: per layer q|k|v, o, "
+                                       "gate|up with the SwiGLU epilogue, down reading h (graph + PDL)"},
         "device_wait_timeouts": timeouts,
         "clocks": clk.summary(),
     }

@@ -15,6 +15,7 @@ import threading
 __all__ = [
     "Bit1Error", "OK", "EINVAL", "ESHAPE", "ERANGE", "ECUDA", "ENAN",
     "F32", "BF16", "F16", "AUTO", "SIMPLE", "LUT", "SPLITK", "TC", "LUT6", "STREAM", "FLAG_PDL",
+    "FLAG_SWIGLU", "EPI_NONE", "EPI_SWIGLU",
     "bit1_pack", "bit1_pack_flags_status", "bit1_gemv", "bit1_gemv_ex",
     "bit1_gemv_workspace_bytes", "bit1_gemv_pick", "bit1_gemv_launches",
     "bit1_xor_patch", "bit1_status_str", "bit1_version", "bit1_device_wait_timeouts",
@@ -30,6 +31,7 @@ OK, EINVAL, ESHAPE, ERANGE, ECUDA, ENAN = 0, 1, 2, 3, 4, 5
 F32, BF16, F16 = 0, 1, 2
 AUTO, SIMPLE, LUT, SPLITK, TC, LUT6, STREAM = 0, 1, 2, 3, 4, 5, 6
 FLAG_PDL = 1
+FLAG_SWIGLU = 2
 EPI_NONE, EPI_SWIGLU = 0, 1
 
 class _Problem(ctypes.Structure):
@@ -205,14 +207,16 @@ def bit1_pack_flags_status(flags: int) -> int:
 def bit1_gemv_ex(bits, scales, x, y=None, y_dtype=None, workspace=None, variant=AUTO, flags=0,
                  stream=None, N=None, K=None):
     """y[B, N] = x[B, K] (bf16) times the packed 1-bit matrix (bits [N, K/8],
-    scales [N, K/128] fp16 patterns).  Returns y (fp32 unless y_dtype/BF16)."""
+    scales [N, K/128] fp16 patterns).  Returns y (fp32 unless y_dtype/BF16).
+    With FLAG_SWIGLU in ``flags`` the rows are (gate, up) pairs and y is
+    h = silu(gate) * up, [B, N/2]."""
     import torch
     B = x.shape[0] if x.dim() == 2 else 1
     K = x.shape[-1] if K is None else K
     N = bits.shape[0] if N is None else N
     if y is None:
         yt = torch.bfloat16 if y_dtype == BF16 else torch.float32
-        y = torch.empty((B, N), dtype=yt, device=x.device)
+        y = torch.empty((B, N // 2 if int(flags) & FLAG_SWIGLU else N), dtype=yt, device=x.device)
     ydt = BF16 if y.dtype == torch.bfloat16 else F32
     if y.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("y must be float32 or bfloat16")

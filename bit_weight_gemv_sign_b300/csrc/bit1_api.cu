@@ -100,7 +100,13 @@ bit1_status gemv_check(const uint8_t* bits, const uint16_t* scales, const uint16
     if (!aligned16(bits) || !aligned16(scales) || !aligned16(x) || !aligned16(y)) return BIT1_EINVAL;
     if (y_dtype != BIT1_F32 && y_dtype != BIT1_BF16) return BIT1_EINVAL;
     if (ws_bytes > 0 && (!workspace || !aligned16(workspace))) return BIT1_EINVAL;
-    if (flags & ~BIT1_FLAG_PDL) return BIT1_EINVAL;
+    if (flags & ~(BIT1_FLAG_PDL | BIT1_FLAG_SWIGLU)) return BIT1_EINVAL;
+    if (flags & BIT1_FLAG_SWIGLU) {
+        // Gate/up pairs: the batch-1 kernels whose lane or warp owns whole rows.
+        if (N % 2 != 0) return BIT1_ESHAPE;
+        if (*variant == BIT1_GEMV_AUTO) *variant = lut_supported(B, N, K) ? BIT1_GEMV_LUT : BIT1_GEMV_STREAM;
+        if (*variant != BIT1_GEMV_LUT && *variant != BIT1_GEMV_STREAM) return BIT1_ESHAPE;
+    }
     if (*variant == BIT1_GEMV_AUTO) *variant = pick_variant(B, N, K, ws_bytes);
     switch (*variant) {
         case BIT1_GEMV_SIMPLE: return BIT1_OK;
@@ -125,6 +131,7 @@ bit1_status gemv_run(const uint8_t* bits, const uint16_t* scales, const uint16_t
     a.y = y; a.y_bf16 = (y_dtype == BIT1_BF16);
     a.workspace = workspace; a.ws_bytes = ws_bytes;
     a.pdl = (flags & BIT1_FLAG_PDL) != 0;
+    a.swiglu = (flags & BIT1_FLAG_SWIGLU) != 0;
     a.stream = stream;
     switch (variant) {
         case BIT1_GEMV_SIMPLE: return from_cuda(launch_gemv_simple(a));
@@ -251,6 +258,7 @@ bit1_status bit1_gemv_ternary(const uint8_t* a, const uint8_t* b, const uint16_t
     if (!shape_ok(B, N, K)) return BIT1_ESHAPE;
     if (!a || !b || !aligned16(a) || !aligned16(b)) return BIT1_EINVAL;
     if (!workspace || !aligned16(workspace)) return BIT1_EINVAL;
+    if (flags & BIT1_FLAG_SWIGLU) return BIT1_EINVAL;      // the halves are combined afterwards
     const size_t half = ternary_half_bytes(B, N);
     if (ws_bytes < 2 * half) return BIT1_EINVAL;
     float* ya = reinterpret_cast<float*>(workspace);

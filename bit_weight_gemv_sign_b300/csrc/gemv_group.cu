@@ -641,6 +641,7 @@ cudaError_t launch_gemv_group1(const GemvArgs& a) {
     pb.N = a.N;
     pb.K = a.K;
     pb.y_dtype = a.y_bf16 ? BIT1_BF16 : BIT1_F32;
+    pb.epilogue = a.swiglu ? BIT1_EPI_SWIGLU : BIT1_EPI_NONE;
     if (!problem_ok(pb)) return cudaErrorInvalidValue;
     std::vector<GProb> probs(1);
     if (!encode_prob(probs[0], pb, 1)) return cudaErrorInvalidValue;

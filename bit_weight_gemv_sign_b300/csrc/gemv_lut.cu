@@ -25,6 +25,10 @@
 //    rows' bits and scales, issued before griddepcontrol.wait so that under
 //    programmatic dependent launch the weight stream starts while the previous
 //    kernel finishes.
+//  * SwiGLU epilogue (rows interleaved as gate/up pairs of a SwiGLU MLP, the
+//    base model's MLP on the Bonsai 27B page, section "Bonsai 27B의 표현
+//    방식"): CTAs and warps take whole pairs, a warp runs a pair's gate row
+//    then its up row, keeps the gate sum and writes h = silu(g) * u.
 #include <utility>
 
 #include "common.cuh"
@@ -105,7 +109,44 @@ __device__ __forceinline__ void load_row(const uint8_t* __restrict__ bits,
     }
 }
 
-template <int M>
+// Sum of one row over this lane's words (the caller then reduces the warp):
+// table lookups, then the group scales, issuing `next` (the prefetch of a
+// later row into the same registers) between the two.
+template <int M, typename Next>
+__device__ __forceinline__ float lut_row(uint32_t (&w)[M], uint32_t (&sv)[LutCfg<M>::NS], uint32_t lb, int o,
+                                         Next&& next) {
+    constexpr int NS = LutCfg<M>::NS;
+    float ws[M];
+    lut_words<M>(w, lb, ws, std::make_index_sequence<M>{});
+    float sc[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) sc[i] = f16_bits_to_f32((uint16_t)sv[i]);
+    next();
+    float acc = 0.f;
+    if constexpr (M % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < M / 4; ++q)
+            acc = fmaf((ws[4 * q] + ws[4 * q + 1]) + (ws[4 * q + 2] + ws[4 * q + 3]), sc[q], acc);
+    } else {
+        float part = 0.f;
+        float s0 = sc[0];
+#pragma unroll
+        for (int j = 0; j < M; ++j) {
+            if (j > 0 && ((o + j) & 3) == 0) {
+                acc = fmaf(part, s0, acc);
+                part = 0.f;
+#pragma unroll
+                for (int i = 0; i + 1 < NS; ++i) sc[i] = sc[i + 1];
+                s0 = sc[0];
+            }
+            part += ws[j];
+        }
+        acc = fmaf(part, s0, acc);
+    }
+    return warp_sum(acc);
+}
+
+template <int M, bool SWIGLU>
 __global__ void __launch_bounds__(kLutThreads, 1)
 k_gemv_lut(const uint8_t* __restrict__ bits, const uint16_t* __restrict__ scales,
            const uint16_t* __restrict__ x, int64_t N, void* __restrict__ y, int y_bf16) {
@@ -118,14 +159,24 @@ k_gemv_lut(const uint8_t* __restrict__ bits, const uint16_t* __restrict__ scales
     float* tab = reinterpret_cast<float*>(smem_raw + (tbase - sraw));
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const int64_t n0 = N * blockIdx.x / gridDim.x, n1 = N * (blockIdx.x + 1) / gridDim.x;
+    // Units: rows, or (gate, up) row pairs with the SwiGLU epilogue.  The
+    // CTA takes units [n0, n1); this warp units n0 + warp + j * nw.  With
+    // pairs its t-th row is row t & 1 of its unit t >> 1.
+    const int64_t U = SWIGLU ? N / 2 : N;
+    const int64_t n0 = U * blockIdx.x / gridDim.x, n1 = U * (blockIdx.x + 1) / gridDim.x;
+    const int64_t mine = n1 - n0 > warp ? (n1 - n0 - warp + nw - 1) / nw : 0;
+    auto pair_row = [&](int64_t t) -> int64_t { return 2 * (n0 + warp + (t >> 1) * nw) + (t & 1); };
 
     uint32_t wb[D][M];
     uint32_t sb[D][NS];
 #pragma unroll
     for (int d = 0; d < D; ++d) {
-        const int64_t row = n0 + warp + (int64_t)d * nw;
-        if (row < n1) load_row<M>(bits, scales, row, lane, wb[d], sb[d]);
+        if constexpr (SWIGLU) {
+            if (d < 2 * mine) load_row<M>(bits, scales, pair_row(d), lane, wb[d], sb[d]);
+        } else {
+            const int64_t row = n0 + warp + (int64_t)d * nw;
+            if (row < n1) load_row<M>(bits, scales, row, lane, wb[d], sb[d]);
+        }
     }
 
     // x is produced by the preceding kernel in a decode step: wait for it here,
@@ -149,40 +200,43 @@ k_gemv_lut(const uint8_t* __restrict__ bits, const uint16_t* __restrict__ scales
 
     const uint32_t lb = tbase + 4u * (uint32_t)lane;
     const int o = (M % 4 == 0) ? 0 : ((lane * M) & 3);  // offset of the lane's first word in its group
+    if constexpr (SWIGLU) {
+        // Gate row then up row of each pair; h = silu(g) * u from the kept gate sum.
+        const int64_t R = 2 * mine;
+        float gate = 0.f;
+        for (int64_t base = 0; base < R; base += D) {
+#pragma unroll
+            for (int d = 0; d < D; ++d) {
+                const int64_t t = base + d;
+                if (t >= R) break;
+                const float acc = lut_row<M>(wb[d], sb[d], lb, o, [&] {
+                    if (t + D < R) load_row<M>(bits, scales, pair_row(t + D), lane, wb[d], sb[d]);
+                });
+                if (!(t & 1)) {
+                    gate = acc;
+                    continue;
+                }
+                const float h = gate / (1.f + expf(-gate)) * acc;
+                const int64_t u = pair_row(t) >> 1;
+                if (lane == 0) {
+                    if (y_bf16)
+                        reinterpret_cast<uint16_t*>(y)[u] = f32_to_bf16_bits(h);
+                    else
+                        reinterpret_cast<float*>(y)[u] = h;
+                }
+            }
+        }
+        return;
+    }
     for (int64_t base = n0 + warp; base < n1; base += (int64_t)D * nw) {
 #pragma unroll
         for (int d = 0; d < D; ++d) {
             const int64_t row = base + (int64_t)d * nw;
             if (row >= n1) break;
-            float ws[M];
-            lut_words<M>(wb[d], lb, ws, std::make_index_sequence<M>{});
-            float sc[NS];
-#pragma unroll
-            for (int i = 0; i < NS; ++i) sc[i] = f16_bits_to_f32((uint16_t)sb[d][i]);
-            const int64_t nrow = row + (int64_t)D * nw;
-            if (nrow < n1) load_row<M>(bits, scales, nrow, lane, wb[d], sb[d]);
-            float acc = 0.f;
-            if constexpr (M % 4 == 0) {
-#pragma unroll
-                for (int q = 0; q < M / 4; ++q)
-                    acc = fmaf((ws[4 * q] + ws[4 * q + 1]) + (ws[4 * q + 2] + ws[4 * q + 3]), sc[q], acc);
-            } else {
-                float part = 0.f;
-                float s0 = sc[0];
-#pragma unroll
-                for (int j = 0; j < M; ++j) {
-                    if (j > 0 && ((o + j) & 3) == 0) {
-                        acc = fmaf(part, s0, acc);
-                        part = 0.f;
-#pragma unroll
-                        for (int i = 0; i + 1 < NS; ++i) sc[i] = sc[i + 1];
-                        s0 = sc[0];
-                    }
-                    part += ws[j];
-                }
-                acc = fmaf(part, s0, acc);
-            }
-            acc = warp_sum(acc);
+            const float acc = lut_row<M>(wb[d], sb[d], lb, o, [&] {
+                const int64_t nrow = row + (int64_t)D * nw;
+                if (nrow < n1) load_row<M>(bits, scales, nrow, lane, wb[d], sb[d]);
+            });
             if (lane == 0) {
                 if (y_bf16)
                     reinterpret_cast<uint16_t*>(y)[row] = f32_to_bf16_bits(acc);
@@ -193,18 +247,19 @@ k_gemv_lut(const uint8_t* __restrict__ bits, const uint16_t* __restrict__ scales
     }
 }
 
-template <int M>
-static cudaError_t launch_lut_m(const GemvArgs& a) {
+template <int M, bool SWIGLU>
+static cudaError_t launch_lut_ms(const GemvArgs& a) {
     static bool configured = false;  // per-instantiation attribute (idempotent, benign race)
     const size_t smem = LutCfg<M>::smem;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute((const void*)k_gemv_lut<M>,
+        cudaError_t e = cudaFuncSetAttribute((const void*)k_gemv_lut<M, SWIGLU>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
     const int sms = sm_count();
-    const int64_t grid = a.N < sms ? a.N : sms;
+    const int64_t units = a.swiglu ? a.N / 2 : a.N;
+    const int64_t grid = units < sms ? units : sms;
     const uint8_t* bits = a.bits;
     const uint16_t* scales = a.scales;
     const uint16_t* x = a.x;
@@ -212,8 +267,13 @@ static cudaError_t launch_lut_m(const GemvArgs& a) {
     void* y = a.y;
     int yb = a.y_bf16;
     void* args[] = {&bits, &scales, &x, &N, &y, &yb};
-    return launch((const void*)k_gemv_lut<M>, dim3((unsigned)grid), dim3(kLutThreads), smem,
+    return launch((const void*)k_gemv_lut<M, SWIGLU>, dim3((unsigned)grid), dim3(kLutThreads), smem,
                   a.stream, a.pdl, args);
+}
+
+template <int M>
+static cudaError_t launch_lut_m(const GemvArgs& a) {
+    return a.swiglu ? launch_lut_ms<M, true>(a) : launch_lut_ms<M, false>(a);
 }
 
 bool lut_supported(int64_t B, int64_t N, int64_t K) {

@@ -20,6 +20,7 @@ struct GemvArgs {
     size_t ws_bytes;
     bool pdl;            // launch with programmatic stream serialization
     cudaStream_t stream;
+    bool swiglu = false; // rows are (gate, up) pairs; y is h = silu(gate) * up, [B][N/2]
 };
 
 // Launch helper: grid/block/smem with optional PDL attribute.

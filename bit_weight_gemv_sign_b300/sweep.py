@@ -18,7 +18,7 @@ import numpy as np
 import torch
 
 from . import synth
-from . import (BF16, F32, FLAG_PDL, AUTO, EPI_NONE, EPI_SWIGLU, GroupPlan, bit1_gemv_ex,
+from . import (BF16, F32, FLAG_PDL, FLAG_SWIGLU, AUTO, EPI_NONE, EPI_SWIGLU, GroupPlan, bit1_gemv_ex,
                bit1_gemv_launches, bit1_ternary_combine, bit1_xor_patch)
 
 
@@ -27,9 +27,22 @@ def _align(n: int, a: int = 256) -> int:
 
 
 class Sweep:
+    """``feed_swiglu``: the matrix after each SwiGLU matrix reads that
+    matrix's output h as its x (gate/up -> down), instead of an x of its own;
+    for the dependent per-matrix chain (run_eager / capture)."""
+
     def __init__(self, mats, seed0: int = 0, batch: int = 1, y_dtype: int = BF16,
-                 device: str = "cuda", variant: int = AUTO):
+                 device: str = "cuda", variant: int = AUTO, feed_swiglu: bool = False):
         self.mats = list(mats)
+        self.fed = {}
+        if feed_swiglu:
+            if y_dtype != BF16:
+                raise ValueError("h feeds the next product as bf16 activations")
+            for i, m in enumerate(self.mats[:-1]):
+                if m.swiglu:
+                    if self.mats[i + 1].K != m.out:
+                        raise ValueError(f"{self.mats[i + 1].name} does not take {m.name}'s h")
+                    self.fed[i + 1] = i
         self.seed0 = seed0
         self.B = batch
         self.y_dtype = y_dtype
@@ -63,6 +76,8 @@ class Sweep:
         return self.scales[o: o + m.N * (m.K // 128)].view(m.N, m.K // 128)
 
     def x_of(self, i, xbuf=None):
+        if i in self.fed and xbuf is None:
+            return self.y_of(self.fed[i])
         m = self.mats[i]
         o = self.x_off[i] // 2
         xb = self.x if xbuf is None else xbuf
@@ -89,7 +104,8 @@ class Sweep:
             bits, scales, x = self.host_matrix(i)
             self.bits_of(i).copy_(torch.from_numpy(bits), non_blocking=False)
             self.scales_of(i).copy_(torch.from_numpy(scales.view(np.int16)))
-            self.x_of(i).copy_(torch.from_numpy(x.view(np.int16)).view(torch.bfloat16))
+            if i not in self.fed:
+                self.x_of(i).copy_(torch.from_numpy(x.view(np.int16)).view(torch.bfloat16))
         torch.cuda.synchronize()
         return self
 
@@ -104,7 +120,9 @@ class Sweep:
                                                 device=self.device, generator=g))
             sc = torch.randn((m.N, m.K // 128), device=self.device, generator=g).abs_().mul_(0.02)
             self.scales_of(i).copy_(sc.half().view(torch.int16))
-            self.x_of(i).copy_(torch.randn((self.B, m.K), device=self.device, generator=g).bfloat16())
+            xr = torch.randn((self.B, m.K), device=self.device, generator=g).bfloat16()
+            if i not in self.fed:
+                self.x_of(i).copy_(xr)
         torch.cuda.synchronize()
         return self
 
@@ -113,12 +131,10 @@ class Sweep:
         return sum(bit1_gemv_launches(self.B, m.N, m.K, self.variant) for m in self.mats)
 
     def run_eager(self, stream=None, pdl: bool = True):
-        if any(m.swiglu for m in self.mats):
-            raise ValueError("the SwiGLU epilogue runs in the grouped launch only (group_plan)")
         for i, m in enumerate(self.mats):
+            flags = (FLAG_PDL if pdl else 0) | (FLAG_SWIGLU if m.swiglu else 0)
             bit1_gemv_ex(self.bits_of(i), self.scales_of(i), self.x_of(i), y=self.y_of(i),
-                         variant=self.variant, flags=FLAG_PDL if pdl else 0, stream=stream,
-                         N=m.N, K=m.K)
+                         variant=self.variant, flags=flags, stream=stream, N=m.N, K=m.K)
 
     def capture(self, pdl: bool = True):
         self.stream = torch.cuda.Stream()
@@ -141,6 +157,8 @@ class Sweep:
         kernel launch.  ``x`` and
         ``y`` replace the activation / output arenas (same layout), e.g. for a
         second I/O slot over the same resident weights."""
+        if self.fed:
+            raise ValueError("a grouped launch runs its problems concurrently: no x may be another's y")
         probs = [(self.bits_of(i), self.scales_of(i), self.x_of(i, x), self.y_of(i, y),
                   EPI_SWIGLU if m.swiglu else EPI_NONE) for i, m in enumerate(self.mats)]
         return GroupPlan(probs, device=self.device, B=self.B)

@@ -145,6 +145,19 @@ def sweep_8b_fused_mlp() -> list:
     return out
 
 
+def decode_chain_8b_fused() -> list:
+    """The 8B-class decode step as a chain of fused matrices: per layer q|k|v
+    as one 6144 x 4096 matrix (they share x), o, gate|up interleaved 24576 x
+    4096 ending in SwiGLU, and down, whose input is that h; then the LM head
+    (145 matrices, the same weights and bytes as ``sweep_8b``)."""
+    out = []
+    for layer in range(36):
+        out += [Mat(f"L{layer}.qkv", 6144, 4096), Mat(f"L{layer}.o", 4096, 4096),
+                Mat(f"L{layer}.gate_up", 24576, 4096, swiglu=True), Mat(f"L{layer}.down", 4096, 12288)]
+    out.append(Mat("lm_head", 151936, 4096))
+    return out
+
+
 PROJ_NAMES_27B = ["q", "k", "v", "o", "gate", "up", "down"]
 
 

@@ -88,6 +88,15 @@ enum bit1_gemv_variant {
 #define BIT1_FLAG_PDL 1u   /* launch with programmatic dependent launch: the
                               kernel prefetches its weights before waiting for
                               the preceding kernel in the stream */
+#define BIT1_FLAG_SWIGLU 2u /* the matrix is a SwiGLU MLP's gate and up
+                              projections with interleaved rows (row 2n gate,
+                              row 2n+1 up of hidden unit n; N even, else
+                              BIT1_ESHAPE) and y receives h = silu(g) * u,
+                              [B][N/2], as BIT1_EPI_SWIGLU below.  Batch 1 on
+                              BIT1_GEMV_LUT or BIT1_GEMV_STREAM (AUTO picks
+                              LUT for K <= 13312, else STREAM); any other
+                              variant or B > 1: BIT1_ESHAPE.  Not accepted by
+                              bit1_gemv_ternary (BIT1_EINVAL). */
 
 /* ------------------------------------------------------------------------
  * bit1_pack -- floating-point weights -> packed sign bits + fp16 scales.

@@ -67,3 +67,19 @@ def assert_swiglu_close(h_gpu: torch.Tensor, h_ref: np.ndarray, g_ref: np.ndarra
         raise AssertionError(f"{what}: {bad.sum()} outputs out of tolerance; first at {tuple(i)}: "
                              f"gpu {hg[tuple(i)]!r} oracle {h_ref[tuple(i)]!r} tol {tol[tuple(i)]!r}")
     return float((err / tol).max()) if err.size else 0.0
+
+
+def swiglu_h_tol(g_ref, u_ref, bound_g, bound_u, h_ref):
+    """Elementwise bound on |h_gpu(bf16) - bf16(h_oracle)|: the SwiGLU
+    tolerance of assert_swiglu_close plus both bf16 roundings."""
+    dg = 1e-3 * bound_g + 1e-6
+    du = 1e-3 * bound_u + 1e-6
+    return 1.1 * dg * (np.abs(u_ref) + du) + np.abs(g_ref) * du + 2 * 2.0 ** -8 * np.abs(h_ref) + 1e-30
+
+
+def carried_bound(scales: np.ndarray, dx: np.ndarray, K: int) -> np.ndarray:
+    """sum_k |s_{n,g(k)}| * dx_{b,k} as [B, N]: how far an input error dx can
+    move each output of the product."""
+    G = K // 128
+    s = np.abs(scales.reshape(-1, G).view(np.float16).astype(np.float64))
+    return dx.reshape(-1, G, 128).sum(axis=2) @ s.T

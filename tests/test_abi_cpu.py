@@ -185,3 +185,50 @@ def test_t5_rejects_on_host(lib):
 def test_selftest_rejects_bad_pointer_on_host(lib):
     assert lib.bit1_selftest_wait_timeout(None, None) == b1.EINVAL
     assert lib.bit1_selftest_wait_timeout(FAKE + 2, None) == b1.EINVAL
+
+
+def test_swiglu_flag_checked_on_host(lib):
+    f = lib.bit1_gemv_ex
+    S = b1.FLAG_SWIGLU
+    assert f(FAKE, FAKE, FAKE, 1, 7, 1024, FAKE, b1.F32, None, 0, 0, S, None) == b1.ESHAPE     # odd rows
+    for v in (b1.SIMPLE, b1.LUT6, b1.SPLITK, b1.TC):
+        assert f(FAKE, FAKE, FAKE, 1, 8, 1024, FAKE, b1.F32, None, 0, v, S, None) == b1.ESHAPE
+    for v in (b1.AUTO, b1.LUT, b1.STREAM):                                                      # batch 1 only
+        assert f(FAKE, FAKE, FAKE, 2, 8, 1024, FAKE, b1.F32, None, 0, v, S, None) == b1.ESHAPE
+    assert f(FAKE, FAKE, FAKE, 1, 8, 1152, FAKE, b1.F32, None, 0, b1.LUT, S, None) == b1.ESHAPE
+    assert f(FAKE, FAKE, FAKE, 1, 8, 1024, FAKE, b1.F32, None, 0, 0, S | 4, None) == b1.EINVAL
+    g = lib.bit1_gemv_ternary
+    assert g(FAKE, FAKE, FAKE, FAKE, 1, 8, 128, FAKE, b1.F32, FAKE, 512, 0, S, None) == b1.EINVAL
+
+
+def test_group_plan_epilogue_checked_on_host(lib):
+    import numpy as np
+    n = lib.bit1_group_plan_bytes(1)
+    raw = np.zeros(n + 128, dtype=np.uint8)
+    off = (-raw.ctypes.data) % 128
+    plan = raw[off:off + n]
+    for N, epi in ((63, b1.EPI_SWIGLU), (64, 2), (64, -1)):
+        p = b1._Problem(FAKE, FAKE, FAKE, FAKE, N, 1024, b1.F32, epi)
+        assert lib.bit1_group_plan(ctypes.byref(p), 1, plan.ctypes.data, n) == b1.ESHAPE, (N, epi)
+
+
+def test_sweep_feeds_swiglu_output_to_the_next_matrix():
+    """Host wiring of the fused chain: the matrix after a SwiGLU matrix reads
+    its h; a grouped plan over such a sweep is refused (its problems run
+    concurrently); a mismatched width is refused."""
+    from bit_weight_gemv_sign_b300 import synth
+    from bit_weight_gemv_sign_b300.sweep import Sweep
+    mats = [synth.Mat("gate_up", 256, 1024, swiglu=True), synth.Mat("down", 64, 128), synth.Mat("o", 64, 1024)]
+    sw = Sweep(mats, device="cpu", feed_swiglu=True)
+    assert sw.fed == {1: 0}
+    assert sw.x_of(1).data_ptr() == sw.y_of(0).data_ptr() and sw.x_of(1).shape == (1, 128)
+    assert sw.y_of(0).shape == (1, 128) and sw.x_of(2).data_ptr() != sw.y_of(1).data_ptr()
+    with pytest.raises(ValueError):
+        sw.group_plan()
+    with pytest.raises(ValueError):
+        Sweep([synth.Mat("gate_up", 256, 1024, swiglu=True), synth.Mat("down", 64, 256)], device="cpu",
+              feed_swiglu=True)
+    with pytest.raises(ValueError):
+        Sweep(mats, device="cpu", feed_swiglu=True, y_dtype=b1.F32)
+    assert sum(m.N * m.K for m in synth.decode_chain_8b_fused()) == sum(m.N * m.K for m in synth.sweep_8b())
+    assert sum(m.N * m.K for m in synth.sweep_8b_fused_mlp()) == sum(m.N * m.K for m in synth.sweep_8b())

@@ -12,7 +12,8 @@ import torch
 import bit_weight_gemv_sign_b300 as b1
 from bit_weight_gemv_sign_b300 import synth
 from bit_weight_gemv_sign_b300.sweep import Sweep
-from tests.helpers import abs_bound, assert_gemv_close, assert_swiglu_close, dev_bf16, dev_u8, dev_u16
+from tests.helpers import (abs_bound, assert_gemv_close, assert_swiglu_close, carried_bound, dev_bf16, dev_u8,
+                           dev_u16, swiglu_h_tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -131,3 +132,124 @@ def test_fused_mlp_sweep_8b_sampled_parity(orc):
         bd = abs_bound(hs.reshape(m.N, -1)[np.stack([2 * units, 2 * units + 1], 1).ravel()], hx, m.K)
         assert_swiglu_close(got, h, gu[:, 0::2], gu[:, 1::2], bd[:, 0::2], bd[:, 1::2],
                             f"fused sweep {m.name}")
+
+
+# ---------------------------------------------------------------- single call (bit1_gemv_ex)
+
+# (N, K): interleaved row counts; ragged pair counts against the CTA split,
+# one K word per lane up to the largest table kernel K, and beyond it
+EX_SHAPES = [(2, 1024), (514, 2048), (2000, 4096), (24576, 4096), (8190, 5120), (4096, 12288),
+             (300, 13312), (600, 16384)]
+
+
+@pytest.mark.parametrize("N,K", EX_SHAPES)
+@pytest.mark.parametrize("variant", [b1.AUTO, b1.LUT, b1.STREAM])
+def test_gemv_ex_swiglu_matches_oracle(orc, N, K, variant):
+    if variant == b1.LUT and K > 13312:
+        pytest.skip("the nibble-table kernel holds K <= 13312")
+    bits, scales = synth.matrix(N, K, 9700 + N % 97 + K // 1024)
+    x = synth.x_for(1, K, 9700 + K // 1024)
+    db, ds, dx = dev_u8(bits), dev_u16(scales), dev_bf16(x).view(1, K)
+    for ydt in (b1.F32, b1.BF16):
+        h = b1.bit1_gemv_ex(db, ds, dx, y_dtype=ydt, variant=variant, flags=b1.FLAG_SWIGLU)
+        torch.cuda.synchronize()
+        assert h.shape == (1, N // 2)
+        yo = orc.gemv(bits, scales, x, 1, N, K)
+        ho = orc.gemv_swiglu(bits, scales, x, 1, N, K)
+        bd = abs_bound(scales, x, K)
+        assert_swiglu_close(h, ho, yo[:, 0::2], yo[:, 1::2], bd[:, 0::2], bd[:, 1::2],
+                            f"gemv_ex SwiGLU N={N} K={K} variant={variant} y={ydt}")
+
+
+def test_gemv_ex_swiglu_equals_grouped_epilogue():
+    """The single call on the grouped kernel (STREAM) and a one-problem grouped
+    plan run the same code: bit-identical h."""
+    N, K = 2050, 5120
+    bits, scales = synth.matrix(N, K, 9800)
+    x = synth.x_for(1, K, 9800)
+    db, ds, dx = dev_u8(bits), dev_u16(scales), dev_bf16(x).view(1, K)
+    h1 = b1.bit1_gemv_ex(db, ds, dx, variant=b1.STREAM, flags=b1.FLAG_SWIGLU)
+    h2 = torch.empty((1, N // 2), device="cuda")
+    b1.GroupPlan([(db, ds, dx.view(K), h2, b1.EPI_SWIGLU)]).run()
+    torch.cuda.synchronize()
+    assert torch.equal(h1, h2)
+
+
+def test_gemv_ex_swiglu_feeds_the_down_projection(orc):
+    """gate/up -> h (bf16) -> down with no kernel in between, under PDL.  The
+    oracle runs the same chain on its own h (rounded to bf16 by torch); the
+    down tolerance adds what the GPU's h may differ from it by (the SwiGLU
+    tolerance plus both bf16 roundings), carried through |W_down|."""
+    H, D = 2048, 1024          # hidden units, model width
+    gb, gs = synth.matrix(2 * H, D, 9900)
+    x = synth.x_for(1, D, 9900)
+    db2, ds2 = synth.matrix(D, H, 9901)
+    h = b1.bit1_gemv_ex(dev_u8(gb), dev_u16(gs), dev_bf16(x).view(1, D), y_dtype=b1.BF16,
+                        flags=b1.FLAG_SWIGLU | b1.FLAG_PDL)
+    y = b1.bit1_gemv_ex(dev_u8(db2), dev_u16(ds2), h, flags=b1.FLAG_PDL)
+    torch.cuda.synchronize()
+    ho = orc.gemv_swiglu(gb, gs, x, 1, 2 * H, D)
+    yo = orc.gemv(gb, gs, x, 1, 2 * H, D)
+    bd = abs_bound(gs, x, D)
+    assert_swiglu_close(h, ho, yo[:, 0::2], yo[:, 1::2], bd[:, 0::2], bd[:, 1::2], "gate/up")
+    hx = synth.to_bf16_bits(ho.astype(np.float32))                 # the oracle's h as bf16
+    ref = orc.gemv(db2, ds2, hx, 1, D, H)
+    dh = swiglu_h_tol(yo[:, 0::2], yo[:, 1::2], bd[:, 0::2], bd[:, 1::2], ho)
+    got = y.float().cpu().numpy().astype(np.float64)
+    tol = 1e-3 * abs_bound(ds2, hx, H) + 1e-6 + carried_bound(ds2, dh, H)
+    assert np.all(np.abs(got - ref) <= tol)
+
+
+def test_fused_decode_chain_layer(orc):
+    """One layer of the fused 8B-class decode chain through the sweep's
+    dependent launches (graph + PDL): q|k|v and o against the oracle, the
+    gate|up h against the oracle's SwiGLU, and down -- which reads the GPU's
+    h -- against the oracle's down of its own h, with the h tolerance carried
+    through |W_down|."""
+    from bit_weight_gemv_sign_b300.synth import decode_chain_8b_fused
+    mats = decode_chain_8b_fused()[:4]
+    sw = Sweep(mats, seed0=1200, batch=1, y_dtype=b1.BF16, feed_swiglu=True).fill()
+    sw.capture(pdl=True)
+    with torch.cuda.stream(sw.stream):
+        sw.replay()
+    sw.stream.synchronize()
+    host = [sw.host_matrix(i) for i in range(4)]
+    for i in (0, 1):
+        m, (hb, hs, hx) = mats[i], host[i]
+        assert_gemv_close(sw.y_of(i), orc.gemv(hb, hs, hx, 1, m.N, m.K), abs_bound(hs, hx, m.K), m.name)
+    m, (gb, gs, gx) = mats[2], host[2]
+    yo = orc.gemv(gb, gs, gx, 1, m.N, m.K)
+    ho = orc.gemv_swiglu(gb, gs, gx, 1, m.N, m.K)
+    bd = abs_bound(gs, gx, m.K)
+    assert_swiglu_close(sw.y_of(2), ho, yo[:, 0::2], yo[:, 1::2], bd[:, 0::2], bd[:, 1::2], m.name)
+    m, (db_, ds_, _) = mats[3], host[3]
+    hx = synth.to_bf16_bits(ho.astype(np.float32))
+    ref = orc.gemv(db_, ds_, hx, 1, m.N, m.K)
+    dh = swiglu_h_tol(yo[:, 0::2], yo[:, 1::2], bd[:, 0::2], bd[:, 1::2], ho)
+    tol = 1e-3 * abs_bound(ds_, hx, m.K) + 1e-6 + carried_bound(ds_, dh, m.K) + 2.0 ** -8 * np.abs(ref)
+    got = sw.y_of(3).float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= tol), m.name
+    with pytest.raises(ValueError):
+        sw.group_plan()
+
+
+def test_gemv_ex_swiglu_rejections():
+    N, K = 64, 1024
+    bits, scales = synth.matrix(N, K, 9950)
+    x = synth.x_for(4, K, 9950)
+    db, ds = dev_u8(bits), dev_u16(scales)
+    dx1 = dev_bf16(x[:1]).view(1, K)
+    dx4 = dev_bf16(x).view(4, K)
+    cases = [
+        (dict(x=dx1, N=63, y=torch.empty((1, 31), device="cuda")), b1.ESHAPE),        # odd rows
+        (dict(x=dx1, variant=b1.SIMPLE), b1.ESHAPE),
+        (dict(x=dx1, variant=b1.LUT6), b1.ESHAPE),
+        (dict(x=dx4), b1.ESHAPE),                                                       # B > 1
+    ]
+    for kw, st in cases:
+        with pytest.raises(b1.Bit1Error) as e:
+            b1.bit1_gemv_ex(db, ds, flags=b1.FLAG_SWIGLU, **kw)
+        assert e.value.status == st, kw
+    with pytest.raises(b1.Bit1Error) as e:
+        b1.bit1_gemv_ex(db, ds, dx1, flags=8)
+    assert e.value.status == b1.EINVAL
