@@ -377,9 +377,10 @@ def _weight_bytes(N, K):
     return N * K // 8 + 2 * N * (K // 128)
 
 
-def _time_calls(torch, b1, N, K, B, variant, reps=30, ws_bytes=None):
+def _time_calls(torch, b1, N, K, B, variant, reps=30, ws_bytes=None, flags=0):
     """Microseconds per bit1_gemv_ex call (graph replay, L2 rotated), or None
-    when the variant does not take the shape."""
+    when the variant does not take the shape.  ``flags`` adds to FLAG_PDL
+    (FLAG_SWIGLU: y is [B, N/2])."""
     if b1.bit1_gemv_launches(B, N, K, variant) == 0:
         return None
     wb = _weight_bytes(N, K)
@@ -389,7 +390,7 @@ def _time_calls(torch, b1, N, K, B, variant, reps=30, ws_bytes=None):
     bits = torch.randint(0, 256, (copies, N, K // 8), dtype=torch.uint8, device="cuda", generator=g)
     sc = (torch.randn((copies, N, K // 128), device="cuda", generator=g).abs_() * 0.02).half().view(torch.int16)
     x = torch.randn((B, K), device="cuda", generator=g).bfloat16()
-    y = torch.empty((B, N), device="cuda")
+    y = torch.empty((B, N // 2 if flags & b1.FLAG_SWIGLU else N), device="cuda")
     if ws_bytes is None:
         ws_bytes = b1.bit1_gemv_workspace_bytes(max(B, 16), N, K) if variant == b1.TC else 0
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
@@ -397,13 +398,13 @@ def _time_calls(torch, b1, N, K, B, variant, reps=30, ws_bytes=None):
     with torch.cuda.stream(s):
         for i in range(3):
             b1.bit1_gemv_ex(bits[i % copies], sc[i % copies], x, y=y, workspace=ws, variant=variant,
-                            flags=b1.FLAG_PDL, stream=s)
+                            flags=b1.FLAG_PDL | flags, stream=s)
         s.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=s):
             for i in range(reps):
                 b1.bit1_gemv_ex(bits[i % copies], sc[i % copies], x, y=y, workspace=ws, variant=variant,
-                                flags=b1.FLAG_PDL, stream=s)
+                                flags=b1.FLAG_PDL | flags, stream=s)
         graph.replay()
         s.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -479,8 +480,14 @@ def extra_pp512(torch, b1):
     N, K, B = 12288, 4096, 512
     us = _time_calls(torch, b1, N, K, B, b1.TC, reps=10, ws_bytes=b1.bit1_gemv_workspace_bytes(B, N, K))
     e = _shape_entry(N, K, B, us)
-    hbm, _ = _peaks()
-    return {"shape": [N, K], "batch": B, **e}
+    # gate and up as one interleaved 24576-row matrix, with and without the
+    # SwiGLU epilogue
+    N2 = 2 * N
+    ws2 = b1.bit1_gemv_workspace_bytes(B, N2, K)
+    us_p = _time_calls(torch, b1, N2, K, B, b1.TC, reps=10, ws_bytes=ws2)
+    us_s = _time_calls(torch, b1, N2, K, B, b1.TC, reps=10, ws_bytes=ws2, flags=b1.FLAG_SWIGLU)
+    return {"shape": [N, K], "batch": B, **e,
+            "gate_up_24576x4096": {"plain": _shape_entry(N2, K, B, us_p), "swiglu": _shape_entry(N2, K, B, us_s)}}
 
 
 def extra_c5_sweep_27b(torch, b1, steps=20):

@@ -245,7 +245,7 @@ def bit1_gemv_tc_noalloc(bits, scales, x, y=None, y_dtype=None, flags=0, stream=
     N = bits.shape[0] if N is None else N
     if y is None:
         yt = torch.bfloat16 if y_dtype == BF16 else torch.float32
-        y = torch.empty((B, N), dtype=yt, device=x.device)
+        y = torch.empty((B, N // 2 if int(flags) & FLAG_SWIGLU else N), dtype=yt, device=x.device)
     if y.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("y must be float32 or bfloat16")
     ydt = BF16 if y.dtype == torch.bfloat16 else F32

@@ -75,6 +75,7 @@ struct TcParams {
     void* y;                  // [B][N]
     int N, K, B, Bp, Ks, chunks, y_bf16;   // B: valid batch rows of all batch chunks of the launch
     int stages;               // A/B stages: 3 when the accumulators fit 128 columns (Bp <= 32), else 2
+    int swiglu;               // rows are (gate, up) pairs; y is h = silu(gate) * up, [B][N/2]
     // Wide mode (Bp > 64): one accumulator per 128-row half (columns h*Bp), two
     // MMA issuers each issuing all eight 16-input slices of a step; Ks = 1.
 };
@@ -110,6 +111,13 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t local_addr, uint32_t rank)
 __device__ __forceinline__ void store_y(const TcParams& p, int b, int row, float v) {
     if (p.y_bf16) reinterpret_cast<uint16_t*>(p.y)[(int64_t)b * p.N + row] = f32_to_bf16_bits(v);
     else reinterpret_cast<float*>(p.y)[(int64_t)b * p.N + row] = v;
+}
+// SwiGLU output of hidden unit `unit` (rows 2 unit, 2 unit + 1): h = silu(g) * u.
+__device__ __forceinline__ void store_h(const TcParams& p, int b, int unit, float g, float u) {
+    const float h = g / (1.f + expf(-g)) * u;
+    const int64_t o = (int64_t)b * (p.N >> 1) + unit;
+    if (p.y_bf16) reinterpret_cast<uint16_t*>(p.y)[o] = f32_to_bf16_bits(h);
+    else reinterpret_cast<float*>(p.y)[o] = h;
 }
 __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, uint32_t bar) {
     asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
@@ -356,6 +364,15 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
                         asm volatile("st.shared.u32 [%0], %1;" ::"r"(wring + 4u * (uint32_t)((cb + k) * kTcRows + r)), "r"(d[k]) : "memory");
+                } else if (p.swiglu) {
+                    // lane 2m holds the gate row, lane 2m+1 the up row of unit row/2
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const bool bv = cb + k < bvalid;
+                        const float v = bv ? __uint_as_float(d[k]) * p.xscale[cb0 + cb + k] : 0.f;
+                        const float u = __shfl_down_sync(0xffffffffu, v, 1);
+                        if (live && bv && !(lane & 1)) store_h(p, cb0 + cb + k, row >> 1, v, u);
+                    }
                 } else if (live) {
 #pragma unroll
                     for (int k = 0; k < 16; ++k)
@@ -452,10 +469,15 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
                 }
                 const float xs = p.xscale[cb0 + b];
                 const int row = mt * kTcRows + r0;
-                if (row + 0 < p.N) store_y(p, cb0 + b, row + 0, acc.x * xs);
-                if (row + 1 < p.N) store_y(p, cb0 + b, row + 1, acc.y * xs);
-                if (row + 2 < p.N) store_y(p, cb0 + b, row + 2, acc.z * xs);
-                if (row + 3 < p.N) store_y(p, cb0 + b, row + 3, acc.w * xs);
+                if (p.swiglu) {          // rows r0, r0 + 1 and r0 + 2, r0 + 3 are two (gate, up) pairs
+                    if (row + 0 < p.N) store_h(p, cb0 + b, (row >> 1) + 0, acc.x * xs, acc.y * xs);
+                    if (row + 2 < p.N) store_h(p, cb0 + b, (row >> 1) + 1, acc.z * xs, acc.w * xs);
+                } else {
+                    if (row + 0 < p.N) store_y(p, cb0 + b, row + 0, acc.x * xs);
+                    if (row + 1 < p.N) store_y(p, cb0 + b, row + 1, acc.y * xs);
+                    if (row + 2 < p.N) store_y(p, cb0 + b, row + 2, acc.z * xs);
+                    if (row + 3 < p.N) store_y(p, cb0 + b, row + 3, acc.w * xs);
+                }
             }
         }
         cluster_sync();
@@ -693,7 +715,7 @@ cudaError_t launch_gemv_tc(const GemvArgs& a) {
         TcParams prm;
         prm.scales = a.scales;
         prm.xscale = xscale;
-        prm.y = static_cast<uint8_t*>(a.y) + b0 * a.N * ysz;
+        prm.y = static_cast<uint8_t*>(a.y) + b0 * (a.swiglu ? a.N / 2 : a.N) * ysz;
         prm.N = (int)a.N;
         prm.K = (int)a.K;
         prm.B = Bci;
@@ -702,6 +724,7 @@ cudaError_t launch_gemv_tc(const GemvArgs& a) {
         prm.chunks = pl.chunks;
         prm.y_bf16 = a.y_bf16;
         prm.stages = 4 * Bp <= 128 ? 3 : 2;
+        prm.swiglu = a.swiglu ? 1 : 0;
         e = launch_tc_main(tm_bits, tm_x, prm, pl.Mt, nbc_launch, pl.smem, a.stream);
         if (e != cudaSuccess) return e;
     }

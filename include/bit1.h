@@ -94,9 +94,11 @@ enum bit1_gemv_variant {
                               BIT1_ESHAPE) and y receives h = silu(g) * u,
                               [B][N/2], as BIT1_EPI_SWIGLU below.  Batch 1 on
                               BIT1_GEMV_LUT or BIT1_GEMV_STREAM (AUTO picks
-                              LUT for K <= 13312, else STREAM); any other
-                              variant or B > 1: BIT1_ESHAPE.  Not accepted by
-                              bit1_gemv_ternary (BIT1_EINVAL). */
+                              LUT for K <= 13312, else STREAM); any batch on
+                              BIT1_GEMV_TC (AUTO picks it from 16 rows with
+                              the tensor cores' workspace); any other variant,
+                              or AUTO at 2-15 rows: BIT1_ESHAPE.  Not accepted
+                              by bit1_gemv_ternary (BIT1_EINVAL). */
 
 /* ------------------------------------------------------------------------
  * bit1_pack -- floating-point weights -> packed sign bits + fp16 scales.

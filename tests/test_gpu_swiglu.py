@@ -233,6 +233,60 @@ def test_fused_decode_chain_layer(orc):
         sw.group_plan()
 
 
+# (N, K, B) on the tensor cores: ragged row tiles, K split over a cluster
+# (few row tiles, long K), batch padding, and batch > 64 (several chunks)
+TC_SHAPES = [(2, 1024, 16), (300, 1024, 16), (1000, 2048, 20), (2048, 4096, 16), (64, 17408, 16),
+             (4100, 2048, 48), (2048, 1024, 100)]
+
+
+@pytest.mark.parametrize("N,K,B", TC_SHAPES)
+def test_gemv_ex_swiglu_tensor_cores(orc, N, K, B):
+    bits, scales = synth.matrix(N, K, 9960 + B)
+    x = synth.x_for(B, K, 9960 + B)
+    db, ds, dx = dev_u8(bits), dev_u16(scales), dev_bf16(x).view(B, K)
+    yo = orc.gemv(bits, scales, x, B, N, K)
+    ho = orc.gemv_swiglu(bits, scales, x, B, N, K)
+    bd = abs_bound(scales, x, K)
+    full = b1.bit1_gemv_workspace_bytes(B, N, K)
+    sizes = [full] + ([b1.bit1_gemv_workspace_bytes(64, N, K)] if B > 64 else [])
+    for ws_bytes in sizes:
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        for ydt in (b1.F32, b1.BF16):
+            for variant in (b1.TC, b1.AUTO):
+                h = b1.bit1_gemv_ex(db, ds, dx, y_dtype=ydt, workspace=ws, variant=variant,
+                                    flags=b1.FLAG_SWIGLU | b1.FLAG_PDL)
+                torch.cuda.synchronize()
+                assert h.shape == (B, N // 2)
+                assert_swiglu_close(h, ho, yo[:, 0::2], yo[:, 1::2], bd[:, 0::2], bd[:, 1::2],
+                                    f"tc SwiGLU N={N} K={K} B={B} ws={ws_bytes} y={ydt} v={variant}")
+    h2 = b1.bit1_gemv_tc_noalloc(db, ds, dx, flags=b1.FLAG_SWIGLU)
+    torch.cuda.synchronize()
+    assert_swiglu_close(h2, ho, yo[:, 0::2], yo[:, 1::2], bd[:, 0::2], bd[:, 1::2], f"tc noalloc SwiGLU N={N}")
+    assert b1.bit1_device_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("B", [64, 256])
+def test_gemv_ex_swiglu_tensor_cores_mlp_gate_up(orc, B):
+    """The 8B MLP's gate/up pair as one interleaved 24576 x 4096 matrix at a
+    decode batch (64: split K) and a prompt batch (256: 128-row chunks):
+    sampled hidden units of every batch row against the oracle."""
+    N, K = 24576, 4096
+    bits, scales = synth.matrix(N, K, 9990 + B)
+    x = synth.x_for(B, K, 9990 + B)
+    ws = torch.empty(b1.bit1_gemv_workspace_bytes(B, N, K), dtype=torch.uint8, device="cuda")
+    h = b1.bit1_gemv_ex(dev_u8(bits), dev_u16(scales), dev_bf16(x).view(B, K), y_dtype=b1.BF16, workspace=ws,
+                        flags=b1.FLAG_SWIGLU)
+    torch.cuda.synchronize()
+    units = _sample(N // 2, 24, 9990 + B)
+    pairs = np.stack([2 * units, 2 * units + 1], 1).ravel()
+    ho = orc.gemv_swiglu_select(bits, scales, x, B, N, K, units)
+    gu = orc.gemv_select(bits, scales, x, B, N, K, pairs)
+    bd = abs_bound(scales[pairs], x, K)
+    assert_swiglu_close(h[:, torch.from_numpy(units).cuda()], ho, gu[:, 0::2], gu[:, 1::2], bd[:, 0::2],
+                        bd[:, 1::2], f"tc SwiGLU gate/up B={B}")
+    assert b1.bit1_device_wait_timeouts() == 0
+
+
 def test_gemv_ex_swiglu_rejections():
     N, K = 64, 1024
     bits, scales = synth.matrix(N, K, 9950)
