@@ -113,11 +113,19 @@ __device__ __forceinline__ void store_y(const TcParams& p, int b, int row, float
     else reinterpret_cast<float*>(p.y)[(int64_t)b * p.N + row] = v;
 }
 // SwiGLU output of hidden unit `unit` (rows 2 unit, 2 unit + 1): h = silu(g) * u.
-__device__ __forceinline__ void store_h(const TcParams& p, int b, int unit, float g, float u) {
-    const float h = g / (1.f + expf(-g)) * u;
+__device__ __forceinline__ void put_h(const TcParams& p, int b, int unit, float h) {
     const int64_t o = (int64_t)b * (p.N >> 1) + unit;
     if (p.y_bf16) reinterpret_cast<uint16_t*>(p.y)[o] = f32_to_bf16_bits(h);
     else reinterpret_cast<float*>(p.y)[o] = h;
+}
+__device__ __forceinline__ void store_h(const TcParams& p, int b, int unit, float g, float u) {
+    put_h(p, b, unit, g / (1.f + expf(-g)) * u);
+}
+// The same with the hardware exponential and reciprocal (a few ulps of h,
+// far inside the products' own tolerance): the direct-store epilogue runs
+// once per batch column of every row, on the CTA's critical path.
+__device__ __forceinline__ void store_h_fast(const TcParams& p, int b, int unit, float g, float u) {
+    put_h(p, b, unit, __fdividef(g, 1.f + __expf(-g)) * u);
 }
 __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, uint32_t bar) {
     asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
@@ -365,13 +373,19 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
                     for (int k = 0; k < 16; ++k)
                         asm volatile("st.shared.u32 [%0], %1;" ::"r"(wring + 4u * (uint32_t)((cb + k) * kTcRows + r)), "r"(d[k]) : "memory");
                 } else if (p.swiglu) {
-                    // lane 2m holds the gate row, lane 2m+1 the up row of unit row/2
+                    // Lane 2m holds the gate row and lane 2m+1 the up row of unit
+                    // row/2.  The pair splits the batch columns: the even lane forms h
+                    // for column 2j, the odd lane for column 2j+1, after one exchange.
+                    const bool odd = lane & 1;
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const bool bv = cb + k < bvalid;
-                        const float v = bv ? __uint_as_float(d[k]) * p.xscale[cb0 + cb + k] : 0.f;
-                        const float u = __shfl_down_sync(0xffffffffu, v, 1);
-                        if (live && bv && !(lane & 1)) store_h(p, cb0 + cb + k, row >> 1, v, u);
+                    for (int j = 0; j < 8; ++j) {
+                        const int c0 = cb + 2 * j;
+                        const float v0 = c0 < bvalid ? __uint_as_float(d[2 * j]) * p.xscale[cb0 + c0] : 0.f;
+                        const float v1 = c0 + 1 < bvalid ? __uint_as_float(d[2 * j + 1]) * p.xscale[cb0 + c0 + 1] : 0.f;
+                        const float w = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+                        const float g = odd ? w : v0, u = odd ? v1 : w;
+                        const int c = c0 + (odd ? 1 : 0);
+                        if (live && c < bvalid) store_h_fast(p, cb0 + c, row >> 1, g, u);
                     }
                 } else if (live) {
 #pragma unroll
