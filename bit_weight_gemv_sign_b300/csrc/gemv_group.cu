@@ -18,6 +18,12 @@
 // chunks of at most 32 groups (4096 inputs); its per-warp TMA rings run ahead
 // across problem and chunk boundaries, so the weight stream does not stall
 // while the next problem's tables are built.
+//
+// SwiGLU epilogue: a problem may be a SwiGLU MLP's gate and up projections
+// with interleaved rows (same page, section "Bonsai 27B의 표현 방식": the base
+// model keeps its SwiGLU MLP).  Lanes 2m and 2m+1 then hold one hidden unit's
+// gate and up sums; one shuffle pairs them and the even lane writes
+// h = silu(g) * u.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 

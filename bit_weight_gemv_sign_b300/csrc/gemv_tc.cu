@@ -40,6 +40,11 @@
 //    fp32 accumulators in its own shared memory; after a cluster barrier, CTA
 //    j sums rows [64j/Ks, 64(j+1)/Ks) x 4 of every CTA's tile through
 //    distributed shared memory in rank order (deterministic) and writes y.
+//  * SwiGLU epilogue (rows interleaved as the gate/up pairs of a SwiGLU MLP,
+//    the base model's MLP on the same page, section "Bonsai 27B의 표현
+//    방식"): the two epilogue lanes of a pair exchange one value per two batch
+//    columns and each writes h = silu(g) * u for one of them; the split-K
+//    reduction sums four consecutive rows, i.e. two whole pairs.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
