@@ -63,6 +63,8 @@ def configure(lib):
     lib.orc_gemv_swiglu_select.restype = ctypes.c_int
     lib.orc_gemv_ternary.argtypes = [p, p, p, p, i64, i64, i64, p]
     lib.orc_gemv_ternary.restype = ctypes.c_int
+    lib.orc_gemv_ternary_swiglu.argtypes = [p, p, p, p, i64, i64, i64, p]
+    lib.orc_gemv_ternary_swiglu.restype = ctypes.c_int
     lib.orc_gemv_ternary_select.argtypes = [p, p, p, p, i64, i64, i64, p, i64, p]
     lib.orc_gemv_ternary_select.restype = ctypes.c_int
     lib.orc_ternary_planes.argtypes = [p, i64, i64, p, p]
@@ -207,6 +209,16 @@ def gemv_ternary(a, b, scales, x, B: int, N: int, K: int) -> np.ndarray:
     if st != OK:
         raise OracleError(st, "gemv_ternary")
     return y
+
+
+def gemv_ternary_swiglu(a, b, scales, x, B: int, N2: int, K: int) -> np.ndarray:
+    """Ternary interleaved gate/up rows -> silu(gate) * up, [B, N2/2]."""
+    a, b, scales, x = _u8(a), _u8(b), _u16(scales), _u16(x)
+    h = np.zeros((B, N2 // 2), dtype=np.float64)
+    st = _load().orc_gemv_ternary_swiglu(_ptr(a), _ptr(b), _ptr(scales), _ptr(x), B, N2, K, _ptr(h))
+    if st != OK:
+        raise OracleError(st, "gemv_ternary_swiglu")
+    return h
 
 
 def gemv_ternary_select(a, b, scales, x, B: int, N: int, K: int, rows) -> np.ndarray:

@@ -382,6 +382,33 @@ int orc_gemv_ternary(const uint8_t *pa, const uint8_t *pb, const uint16_t *scale
     return ORC_OK;
 }
 
+/* Ternary gate/up pair with the SwiGLU activation ([27B-ter], [27B-arch]):
+ * the interleaved layout of orc_gemv_swiglu on ternary rows. */
+int orc_gemv_ternary_swiglu(const uint8_t *pa, const uint8_t *pb, const uint16_t *scales,
+                            const uint16_t *x, int64_t B, int64_t N2, int64_t K, double *h)
+{
+    int st = orc_check_shape(B, N2, K);
+    double *y;
+    if (st != ORC_OK)
+        return st;
+    if (N2 % 2 != 0)
+        return ORC_ESHAPE;
+    if (!pa || !pb || !scales || !x || !h)
+        return ORC_EINVAL;
+    y = (double *)malloc(sizeof(double) * (size_t)B * (size_t)N2);
+    if (!y)
+        return ORC_EINVAL;
+    orc_gemv_ternary_rows(pa, pb, scales, x, B, N2, K, 0, N2, y);
+    for (int64_t b = 0; b < B; b++) {
+        for (int64_t n = 0; n < N2 / 2; n++) {
+            double gt = y[b * N2 + 2 * n], up = y[b * N2 + 2 * n + 1];
+            h[b * (N2 / 2) + n] = gt / (1.0 + exp(-gt)) * up;
+        }
+    }
+    free(y);
+    return ORC_OK;
+}
+
 int orc_gemv_ternary_select(const uint8_t *pa, const uint8_t *pb, const uint16_t *scales,
                             const uint16_t *x, int64_t B, int64_t N, int64_t K,
                             const int64_t *rows, int64_t n_sel, double *y)

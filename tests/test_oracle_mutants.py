@@ -104,7 +104,7 @@ MUTANTS = [
       lambda o: pins.test_swiglu_matches_dense_and_library_silu(o, 6, 256, 2, 1)]),
     ("swiglu_sigmoid_without_g", _HF + " g / (1.0 + exp(-g)) * u", _HF + " 1.0 / (1.0 + exp(-g)) * u",
      [lambda o: pins.test_swiglu_zero_gate_or_zero_up_gives_zero(o)]),
-    ("swiglu_batch_row_ignored", _HF, "\n            h[n] =",
+    ("swiglu_batch_row_ignored", _HF + " g /", "\n            h[n] = g /",
      [lambda o: pins.test_swiglu_matches_dense_and_library_silu(o, 10, 384, 3, 2)]),
     ("swiglu_odd_rows_accepted", "    if (N2 % 2 != 0)\n        return ORC_ESHAPE;\n    if (!bits || !scales || !x || !h)\n",
      "    if (!bits || !scales || !x || !h)\n",
@@ -114,6 +114,12 @@ MUTANTS = [
     ("swiglu_select_gate_up_swapped", _GU + "\n            h[b * n_sel + i] =",
      _GU_SW + "\n            h[b * n_sel + i] =",
      [lambda o: pins.test_swiglu_select_matches_full(o)]),
+    ("ternary_swiglu_gate_up_swapped", "double gt = y[b * N2 + 2 * n], up = y[b * N2 + 2 * n + 1];",
+     "double up = y[b * N2 + 2 * n], gt = y[b * N2 + 2 * n + 1];",
+     [lambda o: pins.test_ternary_swiglu_matches_dense_and_library_silu(o, 8, 256, 2, 1),
+      lambda o: pins.test_ternary_swiglu_without_zeros_is_the_binary_pair(o)]),
+    ("ternary_swiglu_sigmoid_sign", "gt / (1.0 + exp(-gt)) * up", "gt / (1.0 + exp(gt)) * up",
+     [lambda o: pins.test_ternary_swiglu_matches_dense_and_library_silu(o, 8, 256, 2, 1)]),
 ]
 
 

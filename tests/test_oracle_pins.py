@@ -587,6 +587,40 @@ def test_ternary_select_matches_full(orc):
     assert np.array_equal(orc.gemv_ternary_select(a, b, scales, x, B, N, K, rows), full[:, rows])
 
 
+@pytest.mark.parametrize("N2,K,B,seed", [(2, 128, 1, 0), (8, 256, 2, 1), (12, 384, 3, 2)])
+def test_ternary_swiglu_matches_dense_and_library_silu(orc, N2, K, B, seed):
+    """Ternary gate/up pairs: a dense fp64 matmul of the codes (planes built by
+    numpy), then scipy's sigmoid; the tolerance as for the binary pair."""
+    g = synth.rng(500 + seed)
+    t = synth.ternary_codes(N2, K, g)
+    scales = synth.group_scales(N2, K, g, offset=1e-3)
+    x = synth.activations(B, K, g)
+    a, b = _np_planes(t)
+    h = orc.gemv_ternary_swiglu(a, b, scales, x, B, N2, K)
+    y, W, X = _dense_ternary(t, scales, x, N2, K)
+    bd = _bound(W, X)
+    gate, up = y[:, 0::2], y[:, 1::2]
+    want = _silu_np(gate) * up
+    tol = 1e-12 * (1.1 * bd[:, 0::2] * np.abs(up) + np.abs(gate) * bd[:, 1::2]) + 1e-14 * np.abs(want) + 1e-300
+    assert np.all(np.abs(h - want) <= tol)
+
+
+def test_ternary_swiglu_without_zeros_is_the_binary_pair(orc):
+    """Planes a = b (no zero codes) are the binary matrix: the ternary pair
+    equals the binary pair bit for bit; zero codes in a gate or an up row
+    give exactly 0."""
+    N2, K, B = 10, 256, 2
+    bits, scales = synth.matrix(N2, K, 41, scale_offset=1e-3)
+    x = synth.x_for(B, K, 41)
+    assert np.array_equal(orc.gemv_ternary_swiglu(bits, bits, scales, x, B, N2, K),
+                          orc.gemv_swiglu(bits, scales, x, B, N2, K))
+    a, b = bits.copy(), bits.copy()
+    b[4] = ~a[4]          # row 4 (gate of unit 2): all codes 0
+    b[7] = ~a[7]          # row 7 (up of unit 3): all codes 0
+    h = orc.gemv_ternary_swiglu(a, b, scales, x, B, N2, K)
+    assert np.all(h[:, [2, 3]] == 0.0)
+
+
 def test_ternary_rejects_bad_shapes(orc):
     import oracle
     a, b, scales = synth.ternary_matrix(2, 128, 725)
