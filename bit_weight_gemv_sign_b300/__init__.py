@@ -366,14 +366,15 @@ def bit1_gemv_ternary(a, b, scales, x, y=None, y_dtype=None, workspace=None, var
                       stream=None, N=None, K=None):
     """y[B, N] = x[B, K] (bf16) times the ternary matrix given by its planes
     a, b (uint8 [N, K/8]) and scales [N, K/128].  ``workspace`` defaults to
-    a fresh buffer of bit1_gemv_ternary_workspace_bytes bytes."""
+    a fresh buffer of bit1_gemv_ternary_workspace_bytes bytes.  With
+    FLAG_SWIGLU the rows are gate/up pairs and y is [B, N/2]."""
     import torch
     B = x.shape[0] if x.dim() == 2 else 1
     K = x.shape[-1] if K is None else K
     N = a.shape[0] if N is None else N
     if y is None:
         yt = torch.bfloat16 if y_dtype == BF16 else torch.float32
-        y = torch.empty((B, N), dtype=yt, device=x.device)
+        y = torch.empty((B, N // 2 if int(flags) & FLAG_SWIGLU else N), dtype=yt, device=x.device)
     if y.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("y must be float32 or bfloat16")
     ydt = BF16 if y.dtype == torch.bfloat16 else F32

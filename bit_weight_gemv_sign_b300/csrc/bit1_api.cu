@@ -264,7 +264,10 @@ bit1_status bit1_gemv_ternary(const uint8_t* a, const uint8_t* b, const uint16_t
     if (!shape_ok(B, N, K)) return BIT1_ESHAPE;
     if (!a || !b || !aligned16(a) || !aligned16(b)) return BIT1_EINVAL;
     if (!workspace || !aligned16(workspace)) return BIT1_EINVAL;
-    if (flags & BIT1_FLAG_SWIGLU) return BIT1_EINVAL;      // the halves are combined afterwards
+    // SwiGLU: the two binary halves run plain; the combine forms the pairs.
+    const bool swiglu = (flags & BIT1_FLAG_SWIGLU) != 0;
+    if (swiglu && N % 2 != 0) return BIT1_ESHAPE;
+    flags &= ~BIT1_FLAG_SWIGLU;
     const size_t half = ternary_half_bytes(B, N);
     if (ws_bytes < 2 * half) return BIT1_EINVAL;
     float* ya = reinterpret_cast<float*>(workspace);
@@ -281,7 +284,7 @@ bit1_status bit1_gemv_ternary(const uint8_t* a, const uint8_t* b, const uint16_t
     if (st != BIT1_OK) return st;
     st = gemv_run(b, scales, x, B, N, K, yb, BIT1_F32, rest, rest_bytes, variant, flags, s);
     if (st != BIT1_OK) return st;
-    return from_cuda(launch_ternary_combine(ya, yb, B * N, y, y_dtype == BIT1_BF16, s));
+    return from_cuda(launch_ternary_combine(ya, yb, B * N, y, y_dtype == BIT1_BF16, s, swiglu));
 }
 
 int bit1_gemv_ternary_launches(int64_t B, int64_t N, int64_t K, int variant) {

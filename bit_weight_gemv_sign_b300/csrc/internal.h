@@ -72,7 +72,8 @@ unsigned int tc_take_timeouts();
 cudaError_t launch_ternary_planes(const int8_t* codes, int64_t N, int64_t K, uint8_t* a, uint8_t* b,
                                   uint32_t* flags, cudaStream_t stream);
 cudaError_t launch_ternary_combine(const float* ya, const float* yb, int64_t n, void* y, bool y_bf16,
-                                   cudaStream_t stream);
+                                   cudaStream_t stream,
+                                   bool swiglu = false);
 
 // Ternary codes packed five per byte (t5.cu).
 cudaError_t launch_t5_pack(const int8_t* codes, int64_t N, int64_t K, uint8_t* out, uint32_t* flags,

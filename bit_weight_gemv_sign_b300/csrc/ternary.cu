@@ -9,7 +9,8 @@
 // that share the scales and the activations:
 //     y = ( sum_g s_g sum_k a_k x_k  +  sum_g s_g sum_k b_k x_k ) / 2.
 // The binary kernels compute both halves into fp32 scratch; k_ternary_combine
-// forms the mean and the output type.
+// forms the mean and the output type (k_ternary_combine_swiglu: the means of
+// a gate/up pair and h = silu(g) * u).
 #include <algorithm>
 
 #include "common.cuh"
@@ -93,9 +94,41 @@ __global__ void __launch_bounds__(256) k_ternary_combine(const float* __restrict
     }
 }
 
+// SwiGLU pairs (rows interleaved as gate, up; the Bonsai 27B page, section
+// "Bonsai 27B의 표현 방식": the base model's MLP is SwiGLU): element 2i of the
+// flat [B][N] halves is a gate, 2i+1 its up (N even, so pairs never cross batch
+// rows); y[i] = silu(g) * u with g, u the two means.
+template <bool BF16>
+__global__ void __launch_bounds__(256) k_ternary_combine_swiglu(const float2* __restrict__ ya,
+                                                                const float2* __restrict__ yb, int64_t pairs,
+                                                                void* __restrict__ y) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < pairs; i += stride) {
+        const float2 u = __ldg(ya + i), v = __ldg(yb + i);
+        const float g = 0.5f * (u.x + v.x), up = 0.5f * (u.y + v.y);
+        const float h = g / (1.f + expf(-g)) * up;
+        if (BF16)
+            reinterpret_cast<uint16_t*>(y)[i] = f32_to_bf16_bits(h);
+        else
+            reinterpret_cast<float*>(y)[i] = h;
+    }
+}
+
 cudaError_t launch_ternary_combine(const float* ya, const float* yb, int64_t n, void* y, bool y_bf16,
-                                   cudaStream_t stream) {
+                                   cudaStream_t stream, bool swiglu) {
     const int threads = 256;
+    if (swiglu) {
+        const int64_t pairs = n / 2;
+        const int64_t want = (pairs + threads - 1) / threads;
+        const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * 8));
+        const float2* a2 = reinterpret_cast<const float2*>(ya);
+        const float2* b2 = reinterpret_cast<const float2*>(yb);
+        if (y_bf16)
+            k_ternary_combine_swiglu<true><<<blocks, threads, 0, stream>>>(a2, b2, pairs, y);
+        else
+            k_ternary_combine_swiglu<false><<<blocks, threads, 0, stream>>>(a2, b2, pairs, y);
+        return cudaGetLastError();
+    }
     const int64_t want = (n / 4 + threads) / threads;
     const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * 8));
     if (y_bf16)

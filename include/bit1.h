@@ -97,8 +97,9 @@ enum bit1_gemv_variant {
                               LUT for K <= 13312, else STREAM); any batch on
                               BIT1_GEMV_TC (AUTO picks it from 16 rows with
                               the tensor cores' workspace); any other variant,
-                              or AUTO at 2-15 rows: BIT1_ESHAPE.  Not accepted
-                              by bit1_gemv_ternary (BIT1_EINVAL). */
+                              or AUTO at 2-15 rows: BIT1_ESHAPE.
+                              bit1_gemv_ternary applies it in its combine
+                              step instead (any batch, any variant). */
 
 /* ------------------------------------------------------------------------
  * bit1_pack -- floating-point weights -> packed sign bits + fp16 scales.
@@ -330,7 +331,11 @@ bit1_status bit1_ternary_planes(const int8_t *codes, int64_t N, int64_t K,
  * kernel).  Result within 1e-3 * sum_k |s*x_k| + 1e-6 of the exact value
  * (plus the bf16 output rounding for y_dtype = BIT1_BF16).
  *   a, b, scales, x, B, N, K, y, y_dtype, variant, flags : as bit1_gemv_ex
- *                  (the variant and flags apply to both binary passes)
+ *                  (the variant and BIT1_FLAG_PDL apply to both binary
+ *                  passes).  BIT1_FLAG_SWIGLU: rows are interleaved gate/up
+ *                  pairs (N even, else BIT1_ESHAPE); both passes run plain
+ *                  and the combine writes h = silu(g) * u of the two means,
+ *                  [B][N/2], at any batch and with any variant.
  *   workspace    : REQUIRED device scratch of ws_bytes bytes, 16-byte
  *                  aligned: at least the two fp32 halves, 2 * (B*N*4 rounded
  *                  up to 256) bytes, else BIT1_EINVAL; the fastest kernels

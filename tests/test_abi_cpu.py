@@ -200,8 +200,9 @@ def test_swiglu_flag_checked_on_host(lib):
         assert f(FAKE, FAKE, FAKE, 2, 8, 1024, FAKE, b1.F32, None, 0, v, S, None) == b1.ESHAPE
     assert f(FAKE, FAKE, FAKE, 1, 8, 1152, FAKE, b1.F32, None, 0, b1.LUT, S, None) == b1.ESHAPE
     assert f(FAKE, FAKE, FAKE, 1, 8, 1024, FAKE, b1.F32, None, 0, 0, S | 4, None) == b1.EINVAL
-    g = lib.bit1_gemv_ternary
-    assert g(FAKE, FAKE, FAKE, FAKE, 1, 8, 128, FAKE, b1.F32, FAKE, 512, 0, S, None) == b1.EINVAL
+    g = lib.bit1_gemv_ternary                     # pairs formed in the combine: only N must be even
+    assert g(FAKE, FAKE, FAKE, FAKE, 1, 7, 128, FAKE, b1.F32, FAKE, 512, 0, S, None) == b1.ESHAPE
+    assert g(FAKE, FAKE, FAKE, FAKE, 1, 8, 128, FAKE, b1.F32, FAKE, 512, 0, S | 4, None) == b1.EINVAL
 
 
 def test_group_plan_epilogue_checked_on_host(lib):

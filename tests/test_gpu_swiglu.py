@@ -307,3 +307,25 @@ def test_gemv_ex_swiglu_rejections():
     with pytest.raises(b1.Bit1Error) as e:
         b1.bit1_gemv_ex(db, ds, dx1, flags=8)
     assert e.value.status == b1.EINVAL
+
+
+# ---------------------------------------------------------------- ternary (2-bit slots)
+
+@pytest.mark.parametrize("B,N,K,variant", [(1, 2000, 4096, b1.AUTO), (1, 514, 2048, b1.LUT6), (3, 1000, 2048, b1.AUTO),
+                                           (16, 1024, 4096, b1.AUTO), (20, 300, 1024, b1.TC)])
+def test_gemv_ternary_swiglu_matches_oracle(orc, B, N, K, variant):
+    """Ternary gate/up pairs: both binary passes run plain (any variant), the
+    combine forms the two means and h; against the ternary oracle pair."""
+    a, b, scales = synth.ternary_matrix(N, K, 9970 + B)
+    x = synth.x_for(B, K, 9970 + B)
+    da, db_, ds, dx = dev_u8(a), dev_u8(b), dev_u16(scales), dev_bf16(x).view(B, K)
+    yo = orc.gemv_ternary(a, b, scales, x, B, N, K)
+    ho = orc.gemv_ternary_swiglu(a, b, scales, x, B, N, K)
+    bd = abs_bound(scales, x, K)
+    for ydt in (b1.F32, b1.BF16):
+        h = b1.bit1_gemv_ternary(da, db_, ds, dx, y_dtype=ydt, variant=variant, flags=b1.FLAG_SWIGLU)
+        torch.cuda.synchronize()
+        assert h.shape == (B, N // 2)
+        assert_swiglu_close(h, ho, yo[:, 0::2], yo[:, 1::2], bd[:, 0::2], bd[:, 1::2],
+                            f"ternary SwiGLU B={B} N={N} K={K} v={variant} y={ydt}")
+    assert b1.bit1_device_wait_timeouts() == 0
