@@ -226,22 +226,22 @@ k_gemv_lut(const uint8_t* __restrict__ bits, const uint16_t* __restrict__ scales
                 }
             }
         }
-        return;
-    }
-    for (int64_t base = n0 + warp; base < n1; base += (int64_t)D * nw) {
+    } else {
+        for (int64_t base = n0 + warp; base < n1; base += (int64_t)D * nw) {
 #pragma unroll
-        for (int d = 0; d < D; ++d) {
-            const int64_t row = base + (int64_t)d * nw;
-            if (row >= n1) break;
-            const float acc = lut_row<M>(wb[d], sb[d], lb, o, [&] {
-                const int64_t nrow = row + (int64_t)D * nw;
-                if (nrow < n1) load_row<M>(bits, scales, nrow, lane, wb[d], sb[d]);
-            });
-            if (lane == 0) {
-                if (y_bf16)
-                    reinterpret_cast<uint16_t*>(y)[row] = f32_to_bf16_bits(acc);
-                else
-                    reinterpret_cast<float*>(y)[row] = acc;
+            for (int d = 0; d < D; ++d) {
+                const int64_t row = base + (int64_t)d * nw;
+                if (row >= n1) break;
+                const float acc = lut_row<M>(wb[d], sb[d], lb, o, [&] {
+                    const int64_t nrow = row + (int64_t)D * nw;
+                    if (nrow < n1) load_row<M>(bits, scales, nrow, lane, wb[d], sb[d]);
+                });
+                if (lane == 0) {
+                    if (y_bf16)
+                        reinterpret_cast<uint16_t*>(y)[row] = f32_to_bf16_bits(acc);
+                    else
+                        reinterpret_cast<float*>(y)[row] = acc;
+                }
             }
         }
     }
