@@ -281,7 +281,8 @@ bit1_status bit1_selftest_wait_timeout(unsigned int *d_done, bit1_stream_t strea
  *   kernels overlap on the GPU (different streams, or different host threads
  *   without ordering) corrupt each other's results; keep such calls ordered,
  *   e.g. on one stream.
- * Arguments as bit1_gemv_ex (flags: BIT1_FLAG_PDL).  Returns BIT1_ESHAPE if
+ * Arguments as bit1_gemv_ex (flags: BIT1_FLAG_PDL, BIT1_FLAG_SWIGLU).
+ * Returns BIT1_ESHAPE if
  * the shape is outside the tensor-core kernel's limits (K a multiple of 1024)
  * or needs more scratch than BIT1_NOALLOC_SCRATCH_BYTES (only possible for
  * K > 32768: the need is 2 * min(B, 64) rounded up to 16 * K + 256 bytes,
