@@ -864,22 +864,7 @@ def run_mine(args):
         c1.synchronize()
     fused_ms = max_over_ranks(c0.elapsed_time(c1), dist, "cuda") / chain_steps
     fused_launches, fused_bytes = fz.launches_per_step(), fz.weight_bytes
-
-    # secondary: the same fused chain as ONE persistent launch (a grid-wide
-    # barrier between the 145 dependent stages)
-    cp = fz.chain_plan()
-    with torch.cuda.stream(fz.stream):
-        for _ in range(3):
-            cp.run(stream=fz.stream)
-        fz.stream.synchronize()
-        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        c0.record(fz.stream)
-        for _ in range(chain_steps):
-            cp.run(stream=fz.stream)
-        c1.record(fz.stream)
-        c1.synchronize()
-    persist_ms = max_over_ranks(c0.elapsed_time(c1), dist, "cuda") / chain_steps
-    del fz, cp
+    del fz
     torch.cuda.empty_cache()
 
     hbm, src = _peaks()
@@ -914,11 +899,6 @@ def run_mine(args):
                                "launches_per_step": fused_launches,
                                "what": "the same weights as 145 dependent launches: per layer q|k|v, o, "
                                        "gate|up with the SwiGLU epilogue, down reading h (graph + PDL)"},
-        "decode_chain_persistent": {"value": fused_bytes / (persist_ms * 1e-3) / 1e9, "unit": "GB/s",
-                                    "ms_per_step": persist_ms, "tok_s_equiv": 1e3 / persist_ms,
-                                    "launches_per_step": 1,
-                                    "what": "the fused chain's 145 dependent stages in one cooperative launch, "
-                                            "a grid-wide barrier between stages"},
         "device_wait_timeouts": timeouts,
         "clocks": clk.summary(),
     }

@@ -20,7 +20,6 @@ __all__ = [
     "bit1_gemv_workspace_bytes", "bit1_gemv_pick", "bit1_gemv_launches",
     "bit1_xor_patch", "bit1_status_str", "bit1_version", "bit1_device_wait_timeouts",
     "bit1_group_plan_bytes", "bit1_group_plan", "bit1_gemv_group", "GroupPlan",
-    "bit1_chain_plan_bytes", "bit1_chain_plan", "bit1_gemv_chain", "ChainPlan",
     "library_path", "load", "bit1_gemv_tc_noalloc",
     "bit1_ternary_planes", "bit1_gemv_ternary", "bit1_gemv_ternary_workspace_bytes",
     "bit1_gemv_ternary_launches", "bit1_ternary_combine",
@@ -101,12 +100,6 @@ def load():
         lib.bit1_group_plan_batched.restype = i32
         lib.bit1_gemv_group.argtypes = [p, p, ctypes.c_uint, p]
         lib.bit1_gemv_group.restype = i32
-        lib.bit1_chain_plan_bytes.argtypes = [i32]
-        lib.bit1_chain_plan_bytes.restype = sz
-        lib.bit1_chain_plan.argtypes = [ctypes.POINTER(_Problem), i32, p, sz]
-        lib.bit1_chain_plan.restype = i32
-        lib.bit1_gemv_chain.argtypes = [p, p, p]
-        lib.bit1_gemv_chain.restype = i32
         lib.bit1_gemv_tc_noalloc.argtypes = [p, p, p, i64, i64, i64, p, i32, ctypes.c_uint, p]
         lib.bit1_gemv_tc_noalloc.restype = i32
         lib.bit1_ternary_planes.argtypes = [p, i64, i64, p, p, p, p]
@@ -341,66 +334,6 @@ class GroupPlan:
 
     def run(self, flags: int = 0, stream=None) -> None:
         bit1_gemv_group(self.dev.data_ptr(), self.host.ctypes.data, flags, stream)
-
-
-# ---------------------------------------------------------------- dependent chain
-
-def _problem_array(problems):
-    import torch
-    arr = (_Problem * len(problems))()
-    for i, pr in enumerate(problems):
-        bits, scales, x, y = pr[:4]
-        epi = int(pr[4]) if len(pr) > 4 else EPI_NONE
-        if y.dtype not in (torch.float32, torch.bfloat16):
-            raise TypeError("y must be float32 or bfloat16")
-        arr[i] = _Problem(_dptr(bits, "bits"), _dptr(scales, "scales"), _dptr(x, "x"), _dptr(y, "y"),
-                          bits.shape[0], x.shape[-1], BF16 if y.dtype == torch.bfloat16 else F32, epi)
-    return arr
-
-
-def bit1_chain_plan_bytes(count: int) -> int:
-    return int(load().bit1_chain_plan_bytes(int(count)))
-
-
-def bit1_chain_plan(stages, host_plan_ptr: int, plan_bytes: int) -> None:
-    """stages: sequence of (bits, scales, x, y) or (bits, scales, x, y,
-    epilogue) CUDA tensors at batch 1, in execution order; a stage's x may be
-    an earlier stage's y."""
-    arr = _problem_array(stages)
-    _check(load().bit1_chain_plan(arr, len(stages), host_plan_ptr, plan_bytes), "bit1_chain_plan")
-
-
-def bit1_gemv_chain(device_plan_ptr: int, host_plan_ptr: int, stream=None) -> None:
-    _check(load().bit1_gemv_chain(device_plan_ptr, host_plan_ptr, _stream(stream)), "bit1_gemv_chain")
-
-
-class ChainPlan:
-    """A dependent chain of batch-1 products run as one persistent launch: the
-    encoded host copy and its device copy (both 128-byte aligned; the device
-    copy also holds the launch's barrier words).  The tensors named in
-    ``stages`` must stay alive and in place while the plan is used."""
-
-    def __init__(self, stages, device="cuda"):
-        import numpy as np
-        import torch
-        self.stages = list(stages)
-        self.nbytes = bit1_chain_plan_bytes(len(self.stages))
-        self._host_raw = np.zeros(self.nbytes + 128, dtype=np.uint8)
-        off = (-self._host_raw.ctypes.data) % 128
-        self.host = self._host_raw[off: off + self.nbytes]
-        bit1_chain_plan(self.stages, self.host.ctypes.data, self.nbytes)
-        self._dev_raw = torch.empty(self.nbytes + 128, dtype=torch.uint8, device=device)
-        doff = (-self._dev_raw.data_ptr()) % 128
-        self.dev = self._dev_raw[doff: doff + self.nbytes]
-        self.reset()
-
-    def reset(self) -> None:
-        """Copy the host plan (barrier words at zero) to the device again."""
-        import torch
-        self.dev.copy_(torch.from_numpy(self.host))
-
-    def run(self, stream=None) -> None:
-        bit1_gemv_chain(self.dev.data_ptr(), self.host.ctypes.data, stream)
 
 
 # ---------------------------------------------------------------- ternary (2-bit slots)

@@ -227,21 +227,8 @@ const char* bit1_version(void) { return "bit1 0.2 (sm_103a)"; }
 
 unsigned int bit1_device_wait_timeouts(void) {
     const unsigned int a = t6_take_timeouts(), b = group_take_timeouts(), c = tc_take_timeouts();
-    const unsigned int d = chain_take_timeouts();
-    if (a == 0xffffffffu || b == 0xffffffffu || c == 0xffffffffu || d == 0xffffffffu) return 0xffffffffu;
-    return a + b + c + d;
-}
-
-size_t bit1_chain_plan_bytes(int count) { return chain_plan_bytes(count); }
-
-bit1_status bit1_chain_plan(const bit1_gemv_problem* stages, int count, void* host_plan, size_t plan_bytes) {
-    return chain_plan(stages, count, host_plan, plan_bytes);
-}
-
-bit1_status bit1_gemv_chain(void* device_plan, const void* host_plan, bit1_stream_t stream) {
-    if (!device_plan || !host_plan || ((uintptr_t)device_plan & 127) || ((uintptr_t)host_plan & 127))
-        return BIT1_EINVAL;
-    return from_cuda(launch_chain(device_plan, host_plan, (cudaStream_t)stream));
+    if (a == 0xffffffffu || b == 0xffffffffu || c == 0xffffffffu) return 0xffffffffu;
+    return a + b + c;
 }
 
 size_t bit1_group_plan_bytes(int count) { return group_plan_bytes(count); }

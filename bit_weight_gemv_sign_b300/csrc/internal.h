@@ -59,12 +59,6 @@ bool group1_supported(int64_t B, int64_t N, int64_t K);
 cudaError_t launch_gemv_group1(const GemvArgs& a);
 unsigned int group_take_timeouts();
 
-// Dependent chain of batch-1 products in one cooperative launch (chain.cu).
-size_t chain_plan_bytes(int count);
-bit1_status chain_plan(const bit1_gemv_problem* stages, int count, void* host_plan, size_t bytes);
-cudaError_t launch_chain(void* device_plan, const void* host_plan, cudaStream_t stream);
-unsigned int chain_take_timeouts();
-
 // tcgen05 tensor-core batched kernel (gemv_tc.cu): K a multiple of 1024;
 // needs tc_workspace_bytes() of scratch; tc_launch_count() launches per call.
 bool tc_supported(int64_t B, int64_t N, int64_t K);

@@ -18,7 +18,7 @@ import numpy as np
 import torch
 
 from . import synth
-from . import (BF16, F32, FLAG_PDL, FLAG_SWIGLU, AUTO, EPI_NONE, EPI_SWIGLU, ChainPlan, GroupPlan, bit1_gemv_ex,
+from . import (BF16, F32, FLAG_PDL, FLAG_SWIGLU, AUTO, EPI_NONE, EPI_SWIGLU, GroupPlan, bit1_gemv_ex,
                bit1_gemv_launches, bit1_ternary_combine, bit1_xor_patch)
 
 
@@ -162,16 +162,6 @@ class Sweep:
         probs = [(self.bits_of(i), self.scales_of(i), self.x_of(i, x), self.y_of(i, y),
                   EPI_SWIGLU if m.swiglu else EPI_NONE) for i, m in enumerate(self.mats)]
         return GroupPlan(probs, device=self.device, B=self.B)
-
-    def chain_plan(self):
-        """Every matrix of the sweep, in order, as one persistent launch with a
-        grid-wide barrier between consecutive products (batch 1; the matrix
-        after a SwiGLU matrix reads its h when the sweep feeds it)."""
-        if self.B != 1:
-            raise ValueError("the persistent chain runs batch 1")
-        stages = [(self.bits_of(i), self.scales_of(i), self.x_of(i).view(-1), self.y_of(i),
-                   EPI_SWIGLU if m.swiglu else EPI_NONE) for i, m in enumerate(self.mats)]
-        return ChainPlan(stages, device=self.device)
 
     def apply_patch(self, entries, proj_count: int = 7):
         """Apply (or, applied again, remove) a list of (layer, projection, row)

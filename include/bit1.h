@@ -234,39 +234,6 @@ bit1_status bit1_gemv_group(const void *device_plan, const void *host_plan,
                             unsigned flags, bit1_stream_t stream);
 
 /* ------------------------------------------------------------------------
- * Dependent chain: a decode step's products in their data order, as ONE
- * persistent launch.  At batch 1 each product is only 0.3-1.9 us of weight
- * traffic, while a chain of separate launches pays 3-7 us of kernel
- * turn-around per product (web page "Bonsai 27B: 노트북과 폰에서 실행되는 27B급
- * 이진 및 삼진 저비트 LLM", section "하이브리드 어텐션을 위한 저비트 커널": at
- * batch 1 launch and synchronisation latency decide).  Here the stages are
- * separated by a grid-wide barrier inside one cooperative launch (one CTA per
- * SM), and each stage's weights start streaming before the barrier.
- *   Stages run in the given order; stage s may read as its x the y of any
- *   earlier stage (e.g. the bf16 h of a BIT1_EPI_SWIGLU gate/up stage as the
- *   down projection's input).  Each stage is a bit1_gemv_problem with
- *   B = 1: K a multiple of 1024 up to 13312, N >= 1, y_dtype BIT1_F32 or
- *   BIT1_BF16, epilogue BIT1_EPI_NONE or BIT1_EPI_SWIGLU (N even), pointers
- *   16-byte aligned (else BIT1_ESHAPE / BIT1_EINVAL); a stage's own x must
- *   not overlap its own y (BIT1_EINVAL).  Results are bit-identical to
- *   calling bit1_gemv_ex(..., BIT1_GEMV_LUT, ...) stage by stage (with
- *   BIT1_FLAG_SWIGLU for SwiGLU stages).
- *   Use: bit1_chain_plan() writes a caller-owned HOST buffer of
- *   bit1_chain_plan_bytes(count) bytes (128-byte aligned); the caller copies
- *   it unchanged into a writable DEVICE buffer of the same size (128-byte
- *   aligned) and calls bit1_gemv_chain(device_plan, host_plan, stream).  The
- *   device copy holds the barrier words: one launch of a plan at a time, and
- *   if bit1_device_wait_timeouts() reports a barrier wait that gave up, copy
- *   the host plan to the device again before the next launch.  The launch
- *   needs every SM free of other work to start (cooperative launch).
- */
-size_t bit1_chain_plan_bytes(int count);
-bit1_status bit1_chain_plan(const bit1_gemv_problem *stages, int count,
-                            void *host_plan, size_t plan_bytes);
-bit1_status bit1_gemv_chain(void *device_plan, const void *host_plan,
-                            bit1_stream_t stream);
-
-/* ------------------------------------------------------------------------
  * bit1_xor_patch -- the Bankai row-wise sign-flip patch, in place.
  * Every listed row has all of its K sign bits inverted (bytes ^= 0xFF);
  * scales are untouched.  Applying the same list again removes the patch.
