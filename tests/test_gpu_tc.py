@@ -108,6 +108,20 @@ def test_tc_prompt_batch_512(orc):
     assert_gemv_close(y[:, torch.from_numpy(rows).cuda()], ref, abs_bound(scales[rows], x, K), "tc B=512")
 
 
+def test_tc_pp512_up_gate_shape(orc):
+    """The benchmarked prompt-processing configuration: the 8B up/gate shape
+    12288 x 4096 at B = 512 with bit1_gemv_workspace_bytes of scratch (one
+    launch pair, 128-row chunks): sampled rows of every batch row against the
+    oracle."""
+    N, K, B = 12288, 4096, 512
+    bits, scales, x = _problem(N, K, B, 7260)
+    y = _run_tc(bits, scales, x, N, K, B)
+    rows = np.unique(np.concatenate([np.random.default_rng(5120).choice(N, 40, replace=False), [0, N - 1]]))
+    ref = orc.gemv_select(bits, scales, x, B, N, K, rows)
+    assert_gemv_close(y[:, torch.from_numpy(rows).cuda()], ref, abs_bound(scales[rows], x, K), "tc PP512")
+    assert b1.bit1_device_wait_timeouts() == 0
+
+
 def test_tc_row_flip_negates_exactly():
     """Negated weights flow through the same products and the same fixed
     accumulation order, so a flipped row gives the exact negation."""
