@@ -102,16 +102,15 @@ bit1_status gemv_check(const uint8_t* bits, const uint16_t* scales, const uint16
     if (ws_bytes > 0 && (!workspace || !aligned16(workspace))) return BIT1_EINVAL;
     if (flags & ~(BIT1_FLAG_PDL | BIT1_FLAG_SWIGLU)) return BIT1_EINVAL;
     if (flags & BIT1_FLAG_SWIGLU) {
-        // Gate/up pairs: the kernels whose lane, warp or epilogue thread owns
-        // whole rows -- at batch 1 the two table kernels, from 16 rows the
-        // tensor cores.
+        // Gate/up pairs: every kernel but the warp-per-row one pairs rows in
+        // its epilogue -- at batch 1 the two table kernels, at 2-8 rows the
+        // 6-bit cluster kernel, from 16 rows the tensor cores.
         if (N % 2 != 0) return BIT1_ESHAPE;
         if (*variant == BIT1_GEMV_AUTO) {
             if (B == 1) *variant = lut_supported(B, N, K) ? BIT1_GEMV_LUT : BIT1_GEMV_STREAM;
             else *variant = pick_variant(B, N, K, ws_bytes);
         }
-        if (*variant != BIT1_GEMV_LUT && *variant != BIT1_GEMV_STREAM && *variant != BIT1_GEMV_TC)
-            return BIT1_ESHAPE;
+        if (*variant == BIT1_GEMV_SIMPLE) return BIT1_ESHAPE;
     }
     if (*variant == BIT1_GEMV_AUTO) *variant = pick_variant(B, N, K, ws_bytes);
     switch (*variant) {

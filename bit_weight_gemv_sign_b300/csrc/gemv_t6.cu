@@ -67,6 +67,7 @@ struct T6Params {
     int prow;                 // rows per batch row in the partials area (32 x blocks per cluster)
     int KW;                   // warps sharing one row block, each on Gc/KW of its groups (1: no split)
     uint32_t off_tables, off_factors, off_x, off_partials, off_bars;
+    int swiglu;               // rows are (gate, up) pairs; y is h = silu(gate) * up, [NB][N/2]
 };
 
 // ---------------------------------------------------------------- kernel
@@ -240,10 +241,8 @@ k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
     __syncthreads();
     cluster_sync();
     const int R = (rb1 - rb0) * 32;
-    const int lo = (int)((int64_t)R * q / p.Q), hi = (int)((int64_t)R * (q + 1) / p.Q);
     const uint32_t part_s = base + p.off_partials;
-    for (int b = 0; b < NB; ++b)
-    for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+    auto row_sum = [&](int b, int i) {
         float v = 0.f;
         for (int r = 0; r < p.Q; ++r) {
             if constexpr (SPLIT) {
@@ -253,10 +252,35 @@ k_gemv_t6(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
                 v += ld_cluster_f32(part_s + 4u * (uint32_t)(b * p.prow + i), (uint32_t)r);
             }
         }
-        const int row = rb0 * 32 + i;
-        if (row < p.N) {
-            if (p.y_bf16) reinterpret_cast<uint16_t*>(p.y)[(int64_t)b * p.N + row] = f32_to_bf16_bits(v);
-            else reinterpret_cast<float*>(p.y)[(int64_t)b * p.N + row] = v;
+        return v;
+    };
+    if (p.swiglu) {
+        // SwiGLU pairs (rows 2m, 2m+1 = gate, up of unit m; the Bonsai 27B
+        // page, section "Bonsai 27B의 표현 방식"): the ranks split the pairs, one
+        // thread sums both rows of a pair and writes h = silu(g) * u.
+        const int P = R / 2;
+        const int lo = (int)((int64_t)P * q / p.Q), hi = (int)((int64_t)P * (q + 1) / p.Q);
+        for (int b = 0; b < NB; ++b)
+        for (int m = lo + threadIdx.x; m < hi; m += blockDim.x) {
+            const float g = row_sum(b, 2 * m), u = row_sum(b, 2 * m + 1);
+            const int row = rb0 * 32 + 2 * m;
+            if (row < p.N) {
+                const float h = g / (1.f + expf(-g)) * u;
+                const int64_t o = (int64_t)b * (p.N >> 1) + (row >> 1);
+                if (p.y_bf16) reinterpret_cast<uint16_t*>(p.y)[o] = f32_to_bf16_bits(h);
+                else reinterpret_cast<float*>(p.y)[o] = h;
+            }
+        }
+    } else {
+        const int lo = (int)((int64_t)R * q / p.Q), hi = (int)((int64_t)R * (q + 1) / p.Q);
+        for (int b = 0; b < NB; ++b)
+        for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+            const float v = row_sum(b, i);
+            const int row = rb0 * 32 + i;
+            if (row < p.N) {
+                if (p.y_bf16) reinterpret_cast<uint16_t*>(p.y)[(int64_t)b * p.N + row] = f32_to_bf16_bits(v);
+                else reinterpret_cast<float*>(p.y)[(int64_t)b * p.N + row] = v;
+            }
         }
     }
     cluster_sync();
@@ -507,6 +531,7 @@ cudaError_t launch_t6_chunk(const GemvArgs& a, int nb, const uint16_t* x, void* 
     prm.x = x;
     prm.y = y;
     prm.y_bf16 = a.y_bf16;
+    prm.swiglu = a.swiglu ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(pl.ncl * pl.Q));
     cfg.blockDim = dim3((unsigned)(pl.W * 32));
@@ -553,7 +578,8 @@ cudaError_t launch_gemv_t6(const GemvArgs& a) {
     const int64_t chunks = (a.B + nb - 1) / nb;
     for (int64_t i = 0, b0 = 0; i < chunks; ++i) {
         const int n = (int)(a.B / chunks + (i < a.B % chunks ? 1 : 0));
-        const cudaError_t e = launch_t6_chunk(a, n, a.x + b0 * a.K, static_cast<uint8_t*>(a.y) + b0 * a.N * ysz,
+        const int64_t yrow = a.swiglu ? a.N / 2 : a.N;    // outputs per batch row
+        const cudaError_t e = launch_t6_chunk(a, n, a.x + b0 * a.K, static_cast<uint8_t*>(a.y) + b0 * yrow * ysz,
                                               a.pdl || b0 > 0);
         if (e != cudaSuccess) return e;
         b0 += n;

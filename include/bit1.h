@@ -92,12 +92,11 @@ enum bit1_gemv_variant {
                               projections with interleaved rows (row 2n gate,
                               row 2n+1 up of hidden unit n; N even, else
                               BIT1_ESHAPE) and y receives h = silu(g) * u,
-                              [B][N/2], as BIT1_EPI_SWIGLU below.  Batch 1 on
-                              BIT1_GEMV_LUT or BIT1_GEMV_STREAM (AUTO picks
-                              LUT for K <= 13312, else STREAM); any batch on
-                              BIT1_GEMV_TC (AUTO picks it from 16 rows with
-                              the tensor cores' workspace); any other variant,
-                              or AUTO at 2-15 rows: BIT1_ESHAPE.
+                              [B][N/2], as BIT1_EPI_SWIGLU below.  Every
+                              variant but BIT1_GEMV_SIMPLE (BIT1_ESHAPE) takes
+                              it within its own shape limits; AUTO picks LUT
+                              (K <= 13312, else STREAM) at batch 1 and its
+                              usual choice otherwise.
                               bit1_gemv_ternary applies it in its combine
                               step instead (any batch, any variant). */
 

@@ -191,13 +191,16 @@ def test_swiglu_flag_checked_on_host(lib):
     f = lib.bit1_gemv_ex
     S = b1.FLAG_SWIGLU
     assert f(FAKE, FAKE, FAKE, 1, 7, 1024, FAKE, b1.F32, None, 0, 0, S, None) == b1.ESHAPE     # odd rows
-    for v in (b1.SIMPLE, b1.LUT6, b1.SPLITK):
-        assert f(FAKE, FAKE, FAKE, 1, 8, 1024, FAKE, b1.F32, None, 0, v, S, None) == b1.ESHAPE
+    assert f(FAKE, FAKE, FAKE, 1, 8, 1024, FAKE, b1.F32, None, 0, b1.SIMPLE, S, None) == b1.ESHAPE
+    for v in (b1.LUT6, b1.SPLITK):                    # the 6-bit kernels' own limit: K a multiple of 1024
+        assert f(FAKE, FAKE, FAKE, 2, 8, 1152, FAKE, b1.F32, None, 0, v, S, None) == b1.ESHAPE
     # the tensor cores take the flag at any batch, with their workspace
     assert f(FAKE, FAKE, FAKE, 1, 8, 1024, FAKE, b1.F32, None, 0, b1.TC, S, None) == b1.EINVAL
     assert f(FAKE, FAKE, FAKE, 2, 8, 1024, FAKE, b1.F32, None, 0, b1.TC, S, None) == b1.EINVAL
-    for v in (b1.AUTO, b1.LUT, b1.STREAM):                                                      # batch 1 only
+    for v in (b1.LUT, b1.STREAM):                                                               # batch 1 only
         assert f(FAKE, FAKE, FAKE, 2, 8, 1024, FAKE, b1.F32, None, 0, v, S, None) == b1.ESHAPE
+    # AUTO at 2 rows where only the warp-per-row kernel takes the shape
+    assert f(FAKE, FAKE, FAKE, 2, 8, 1152, FAKE, b1.F32, None, 0, b1.AUTO, S, None) == b1.ESHAPE
     assert f(FAKE, FAKE, FAKE, 1, 8, 1152, FAKE, b1.F32, None, 0, b1.LUT, S, None) == b1.ESHAPE
     assert f(FAKE, FAKE, FAKE, 1, 8, 1024, FAKE, b1.F32, None, 0, 0, S | 4, None) == b1.EINVAL
     g = lib.bit1_gemv_ternary                     # pairs formed in the combine: only N must be even
