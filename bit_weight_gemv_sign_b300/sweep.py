@@ -202,6 +202,9 @@ class TernarySweep(Sweep):
     one combine launch serves every matrix."""
 
     def __init__(self, mats, seed0: int = 0, y_dtype: int = BF16, device: str = "cuda"):
+        if any(m.swiglu for m in mats):
+            raise ValueError("the ternary sweep combines plain products (use bit1_gemv_ternary with "
+                             "FLAG_SWIGLU for a ternary gate/up pair)")
         super().__init__(mats, seed0=seed0, batch=1, y_dtype=y_dtype, device=device)
         self.bits_b = torch.empty_like(self.bits)
         self.row_off = []

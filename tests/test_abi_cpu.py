@@ -239,3 +239,10 @@ def test_sweep_feeds_swiglu_output_to_the_next_matrix():
         Sweep(mats, device="cpu", feed_swiglu=True, y_dtype=b1.F32)
     assert sum(m.N * m.K for m in synth.decode_chain_8b_fused()) == sum(m.N * m.K for m in synth.sweep_8b())
     assert sum(m.N * m.K for m in synth.sweep_8b_fused_mlp()) == sum(m.N * m.K for m in synth.sweep_8b())
+
+
+def test_ternary_sweep_refuses_swiglu_matrices():
+    from bit_weight_gemv_sign_b300 import synth
+    from bit_weight_gemv_sign_b300.sweep import TernarySweep
+    with pytest.raises(ValueError):
+        TernarySweep([synth.Mat("gate_up", 256, 1024, swiglu=True)], device="cpu")
