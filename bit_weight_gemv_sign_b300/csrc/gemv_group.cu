@@ -180,7 +180,22 @@ __device__ __forceinline__ void g_issue(const GProb* P, const GIter& it, uint32_
     tma_2d(st + 4096u, &pr.tm_sc, g, it.b * 32, bar);
 }
 
-template <int NB, int CG>
+// Batch 1, one 8-group slice of a 32-row block: group JJ of the slice reads
+// its 16 sign bytes at the swizzled offset (row r's chunk c lands at
+// r*128 + ((c ^ (r % 8)) * 16); `a0` is the lane's address for chunk 0 and the
+// stage is 1024-byte aligned, so chunk JJ is a0 ^ (JJ * 16)), looks them up
+// in its 22 tables and adds s_g * 2^m_g times the sum to acc.
+template <int JJ>
+__device__ __forceinline__ float g_slice1(uint32_t a0, uint32_t tg0, const uint32_t (&svw)[4],
+                                          const uint32_t (&fw)[8], float acc) {
+    const uint4 wv = lds128(a0 ^ (uint32_t)(JJ << 4));
+    const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+    const float pt = t6_groupj<JJ>(w4, tg0, std::make_index_sequence<kT6Fields>{});
+    const float sc = f16_bits_to_f32((uint16_t)(svw[JJ >> 1] >> (16 * (JJ & 1))));
+    return fmaf(pt, sc * __uint_as_float(fw[JJ]), acc);
+}
+
+template <int NB, int CG, int S>
 __device__ __forceinline__ void g_body(const uint8_t* plan) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
@@ -188,7 +203,7 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
     uint8_t* sm = smem_raw + (base - raw);
 
     const GHeader* H = reinterpret_cast<const GHeader*>(plan);
-    const int W = H->W, S = H->S, prows = H->part_rows;
+    const int W = H->W, prows = H->part_rows;   // H->S == S (the launch picks the instantiation)
     GCtx<CG> cx;
     cx.P = reinterpret_cast<const GProb*>(plan + H->probs_off);
     cx.R = reinterpret_cast<const GRange*>(plan + H->ranges_off)[blockIdx.x];
@@ -249,8 +264,11 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
     const uint32_t fac_s = base + H->off_fac;
 
     int k = 0;          // stages consumed by this warp
+    int sk = 0;         // k % S: ring slot of stage k
+    uint32_t ph = 0;    // (k / S) & 1: its mbarrier phase parity
     int kfail = -1;     // stage whose bounded wait gave up
     bool ok = true;
+    const uint32_t lane_a0 = (uint32_t)lane * 128u + ((uint32_t)(lane & 7) << 4);   // chunk 0 of row `lane`
     for (int p = cx.R.p0; p <= cx.R.p1; ++p) {
       const GProb& pr = P[p];
       const int4 pi = cx.info(p);             // RB, G, nch, N
@@ -304,29 +322,30 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
 #pragma unroll
                 for (int bb = 0; bb < NB; ++bb) acc[bb] = 0.f;
                 for (int j = 0; j < nsl; ++j, ++k) {
-                    const int s = k % S;
-                    if (ok && !mbar_wait(bars + 8u * s, (uint32_t)(k / S) & 1u)) {
+                    if (ok && !mbar_wait(bars + 8u * sk, ph)) {
                         if (lane == 0) atomicOr(&g_group_wait_timeouts, 1u);
                         ok = false;
                         kfail = k;
                     }
                     if (ok) {
-                        const uint32_t st = stages + (uint32_t)s * kGStageBytes;
+                        const uint32_t st = stages + (uint32_t)sk * kGStageBytes;
                         const uint4 sv = lds128(st + 4096u + 16u * lane);       // 8 scales of row `lane`
                         const uint32_t svw[4] = {sv.x, sv.y, sv.z, sv.w};
                         if constexpr (NB == 1) {
                             const uint4 fa = lds128(fac_s + 32u * j), fb = lds128(fac_s + 32u * j + 16u);
                             const uint32_t fw[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
-#pragma unroll
-                            for (int jj = 0; jj < 8; ++jj) {
-                                const uint32_t L = (uint32_t)lane * 128u + ((uint32_t)(jj ^ (lane & 7)) << 4);
-                                const uint4 wv = lds128(st + L);
-                                const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
-                                const float pt = t6_group(w4, tb + (uint32_t)(8 * j + jj) * kT6GroupBytes,
-                                                          std::make_index_sequence<kT6Fields>{});
-                                const float sc = f16_bits_to_f32((uint16_t)(svw[jj >> 1] >> (16 * (jj & 1))));
-                                acc[0] = fmaf(pt * sc, __uint_as_float(fw[jj]), acc[0]);
-                            }
+                            const uint32_t a0 = st + lane_a0;
+                            const uint32_t tg0 = tb + (uint32_t)(8 * j) * kT6GroupBytes;
+                            float a = acc[0];
+                            a = g_slice1<0>(a0, tg0, svw, fw, a);
+                            a = g_slice1<1>(a0, tg0, svw, fw, a);
+                            a = g_slice1<2>(a0, tg0, svw, fw, a);
+                            a = g_slice1<3>(a0, tg0, svw, fw, a);
+                            a = g_slice1<4>(a0, tg0, svw, fw, a);
+                            a = g_slice1<5>(a0, tg0, svw, fw, a);
+                            a = g_slice1<6>(a0, tg0, svw, fw, a);
+                            a = g_slice1<7>(a0, tg0, svw, fw, a);
+                            acc[0] = a;
                         } else {
                             // Several batch rows: the 16 sign bytes of a group are read
                             // once and looked up in every row's tables.
@@ -348,8 +367,12 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
                     }
                     __syncwarp();
                     if (lane == 0 && ok && !cx.done(prod))
-                        g_issue<CG>(P, prod, stages + (uint32_t)(k % S) * kGStageBytes, bars + 8u * (k % S));
+                        g_issue<CG>(P, prod, stages + (uint32_t)sk * kGStageBytes, bars + 8u * sk);
                     if (!cx.done(prod)) cx.next(prod);
+                    if (++sk == S) {
+                        sk = 0;
+                        ph ^= 1u;
+                    }
                 }
                 const int row = b * 32 + lane;
                 const int li = (b - sb) * 32 + lane;           // row within the sub-segment
@@ -395,18 +418,22 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
     }
 }
 
+// S: TMA stages per warp ring (the plan's H->S; one instantiation per value
+// the planner can choose).
+template <int S>
 __global__ void __launch_bounds__(kGWarps * 32, 1) k_gemv_group(const uint8_t* __restrict__ plan) {
-    g_body<1, g_chunk_groups(1)>(plan);
+    g_body<1, g_chunk_groups(1), S>(plan);
 }
 
 // Several batch rows per problem: at most 16 warps, so 128 registers a thread.
-template <int NB>
+template <int NB, int S>
 __global__ void __launch_bounds__(16 * 32, 1) k_gemv_group_b(const uint8_t* __restrict__ plan) {
-    g_body<NB, g_chunk_groups(NB)>(plan);
+    g_body<NB, g_chunk_groups(NB), S>(plan);
 }
 
+template <int S>
 __global__ void __launch_bounds__(kGWarps * 32, 1) k_gemv_group1(const __grid_constant__ GSingle plan) {
-    g_body<1, g_chunk_groups(1)>(reinterpret_cast<const uint8_t*>(&plan));
+    g_body<1, g_chunk_groups(1), S>(reinterpret_cast<const uint8_t*>(&plan));
 }
 
 // ---------------------------------------------------------------- host
@@ -617,13 +644,15 @@ bit1_status group_plan(const bit1_gemv_problem* problems, int count, int nb, voi
 cudaError_t launch_group(const void* device_plan, const void* host_plan, bool pdl, cudaStream_t stream) {
     const GHeader* h = static_cast<const GHeader*>(host_plan);
     const void* fn = nullptr;
+    if (h->S != 1 && h->S != 2) return cudaErrorInvalidValue;
+    const bool s2 = h->S == 2;
     switch (h->nb) {
-        case 1: fn = (const void*)k_gemv_group; break;
-        case 2: fn = (const void*)k_gemv_group_b<2>; break;
-        case 3: fn = (const void*)k_gemv_group_b<3>; break;
-        case 4: fn = (const void*)k_gemv_group_b<4>; break;
-        case 5: fn = (const void*)k_gemv_group_b<5>; break;
-        case 6: fn = (const void*)k_gemv_group_b<6>; break;
+        case 1: fn = s2 ? (const void*)k_gemv_group<2> : (const void*)k_gemv_group<1>; break;
+        case 2: fn = s2 ? (const void*)k_gemv_group_b<2, 2> : (const void*)k_gemv_group_b<2, 1>; break;
+        case 3: fn = s2 ? (const void*)k_gemv_group_b<3, 2> : (const void*)k_gemv_group_b<3, 1>; break;
+        case 4: fn = s2 ? (const void*)k_gemv_group_b<4, 2> : (const void*)k_gemv_group_b<4, 1>; break;
+        case 5: fn = s2 ? (const void*)k_gemv_group_b<5, 2> : (const void*)k_gemv_group_b<5, 1>; break;
+        case 6: fn = s2 ? (const void*)k_gemv_group_b<6, 2> : (const void*)k_gemv_group_b<6, 1>; break;
         default: return cudaErrorInvalidValue;
     }
     cudaError_t e = set_smem_attr(fn);
@@ -662,10 +691,12 @@ cudaError_t launch_gemv_group1(const GemvArgs& a) {
     single.h.probs_off = (int)offsetof(GSingle, p);
     std::memcpy(single.r, ranges.data(), ranges.size() * sizeof(GRange));
     single.p = probs[0];
-    cudaError_t e = set_smem_attr((const void*)k_gemv_group1);
+    if (single.h.S != 1 && single.h.S != 2) return cudaErrorInvalidValue;
+    const void* fn = single.h.S == 2 ? (const void*)k_gemv_group1<2> : (const void*)k_gemv_group1<1>;
+    cudaError_t e = set_smem_attr(fn);
     if (e != cudaSuccess) return e;
     void* args[] = {(void*)&single};
-    return launch((const void*)k_gemv_group1, dim3((unsigned)single.h.nctas), dim3((unsigned)(single.h.W * 32)),
+    return launch(fn, dim3((unsigned)single.h.nctas), dim3((unsigned)(single.h.W * 32)),
                   (size_t)single.h.smem_bytes, a.stream, a.pdl, args);
 }
 

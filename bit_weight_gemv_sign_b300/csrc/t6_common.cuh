@@ -140,5 +140,33 @@ __device__ __forceinline__ float t6_group(const uint32_t (&w)[4], uint32_t tg, s
     return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
+// The same lookup for group JJ of a run of consecutive groups whose tables
+// start at the 128-byte aligned address tg0: the group's offset JJ * 2816 and
+// the field's F * 128 both ride in the load's immediate, so forming the
+// address costs only the field extraction (shift, then one and-or).
+template <int F, int JJ>
+__device__ __forceinline__ unsigned short t6_ldj(const uint32_t (&w)[4], uint32_t tg0) {
+    constexpr int O = 6 * F, QW = O >> 5, S = O & 31;
+    uint32_t v;
+    if constexpr (F == 21) v = (w[3] >> 29) & 0x6u;
+    else if constexpr (S == 0) v = (w[QW] << 1) & 0x7Eu;
+    else if constexpr (S + 6 <= 32) v = (w[QW] >> (S - 1)) & 0x7Eu;
+    else v = __funnelshift_r(w[QW], w[QW + 1], S - 1) & 0x7Eu;
+    unsigned short t;
+    asm("ld.shared.b16 %0, [%1+%2];" : "=h"(t) : "r"(v | tg0), "n"(JJ * kT6GroupBytes + F * kT6TableBytes));
+    return t;
+}
+
+// Sum of the 22 entries of group JJ (relative to tg0) in two interleaved fp32
+// chains: one widening add per entry and a single add to join the chains.
+template <int JJ, size_t... F>
+__device__ __forceinline__ float t6_groupj(const uint32_t (&w)[4], uint32_t tg0, std::index_sequence<F...>) {
+    unsigned short t[sizeof...(F)];
+    ((t[F] = t6_ldj<(int)F, JJ>(w, tg0)), ...);
+    float acc[2] = {0.f, 0.f};
+    ((acc[F & 1] = t6_add(t[F], acc[F & 1])), ...);
+    return acc[0] + acc[1];
+}
+
 
 }  // namespace bit1
