@@ -1,7 +1,9 @@
 // C ABI of the bit1 library: argument validation (on the host, before any
 // CUDA call, so that a rejected call launches and modifies nothing), kernel
 // selection and launch.  Declarations and their documentation: bit1.h.
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "internal.h"
@@ -23,6 +25,26 @@ cudaError_t launch(const void* func, dim3 grid, dim3 block, size_t smem, cudaStr
         cfg.numAttrs = 1;
     }
     return cudaLaunchKernelExC(&cfg, func, args);
+}
+
+cudaError_t func_attrs(const void* fn, int smem_bytes, bool nonportable_clusters) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, int> done;   // (device, kernel) -> smem limit set
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = done.find({dev, fn});
+    if (it != done.end() && it->second >= smem_bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e == cudaSuccess && nonportable_clusters)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();     // do not leave the failure pending for the next launch
+        return e;
+    }
+    done[{dev, fn}] = smem_bytes;
+    return cudaSuccess;
 }
 
 int sm_count() {

@@ -249,14 +249,9 @@ k_gemv_lut(const uint8_t* __restrict__ bits, const uint16_t* __restrict__ scales
 
 template <int M, bool SWIGLU>
 static cudaError_t launch_lut_ms(const GemvArgs& a) {
-    static bool configured = false;  // per-instantiation attribute (idempotent, benign race)
     const size_t smem = LutCfg<M>::smem;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute((const void*)k_gemv_lut<M, SWIGLU>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    const cudaError_t e = func_attrs((const void*)k_gemv_lut<M, SWIGLU>, (int)smem, false);
+    if (e != cudaSuccess) return e;
     const int sms = sm_count();
     const int64_t units = a.swiglu ? a.N / 2 : a.N;
     const int64_t grid = units < sms ? units : sms;

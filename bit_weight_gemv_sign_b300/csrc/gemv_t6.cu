@@ -342,11 +342,7 @@ int q_candidates(int64_t G, int nb, int* out) {
     return n;
 }
 
-cudaError_t t6_set_attrs(const void* fn) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kT6MaxSmem);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    return e;
-}
+cudaError_t t6_set_attrs(const void* fn) { return func_attrs(fn, kT6MaxSmem, true); }
 
 // Clusters of size Q that can be resident at once with this kernel, block
 // size and shared memory (clusters must fit inside one GPC, so this can be
@@ -597,7 +593,9 @@ __global__ void __launch_bounds__(32, 1) k_wait_selftest(unsigned int* __restric
     if (threadIdx.x == 0) {
         mbar_init(b, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        if (!mbar_wait(b, 0u)) atomicOr(&g_bit1_wait_timeouts, 16u);
+        // A bound of its own, 2^12 polls (milliseconds), so that the test of
+        // the failure path does not hold the GPU for the kernels' 16 s bound.
+        if (!mbar_wait_polls(b, 0u, 1u << 12)) atomicOr(&g_bit1_wait_timeouts, 16u);
         *done = 1u;
     }
 }

@@ -539,15 +539,7 @@ size_t tc_smem(int Bp) {
     return std::max<size_t>(need, 120 * 1024);      // keeps a second CTA off the SM
 }
 
-void tc_set_attrs_once(cudaError_t* err) {
-    static std::once_flag once;
-    static cudaError_t e = cudaSuccess;
-    std::call_once(once, [] {
-        e = cudaFuncSetAttribute((const void*)k_gemv_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e == cudaSuccess) e = cudaFuncSetAttribute((const void*)k_gemv_tc, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    });
-    *err = e;
-}
+void tc_set_attrs(cudaError_t* err) { *err = func_attrs((const void*)k_gemv_tc, 227 * 1024, true); }
 
 // Co-resident clusters of size ks for this kernel (0 when the query fails).
 int tc_max_clusters(int ks, size_t smem) {
@@ -665,7 +657,7 @@ cudaError_t launch_gemv_tc(const GemvArgs& a) {
     auto enc = tc_encode();
     if (!enc) return cudaErrorNotSupported;
     cudaError_t e;
-    tc_set_attrs_once(&e);
+    tc_set_attrs(&e);
     if (e != cudaSuccess) return e;
     // All batch chunks in one launch pair when the scratch holds them.  Narrow
     // (64-row chunks, K split over a cluster) or wide (128-row chunks: each

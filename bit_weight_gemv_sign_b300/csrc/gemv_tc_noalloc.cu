@@ -17,12 +17,10 @@ constexpr int kNoAllocMaxDevices = 64;
 // device.
 __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-struct DeviceScratch {
-    std::once_flag once;
-    void* ptr = nullptr;
-    cudaError_t err = cudaSuccess;
-};
-DeviceScratch g_scratch[kNoAllocMaxDevices];
+// The scratch's device address, per device: set once obtained; a failed
+// lookup is not remembered, so a later call on that device tries again.
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kNoAllocMaxDevices] = {};
 
 }  // namespace
 }  // namespace bit1
@@ -39,9 +37,19 @@ extern "C" bit1_status bit1_gemv_tc_noalloc(const uint8_t* bits, const uint16_t*
     if (need == 0 || need > kNoAllocScratchBytes) return BIT1_ESHAPE;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return BIT1_ECUDA;
-    DeviceScratch& d = g_scratch[dev];
-    std::call_once(d.once, [&d] { d.err = cudaGetSymbolAddress(&d.ptr, g_noalloc_scratch); });
-    if (d.err != cudaSuccess || d.ptr == nullptr) return BIT1_ECUDA;
-    return bit1_gemv_ex(bits, scales, x, B, N, K, y, y_dtype, d.ptr, kNoAllocScratchBytes, BIT1_GEMV_TC, flags,
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_scratch_mu);
+        if (!g_scratch_ptr[dev]) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+                (void)cudaGetLastError();     // leave no pending error behind
+                return BIT1_ECUDA;
+            }
+            g_scratch_ptr[dev] = p;
+        }
+        scratch = g_scratch_ptr[dev];
+    }
+    return bit1_gemv_ex(bits, scales, x, B, N, K, y, y_dtype, scratch, kNoAllocScratchBytes, BIT1_GEMV_TC, flags,
                         stream);
 }

@@ -23,6 +23,12 @@ struct GemvArgs {
     bool swiglu = false; // rows are (gate, up) pairs; y is h = silu(gate) * up, [B][N/2]
 };
 
+// Raise a kernel's dynamic shared-memory limit to smem_bytes (and allow
+// non-portable cluster sizes when asked) on the current device.  Function
+// attributes are per device, so this runs once per (device, kernel); a
+// failure is returned and retried on the next call.
+cudaError_t func_attrs(const void* fn, int smem_bytes, bool nonportable_clusters);
+
 // Launch helper: grid/block/smem with optional PDL attribute.
 cudaError_t launch(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                    bool pdl, void** args);

@@ -263,13 +263,8 @@ cudaError_t launch_gemv_t5lut(const uint8_t* packed, const uint16_t* scales, con
     prm.off_acc = off;    off += (uint32_t)(prm.bpc * 32 * 4);
     const size_t smem = 128 + (size_t)off;
     if (smem > 227 * 1024) return cudaErrorNotSupported;
-    static bool attr_set = false;
-    if (!attr_set) {
-        const cudaError_t e = cudaFuncSetAttribute((const void*)k_gemv_t5lut,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    const cudaError_t e = func_attrs((const void*)k_gemv_t5lut, 227 * 1024, false);
+    if (e != cudaSuccess) return e;
     void* args[] = {(void*)&prm};
     return launch((const void*)k_gemv_t5lut, dim3((unsigned)grid), dim3(kL5Threads), smem, stream, false, args);
 }

@@ -23,9 +23,10 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-// Bounded wait on an mbarrier phase: false if it did not complete in time.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < (1u << 22); ++i) {
+// Bounded wait on an mbarrier phase: false if it did not complete within
+// `polls` suspending try_waits.
+__device__ __forceinline__ bool mbar_wait_polls(uint32_t bar, uint32_t parity, uint32_t polls) {
+    for (uint32_t i = 0; i < polls; ++i) {
         uint32_t done;
         asm volatile("{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p;}"
                      : "=r"(done) : "r"(bar), "r"(parity) : "memory");
@@ -33,9 +34,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     }
     return false;
 }
+// The kernels' bound: 2^22 polls (about 16 s on B300), far beyond any copy.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    return mbar_wait_polls(bar, parity, 1u << 22);
+}
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
                  ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar) : "memory");
+}
+// Prefetch a 2-D tensor tile into L2 (no shared memory, no completion): a
+// later tma_2d of the same tile then finds it in L2.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 ::"l"(map), "r"(c0), "r"(c1) : "memory");
 }
 // 1-D bulk copy global -> shared, completion on an mbarrier (sizes and both
 // addresses multiples of 16 bytes).

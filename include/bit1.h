@@ -255,8 +255,9 @@ bit1_status bit1_xor_patch(uint8_t *bits, int64_t N, int64_t K,
 unsigned int bit1_device_wait_timeouts(void);
 
 /* Self-test of that failure path: launches one kernel whose bounded wait is
- * on a barrier that nothing completes.  The wait gives up after its limit
- * (2^22 polls of a suspending try_wait: about 16 s on B300), the kernel
+ * on a barrier that nothing completes.  The wait gives up after a short limit
+ * of its own (2^12 polls of a suspending try_wait: milliseconds on B300; the
+ * product kernels allow 2^22 polls, about 16 s), the kernel
  * records the event (the next bit1_device_wait_timeouts() is nonzero),
  * writes 1 to the device uint32 *d_done and exits normally; the context
  * stays usable.  No fault, trap or hang is involved.  BIT1_EINVAL on a null
@@ -266,16 +267,19 @@ bit1_status bit1_selftest_wait_timeout(unsigned int *d_done, bit1_stream_t strea
 /* ------------------------------------------------------------------------
  * bit1_gemv_tc_noalloc -- the tensor-core batched product (bit1_gemv_ex with
  * variant BIT1_GEMV_TC) without a caller workspace.  The pages have no
- * counterpart of this call; it exists for callers that cannot allocate
- * device memory around the product: code that runs while a CUDA graph is
- * being captured (cudaMalloc is not permitted during capture), real-time
- * paths that must not enter an allocator, and plain C hosts that have no
- * device allocator of their own to size a workspace with.
- *   Scratch: one file-scope device array of BIT1_NOALLOC_SCRATCH_BYTES per
- *   device (the kernel stages at most 64 batch rows of K fp16 activations
- *   plus 256 bytes per launch, so any B with K <= 32768 fits).  Its address
- *   is taken with cudaGetSymbolAddress once per device, on the first call
- *   on that device: make that first call before any stream capture.
+ * counterpart of this call.  It is for callers that cannot allocate device
+ * memory around the product: real-time paths that must not enter an
+ * allocator (cudaMalloc can block and synchronise the device), and plain C
+ * hosts that have no device allocator of their own to size a workspace with.
+ *   Scratch: one file-scope device array of BIT1_NOALLOC_SCRATCH_BYTES,
+ *   which every GPU that loads the library holds until the process exits.
+ *   A batch whose fp16 activations fit in it whole (2 * B * K bytes plus 256
+ *   per 64-row chunk, e.g. B = 512 at K = 4096) is staged at once; a larger
+ *   one is staged one 64-row chunk at a time, each chunk reusing the array,
+ *   so any B with K <= 32768 fits.  Its address is taken with
+ *   cudaGetSymbolAddress once per device, on the first call on that device
+ *   (a failed lookup is tried again on the next call): make that first call
+ *   before any stream capture.
  *   Races: every call on a device uses the same scratch, so two calls whose
  *   kernels overlap on the GPU (different streams, or different host threads
  *   without ordering) corrupt each other's results; keep such calls ordered,

@@ -32,7 +32,7 @@ def test_bounded_wait_gives_up_and_the_context_survives(orc):
     seconds = time.perf_counter() - t0
     assert int(done.item()) == 1                    # the kernel ran to its end
     assert b1.bit1_device_wait_timeouts() & 16      # and recorded the timeout
-    assert seconds < 30, seconds
+    assert seconds < 2, seconds                     # the self-test's own short bound
     print(f"bounded wait gave up after {seconds:.3f} s")
     N, K = 512, 4096
     bits, scales = synth.matrix(N, K, 4242)
