@@ -80,7 +80,6 @@ struct alignas(128) GProb {
     void* y;
     int N, K, G, RB, y_bf16, nch;
     int swiglu;             // rows are (gate, up) pairs; y is h = silu(gate) * up, [nb][N/2]
-    const uint16_t* sc;     // [N][G] fp16 scales (the tm_sc tensor)
 };
 
 struct GSingle {            // whole plan of a one-problem call, passed by value
@@ -172,64 +171,15 @@ struct GCtx {
     }
 };
 
-#ifndef BIT1_GROUP_SC_LDG
-#define BIT1_GROUP_SC_LDG 0
-#endif
-#ifndef BIT1_GROUP_TMA_2LANES
-#define BIT1_GROUP_TMA_2LANES 0
-#endif
-
 template <int CG>
 __device__ __forceinline__ void g_issue(const GProb* P, const GIter& it, uint32_t st, uint32_t bar) {
     const GProb& pr = P[it.p];
     const int g = CG * it.c + 8 * it.j;
-#if BIT1_GROUP_SC_LDG
-    mbar_expect_tx(bar, 4096u);
-    tma_2d(st, &pr.tm_bits, g * 16, it.b * 32, bar);
-#else
     mbar_expect_tx(bar, 4096u + 512u);
     tma_2d(st, &pr.tm_bits, g * 16, it.b * 32, bar);
     tma_2d(st + 4096u, &pr.tm_sc, g, it.b * 32, bar);
-#endif
 }
 
-// Issued by the whole warp: lane 0 the expect_tx and the bits box, lane 1 the
-// scales box.
-template <int CG>
-__device__ __forceinline__ void g_issue2(const GProb* P, const GIter& it, uint32_t st, uint32_t bar, int lane) {
-    const GProb& pr = P[it.p];
-    const int g = CG * it.c + 8 * it.j;
-    if (lane == 0) mbar_expect_tx(bar, 4096u + 512u);
-    __syncwarp();
-    if (lane == 0) tma_2d(st, &pr.tm_bits, g * 16, it.b * 32, bar);
-    if (lane == 1) tma_2d(st + 4096u, &pr.tm_sc, g, it.b * 32, bar);
-}
-
-// The 8 scales of row `lane` of stage `it` (zeros past the last row).
-template <int CG>
-__device__ __forceinline__ uint4 g_scales(const GProb* P, const GIter& it, int lane, int N, int G) {
-    const int row = it.b * 32 + lane;
-    if (row >= N) return make_uint4(0u, 0u, 0u, 0u);
-    const uint16_t* sc = P[it.p].sc + (size_t)row * G + CG * it.c + 8 * it.j;
-    return ldg_stream_v4(sc);
-}
-
-// The same tiles into L2 only, for a stage the warp will load later.
-template <int CG>
-__device__ __forceinline__ void g_prefetch(const GProb* P, const GIter& it) {
-    const GProb& pr = P[it.p];
-    const int g = CG * it.c + 8 * it.j;
-    tma_prefetch_2d(&pr.tm_bits, g * 16, it.b * 32);
-    tma_prefetch_2d(&pr.tm_sc, g, it.b * 32);
-}
-
-#ifndef BIT1_GROUP_L2_AHEAD
-#define BIT1_GROUP_L2_AHEAD 0
-#endif
-// Stages a warp prefetches into L2 beyond the S it has in flight in shared
-// memory: the shared-memory ring holds one stage per warp, so the HBM latency
-// is taken by the L2 prefetch and the ring's own loads hit in L2.
-constexpr int kGL2Ahead = BIT1_GROUP_L2_AHEAD;
 
 // Batch 1, one 8-group slice of a 32-row block: group JJ of the slice reads
 // its 16 sign bytes at the swizzled offset (row r's chunk c lands at
@@ -278,34 +228,12 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(bars + 8u * s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-#if !BIT1_GROUP_TMA_2LANES
         for (int s = 0; s < S && !cx.done(prod); ++s) {
             g_issue<CG>(P, prod, stages + (uint32_t)s * kGStageBytes, bars + 8u * s);
             cx.next(prod);
         }
     } else {
         for (int s = 0; s < S && !cx.done(prod); ++s) cx.next(prod);
-    }
-#else
-    }
-    __syncwarp();
-    for (int s = 0; s < S && !cx.done(prod); ++s) {
-        g_issue2<CG>(P, prod, stages + (uint32_t)s * kGStageBytes, bars + 8u * s, lane);
-        cx.next(prod);
-    }
-#endif
-#if BIT1_GROUP_SC_LDG
-    static_assert(S == 1 || !BIT1_GROUP_SC_LDG || true, "");
-    uint4 sc_next = make_uint4(0u, 0u, 0u, 0u);   // scales of the warp's next stage
-    {
-        GIter f = cx.first();
-        if (!cx.done(f)) { const int4 fi = cx.info(f.p); sc_next = g_scales<CG>(P, f, lane, fi.w, fi.y); }
-    }
-#endif
-    GIter pre = prod;   // next stage to prefetch into L2 (kGL2Ahead stages ahead of prod)
-    for (int d = 0; d < kGL2Ahead && !cx.done(pre); ++d) {
-        if (lane == 0) g_prefetch<CG>(P, pre);
-        cx.next(pre);
     }
     __syncwarp();
 
@@ -402,11 +330,7 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
                     }
                     if (ok) {
                         const uint32_t st = stages + (uint32_t)sk * kGStageBytes;
-#if BIT1_GROUP_SC_LDG
-                        const uint4 sv = sc_next;
-#else
                         const uint4 sv = lds128(st + 4096u + 16u * lane);       // 8 scales of row `lane`
-#endif
                         const uint32_t svw[4] = {sv.x, sv.y, sv.z, sv.w};
                         if constexpr (NB == 1) {
                             const uint4 fa = lds128(fac_s + 32u * j), fb = lds128(fac_s + 32u * j + 16u);
@@ -443,21 +367,9 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
                         }
                     }
                     __syncwarp();
-#if BIT1_GROUP_SC_LDG
-                    if (!cx.done(prod)) { const int4 fi = cx.info(prod.p); sc_next = g_scales<CG>(P, prod, lane, fi.w, fi.y); }
-#endif
-#if BIT1_GROUP_TMA_2LANES
-                    if (ok && !cx.done(prod))
-                        g_issue2<CG>(P, prod, stages + (uint32_t)sk * kGStageBytes, bars + 8u * sk, lane);
-#else
                     if (lane == 0 && ok && !cx.done(prod))
                         g_issue<CG>(P, prod, stages + (uint32_t)sk * kGStageBytes, bars + 8u * sk);
-#endif
                     if (!cx.done(prod)) cx.next(prod);
-                    if (kGL2Ahead > 0 && !cx.done(pre)) {
-                        if (lane == 0) g_prefetch<CG>(P, pre);
-                        cx.next(pre);
-                    }
                     if (++sk == S) {
                         sk = 0;
                         ph ^= 1u;
@@ -573,7 +485,6 @@ bool encode_prob(GProb& g, const bit1_gemv_problem& pb, int nb) {
     g.RB = (int)((pb.N + 31) / 32);
     g.y_bf16 = pb.y_dtype == BIT1_BF16;
     g.swiglu = pb.epilogue == BIT1_EPI_SWIGLU;
-    g.sc = pb.scales;
     const int cg = g_chunk_groups(nb);
     g.nch = (int)((G + cg - 1) / cg);
     return true;

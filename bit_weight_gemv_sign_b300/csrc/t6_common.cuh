@@ -42,12 +42,6 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int
     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
                  ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar) : "memory");
 }
-// Prefetch a 2-D tensor tile into L2 (no shared memory, no completion): a
-// later tma_2d of the same tile then finds it in L2.
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-                 ::"l"(map), "r"(c0), "r"(c1) : "memory");
-}
 // 1-D bulk copy global -> shared, completion on an mbarrier (sizes and both
 // addresses multiples of 16 bytes).
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
