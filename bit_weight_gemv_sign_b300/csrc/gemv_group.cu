@@ -89,17 +89,31 @@ struct GSingle {            // whole plan of a one-problem call, passed by value
 };
 
 // ---------------------------------------------------------------- device
+// A CTA's work is a sequence of phases: for each problem p of its range, the
+// blocks [bs(p), be(p)), cut into sub-segments of at most mb(p) blocks (only
+// problems with more than one K chunk are cut: their row partials live in
+// shared memory between chunks); per sub-segment, chunk by chunk.  The tables
+// of a phase are built by the whole CTA between two barriers, so a warp that
+// runs out of work in a phase waits for the slowest one.  Within a phase of
+// n blocks, warp w therefore takes blocks w, w + W, ... of the first
+// q = floor(n / W) * W only (every warp the same count); with TAIL the
+// r = n - qW blocks left over are cut into their 8-group slices and those
+// r * nsl single-slice units go to the warps in turn (unit u to warp u % W),
+// so the imbalance at the phase's end is at most one slice instead of one
+// block.  The units' partial sums are added in slice order afterwards (a
+// fixed order: results do not depend on timing).  Without TAIL (several
+// batch rows, whose unit partials would not fit) warp w takes every W-th
+// block of the phase.
 struct GIter {               // position in one warp's sequence of stages
-    int p, sb, c, b, j;      // problem, sub-segment start block, chunk, block, slice
-    int nsl;                 // slices of chunk c of problem p
+    int p, sb, c;            // phase: problem, sub-segment start block, chunk
+    int b, j;                // stage: block and 8-group slice
+    int k, nk;               // this warp's stage index within the phase, and its stage count
+    int nsl, q, kf;          // slices per block of the chunk; full blocks per warp; q * nsl
+    int g0;                  // first group of the chunk
+    const CUtensorMap* tm;   // the problem's bits tensor map (its scales map follows it)
 };
 
-// A CTA's work: for each problem p of its range, the blocks [bs(p), be(p)),
-// cut into sub-segments of at most mb(p) blocks (only problems with more than
-// one K chunk are cut: their row partials live in shared memory between
-// chunks); per sub-segment, chunk by chunk; per chunk, this warp's blocks
-// (every W-th); per block, the chunk's 8-group slices.
-template <int CG>
+template <int CG, bool TAIL>
 struct GCtx {
     const GProb* P;
     const int4* I;          // shared memory: {RB, G, nch, N} of problems R.p0.. (index p - R.p0)
@@ -115,29 +129,11 @@ struct GCtx {
         const int cg = min(CG, info(p).y - CG * c);
         return cg >> 3;
     }
-    __device__ __forceinline__ bool done(const GIter& it) const { return it.p > R.p1; }
-    // Move to the first valid stage at or after `it` (a block of this warp).
-    __device__ __forceinline__ void settle(GIter& it) const {
-        while (it.p <= R.p1) {
-            if (it.sb < be(it.p) && it.b < se(it.p, it.sb)) {
-                it.nsl = slices(it.p, it.c);
-                return;
-            }
-            if (it.sb < be(it.p) && ++it.c < nch(it.p)) {
-                it.b = it.sb + w;              // next chunk, same sub-segment
-            } else if (it.sb < be(it.p) && (it.sb += mb(it.p)) < be(it.p)) {
-                it.c = 0;                      // next sub-segment
-                it.b = it.sb + w;
-            } else {
-                ++it.p;                        // next problem
-                if (it.p > R.p1) return;
-                it.sb = bs(it.p);
-                it.c = 0;
-                it.b = it.sb + w;
-            }
-            it.j = 0;
-        }
+    // Full blocks of warp w in a phase of n blocks.
+    __device__ __forceinline__ int full_blocks(int n) const {
+        return TAIL ? n / W : (w < n ? (n - 1 - w) / W + 1 : 0);
     }
+    __device__ __forceinline__ bool done(const GIter& it) const { return it.p > R.p1; }
     // CTA-level phases (problem, sub-segment, chunk), in execution order.
     __device__ __forceinline__ bool next_phase(int& p, int& sb, int& c) const {
         if (++c < nch(p)) return true;
@@ -158,26 +154,92 @@ struct GCtx {
         }
         return false;
     }
+    // This warp's stage count in phase (it.p, it.sb, it.c).
+    __device__ __forceinline__ void enter(GIter& it) const {
+        const int n = se(it.p, it.sb) - it.sb;
+        it.g0 = CG * it.c;
+        it.tm = &P[it.p].tm_bits;
+        it.nsl = slices(it.p, it.c);
+        it.q = full_blocks(n);
+        it.k = 0;
+        it.kf = it.q * it.nsl;
+        it.nk = it.kf;
+        if (TAIL) {
+            const int nu = (n - it.q * W) * it.nsl;
+            if (w < nu) it.nk += (nu - 1 - w) / W + 1;
+        }
+    }
+    // Block and slice of stage it.k of the phase (from scratch; next() steps
+    // through the full blocks incrementally).
+    __device__ __forceinline__ void pos(GIter& it) const {
+        if (it.k < it.kf) {
+            const int i = it.k / it.nsl;
+            it.j = it.k - i * it.nsl;
+            it.b = it.sb + w + W * i;
+        } else {
+            const int u = w + W * (it.k - it.kf);
+            const int i = u / it.nsl;
+            it.j = u - i * it.nsl;
+            it.b = it.sb + it.q * W + i;
+        }
+    }
+    // Move to the first stage at or after `it` (a later phase if this one is used up).
+    __device__ __forceinline__ void settle(GIter& it) const {
+        while (it.k >= it.nk) {
+            if (!next_phase(it.p, it.sb, it.c)) {
+                it.p = R.p1 + 1;
+                return;
+            }
+            enter(it);
+        }
+        pos(it);
+    }
     __device__ __forceinline__ GIter first() const {
-        GIter it{R.p0, bs(R.p0), 0, bs(R.p0) + w, 0, 0};
+        GIter it{};
+        if (!first_phase(it.p, it.sb, it.c)) {
+            it.p = R.p1 + 1;
+            return it;
+        }
+        enter(it);
         settle(it);
         return it;
     }
     __device__ __forceinline__ void next(GIter& it) const {
-        if (++it.j < it.nsl) return;
-        it.j = 0;
-        it.b += W;
+        ++it.k;
+        if (it.k < it.kf) {                 // the common case: the next slice of a full block
+            if (++it.j == it.nsl) {
+                it.j = 0;
+                it.b += W;
+            }
+            return;
+        }
         settle(it);
     }
 };
 
-template <int CG>
-__device__ __forceinline__ void g_issue(const GProb* P, const GIter& it, uint32_t st, uint32_t bar) {
-    const GProb& pr = P[it.p];
-    const int g = CG * it.c + 8 * it.j;
+static_assert(offsetof(GProb, tm_sc) == offsetof(GProb, tm_bits) + sizeof(CUtensorMap), "maps adjacent");
+
+__device__ __forceinline__ void g_issue(const GIter& it, uint32_t st, uint32_t bar) {
+    const int g = it.g0 + 8 * it.j;
     mbar_expect_tx(bar, 4096u + 512u);
-    tma_2d(st, &pr.tm_bits, g * 16, it.b * 32, bar);
-    tma_2d(st + 4096u, &pr.tm_sc, g, it.b * 32, bar);
+    tma_2d(st, it.tm, g * 16, it.b * 32, bar);
+    tma_2d(st + 4096u, it.tm + 1, g, it.b * 32, bar);
+}
+
+// The same, executed by the whole warp and carried out by the lanes whose
+// `on` is set (one lane): a predicated block instead of a divergent branch
+// around the copies, which cost the warp a reconvergence on every stage.
+__device__ __forceinline__ void g_issue_pred(const GIter& it, uint32_t st, uint32_t bar, bool on) {
+    const int g = it.g0 + 8 * it.j;
+    asm volatile("{ .reg .pred p; setp.ne.u32 p, %0, 0;\n\t"
+                 "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%1], 4608;\n\t"
+                 "@p cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%2], [%3, {%4, %5}], [%1];\n\t"
+                 "@p cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%6], [%7, {%8, %5}], [%1]; }"
+                 ::"r"(on ? 1u : 0u), "r"(bar), "r"(st), "l"(it.tm), "r"(g * 16), "r"(it.b * 32), "r"(st + 4096u),
+                   "l"(it.tm + 1), "r"(g)
+                 : "memory");
 }
 
 
@@ -205,7 +267,8 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
 
     const GHeader* H = reinterpret_cast<const GHeader*>(plan);
     const int W = H->W, prows = H->part_rows;   // H->S == S (the launch picks the instantiation)
-    GCtx<CG> cx;
+    constexpr bool TAIL = NB == 1;
+    GCtx<CG, TAIL> cx;
     cx.P = reinterpret_cast<const GProb*>(plan + H->probs_off);
     cx.R = reinterpret_cast<const GRange*>(plan + H->ranges_off)[blockIdx.x];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -229,7 +292,7 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
         for (int s = 0; s < S; ++s) mbar_init(bars + 8u * s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         for (int s = 0; s < S && !cx.done(prod); ++s) {
-            g_issue<CG>(P, prod, stages + (uint32_t)s * kGStageBytes, bars + 8u * s);
+            g_issue(prod, stages + (uint32_t)s * kGStageBytes, bars + 8u * s);
             cx.next(prod);
         }
     } else {
@@ -260,6 +323,7 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
     const uint16_t* xr = reinterpret_cast<const uint16_t*>(sm + H->off_xraw);
     float* fac = reinterpret_cast<float*>(sm + H->off_fac);
     float* part = reinterpret_cast<float*>(sm + H->off_part);
+    float* upart = part + NB * prows;          // TAIL: partial sums of the single-slice units
     uint8_t* tabs = sm + H->off_tables;
     const uint32_t tb = base + H->off_tables;
     const uint32_t fac_s = base + H->off_fac;
@@ -303,11 +367,31 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
                 }
             }
             __syncthreads();
-            for (int t = threadIdx.x; t < NB * cg * kT6Fields * 4; t += blockDim.x) {
-                const int tt = t >> 2, bg = tt / kT6Fields, f = tt - bg * kT6Fields;
-                const int b = bg / cg, g = bg - b * cg;
-                t6_build_pair(tabs + (b * CG + g) * kT6GroupBytes + f * kT6TableBytes, xr + (b * CG + g) * 128,
-                              fac[b * 2 * CG + CG + g], f, t & 3, tt & 1);
+            if constexpr (NB == 1) {
+                // Table tt = (group g, field f) with tt = 22 g + f; thread t builds a
+                // quarter of table t / 4.  The block's threads step tt by
+                // blockDim.x / 4 (a multiple of 4), so (g, f) advance by a fixed
+                // amount: no division per table.
+                const int step = (int)blockDim.x >> 2, sg = step / kT6Fields, sf = step - sg * kT6Fields;
+                int tt = (int)threadIdx.x >> 2;
+                int g = tt / kT6Fields, f = tt - g * kT6Fields;
+                for (; g < cg; tt += step) {
+                    t6_build_pair(tabs + g * kT6GroupBytes + f * kT6TableBytes, xr + g * 128, fac[CG + g], f,
+                                  threadIdx.x & 3, tt & 1);
+                    g += sg;
+                    f += sf;
+                    if (f >= kT6Fields) {
+                        f -= kT6Fields;
+                        ++g;
+                    }
+                }
+            } else {
+                for (int t = threadIdx.x; t < NB * cg * kT6Fields * 4; t += blockDim.x) {
+                    const int tt = t >> 2, bg = tt / kT6Fields, f = tt - bg * kT6Fields;
+                    const int b = bg / cg, g = bg - b * cg;
+                    t6_build_pair(tabs + (b * CG + g) * kT6GroupBytes + f * kT6TableBytes, xr + (b * CG + g) * 128,
+                                  fac[b * 2 * CG + CG + g], f, t & 3, tt & 1);
+                }
             }
             __syncthreads();
             if (threadIdx.x == 0) {                            // raw x consumed: fetch the next phase's
@@ -316,65 +400,71 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
             }
             if (p == cx.R.p0 && sb == cx.bs(p) && c == 0) pdl_launch_dependents();
 
-            // --- this warp's blocks of the sub-segment, for chunk c
+            // --- this warp's work of the phase: stages (block, slice) in the
+            // order the warp's ring was filled (GCtx::pos)
             const int nsl = cg >> 3;
-            for (int b = sb + warp; b < be; b += W) {
-                float acc[NB];
+            // One stage: wait for its copy, add its 8 groups to acc, refill the
+            // ring slot with the warp's next stage.
+            auto consume = [&](int j, float (&acc)[NB]) {
+                if (ok && !mbar_wait(bars + 8u * sk, ph)) {
+                    if (lane == 0) atomicOr(&g_group_wait_timeouts, 1u);
+                    ok = false;
+                    kfail = k;
+                }
+                // Computed even after a failed wait (the launch is then already
+                // flagged; every table address stays inside the tables), so the
+                // stage path has no branch around it.
+                {
+                    const uint32_t st = stages + (uint32_t)sk * kGStageBytes;
+                    const uint4 sv = lds128(st + 4096u + 16u * lane);       // 8 scales of row `lane`
+                    const uint32_t svw[4] = {sv.x, sv.y, sv.z, sv.w};
+                    if constexpr (NB == 1) {
+                        const uint4 fa = lds128(fac_s + 32u * j), fb = lds128(fac_s + 32u * j + 16u);
+                        const uint32_t fw[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+                        const uint32_t a0 = st + lane_a0;
+                        const uint32_t tg0 = tb + (uint32_t)(8 * j) * kT6GroupBytes;
+                        float a = acc[0];
+                        a = g_slice1<0>(a0, tg0, svw, fw, a);
+                        a = g_slice1<1>(a0, tg0, svw, fw, a);
+                        a = g_slice1<2>(a0, tg0, svw, fw, a);
+                        a = g_slice1<3>(a0, tg0, svw, fw, a);
+                        a = g_slice1<4>(a0, tg0, svw, fw, a);
+                        a = g_slice1<5>(a0, tg0, svw, fw, a);
+                        a = g_slice1<6>(a0, tg0, svw, fw, a);
+                        a = g_slice1<7>(a0, tg0, svw, fw, a);
+                        acc[0] = a;
+                    } else {
+                        // Several batch rows: the 16 sign bytes of a group are read
+                        // once and looked up in every row's tables.
 #pragma unroll
-                for (int bb = 0; bb < NB; ++bb) acc[bb] = 0.f;
-                for (int j = 0; j < nsl; ++j, ++k) {
-                    if (ok && !mbar_wait(bars + 8u * sk, ph)) {
-                        if (lane == 0) atomicOr(&g_group_wait_timeouts, 1u);
-                        ok = false;
-                        kfail = k;
-                    }
-                    if (ok) {
-                        const uint32_t st = stages + (uint32_t)sk * kGStageBytes;
-                        const uint4 sv = lds128(st + 4096u + 16u * lane);       // 8 scales of row `lane`
-                        const uint32_t svw[4] = {sv.x, sv.y, sv.z, sv.w};
-                        if constexpr (NB == 1) {
-                            const uint4 fa = lds128(fac_s + 32u * j), fb = lds128(fac_s + 32u * j + 16u);
-                            const uint32_t fw[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
-                            const uint32_t a0 = st + lane_a0;
-                            const uint32_t tg0 = tb + (uint32_t)(8 * j) * kT6GroupBytes;
-                            float a = acc[0];
-                            a = g_slice1<0>(a0, tg0, svw, fw, a);
-                            a = g_slice1<1>(a0, tg0, svw, fw, a);
-                            a = g_slice1<2>(a0, tg0, svw, fw, a);
-                            a = g_slice1<3>(a0, tg0, svw, fw, a);
-                            a = g_slice1<4>(a0, tg0, svw, fw, a);
-                            a = g_slice1<5>(a0, tg0, svw, fw, a);
-                            a = g_slice1<6>(a0, tg0, svw, fw, a);
-                            a = g_slice1<7>(a0, tg0, svw, fw, a);
-                            acc[0] = a;
-                        } else {
-                            // Several batch rows: the 16 sign bytes of a group are read
-                            // once and looked up in every row's tables.
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const uint32_t L = (uint32_t)lane * 128u + ((uint32_t)(jj ^ (lane & 7)) << 4);
+                            const uint4 wv = lds128(st + L);
+                            const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+                            const float sc = f16_bits_to_f32((uint16_t)(svw[jj >> 1] >> (16 * (jj & 1))));
 #pragma unroll
-                            for (int jj = 0; jj < 8; ++jj) {
-                                const uint32_t L = (uint32_t)lane * 128u + ((uint32_t)(jj ^ (lane & 7)) << 4);
-                                const uint4 wv = lds128(st + L);
-                                const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
-                                const float sc = f16_bits_to_f32((uint16_t)(svw[jj >> 1] >> (16 * (jj & 1))));
-#pragma unroll
-                                for (int bb = 0; bb < NB; ++bb) {
-                                    const int g = bb * CG + 8 * j + jj;
-                                    const float pt = t6_group(w4, tb + (uint32_t)g * kT6GroupBytes,
-                                                              std::make_index_sequence<kT6Fields>{});
-                                    acc[bb] = fmaf(pt * sc, fac[bb * 2 * CG + 8 * j + jj], acc[bb]);
-                                }
+                            for (int bb = 0; bb < NB; ++bb) {
+                                const int g = bb * CG + 8 * j + jj;
+                                const float pt = t6_group(w4, tb + (uint32_t)g * kT6GroupBytes,
+                                                          std::make_index_sequence<kT6Fields>{});
+                                acc[bb] = fmaf(pt * sc, fac[bb * 2 * CG + 8 * j + jj], acc[bb]);
                             }
                         }
                     }
-                    __syncwarp();
-                    if (lane == 0 && ok && !cx.done(prod))
-                        g_issue<CG>(P, prod, stages + (uint32_t)sk * kGStageBytes, bars + 8u * sk);
-                    if (!cx.done(prod)) cx.next(prod);
-                    if (++sk == S) {
-                        sk = 0;
-                        ph ^= 1u;
-                    }
                 }
+                __syncwarp();
+                g_issue_pred(prod, stages + (uint32_t)sk * kGStageBytes, bars + 8u * sk,
+                             lane == 0 && ok && !cx.done(prod));
+                if (!cx.done(prod)) cx.next(prod);
+                ++k;
+                if (++sk == S) {
+                    sk = 0;
+                    ph ^= 1u;
+                }
+            };
+            // Block b's sums for chunk c: carried in `part` to the next chunk,
+            // or, after the last chunk, through the epilogue into y.
+            auto finish = [&](int b, float (&acc)[NB]) {
                 const int row = b * 32 + lane;
                 const int li = (b - sb) * 32 + lane;           // row within the sub-segment
                 if (pi.z > 1) {
@@ -384,7 +474,7 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
                         acc[bb] = (c == 0) ? acc[bb] : part[pl] + acc[bb];
                         if (c + 1 < pi.z) part[pl] = acc[bb];
                     }
-                    if (c + 1 < pi.z) continue;
+                    if (c + 1 < pi.z) return;
                 }
                 if (pr.swiglu) {
                     // Lane 2m holds the gate row and lane 2m+1 the up row of hidden
@@ -406,6 +496,33 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
                         const int64_t o = (int64_t)bb * pi.w + row;
                         if (pr.y_bf16) reinterpret_cast<uint16_t*>(pr.y)[o] = f32_to_bf16_bits(acc[bb]);
                         else reinterpret_cast<float*>(pr.y)[o] = acc[bb];
+                    }
+                }
+            };
+            const int n = be - sb;
+            const int q = cx.full_blocks(n);
+            for (int i = 0; i < q; ++i) {
+                float acc[NB];
+#pragma unroll
+                for (int bb = 0; bb < NB; ++bb) acc[bb] = 0.f;
+                for (int j = 0; j < nsl; ++j) consume(j, acc);
+                finish(sb + warp + W * i, acc);
+            }
+            if constexpr (TAIL) {
+                // The r blocks left over, one slice per unit; then, after a
+                // barrier, each block's unit partials in slice order.
+                const int r = n - q * W, nu = r * nsl;
+                if (nu > 0) {
+                    for (int u = warp; u < nu; u += W) {
+                        float acc[1] = {0.f};
+                        consume(u - (u / nsl) * nsl, acc);
+                        upart[u * 32 + lane] = acc[0];
+                    }
+                    __syncthreads();
+                    for (int i = warp; i < r; i += W) {
+                        float acc[1] = {0.f};
+                        for (int j = 0; j < nsl; ++j) acc[0] += upart[(i * nsl + j) * 32 + lane];
+                        finish(sb + q * W + i, acc);
                     }
                 }
             }
@@ -494,12 +611,21 @@ bool encode_prob(GProb& g, const bit1_gemv_problem& pb, int nb) {
 // CTA's time: a block costs K (its bytes are proportional to K; its lookups
 // to K times the batch rows) and every table build (first block of a problem
 // in the CTA, and every seg-th block of a problem with several K chunks)
-// costs kGBuildCost per chunk, scaled by the chunk's tables (nb * CG groups
-// against 32 at batch 1).  A
-// greedy pass packs blocks in order under a per-CTA budget; a binary search
-// finds the smallest budget that fits in nctas CTAs.  Then the shared memory
-// layout; false if it does not fit.
-constexpr double kGBuildCost = 6.0 * 4096;    // one chunk build ~ six 4096-wide blocks (measured)
+// costs phase_cost() per chunk.  A greedy pass packs blocks in order under a
+// per-CTA budget; a binary search finds the smallest budget that fits in
+// nctas CTAs.  Then the shared memory layout; false if it does not fit.
+// Batch 1, fitted on one B300 so that CTA finishing times do not grow with
+// their phase count (8B- and 27B-class sweeps): a phase costs about six
+// 4096-wide blocks plus six more for a full chunk of tables.
+constexpr double kGBuildCost = 6.0 * 4096;    // several rows: one chunk build ~ six 4096-wide blocks (measured)
+constexpr double kGPhaseFixed = 6.0 * 4096;   // batch 1: a phase's barriers, activations, prescales
+constexpr double kGPhaseTables = 6.0 * 4096;  // batch 1: building a full chunk's tables (32 groups)
+
+// Cost of the table builds of one pass over all K chunks of problem p.
+double phase_cost(const GProb& pr, int nb) {
+    if (nb > 1) return kGBuildCost * pr.nch * (nb * g_chunk_groups(nb) / 32.0);
+    return kGPhaseFixed * pr.nch + kGPhaseTables * (double)pr.G / g_chunk_groups(1);
+}
 
 int partition(const std::vector<GProb>& probs, double T, std::vector<GRange>* out, int nb) {
     const int n = (int)probs.size();
@@ -511,7 +637,7 @@ int partition(const std::vector<GProb>& probs, double T, std::vector<GRange>* ou
     for (int p = 0; p < n; ++p) {
         int taken = 0;
         const double c = (double)probs[p].K * rowf;
-        const double build = kGBuildCost * probs[p].nch * (nb * g_chunk_groups(nb) / 32.0);
+        const double build = phase_cost(probs[p], nb);
         for (int b = 0; b < probs[p].RB; ++b) {
             double add = c;
             if (taken == 0 || (probs[p].nch > 1 && taken % seg == 0)) add += build;
@@ -537,8 +663,8 @@ bool plan_layout(const std::vector<GProb>& probs, int nctas, int nb, GHeader& h,
     const double rowf = 1.0 + 0.8 * (nb - 1);
     double total = 0.0;
     for (int p = 0; p < n; ++p)
-        total += (double)probs[p].RB * probs[p].K * rowf + kGBuildCost * probs[p].nch * (nb * CG / 32.0);
-    double lo = total / nctas, hi = total + kGBuildCost * nb * 8;
+        total += (double)probs[p].RB * probs[p].K * rowf + phase_cost(probs[p], nb);
+    double lo = total / nctas, hi = total + (kGBuildCost + kGPhaseFixed + kGPhaseTables) * nb * 8;
     for (int it = 0; it < 60 && hi - lo > 1e-4 * lo; ++it) {
         const double mid = 0.5 * (lo + hi);
         if (partition(probs, mid, nullptr, nb) <= nctas) hi = mid;
@@ -576,6 +702,7 @@ bool plan_layout(const std::vector<GProb>& probs, int nctas, int nb, GHeader& h,
             const uint32_t off_xraw = off;    off += nb * CG * 128 * 2;
             const uint32_t off_pinfo = off;   off += kGMaxProbsPerCta * 16;
             const uint32_t off_part = off;    off += (uint32_t)(part_rows * nb) * 4;
+            if (nb == 1) off += (uint32_t)((W - 1) * (CG / 8) * 32) * 4;   // unit partials (see GCtx)
             off = (off + 7u) & ~7u;
             const uint32_t off_bars = off;    off += W * S * 8 + 8;
             const size_t smem = 1024 + (size_t)off;
