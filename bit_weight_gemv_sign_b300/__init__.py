@@ -21,6 +21,7 @@ __all__ = [
     "bit1_xor_patch", "bit1_status_str", "bit1_version", "bit1_device_wait_timeouts",
     "bit1_group_plan_bytes", "bit1_group_plan", "bit1_gemv_group", "GroupPlan",
     "library_path", "load", "bit1_gemv_tc_noalloc",
+    "LAYOUT_CANONICAL", "LAYOUT_G128X", "bit1_repack_g128x", "bit1_unpack_g128x",
     "bit1_ternary_planes", "bit1_gemv_ternary", "bit1_gemv_ternary_workspace_bytes",
     "bit1_gemv_ternary_launches", "bit1_ternary_combine",
     "bit1_t5_pack", "bit1_t5_to_planes", "bit1_gemv_t5", "bit1_gemv_t5_launches",
@@ -33,6 +34,7 @@ AUTO, SIMPLE, LUT, SPLITK, TC, LUT6, STREAM = 0, 1, 2, 3, 4, 5, 6
 FLAG_PDL = 1
 FLAG_SWIGLU = 2
 EPI_NONE, EPI_SWIGLU = 0, 1
+LAYOUT_CANONICAL, LAYOUT_G128X = 0, 1
 
 class _Problem(ctypes.Structure):
     _fields_ = [("bits", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("x", ctypes.c_void_p),
@@ -98,6 +100,12 @@ def load():
         lib.bit1_group_plan.restype = i32
         lib.bit1_group_plan_batched.argtypes = [ctypes.POINTER(_Problem), i32, i32, p, sz]
         lib.bit1_group_plan_batched.restype = i32
+        lib.bit1_group_plan_ex.argtypes = [ctypes.POINTER(_Problem), i32, i32, i32, p, sz]
+        lib.bit1_group_plan_ex.restype = i32
+        lib.bit1_repack_g128x.argtypes = [p, i64, i64, p, p]
+        lib.bit1_repack_g128x.restype = i32
+        lib.bit1_unpack_g128x.argtypes = [p, i64, i64, p, p]
+        lib.bit1_unpack_g128x.restype = i32
         lib.bit1_gemv_group.argtypes = [p, p, ctypes.c_uint, p]
         lib.bit1_gemv_group.restype = i32
         lib.bit1_gemv_tc_noalloc.argtypes = [p, p, p, i64, i64, i64, p, i32, ctypes.c_uint, p]
@@ -286,11 +294,13 @@ def bit1_group_plan_bytes(count: int) -> int:
     return int(load().bit1_group_plan_bytes(int(count)))
 
 
-def bit1_group_plan(problems, host_plan_ptr: int, plan_bytes: int, B: int = 1) -> None:
+def bit1_group_plan(problems, host_plan_ptr: int, plan_bytes: int, B: int = 1,
+                    layout: int = LAYOUT_CANONICAL) -> None:
     """problems: sequence of (bits, scales, x, y) or (bits, scales, x, y,
     epilogue) CUDA tensors; x is [B, K] (or [K] at B = 1) bf16 and y [B, N]
     ([B, N/2] with EPI_SWIGLU, the rows then interleaved gate/up pairs).
-    B > 1 calls bit1_group_plan_batched."""
+    B > 1 calls bit1_group_plan_batched; a non-canonical ``layout`` (every
+    problem's bits converted with bit1_repack_g128x) bit1_group_plan_ex."""
     import torch
     arr = (_Problem * len(problems))()
     for i, pr in enumerate(problems):
@@ -300,11 +310,38 @@ def bit1_group_plan(problems, host_plan_ptr: int, plan_bytes: int, B: int = 1) -
             raise TypeError("y must be float32 or bfloat16")
         arr[i] = _Problem(_dptr(bits, "bits"), _dptr(scales, "scales"), _dptr(x, "x"), _dptr(y, "y"),
                           bits.shape[0], x.shape[-1], BF16 if y.dtype == torch.bfloat16 else F32, epi)
-    if B == 1:
+    if layout != LAYOUT_CANONICAL:
+        st = load().bit1_group_plan_ex(arr, len(problems), int(B), int(layout), host_plan_ptr, plan_bytes)
+    elif B == 1:
         st = load().bit1_group_plan(arr, len(problems), host_plan_ptr, plan_bytes)
     else:
         st = load().bit1_group_plan_batched(arr, len(problems), int(B), host_plan_ptr, plan_bytes)
     _check(st, "bit1_group_plan")
+
+
+def bit1_repack_g128x(bits, out=None, stream=None, N=None, K=None):
+    """Sign bits uint8 [N, K/8] (CUDA, canonical layout) -> the g128x layout
+    (``out`` may be ``bits`` itself: converted in place).  Returns out."""
+    import torch
+    N = bits.shape[0] if N is None else N
+    K = bits.shape[-1] * 8 if K is None else K
+    if out is None:
+        out = torch.empty_like(bits)
+    _check(load().bit1_repack_g128x(_dptr(bits, "bits"), N, K, _dptr(out, "out"), _stream(stream)),
+           "bit1_repack_g128x")
+    return out
+
+
+def bit1_unpack_g128x(bits, out=None, stream=None, N=None, K=None):
+    """The inverse of bit1_repack_g128x."""
+    import torch
+    N = bits.shape[0] if N is None else N
+    K = bits.shape[-1] * 8 if K is None else K
+    if out is None:
+        out = torch.empty_like(bits)
+    _check(load().bit1_unpack_g128x(_dptr(bits, "bits"), N, K, _dptr(out, "out"), _stream(stream)),
+           "bit1_unpack_g128x")
+    return out
 
 
 def bit1_gemv_group(device_plan_ptr: int, host_plan_ptr: int, flags: int = 0, stream=None) -> None:
@@ -317,7 +354,7 @@ class GroupPlan:
     128-byte aligned).  The tensors named in ``problems`` must stay alive and
     in place while the plan is used."""
 
-    def __init__(self, problems, device="cuda", B: int = 1):
+    def __init__(self, problems, device="cuda", B: int = 1, layout: int = LAYOUT_CANONICAL):
         import numpy as np
         import torch
         self.problems = list(problems)
@@ -326,7 +363,8 @@ class GroupPlan:
         self._host_raw = np.zeros(self.nbytes + 128, dtype=np.uint8)
         off = (-self._host_raw.ctypes.data) % 128
         self.host = self._host_raw[off: off + self.nbytes]
-        bit1_group_plan(self.problems, self.host.ctypes.data, self.nbytes, self.B)
+        self.layout = int(layout)
+        bit1_group_plan(self.problems, self.host.ctypes.data, self.nbytes, self.B, self.layout)
         self._dev_raw = torch.empty(self.nbytes + 128, dtype=torch.uint8, device=device)
         doff = (-self._dev_raw.data_ptr()) % 128
         self.dev = self._dev_raw[doff: doff + self.nbytes]

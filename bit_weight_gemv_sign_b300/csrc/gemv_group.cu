@@ -57,7 +57,7 @@ __host__ __device__ constexpr int g_chunk_groups(int nb) { return nb == 1 ? 32 :
 // partials stay at about 16 KB.
 __host__ __device__ constexpr int g_seg_blocks(int nb) { return nb == 1 ? 128 : nb == 2 ? 64 : nb <= 4 ? 32 : 16; }
 
-struct GHeader {            // 64 bytes
+struct GHeader {            // 128 bytes
     int count, nctas, W, S;
     uint32_t off_tables;
     int nb;                 // batch rows: x is [nb][K], y is [nb][N] for every problem
@@ -66,8 +66,10 @@ struct GHeader {            // 64 bytes
     int seg_blocks;         // row blocks per sub-segment of a problem with K > 4096
     uint32_t off_xraw;      // raw bf16 activations of the next phase (bulk copy target)
     uint32_t off_pinfo;     // per-problem {RB, G, nch, N} of the CTA's range
+    int layout;             // sign-bit layout of every problem (kLayoutCanonical or kLayoutG128x)
+    int pad[15];
 };
-static_assert(sizeof(GHeader) == 64, "header size");
+static_assert(sizeof(GHeader) == 128, "header size");
 
 struct GRange {             // blocks from (p0, b0) up to, not including, (p1, b1)
     int p0, b0, p1, b1;
@@ -248,17 +250,17 @@ __device__ __forceinline__ void g_issue_pred(const GIter& it, uint32_t st, uint3
 // r*128 + ((c ^ (r % 8)) * 16); `a0` is the lane's address for chunk 0 and the
 // stage is 1024-byte aligned, so chunk JJ is a0 ^ (JJ * 16)), looks them up
 // in its 22 tables and adds s_g * 2^m_g times the sum to acc.
-template <int JJ>
+template <int L, int JJ>
 __device__ __forceinline__ float g_slice1(uint32_t a0, uint32_t tg0, const uint32_t (&svw)[4],
                                           const uint32_t (&fw)[8], float acc) {
     const uint4 wv = lds128(a0 ^ (uint32_t)(JJ << 4));
     const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
-    const float pt = t6_groupj<JJ>(w4, tg0, std::make_index_sequence<kT6Fields>{});
+    const float pt = t6_groupj<L, JJ>(w4, tg0, std::make_index_sequence<kT6Fields>{});
     const float sc = f16_bits_to_f32((uint16_t)(svw[JJ >> 1] >> (16 * (JJ & 1))));
     return fmaf(pt, sc * __uint_as_float(fw[JJ]), acc);
 }
 
-template <int NB, int CG, int S>
+template <int NB, int CG, int S, int L>
 __device__ __forceinline__ void g_body(const uint8_t* plan) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
@@ -424,29 +426,29 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
                         const uint32_t a0 = st + lane_a0;
                         const uint32_t tg0 = tb + (uint32_t)(8 * j) * kT6GroupBytes;
                         float a = acc[0];
-                        a = g_slice1<0>(a0, tg0, svw, fw, a);
-                        a = g_slice1<1>(a0, tg0, svw, fw, a);
-                        a = g_slice1<2>(a0, tg0, svw, fw, a);
-                        a = g_slice1<3>(a0, tg0, svw, fw, a);
-                        a = g_slice1<4>(a0, tg0, svw, fw, a);
-                        a = g_slice1<5>(a0, tg0, svw, fw, a);
-                        a = g_slice1<6>(a0, tg0, svw, fw, a);
-                        a = g_slice1<7>(a0, tg0, svw, fw, a);
+                        a = g_slice1<L, 0>(a0, tg0, svw, fw, a);
+                        a = g_slice1<L, 1>(a0, tg0, svw, fw, a);
+                        a = g_slice1<L, 2>(a0, tg0, svw, fw, a);
+                        a = g_slice1<L, 3>(a0, tg0, svw, fw, a);
+                        a = g_slice1<L, 4>(a0, tg0, svw, fw, a);
+                        a = g_slice1<L, 5>(a0, tg0, svw, fw, a);
+                        a = g_slice1<L, 6>(a0, tg0, svw, fw, a);
+                        a = g_slice1<L, 7>(a0, tg0, svw, fw, a);
                         acc[0] = a;
                     } else {
                         // Several batch rows: the 16 sign bytes of a group are read
                         // once and looked up in every row's tables.
 #pragma unroll
                         for (int jj = 0; jj < 8; ++jj) {
-                            const uint32_t L = (uint32_t)lane * 128u + ((uint32_t)(jj ^ (lane & 7)) << 4);
-                            const uint4 wv = lds128(st + L);
+                            const uint32_t la = (uint32_t)lane * 128u + ((uint32_t)(jj ^ (lane & 7)) << 4);
+                            const uint4 wv = lds128(st + la);
                             const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
                             const float sc = f16_bits_to_f32((uint16_t)(svw[jj >> 1] >> (16 * (jj & 1))));
 #pragma unroll
                             for (int bb = 0; bb < NB; ++bb) {
                                 const int g = bb * CG + 8 * j + jj;
-                                const float pt = t6_group(w4, tb + (uint32_t)g * kT6GroupBytes,
-                                                          std::make_index_sequence<kT6Fields>{});
+                                const float pt = T6GroupL<L>::run(w4, tb + (uint32_t)g * kT6GroupBytes,
+                                                                  std::make_index_sequence<kT6Fields>{});
                                 acc[bb] = fmaf(pt * sc, fac[bb * 2 * CG + 8 * j + jj], acc[bb]);
                             }
                         }
@@ -536,22 +538,22 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
     }
 }
 
-// S: TMA stages per warp ring (the plan's H->S; one instantiation per value
-// the planner can choose).
-template <int S>
+// S: TMA stages per warp ring (the plan's H->S); L: the sign-bit layout (the
+// plan's H->layout).  One instantiation per value the planner can choose.
+template <int S, int L>
 __global__ void __launch_bounds__(kGWarps * 32, 1) k_gemv_group(const uint8_t* __restrict__ plan) {
-    g_body<1, g_chunk_groups(1), S>(plan);
+    g_body<1, g_chunk_groups(1), S, L>(plan);
 }
 
 // Several batch rows per problem: at most 16 warps, so 128 registers a thread.
-template <int NB, int S>
+template <int NB, int S, int L>
 __global__ void __launch_bounds__(16 * 32, 1) k_gemv_group_b(const uint8_t* __restrict__ plan) {
-    g_body<NB, g_chunk_groups(NB), S>(plan);
+    g_body<NB, g_chunk_groups(NB), S, L>(plan);
 }
 
 template <int S>
 __global__ void __launch_bounds__(kGWarps * 32, 1) k_gemv_group1(const __grid_constant__ GSingle plan) {
-    g_body<1, g_chunk_groups(1), S>(reinterpret_cast<const uint8_t*>(&plan));
+    g_body<1, g_chunk_groups(1), S, kLayoutCanonical>(reinterpret_cast<const uint8_t*>(&plan));
 }
 
 // ---------------------------------------------------------------- host
@@ -739,14 +741,16 @@ cudaError_t set_smem_attr(const void* f) {
 
 size_t group_plan_bytes(int count) {
     if (count < 1) return 0;
-    const size_t ranges = 64 + (size_t)kGMaxCtas * sizeof(GRange);
+    const size_t ranges = sizeof(GHeader) + (size_t)kGMaxCtas * sizeof(GRange);
     const size_t probs_off = (ranges + 127) & ~(size_t)127;
     return probs_off + (size_t)count * sizeof(GProb);
 }
 
-bit1_status group_plan(const bit1_gemv_problem* problems, int count, int nb, void* host_plan, size_t bytes) {
+bit1_status group_plan(const bit1_gemv_problem* problems, int count, int nb, int layout, void* host_plan,
+                       size_t bytes) {
     if (count < 1 || !problems || !host_plan) return BIT1_EINVAL;
     if (nb < 1 || nb > kGMaxNB) return BIT1_ESHAPE;
+    if (layout != kLayoutCanonical && layout != kLayoutG128x) return BIT1_EINVAL;
     if (bytes < group_plan_bytes(count) || ((uintptr_t)host_plan & 127)) return BIT1_EINVAL;
     for (int i = 0; i < count; ++i)
         if (!problem_ok(problems[i])) return BIT1_ESHAPE;
@@ -757,7 +761,8 @@ bit1_status group_plan(const bit1_gemv_problem* problems, int count, int nb, voi
     std::vector<GRange> ranges;
     const int nctas = std::min(sm_count(), kGMaxCtas);
     if (!plan_layout(probs, nctas, nb, h, ranges)) return BIT1_ESHAPE;
-    const size_t r_off = 64;
+    h.layout = layout;
+    const size_t r_off = sizeof(GHeader);
     const size_t p_off = (r_off + (size_t)kGMaxCtas * sizeof(GRange) + 127) & ~(size_t)127;
     h.ranges_off = (int)r_off;
     h.probs_off = (int)p_off;
@@ -769,20 +774,28 @@ bit1_status group_plan(const bit1_gemv_problem* problems, int count, int nb, voi
     return BIT1_OK;
 }
 
+template <int L>
+const void* group_kernel_s(int nb, bool s2) {
+    switch (nb) {
+        case 1: return s2 ? (const void*)k_gemv_group<2, L> : (const void*)k_gemv_group<1, L>;
+        case 2: return s2 ? (const void*)k_gemv_group_b<2, 2, L> : (const void*)k_gemv_group_b<2, 1, L>;
+        case 3: return s2 ? (const void*)k_gemv_group_b<3, 2, L> : (const void*)k_gemv_group_b<3, 1, L>;
+        case 4: return s2 ? (const void*)k_gemv_group_b<4, 2, L> : (const void*)k_gemv_group_b<4, 1, L>;
+        case 5: return s2 ? (const void*)k_gemv_group_b<5, 2, L> : (const void*)k_gemv_group_b<5, 1, L>;
+        case 6: return s2 ? (const void*)k_gemv_group_b<6, 2, L> : (const void*)k_gemv_group_b<6, 1, L>;
+        default: return nullptr;
+    }
+}
+template <int L>
+const void* group_kernel(int nb, int S) { return group_kernel_s<L>(nb, S == 2); }
+
 cudaError_t launch_group(const void* device_plan, const void* host_plan, bool pdl, cudaStream_t stream) {
     const GHeader* h = static_cast<const GHeader*>(host_plan);
-    const void* fn = nullptr;
     if (h->S != 1 && h->S != 2) return cudaErrorInvalidValue;
-    const bool s2 = h->S == 2;
-    switch (h->nb) {
-        case 1: fn = s2 ? (const void*)k_gemv_group<2> : (const void*)k_gemv_group<1>; break;
-        case 2: fn = s2 ? (const void*)k_gemv_group_b<2, 2> : (const void*)k_gemv_group_b<2, 1>; break;
-        case 3: fn = s2 ? (const void*)k_gemv_group_b<3, 2> : (const void*)k_gemv_group_b<3, 1>; break;
-        case 4: fn = s2 ? (const void*)k_gemv_group_b<4, 2> : (const void*)k_gemv_group_b<4, 1>; break;
-        case 5: fn = s2 ? (const void*)k_gemv_group_b<5, 2> : (const void*)k_gemv_group_b<5, 1>; break;
-        case 6: fn = s2 ? (const void*)k_gemv_group_b<6, 2> : (const void*)k_gemv_group_b<6, 1>; break;
-        default: return cudaErrorInvalidValue;
-    }
+    if (h->layout != kLayoutCanonical && h->layout != kLayoutG128x) return cudaErrorInvalidValue;
+    const void* fn = h->layout == kLayoutG128x ? group_kernel<kLayoutG128x>(h->nb, h->S)
+                                               : group_kernel<kLayoutCanonical>(h->nb, h->S);
+    if (!fn) return cudaErrorInvalidValue;
     cudaError_t e = set_smem_attr(fn);
     if (e != cudaSuccess) return e;
     const uint8_t* dp = static_cast<const uint8_t*>(device_plan);

@@ -36,6 +36,10 @@ cudaError_t launch(const void* func, dim3 grid, dim3 block, size_t smem, cudaStr
 cudaError_t launch_pack(const void* w, int dtype, int64_t N, int64_t K, uint8_t* bits,
                         uint16_t* scales, uint32_t* flags, cudaStream_t stream);
 
+// Sign bits between the canonical and the g128x layout (layout.cu); in == out allowed.
+cudaError_t launch_relayout(const uint8_t* in, uint8_t* out, int64_t N, int64_t K, bool to_g128x,
+                            cudaStream_t stream);
+
 cudaError_t launch_xor_patch(uint8_t* bits, int64_t N, int64_t K, const int32_t* rows,
                              int64_t n_rows, cudaStream_t stream);
 
@@ -59,7 +63,8 @@ cudaError_t launch_wait_selftest(unsigned int* d_done, cudaStream_t stream);
 
 // Grouped persistent kernel (gemv_group.cu).
 size_t group_plan_bytes(int count);
-bit1_status group_plan(const bit1_gemv_problem* problems, int count, int nb, void* host_plan, size_t bytes);
+bit1_status group_plan(const bit1_gemv_problem* problems, int count, int nb, int layout, void* host_plan,
+                       size_t bytes);
 cudaError_t launch_group(const void* device_plan, const void* host_plan, bool pdl, cudaStream_t stream);
 bool group1_supported(int64_t B, int64_t N, int64_t K);
 cudaError_t launch_gemv_group1(const GemvArgs& a);

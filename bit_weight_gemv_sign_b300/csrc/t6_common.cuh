@@ -145,33 +145,84 @@ __device__ __forceinline__ float t6_group(const uint32_t (&w)[4], uint32_t tg, s
     return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
-// The same lookup for group JJ of a run of consecutive groups whose tables
-// start at the 128-byte aligned address tg0: the group's offset JJ * 2816 and
-// the field's F * 128 both ride in the load's immediate, so forming the
-// address costs only the field extraction (shift, then one and-or).
-template <int F, int JJ>
-__device__ __forceinline__ unsigned short t6_ldj(const uint32_t (&w)[4], uint32_t tg0) {
+// ---------------------------------------------------------------- layouts
+// Sign bits of a 128-input group as stored in memory: 16 bytes = 4 words.
+//  * Layout 0 (canonical): input k of the group is bit k % 32 of word k / 32
+//    (row-major, least significant bit first).  Field F (inputs 6F..6F+5) is
+//    extracted with a shift and a mask.
+//  * Layout 1 ("g128x", a permutation of the bits within each group, so that
+//    a whole-row XOR still flips exactly that row): words 0-2 hold fields
+//    0..11 at bits 1-6 of their bytes (field F in byte F of the 12; input
+//    6F + i at bit 8F + 1 + i), and bits 0 and 7 of those 12 bytes hold the
+//    24 inputs of fields 12..15: input 72 + 6j + i (j = 0..3, i = 0..5) sits
+//    in word i / 2, at bit 7 of byte j if i is even, else at bit 0 of byte
+//    (j + 1) % 4.  Word 3 is as in layout 0 (fields 16..20 and the last two
+//    inputs).  Then one mask per word and one byte permute per field give
+//    fields 0..11, three rotations and three and-ors gather fields 12..15
+//    into the bytes of one word (rotating word q right by 6 - 2q brings its
+//    bit 7 of byte j and bit 0 of byte j + 1 to bits 8j + 1 + 2q and 8j + 2 + 2q),
+//    and a byte permute gives each of them: 37 integer operations per group
+//    instead of 44.  The fields cover the same inputs as in layout 0, so the
+//    tables are the same.
+constexpr int kLayoutCanonical = BIT1_LAYOUT_CANONICAL;
+constexpr int kLayoutG128x = BIT1_LAYOUT_G128X;
+
+// Field F of group w[0..3] in layout L, times 2 (the byte offset of its fp16
+// entry), in the low byte of a copy of tg0 (a 256-byte aligned table base).
+template <int L, int F>
+__device__ __forceinline__ uint32_t t6_addr(const uint32_t (&w)[4], uint32_t tg0) {
     constexpr int O = 6 * F, QW = O >> 5, S = O & 31;
-    uint32_t v;
-    if constexpr (F == 21) v = (w[3] >> 29) & 0x6u;
-    else if constexpr (S == 0) v = (w[QW] << 1) & 0x7Eu;
-    else if constexpr (S + 6 <= 32) v = (w[QW] >> (S - 1)) & 0x7Eu;
-    else v = __funnelshift_r(w[QW], w[QW + 1], S - 1) & 0x7Eu;
+    if constexpr (L == kLayoutG128x && F < 12) {
+        const uint32_t m = w[F >> 2] & 0x7E7E7E7Eu;                     // shared by four fields
+        return __byte_perm(m, tg0, 0x7650u | (uint32_t)(F & 3));
+    } else if constexpr (L == kLayoutG128x && F < 16) {
+        const uint32_t v = (__funnelshift_r(w[0], w[0], 6) & 0x06060606u) |
+                           (__funnelshift_r(w[1], w[1], 4) & 0x18181818u) |
+                           (__funnelshift_r(w[2], w[2], 2) & 0x60606060u);   // shared by four fields
+        return __byte_perm(v, tg0, 0x7650u | (uint32_t)(F - 12));
+    } else {
+        uint32_t v;
+        if constexpr (F == 21) v = (w[3] >> 29) & 0x6u;
+        else if constexpr (S == 0) v = (w[QW] << 1) & 0x7Eu;
+        else if constexpr (S + 6 <= 32) v = (w[QW] >> (S - 1)) & 0x7Eu;
+        else v = __funnelshift_r(w[QW], w[QW + 1], S - 1) & 0x7Eu;
+        return v | tg0;
+    }
+}
+
+// The lookup for group JJ of a run of consecutive groups whose tables start
+// at the 256-byte aligned address tg0: the group's offset JJ * 2816 and the
+// field's F * 128 both ride in the load's immediate, so forming the address
+// costs only the field extraction.
+template <int L, int F, int JJ>
+__device__ __forceinline__ unsigned short t6_ldj(const uint32_t (&w)[4], uint32_t tg0) {
     unsigned short t;
-    asm("ld.shared.b16 %0, [%1+%2];" : "=h"(t) : "r"(v | tg0), "n"(JJ * kT6GroupBytes + F * kT6TableBytes));
+    asm("ld.shared.b16 %0, [%1+%2];" : "=h"(t) : "r"(t6_addr<L, F>(w, tg0)), "n"(JJ * kT6GroupBytes + F * kT6TableBytes));
     return t;
 }
 
 // Sum of the 22 entries of group JJ (relative to tg0) in two interleaved fp32
 // chains: one widening add per entry and a single add to join the chains.
-template <int JJ, size_t... F>
+template <int L, int JJ, size_t... F>
 __device__ __forceinline__ float t6_groupj(const uint32_t (&w)[4], uint32_t tg0, std::index_sequence<F...>) {
     unsigned short t[sizeof...(F)];
-    ((t[F] = t6_ldj<(int)F, JJ>(w, tg0)), ...);
+    ((t[F] = t6_ldj<L, (int)F, JJ>(w, tg0)), ...);
     float acc[2] = {0.f, 0.f};
     ((acc[F & 1] = t6_add(t[F], acc[F & 1])), ...);
     return acc[0] + acc[1];
 }
 
+// Layout-aware form of t6_group (tg: the group's 256-byte aligned tables).
+template <int L>
+struct T6GroupL {
+    template <size_t... F>
+    static __device__ __forceinline__ float run(const uint32_t (&w)[4], uint32_t tg, std::index_sequence<F...>) {
+        unsigned short t[sizeof...(F)];
+        ((t[F] = t6_ldj<L, (int)F, 0>(w, tg)), ...);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        ((acc[F & 3] = t6_add(t[F], acc[F & 3])), ...);
+        return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    }
+};
 
 }  // namespace bit1

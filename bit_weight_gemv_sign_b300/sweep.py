@@ -18,8 +18,9 @@ import numpy as np
 import torch
 
 from . import synth
-from . import (BF16, F32, FLAG_PDL, FLAG_SWIGLU, AUTO, EPI_NONE, EPI_SWIGLU, GroupPlan, bit1_gemv_ex,
-               bit1_gemv_launches, bit1_ternary_combine, bit1_xor_patch)
+from . import (BF16, F32, FLAG_PDL, FLAG_SWIGLU, AUTO, EPI_NONE, EPI_SWIGLU, LAYOUT_CANONICAL, LAYOUT_G128X,
+               GroupPlan, bit1_gemv_ex, bit1_gemv_launches, bit1_repack_g128x, bit1_unpack_g128x, bit1_ternary_combine,
+               bit1_xor_patch)
 
 
 def _align(n: int, a: int = 256) -> int:
@@ -151,6 +152,27 @@ class Sweep:
     def replay(self):
         self.graph.replay()
 
+    def to_g128x(self):
+        """Convert every matrix's bits to the g128x layout in place (for
+        grouped launches built with layout=LAYOUT_G128X; the per-matrix
+        calls read the canonical layout).  Row patches apply unchanged."""
+        for i in range(len(self.mats)):
+            b = self.bits_of(i)
+            bit1_repack_g128x(b, out=b)
+        torch.cuda.synchronize()
+        self.layout = LAYOUT_G128X
+        return self
+
+    def to_canonical(self):
+        """The inverse of to_g128x (for the per-matrix calls)."""
+        if getattr(self, "layout", LAYOUT_CANONICAL) == LAYOUT_G128X:
+            for i in range(len(self.mats)):
+                b = self.bits_of(i)
+                bit1_unpack_g128x(b, out=b)
+            torch.cuda.synchronize()
+        self.layout = LAYOUT_CANONICAL
+        return self
+
     def group_plan(self, x=None, y=None):
         """One grouped launch over every matrix of the sweep (each with its own
         input, ``batch`` rows of it): the plan is built once; run() is one
@@ -161,7 +183,7 @@ class Sweep:
             raise ValueError("a grouped launch runs its problems concurrently: no x may be another's y")
         probs = [(self.bits_of(i), self.scales_of(i), self.x_of(i, x), self.y_of(i, y),
                   EPI_SWIGLU if m.swiglu else EPI_NONE) for i, m in enumerate(self.mats)]
-        return GroupPlan(probs, device=self.device, B=self.B)
+        return GroupPlan(probs, device=self.device, B=self.B, layout=getattr(self, "layout", LAYOUT_CANONICAL))
 
     def apply_patch(self, entries, proj_count: int = 7):
         """Apply (or, applied again, remove) a list of (layer, projection, row)

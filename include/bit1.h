@@ -228,9 +228,47 @@ bit1_status bit1_group_plan(const bit1_gemv_problem *problems, int count,
  * the same bit1_gemv_group call. */
 bit1_status bit1_group_plan_batched(const bit1_gemv_problem *problems, int count,
                                     int B, void *host_plan, size_t plan_bytes);
+/* The same with an explicit sign-bit layout shared by every problem of the
+ * plan: BIT1_LAYOUT_CANONICAL (the layout above; bit1_group_plan and
+ * bit1_group_plan_batched) or BIT1_LAYOUT_G128X (bits converted with
+ * bit1_repack_g128x, below).  1 <= B <= 6.  BIT1_EINVAL for another layout
+ * value; otherwise as bit1_group_plan_batched.  Results do not depend on the
+ * layout: each field of six inputs is looked up in the same table either
+ * way, only its position in the 16 bytes of the group differs. */
+#define BIT1_LAYOUT_CANONICAL 0
+#define BIT1_LAYOUT_G128X     1
+bit1_status bit1_group_plan_ex(const bit1_gemv_problem *problems, int count, int B,
+                               int layout, void *host_plan, size_t plan_bytes);
+
 /* flags: BIT1_FLAG_PDL or 0. */
 bit1_status bit1_gemv_group(const void *device_plan, const void *host_plan,
                             unsigned flags, bit1_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * bit1_repack_g128x / bit1_unpack_g128x -- convert packed sign bits between
+ * the canonical layout and the g128x layout, a fixed permutation of the 128
+ * bits of every group (the pages fix no bit layout beyond "packed 1-bit";
+ * this one is this library's, chosen for the cost of reading it):
+ *   input k of a group (0 <= k < 128), canonical bit k, is stored at
+ *     k <  72:  bit 8*(k/6) + 1 + k%6                 (bits 1-6 of bytes 0..11)
+ *     k <  96:  j = (k-72)/6, i = (k-72)%6, in word i/2 (bytes 4*(i/2)..),
+ *               bit 7 of byte j if i is even, else bit 0 of byte (j+1)%4
+ *     k >= 96:  bit k                                  (word 3 unchanged)
+ * (bit b of the group is bit b%8 of byte b/8).  The grouped kernel then forms
+ * each lookup index of bytes 0..11 with one byte permute instead of a shift
+ * and a mask.  Rows keep their own bits, so bit1_xor_patch flips the same
+ * rows in either layout and applying it commutes with the conversion; the
+ * scales are not touched.  Only plans built with BIT1_LAYOUT_G128X read the
+ * g128x layout; every other call takes the canonical one.
+ *   bits : device [N][K/8] in the source layout; out: device [N][K/8] (may
+ *          be bits itself: converted in place).  16-byte aligned.
+ * BIT1_ESHAPE for K not a multiple of 128 (or N, K < 1); BIT1_EINVAL for a
+ * null or misaligned pointer.  Asynchronous on `stream`.  Allocates nothing.
+ */
+bit1_status bit1_repack_g128x(const uint8_t *bits, int64_t N, int64_t K, uint8_t *out,
+                              bit1_stream_t stream);
+bit1_status bit1_unpack_g128x(const uint8_t *bits, int64_t N, int64_t K, uint8_t *out,
+                              bit1_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * bit1_xor_patch -- the Bankai row-wise sign-flip patch, in place.

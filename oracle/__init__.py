@@ -84,6 +84,10 @@ def configure(lib):
     lib.orc_xor_patch.argtypes = [p, i64, i64, p, i64]
     lib.orc_xor_patch.restype = ctypes.c_int
     lib.orc_pack.argtypes = [p, ctypes.c_int, i64, i64, p, p]
+    lib.orc_g128x_repack.argtypes = [p, i64, i64, p]
+    lib.orc_g128x_repack.restype = ctypes.c_int
+    lib.orc_g128x_unpack.argtypes = [p, i64, i64, p]
+    lib.orc_g128x_unpack.restype = ctypes.c_int
     lib.orc_pack.restype = ctypes.c_int
     return lib
 
@@ -305,6 +309,27 @@ def xor_patch_status(bits, N: int, K: int, rows) -> int:
     out = _u8(bits).copy()
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
     return int(_load().orc_xor_patch(_ptr(out), N, K, _ptr(rows), rows.size))
+
+
+def g128x_repack(bits, N: int, K: int) -> np.ndarray:
+    """Canonical sign bits [N, K/8] -> the library's g128x storage layout
+    (a per-group bit permutation; see the C source for its definition)."""
+    src = _u8(bits)
+    out = np.zeros_like(src)
+    st = _load().orc_g128x_repack(_ptr(src), N, K, _ptr(out))
+    if st != OK:
+        raise OracleError(st, "g128x_repack")
+    return out
+
+
+def g128x_unpack(bits, N: int, K: int) -> np.ndarray:
+    """The inverse of g128x_repack."""
+    src = _u8(bits)
+    out = np.zeros_like(src)
+    st = _load().orc_g128x_unpack(_ptr(src), N, K, _ptr(out))
+    if st != OK:
+        raise OracleError(st, "g128x_unpack")
+    return out
 
 
 def pack(w, dtype: int, N: int, K: int):

@@ -667,6 +667,67 @@ int orc_xor_patch(uint8_t *bits, int64_t N, int64_t K, const int32_t *rows,
     return ORC_OK;
 }
 
+/* ---- the g128x storage layout -------------------------------------------
+ * Not from the pages (they fix no bit layout beyond "packed 1-bit"): a
+ * storage format of the library under test, a permutation of the 128 sign
+ * bits of every group, written here from its stated definition so that the
+ * library's conversion can be checked bit for bit.  Group bit b is bit b % 8
+ * of byte b / 8 of the group's 16 bytes.  For input k of the group:
+ *   inputs 0..71, six per field f = k / 6: byte f (of bytes 0..11), bit
+ *   1 + k % 6 (bits 1..6 of the byte, in input order);
+ *   inputs 72..95, six per field j = (k - 72) / 6 with i = (k - 72) % 6:
+ *   in the bytes of 32-bit word i / 2 (bytes 4 (i / 2) .. 4 (i / 2) + 3),
+ *   bit 7 of its byte j when i is even, bit 0 of its byte (j + 1) mod 4
+ *   when i is odd;
+ *   inputs 96..127: bit k (unchanged).
+ * One byte and one bit at a time. */
+static int orc_g128x_bit(int k)
+{
+    if (k < 72)
+        return (k / 6) * 8 + 1 + k % 6;
+    if (k < 96) {
+        int j = (k - 72) / 6, i = (k - 72) % 6;
+        int word = i / 2;
+        if (i % 2 == 0)
+            return word * 32 + j * 8 + 7;
+        return word * 32 + ((j + 1) % 4) * 8 + 0;
+    }
+    return k;
+}
+
+static int orc_g128x_convert(const uint8_t *in, int64_t N, int64_t K, uint8_t *out, int to_g128x)
+{
+    int st = orc_check_shape(1, N, K);
+    if (st != ORC_OK)
+        return st;
+    if (!in || !out)
+        return ORC_EINVAL;
+    for (int64_t n = 0; n < N; n++) {
+        for (int64_t g = 0; g < K / 128; g++) {
+            const uint8_t *src = in + n * (K / 8) + 16 * g;
+            uint8_t grp[16] = {0};
+            for (int k = 0; k < 128; k++) {
+                int from = to_g128x ? k : orc_g128x_bit(k);
+                int to = to_g128x ? orc_g128x_bit(k) : k;
+                if ((src[from / 8] >> (from % 8)) & 1)
+                    grp[to / 8] |= (uint8_t)(1u << (to % 8));
+            }
+            memcpy(out + n * (K / 8) + 16 * g, grp, 16);
+        }
+    }
+    return ORC_OK;
+}
+
+int orc_g128x_repack(const uint8_t *in, int64_t N, int64_t K, uint8_t *out)
+{
+    return orc_g128x_convert(in, N, K, out, 1);
+}
+
+int orc_g128x_unpack(const uint8_t *in, int64_t N, int64_t K, uint8_t *out)
+{
+    return orc_g128x_convert(in, N, K, out, 0);
+}
+
 /* ---- packing ----------------------------------------------------------
  * Floating-point weights [N][K] (fp32, bf16 or fp16 bit patterns) -> sign
  * bits and fp16 group scales, by the readings listed at the top. */

@@ -246,3 +246,12 @@ def test_ternary_sweep_refuses_swiglu_matrices():
     from bit_weight_gemv_sign_b300.sweep import TernarySweep
     with pytest.raises(ValueError):
         TernarySweep([synth.Mat("gate_up", 256, 1024, swiglu=True)], device="cpu")
+
+
+def test_g128x_conversion_and_plan_layout_rejected_on_host(lib):
+    f = ctypes.c_void_p(FAKE)
+    assert lib.bit1_repack_g128x(f, 4, 120, f, None) == b1.ESHAPE                     # K % 128
+    assert lib.bit1_repack_g128x(ctypes.c_void_p(FAKE + 8), 4, 128, f, None) == b1.EINVAL   # misaligned
+    assert lib.bit1_unpack_g128x(None, 4, 128, f, None) == b1.EINVAL                  # null
+    assert lib.bit1_unpack_g128x(f, 0, 128, f, None) == b1.ESHAPE                     # no rows
+    assert lib.bit1_group_plan_ex(None, 1, 1, 7, None, 0) == b1.EINVAL                # layout value

@@ -742,3 +742,61 @@ def test_t5_footprint_between_ideal_and_slots(orc):
     gb = total * 1.75 / 8 / 1e9
     assert fig["bonsai_27b_ternary_gigabytes"]["value"] < gb < fig["bonsai_27b_ternary_deployed_gigabytes"]["value"]
     assert orc.t5_footprint_bytes(N, K) < orc.ternary_footprint_bytes(N, K)
+
+
+# ---------------------------------------------------------------- g128x layout
+# A storage format of the library (not from the pages).  What pins the
+# oracle's conversion is that it is a permutation of the 128 bits of each
+# group, acting on each group alone: then every bit keeps its value and a
+# whole-row XOR commutes with it.  That the library's kernels read the
+# permuted bits as the same inputs is checked on the GPU (a grouped product
+# over converted bits equals the canonical one bit for bit).
+
+def test_g128x_is_a_permutation_of_each_group(orc):
+    K = 128
+    eye = np.zeros((128, K // 8), dtype=np.uint8)
+    for k in range(128):
+        eye[k, k // 8] = 1 << (k % 8)
+    out = orc.g128x_repack(eye, 128, K)
+    ones = np.unpackbits(out, axis=1, bitorder="little")
+    assert np.all(ones.sum(axis=1) == 1)                  # one bit in, one bit out
+    pos = ones.argmax(axis=1)
+    assert sorted(pos.tolist()) == list(range(128))       # all 128 positions used once
+    assert np.array_equal(orc.g128x_unpack(out, 128, K), eye)
+
+
+def test_g128x_inverse_complement_and_groupwise(orc):
+    N, K = 5, 1024
+    bits = synth.sign_bits(N, K, synth.rng(930))
+    r = orc.g128x_repack(bits, N, K)
+    assert np.array_equal(orc.g128x_unpack(r, N, K), bits)
+    assert not np.array_equal(r, bits)
+    # bit counts are kept per group, and complementing (a whole-row XOR)
+    # commutes with the conversion
+    cnt = lambda a: np.unpackbits(a.reshape(N, K // 128, 16), axis=2).sum(axis=2)
+    assert np.array_equal(cnt(r), cnt(bits))
+    assert np.array_equal(orc.g128x_repack(bits ^ 0xFF, N, K), r ^ 0xFF)
+    # each group is converted on its own: changing one group changes only it
+    b2 = bits.copy()
+    b2[2, 16 * 3: 16 * 4] ^= 0x5A
+    d = orc.g128x_repack(b2, N, K) != r
+    assert d[2, 16 * 3: 16 * 4].any() and d.sum() == d[2, 16 * 3: 16 * 4].sum()
+    # the same permutation in every group and row
+    assert np.array_equal(orc.g128x_repack(bits[:, :16], N, 128), r[:, :16])
+
+
+def test_g128x_leaves_the_last_word_and_keeps_fields_together(orc):
+    """The layout's purpose, on the unit vectors: inputs 96..127 keep their
+    positions, each field of six inputs 6f..6f+5 (f < 12) lands in one byte
+    (bits 1..6, in order), and the 24 inputs 72..95 fill bits 0 and 7 of
+    bytes 0..11."""
+    K = 128
+    pos = []
+    for k in range(128):
+        e = np.zeros((1, 16), dtype=np.uint8)
+        e[0, k // 8] = 1 << (k % 8)
+        pos.append(int(np.unpackbits(orc.g128x_repack(e, 1, K), bitorder="little").argmax()))
+    assert pos[96:] == list(range(96, 128))
+    for f in range(12):
+        assert [pos[6 * f + i] for i in range(6)] == [8 * f + 1 + i for i in range(6)]
+    assert sorted(pos[72:96]) == sorted([8 * b for b in range(12)] + [8 * b + 7 for b in range(12)])
