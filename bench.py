@@ -750,7 +750,10 @@ def run_mine(args):
     # The sign bits are converted once, at load, to the g128x layout (a
     # within-group bit permutation that the grouped kernel reads with fewer
     # integer operations; the same bytes, row patches unchanged).
-    sw = Sweep(synth.sweep_8b(), seed0=0, batch=1, y_dtype=b1.BF16).fill().to_g128x()
+    mats = synth.sweep_8b()
+    if args.layers is not None:    # a smaller case of the same sweep, for profiling
+        mats = mats[:7 * args.layers] + mats[-1:]
+    sw = Sweep(mats, seed0=0, batch=1, y_dtype=b1.BF16).fill().to_g128x()
     plan = sw.group_plan()          # one persistent launch over all 253 GEMVs
     s = torch.cuda.Stream()
 
@@ -759,8 +762,12 @@ def run_mine(args):
             dist.barrier()
         torch.cuda.synchronize()
 
+    # Consecutive steps are launched with programmatic dependent launch: a
+    # step's kernel starts streaming its weights while the previous step
+    # drains, and reads its activations only after the previous step has
+    # completed (griddepcontrol.wait), as a dependent decode loop would.
     def step():
-        plan.run(stream=s)
+        plan.run(flags=b1.FLAG_PDL, stream=s)
 
     # The clock sampler starts first (the nvidia-smi poller needs a moment to
     # come up).  Then the GPU is kept busy with the same step for SETTLE_S of
@@ -770,6 +777,16 @@ def run_mine(args):
     # between the idle gap and the timed region.
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     settle_steps = 0
+    # The K timed steps are captured once as a CUDA graph (K launches), so
+    # that the first step of the window does not wait on the host's launch
+    # call after the barrier.
+    with torch.cuda.stream(s):
+        step()
+        s.synchronize()
+        g_steps = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_steps, stream=s):
+            for _ in range(args.steps):
+                step()
     with ClockSampler(local) as clk, torch.cuda.stream(s):
         t_end = time.perf_counter() + SETTLE_S
         while time.perf_counter() < t_end:
@@ -781,8 +798,7 @@ def run_mine(args):
             step()
         barrier()
         e0.record(s)
-        for _ in range(args.steps):
-            step()
+        g_steps.replay()
         e1.record(s)
         e1.synchronize()
     barrier()
@@ -896,10 +912,16 @@ def run_mine(args):
         "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch": 1, "weight_bytes_per_step": sw.weight_bytes,
+        "config": {"workload": WORKLOAD if args.layers is None else
+                   f"profiling case: the first {args.layers} layers of the 8B-class sweep and its LM head "
+                   f"({len(mats)} GEMVs; not the benchmarked workload)",
+                   "batch": 1, "weight_bytes_per_step": sw.weight_bytes,
                    "l2": "inputs larger than L2 (1.06 GB of weights per step vs 126 MB L2)",
                    "compute": "1-bit sign weights x bf16 activations, fp32 accumulation, bf16 output",
-                   "launch": "one grouped persistent launch of the 253 independent GEMVs per step",
+                   "launch": "one grouped persistent launch of the 253 independent GEMVs per step; the K timed "
+                             "steps as one CUDA graph of K launches chained with programmatic dependent launch "
+                             "(a step streams its weights while the previous one drains and reads its "
+                             "activations only after it completed)",
                    "layout": "sign bits in the g128x layout (bit1_repack_g128x once at load; same bytes)",
                    "settle": f"{settle_steps} untimed steps ({SETTLE_S} s, GPU busy) before the warm-up steps",
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
@@ -957,6 +979,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="profiling: only the first L decoder layers of the sweep and its LM head")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the other configurations (tiny, projections, crossover, 27B sweep)")
     args = ap.parse_args()

@@ -129,3 +129,28 @@ def test_sweep_8b_g128x_benchmarked_launch_sampled_parity(orc):
         ref = orc.gemv_select(hb, hs, hx, 1, m.N, m.K, rows)
         got = sw.y_of(i)[:, torch.from_numpy(rows).cuda()]
         assert_gemv_close(got, ref, abs_bound(hs[rows], hx, m.K), f"g128x sweep matrix {i} ({m.name})")
+
+
+def test_dependent_grouped_launches_with_pdl(orc):
+    """Two grouped launches in a row with programmatic dependent launch, the
+    second reading the first one's output as its activations (a decode
+    step's dependence): the second kernel starts streaming its weights early
+    but reads x only after the first has completed."""
+    N, K = 4096, 4096
+    b_a, s_a = synth.matrix(N, K, 7400)
+    b_b, s_b = synth.matrix(N, K, 7401)
+    da, db = b1.bit1_repack_g128x(dev_u8(b_a)), b1.bit1_repack_g128x(dev_u8(b_b))
+    xa = dev_bf16(synth.x_for(1, K, 7402)).view(1, K)
+    h = torch.randn((1, K), device="cuda").bfloat16()        # stale contents the second launch must not see
+    yb = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    pa = b1.GroupPlan([(da, dev_u16(s_a), xa, h)], layout=b1.LAYOUT_G128X)
+    pb = b1.GroupPlan([(db, dev_u16(s_b), h, yb)], layout=b1.LAYOUT_G128X)
+    for step in range(3):
+        pa.run(flags=b1.FLAG_PDL)
+        pb.run(flags=b1.FLAG_PDL)
+    torch.cuda.synchronize()
+    assert b1.bit1_device_wait_timeouts() == 0
+    xh = xa.view(torch.int16).cpu().numpy().view(np.uint16).reshape(1, K)
+    assert_gemv_close(h, orc.gemv(b_a, s_a, xh, 1, N, K), abs_bound(s_a, xh, K), "first launch")
+    hh = h.view(torch.int16).cpu().numpy().view(np.uint16).reshape(1, K)
+    assert_gemv_close(yb, orc.gemv(b_b, s_b, hh, 1, N, K), abs_bound(s_b, hh, K), "second launch on the first's output")
