@@ -75,15 +75,36 @@ bool shape_ok(int64_t B, int64_t N, int64_t K) {
 
 bit1_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BIT1_OK : BIT1_ECUDA; }
 
-// Batch >= 16 with enough scratch: the tensor-core kernel.  Batch 1 below
-// 65536 rows: the nibble-table kernel (one launch of it is the shortest for
-// the projection sizes of 8B-27B models: less set-up than the cluster
-// kernel); larger or batched: the 6-bit-table kernel (up to 8 batch rows per
-// launch); what none of them takes: one warp per row.
+// Whether the tensor-core kernel beats the 6-bit tables at batch B, from
+// per-call times measured on one B300 (graph replay, weights rotated past
+// L2).  The tensor cores take 11-25 us per call almost independently of B
+// (4096x4096 11 us, 12288x4096 18, 4096x12288 18, 17408x5120 21, 5120x17408
+// 24); the tables grow with B.  Crossovers: 4096x4096 and 4096x12288 from
+// B = 4, 17408x5120 from B = 5, 12288x4096 from B = 8.  Where the tables
+// cannot take the shape (no cluster split of K, e.g. K = 17408) the rest is
+// far slower (warp-per-row: 800 us at B = 2 on 5120x17408).
+bool tc_beats_tables(int64_t B, int64_t N, int64_t K, bool t6_ok) {
+    if (B >= 16) return true;
+    if (B < 2) return false;
+    if (!t6_ok || B >= 8) return true;
+    if (N <= 8192) return B >= 4;
+    return B >= 5 && (double)N * (double)K >= 64e6;
+}
+
+// With enough scratch, the tensor-core kernel where it is faster (above).
+// Batch 1 below 65536 rows: the nibble-table kernel (one launch of it is the
+// shortest for the projection sizes of 8B-27B models: less set-up than the
+// cluster kernel); otherwise the 6-bit-table kernel (up to 8 batch rows per
+// launch); shapes it cannot split (K = 17408): the grouped kernel with the
+// one problem (up to 6 rows per launch, any K that is a multiple of 1024);
+// what none of them takes: one warp per row.
 int pick_variant(int64_t B, int64_t N, int64_t K, size_t ws_bytes) {
-    if (B >= 16 && tc_supported(B, N, K) && ws_bytes >= tc_min_workspace_bytes(B, N, K)) return BIT1_GEMV_TC;
+    const bool t6_ok = t6_supported(B, N, K);
+    if (tc_supported(B, N, K) && ws_bytes >= tc_min_workspace_bytes(B, N, K) && tc_beats_tables(B, N, K, t6_ok))
+        return BIT1_GEMV_TC;
     if (B == 1 && N < 65536 && lut_supported(B, N, K)) return BIT1_GEMV_LUT;
-    if (t6_supported(B, N, K)) return BIT1_GEMV_LUT6;
+    if (t6_ok) return BIT1_GEMV_LUT6;
+    if (group1_supported(B, N, K)) return BIT1_GEMV_STREAM;
     if (lut_supported(B, N, K)) return BIT1_GEMV_LUT;
     return BIT1_GEMV_SIMPLE;
 }
@@ -198,7 +219,7 @@ bit1_status bit1_gemv(const uint8_t* bits, const uint16_t* scales, const uint16_
 
 size_t bit1_gemv_workspace_bytes(int64_t B, int64_t N, int64_t K) {
     if (!shape_ok(B, N, K)) return 0;
-    if (B >= 16 && tc_supported(B, N, K)) return tc_workspace_bytes(B, N, K);
+    if (tc_supported(B, N, K) && tc_beats_tables(B, N, K, t6_supported(B, N, K))) return tc_workspace_bytes(B, N, K);
     return 0;
 }
 
@@ -215,7 +236,7 @@ int bit1_gemv_launches(int64_t B, int64_t N, int64_t K, int variant) {
         case BIT1_GEMV_LUT: return lut_supported(B, N, K) ? 1 : 0;
         case BIT1_GEMV_SPLITK:
         case BIT1_GEMV_LUT6: return t6_launch_count(B, N, K);
-        case BIT1_GEMV_STREAM: return group1_supported(B, N, K) ? 1 : 0;
+        case BIT1_GEMV_STREAM: return group1_supported(B, N, K) ? group1_launch_count(B) : 0;
         case BIT1_GEMV_TC: return tc_launch_count(B, N, K);
         default: return 0;
     }

@@ -556,6 +556,12 @@ __global__ void __launch_bounds__(kGWarps * 32, 1) k_gemv_group1(const __grid_co
     g_body<1, g_chunk_groups(1), S, kLayoutCanonical>(reinterpret_cast<const uint8_t*>(&plan));
 }
 
+// One problem at 2-6 batch rows (bit1_gemv_ex with BIT1_GEMV_STREAM).
+template <int NB, int S>
+__global__ void __launch_bounds__(16 * 32, 1) k_gemv_group1b(const __grid_constant__ GSingle plan) {
+    g_body<NB, g_chunk_groups(NB), S, kLayoutCanonical>(reinterpret_cast<const uint8_t*>(&plan));
+}
+
 // ---------------------------------------------------------------- host
 namespace {
 
@@ -805,40 +811,79 @@ cudaError_t launch_group(const void* device_plan, const void* host_plan, bool pd
 }
 
 bool group1_supported(int64_t B, int64_t N, int64_t K) {
-    return B == 1 && N >= 1 && N <= (1LL << 30) && K >= 1024 && K % 1024 == 0 && K <= (1LL << 20);
+    return B >= 1 && N >= 1 && N <= (1LL << 30) && K >= 1024 && K % 1024 == 0 && K <= (1LL << 20);
 }
 
+int group1_launch_count(int64_t B) { return (int)((B + kGMaxNB - 1) / kGMaxNB); }
+
+namespace {
+
+template <int NB>
+const void* group1_kernel(int S) {
+    if constexpr (NB == 1) return S == 2 ? (const void*)k_gemv_group1<2> : (const void*)k_gemv_group1<1>;
+    else return S == 2 ? (const void*)k_gemv_group1b<NB, 2> : (const void*)k_gemv_group1b<NB, 1>;
+}
+
+const void* group1_kernel_nb(int nb, int S) {
+    switch (nb) {
+        case 1: return group1_kernel<1>(S);
+        case 2: return group1_kernel<2>(S);
+        case 3: return group1_kernel<3>(S);
+        case 4: return group1_kernel<4>(S);
+        case 5: return group1_kernel<5>(S);
+        case 6: return group1_kernel<6>(S);
+        default: return nullptr;
+    }
+}
+
+}  // namespace
+
+// One problem as a grouped launch: B rows in ceil(B / 6) launches of balanced
+// row counts (7 rows: 4 + 3), each with its plan passed by value.
 cudaError_t launch_gemv_group1(const GemvArgs& a) {
-    bit1_gemv_problem pb{};
-    pb.bits = a.bits;
-    pb.scales = a.scales;
-    pb.x = a.x;
-    pb.y = a.y;
-    pb.N = a.N;
-    pb.K = a.K;
-    pb.y_dtype = a.y_bf16 ? BIT1_BF16 : BIT1_F32;
-    pb.epilogue = a.swiglu ? BIT1_EPI_SWIGLU : BIT1_EPI_NONE;
-    if (!problem_ok(pb)) return cudaErrorInvalidValue;
-    std::vector<GProb> probs(1);
-    if (!encode_prob(probs[0], pb, 1)) return cudaErrorInvalidValue;
-    static GSingle single;  // large: keep off the stack; filled and copied into the launch
+    if (!group1_supported(a.B, a.N, a.K)) return cudaErrorInvalidValue;
+    const int launches = group1_launch_count(a.B);
+    const int64_t out_n = a.swiglu ? a.N / 2 : a.N;
+    const size_t ysz = a.y_bf16 ? 2 : 4;
+    static GSingle single;  // large: keep off the stack; filled and copied into each launch
     static std::mutex mu;
     std::lock_guard<std::mutex> lk(mu);
-    std::memset(&single, 0, sizeof(single));
-    std::vector<GRange> ranges;
-    const int nctas = std::min(sm_count(), kGMaxCtas);
-    if (!plan_layout(probs, nctas, 1, single.h, ranges)) return cudaErrorInvalidValue;
-    single.h.ranges_off = (int)offsetof(GSingle, r);
-    single.h.probs_off = (int)offsetof(GSingle, p);
-    std::memcpy(single.r, ranges.data(), ranges.size() * sizeof(GRange));
-    single.p = probs[0];
-    if (single.h.S != 1 && single.h.S != 2) return cudaErrorInvalidValue;
-    const void* fn = single.h.S == 2 ? (const void*)k_gemv_group1<2> : (const void*)k_gemv_group1<1>;
-    cudaError_t e = set_smem_attr(fn);
-    if (e != cudaSuccess) return e;
-    void* args[] = {(void*)&single};
-    return launch(fn, dim3((unsigned)single.h.nctas), dim3((unsigned)(single.h.W * 32)),
-                  (size_t)single.h.smem_bytes, a.stream, a.pdl, args);
+    int64_t b0 = 0;
+    for (int l = 0; l < launches; ++l) {
+        const int nb = (int)((a.B - b0 + (launches - l) - 1) / (launches - l));
+        bit1_gemv_problem pb{};
+        pb.bits = a.bits;
+        pb.scales = a.scales;
+        pb.x = a.x + b0 * a.K;
+        pb.y = static_cast<uint8_t*>(a.y) + (size_t)b0 * (size_t)out_n * ysz;
+        pb.N = a.N;
+        pb.K = a.K;
+        pb.y_dtype = a.y_bf16 ? BIT1_BF16 : BIT1_F32;
+        pb.epilogue = a.swiglu ? BIT1_EPI_SWIGLU : BIT1_EPI_NONE;
+        if (!problem_ok(pb)) return cudaErrorInvalidValue;
+        std::vector<GProb> probs(1);
+        if (!encode_prob(probs[0], pb, nb)) return cudaErrorInvalidValue;
+        std::memset(&single, 0, sizeof(single));
+        std::vector<GRange> ranges;
+        const int nctas = std::min(sm_count(), kGMaxCtas);
+        if (!plan_layout(probs, nctas, nb, single.h, ranges)) return cudaErrorInvalidValue;
+        single.h.layout = kLayoutCanonical;
+        single.h.ranges_off = (int)offsetof(GSingle, r);
+        single.h.probs_off = (int)offsetof(GSingle, p);
+        std::memcpy(single.r, ranges.data(), ranges.size() * sizeof(GRange));
+        single.p = probs[0];
+        if (single.h.S != 1 && single.h.S != 2) return cudaErrorInvalidValue;
+        const void* fn = group1_kernel_nb(nb, single.h.S);
+        if (!fn) return cudaErrorInvalidValue;
+        cudaError_t e = set_smem_attr(fn);
+        if (e != cudaSuccess) return e;
+        void* args[] = {(void*)&single};
+        e = launch(fn, dim3((unsigned)single.h.nctas), dim3((unsigned)(single.h.W * 32)), (size_t)single.h.smem_bytes,
+                   a.stream, a.pdl, args);
+        if (e != cudaSuccess) return e;
+        b0 += nb;
+    }
+    return cudaSuccess;
 }
 
 unsigned int group_take_timeouts() {

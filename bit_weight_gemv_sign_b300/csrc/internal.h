@@ -67,6 +67,7 @@ bit1_status group_plan(const bit1_gemv_problem* problems, int count, int nb, int
                        size_t bytes);
 cudaError_t launch_group(const void* device_plan, const void* host_plan, bool pdl, cudaStream_t stream);
 bool group1_supported(int64_t B, int64_t N, int64_t K);
+int group1_launch_count(int64_t B);          // ceil(B / 6): up to 6 rows per launch
 cudaError_t launch_gemv_group1(const GemvArgs& a);
 unsigned int group_take_timeouts();
 

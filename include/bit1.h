@@ -64,7 +64,12 @@ enum bit1_dtype {
 
 /* Kernel selection for bit1_gemv_ex.  AUTO picks by shape (the same choice
  * bit1_gemv makes); the others force one kernel and return BIT1_ESHAPE if
- * that kernel cannot take the shape. */
+ * that kernel cannot take the shape.  AUTO, from per-call times measured on
+ * one B300: the tensor cores when the workspace allows them and they are the
+ * faster (B >= 16; B >= 8; B >= 4 for N <= 8192; B >= 5 for N*K >= 64M;
+ * any B >= 2 where the 6-bit tables cannot split K), else at batch 1 the
+ * nibble-table kernel below 65536 rows, else the 6-bit tables, else the
+ * grouped kernel with the one problem (STREAM), else one warp per row. */
 enum bit1_gemv_variant {
     BIT1_GEMV_AUTO = 0,
     BIT1_GEMV_SIMPLE = 1,  /* any shape; one warp per row (reference-quality) */
@@ -79,9 +84,12 @@ enum bit1_gemv_variant {
                               tables per batch row, TMA-staged weights, K split
                               over a thread-block cluster; up to 8 batch rows
                               per launch (larger batches: several launches) */
-    BIT1_GEMV_STREAM = 6   /* batch 1, K a multiple of 1024: the grouped kernel
-                              below with one problem (one CTA per SM streaming a
-                              contiguous row range, full-K tables, no clusters) */
+    BIT1_GEMV_STREAM = 6   /* K a multiple of 1024: the grouped kernel below
+                              with the one problem (one CTA per SM streaming a
+                              contiguous row range, full-K tables, no clusters;
+                              no workspace); up to 6 batch rows per launch
+                              (larger batches: ceil(B / 6) launches of
+                              balanced row counts) */
 };
 
 /* bit1_gemv_ex flags. */
@@ -157,7 +165,8 @@ bit1_status bit1_gemv_ex(const uint8_t *bits, const uint16_t *scales,
                          int variant, unsigned flags, bit1_stream_t stream);
 
 /* Scratch bytes that let bit1_gemv use its fastest kernel for this shape
- * (0 when no kernel needs scratch).  On the tensor cores (B >= 16) this is
+ * (0 when no kernel needs scratch).  On the tensor cores (where AUTO takes
+ * them, see enum bit1_gemv_variant) this is
  * the fp16 copy of every batch row's activations plus one float per row,
  * so a batch beyond 64 rows runs as one launch pair; any workspace of at
  * least one 64-row chunk's share (16 * ceil(min(B, 64) / 16) * K * 2 bytes

@@ -92,7 +92,7 @@ def test_pick_and_launch_counts(lib):
     assert b1.bit1_gemv_pick(1, 4096, 12288) == b1.LUT
     assert b1.bit1_gemv_pick(1, 70000, 12288) == b1.LUT6
     assert b1.bit1_gemv_pick(1, 4096, 13312) == b1.LUT
-    assert b1.bit1_gemv_pick(1, 5120, 17408) == b1.SIMPLE   # no table kernel takes K = 17 x 1024
+    assert b1.bit1_gemv_pick(1, 5120, 17408) == b1.STREAM   # no table kernel splits K = 17 x 1024: the grouped one
     assert b1.bit1_gemv_pick(1, 4096, 1152) == b1.SIMPLE
     assert b1.bit1_gemv_pick(0, 4096, 4096) == 0
     assert b1.bit1_gemv_launches(1, 4096, 4096, b1.AUTO) == 1
@@ -103,7 +103,22 @@ def test_pick_and_launch_counts(lib):
     assert b1.bit1_gemv_pick(16, 12288, 4096) == b1.LUT6
     ws = b1.bit1_gemv_workspace_bytes(16, 12288, 4096)
     assert ws > 0 and b1.bit1_gemv_pick(16, 12288, 4096, ws) == b1.TC
-    assert b1.bit1_gemv_pick(8, 12288, 4096, 1 << 30) == b1.LUT6
+    # the measured crossover with scratch: 12288x4096 from 8 rows, N <= 8192 from 4,
+    # 17408x5120 (89M weights) from 5; every batch of 2+ rows where the tables
+    # cannot split K
+    big = 1 << 30
+    assert b1.bit1_gemv_pick(6, 12288, 4096, big) == b1.LUT6
+    assert b1.bit1_gemv_pick(8, 12288, 4096, big) == b1.TC
+    assert b1.bit1_gemv_pick(3, 4096, 12288, big) == b1.LUT6
+    assert b1.bit1_gemv_pick(4, 4096, 12288, big) == b1.TC
+    assert b1.bit1_gemv_pick(4, 17408, 5120, big) == b1.LUT6
+    assert b1.bit1_gemv_pick(5, 17408, 5120, big) == b1.TC
+    assert b1.bit1_gemv_pick(2, 5120, 17408, big) == b1.TC
+    assert b1.bit1_gemv_pick(1, 5120, 17408, big) == b1.STREAM
+    # without scratch, K = 17408 at 2-8 rows: the grouped kernel, up to 6 rows a launch
+    assert b1.bit1_gemv_pick(4, 5120, 17408) == b1.STREAM
+    assert b1.bit1_gemv_launches(6, 5120, 17408, b1.STREAM) == 1
+    assert b1.bit1_gemv_launches(8, 5120, 17408, b1.STREAM) == 2
     assert b1.bit1_gemv_launches(4, 12288, 4096, b1.LUT6) == 1
     assert b1.bit1_gemv_launches(16, 12288, 4096, b1.LUT6) >= 2
     assert b1.bit1_gemv_launches(16, 12288, 4096, b1.TC) == 2
@@ -197,8 +212,8 @@ def test_swiglu_flag_checked_on_host(lib):
     # the tensor cores take the flag at any batch, with their workspace
     assert f(FAKE, FAKE, FAKE, 1, 8, 1024, FAKE, b1.F32, None, 0, b1.TC, S, None) == b1.EINVAL
     assert f(FAKE, FAKE, FAKE, 2, 8, 1024, FAKE, b1.F32, None, 0, b1.TC, S, None) == b1.EINVAL
-    for v in (b1.LUT, b1.STREAM):                                                               # batch 1 only
-        assert f(FAKE, FAKE, FAKE, 2, 8, 1024, FAKE, b1.F32, None, 0, v, S, None) == b1.ESHAPE
+    assert f(FAKE, FAKE, FAKE, 2, 8, 1024, FAKE, b1.F32, None, 0, b1.LUT, S, None) == b1.ESHAPE  # batch 1 only
+    assert f(FAKE, FAKE, FAKE, 2, 8, 1152, FAKE, b1.F32, None, 0, b1.STREAM, S, None) == b1.ESHAPE  # K % 1024
     # AUTO at 2 rows where only the warp-per-row kernel takes the shape
     assert f(FAKE, FAKE, FAKE, 2, 8, 1152, FAKE, b1.F32, None, 0, b1.AUTO, S, None) == b1.ESHAPE
     assert f(FAKE, FAKE, FAKE, 1, 8, 1152, FAKE, b1.F32, None, 0, b1.LUT, S, None) == b1.ESHAPE

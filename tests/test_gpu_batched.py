@@ -94,3 +94,40 @@ def test_splitk_names_the_cluster_split_kernel():
     b = _run(bits, scales, x, N, K, B, variant=b1.LUT6)
     assert torch.equal(a, b)
     assert b1.bit1_gemv_launches(B, N, K, b1.SPLITK) == b1.bit1_gemv_launches(B, N, K, b1.LUT6)
+
+
+# K = 17408 (the 27B-class down projection, 17 x 1024) has no cluster split
+# for the 6-bit tables; without a workspace AUTO runs it on the grouped kernel
+# (BIT1_GEMV_STREAM: up to 6 rows per launch), with one on the tensor cores.
+@pytest.mark.parametrize("B", [2, 4, 8])
+def test_k17408_small_batch_grouped_and_tensor_cores(orc, B):
+    N, K = 5120, 17408
+    bits, scales, x = _problem(N, K, B, 8200 + B)
+    assert b1.bit1_gemv_pick(B, N, K) == b1.STREAM
+    assert b1.bit1_gemv_launches(B, N, K, b1.STREAM) == (B + 5) // 6
+    # with bit1_gemv_workspace_bytes of scratch AUTO takes the tensor cores
+    assert b1.bit1_gemv_launches(B, N, K, b1.AUTO) == b1.bit1_gemv_launches(B, N, K, b1.TC)
+    ref = orc.gemv(bits, scales, x, B, N, K)
+    bound = abs_bound(scales, x, K)
+    y = _run(bits, scales, x, N, K, B, variant=b1.AUTO)
+    assert_gemv_close(y, ref, bound, f"grouped N={N} K={K} B={B}")
+    yb = _run(bits, scales, x, N, K, B, variant=b1.STREAM, y_dtype=b1.BF16)
+    assert_gemv_close(yb, ref, bound, f"grouped bf16 N={N} K={K} B={B}")
+    ws = torch.empty(b1.bit1_gemv_workspace_bytes(B, N, K), dtype=torch.uint8, device="cuda")
+    assert b1.bit1_gemv_pick(B, N, K, ws.numel()) == b1.TC
+    yt = b1.bit1_gemv_ex(dev_u8(bits), dev_u16(scales), dev_bf16(x).view(B, K), workspace=ws, N=N, K=K)
+    torch.cuda.synchronize()
+    assert_gemv_close(yt, ref, bound, f"tensor cores N={N} K={K} B={B}")
+    assert b1.bit1_device_wait_timeouts() == 0
+
+
+def test_stream_rows_split_over_launches():
+    """Seven rows run as two grouped launches, of 4 and 3 rows: the result
+    equals those two launches made separately, row for row."""
+    N, K = 3000, 4096
+    bits, scales, x = _problem(N, K, 7, 8210)
+    assert b1.bit1_gemv_launches(7, N, K, b1.STREAM) == 2
+    y7 = _run(bits, scales, x, N, K, 7, variant=b1.STREAM)
+    y4 = _run(bits, scales, x[:4], N, K, 4, variant=b1.STREAM)
+    y3 = _run(bits, scales, x[4:], N, K, 3, variant=b1.STREAM)
+    assert torch.equal(y7[:4], y4) and torch.equal(y7[4:], y3)

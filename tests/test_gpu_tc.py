@@ -194,8 +194,11 @@ def test_tc_workspace_rules():
     assert b1.bit1_gemv_pick(B, N, K, need) == b1.TC
     # K not a multiple of 1024: the tensor-core kernel refuses the shape
     assert b1.bit1_gemv_launches(B, 512, 1152, b1.TC) == 0
-    # batch < 16: AUTO never picks the tensor cores
-    assert b1.bit1_gemv_pick(8, N, K, 1 << 30) != b1.TC
+    # batch 1: AUTO never picks the tensor cores; batch 8 (past the measured
+    # crossover) takes them when the scratch is there
+    assert b1.bit1_gemv_pick(1, N, K, 1 << 30) != b1.TC
+    assert b1.bit1_gemv_pick(8, N, K, 1 << 30) == b1.TC
+    assert b1.bit1_gemv_pick(8, N, K, 0) != b1.TC
 
 
 @pytest.mark.parametrize("B", [100, 200])
