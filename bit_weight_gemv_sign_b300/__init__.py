@@ -20,6 +20,7 @@ __all__ = [
     "bit1_gemv_workspace_bytes", "bit1_gemv_pick", "bit1_gemv_launches",
     "bit1_xor_patch", "bit1_status_str", "bit1_version", "bit1_device_wait_timeouts",
     "bit1_group_plan_bytes", "bit1_group_plan", "bit1_gemv_group", "GroupPlan",
+    "bit1_group_tc_plan_bytes", "bit1_group_tc_workspace_bytes", "bit1_group_plan_tc",
     "library_path", "load", "bit1_gemv_tc_noalloc",
     "LAYOUT_CANONICAL", "LAYOUT_G128X", "bit1_repack_g128x", "bit1_unpack_g128x",
     "bit1_ternary_planes", "bit1_gemv_ternary", "bit1_gemv_ternary_workspace_bytes",
@@ -108,6 +109,12 @@ def load():
         lib.bit1_unpack_g128x.restype = i32
         lib.bit1_gemv_group.argtypes = [p, p, ctypes.c_uint, p]
         lib.bit1_gemv_group.restype = i32
+        lib.bit1_group_tc_plan_bytes.argtypes = [i32]
+        lib.bit1_group_tc_plan_bytes.restype = sz
+        lib.bit1_group_tc_workspace_bytes.argtypes = [ctypes.POINTER(_Problem), i32, i32]
+        lib.bit1_group_tc_workspace_bytes.restype = sz
+        lib.bit1_group_plan_tc.argtypes = [ctypes.POINTER(_Problem), i32, i32, p, sz, p, sz]
+        lib.bit1_group_plan_tc.restype = i32
         lib.bit1_gemv_tc_noalloc.argtypes = [p, p, p, i64, i64, i64, p, i32, ctypes.c_uint, p]
         lib.bit1_gemv_tc_noalloc.restype = i32
         lib.bit1_ternary_planes.argtypes = [p, i64, i64, p, p, p, p]
@@ -294,13 +301,7 @@ def bit1_group_plan_bytes(count: int) -> int:
     return int(load().bit1_group_plan_bytes(int(count)))
 
 
-def bit1_group_plan(problems, host_plan_ptr: int, plan_bytes: int, B: int = 1,
-                    layout: int = LAYOUT_CANONICAL) -> None:
-    """problems: sequence of (bits, scales, x, y) or (bits, scales, x, y,
-    epilogue) CUDA tensors; x is [B, K] (or [K] at B = 1) bf16 and y [B, N]
-    ([B, N/2] with EPI_SWIGLU, the rows then interleaved gate/up pairs).
-    B > 1 calls bit1_group_plan_batched; a non-canonical ``layout`` (every
-    problem's bits converted with bit1_repack_g128x) bit1_group_plan_ex."""
+def _problem_array(problems):
     import torch
     arr = (_Problem * len(problems))()
     for i, pr in enumerate(problems):
@@ -310,6 +311,35 @@ def bit1_group_plan(problems, host_plan_ptr: int, plan_bytes: int, B: int = 1,
             raise TypeError("y must be float32 or bfloat16")
         arr[i] = _Problem(_dptr(bits, "bits"), _dptr(scales, "scales"), _dptr(x, "x"), _dptr(y, "y"),
                           bits.shape[0], x.shape[-1], BF16 if y.dtype == torch.bfloat16 else F32, epi)
+    return arr
+
+
+def bit1_group_tc_plan_bytes(count: int) -> int:
+    return int(load().bit1_group_tc_plan_bytes(int(count)))
+
+
+def bit1_group_tc_workspace_bytes(problems, B: int) -> int:
+    """Workspace bytes of a tensor-core grouped plan (0 on invalid arguments)."""
+    return int(load().bit1_group_tc_workspace_bytes(_problem_array(problems), len(problems), int(B)))
+
+
+def bit1_group_plan_tc(problems, B: int, workspace, host_plan_ptr: int, plan_bytes: int) -> None:
+    """Encode a tensor-core grouped plan (problems as for bit1_group_plan, x
+    [B, K] for every problem) using ``workspace`` (uint8 CUDA tensor of at
+    least bit1_group_tc_workspace_bytes bytes)."""
+    st = load().bit1_group_plan_tc(_problem_array(problems), len(problems), int(B), _dptr(workspace, "workspace"),
+                                   workspace.numel() * workspace.element_size(), host_plan_ptr, plan_bytes)
+    _check(st, "bit1_group_plan_tc")
+
+
+def bit1_group_plan(problems, host_plan_ptr: int, plan_bytes: int, B: int = 1,
+                    layout: int = LAYOUT_CANONICAL) -> None:
+    """problems: sequence of (bits, scales, x, y) or (bits, scales, x, y,
+    epilogue) CUDA tensors; x is [B, K] (or [K] at B = 1) bf16 and y [B, N]
+    ([B, N/2] with EPI_SWIGLU, the rows then interleaved gate/up pairs).
+    B > 1 calls bit1_group_plan_batched; a non-canonical ``layout`` (every
+    problem's bits converted with bit1_repack_g128x) bit1_group_plan_ex."""
+    arr = _problem_array(problems)
     if layout != LAYOUT_CANONICAL:
         st = load().bit1_group_plan_ex(arr, len(problems), int(B), int(layout), host_plan_ptr, plan_bytes)
     elif B == 1:
@@ -352,19 +382,34 @@ def bit1_gemv_group(device_plan_ptr: int, host_plan_ptr: int, flags: int = 0, st
 class GroupPlan:
     """A grouped-GEMV plan: the encoded host copy and its device copy (both
     128-byte aligned).  The tensors named in ``problems`` must stay alive and
-    in place while the plan is used."""
+    in place while the plan is used.  ``tensor_cores``: the tcgen05 grouped
+    kernel (B <= 64, canonical layout; the plan owns its workspace)."""
 
-    def __init__(self, problems, device="cuda", B: int = 1, layout: int = LAYOUT_CANONICAL):
+    def __init__(self, problems, device="cuda", B: int = 1, layout: int = LAYOUT_CANONICAL,
+                 tensor_cores: bool = False):
         import numpy as np
         import torch
         self.problems = list(problems)
         self.B = int(B)
-        self.nbytes = bit1_group_plan_bytes(len(self.problems))
+        self.tensor_cores = bool(tensor_cores)
+        self.layout = int(layout)
+        if self.tensor_cores:
+            if self.layout != LAYOUT_CANONICAL:
+                raise ValueError("the tensor-core grouped kernel takes the canonical layout")
+            self.nbytes = bit1_group_tc_plan_bytes(len(self.problems))
+            nws = bit1_group_tc_workspace_bytes(self.problems, self.B)
+            if nws == 0:
+                raise Bit1Error(ESHAPE, "bit1_group_tc_workspace_bytes")
+            self.workspace = torch.empty(nws, dtype=torch.uint8, device=device)
+        else:
+            self.nbytes = bit1_group_plan_bytes(len(self.problems))
         self._host_raw = np.zeros(self.nbytes + 128, dtype=np.uint8)
         off = (-self._host_raw.ctypes.data) % 128
         self.host = self._host_raw[off: off + self.nbytes]
-        self.layout = int(layout)
-        bit1_group_plan(self.problems, self.host.ctypes.data, self.nbytes, self.B, self.layout)
+        if self.tensor_cores:
+            bit1_group_plan_tc(self.problems, self.B, self.workspace, self.host.ctypes.data, self.nbytes)
+        else:
+            bit1_group_plan(self.problems, self.host.ctypes.data, self.nbytes, self.B, self.layout)
         self._dev_raw = torch.empty(self.nbytes + 128, dtype=torch.uint8, device=device)
         doff = (-self._dev_raw.data_ptr()) % 128
         self.dev = self._dev_raw[doff: doff + self.nbytes]

@@ -1,6 +1,7 @@
 // C ABI of the bit1 library: argument validation (on the host, before any
 // CUDA call, so that a rejected call launches and modifies nothing), kernel
 // selection and launch.  Declarations and their documentation: bit1.h.
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -269,8 +270,9 @@ const char* bit1_version(void) { return "bit1 0.2 (sm_103a)"; }
 
 unsigned int bit1_device_wait_timeouts(void) {
     const unsigned int a = t6_take_timeouts(), b = group_take_timeouts(), c = tc_take_timeouts();
-    if (a == 0xffffffffu || b == 0xffffffffu || c == 0xffffffffu) return 0xffffffffu;
-    return a + b + c;
+    const unsigned int d = tcg_take_timeouts();
+    if (a == 0xffffffffu || b == 0xffffffffu || c == 0xffffffffu || d == 0xffffffffu) return 0xffffffffu;
+    return a + b + c + d;
 }
 
 size_t bit1_group_plan_bytes(int count) { return group_plan_bytes(count); }
@@ -405,7 +407,23 @@ bit1_status bit1_gemv_group(const void* device_plan, const void* host_plan, unsi
     if (!device_plan || !host_plan || ((uintptr_t)device_plan & 127) || ((uintptr_t)host_plan & 127))
         return BIT1_EINVAL;
     if (flags & ~BIT1_FLAG_PDL) return BIT1_EINVAL;
-    return from_cuda(launch_group(device_plan, host_plan, (flags & BIT1_FLAG_PDL) != 0, (cudaStream_t)stream));
+    int kind;
+    std::memcpy(&kind, static_cast<const uint8_t*>(host_plan) + kPlanKindOffset, sizeof(kind));
+    const bool pdl = (flags & BIT1_FLAG_PDL) != 0;
+    if (kind == kPlanKindTensor) return from_cuda(launch_tc_group(device_plan, host_plan, pdl, (cudaStream_t)stream));
+    if (kind != kPlanKindTables) return BIT1_EINVAL;
+    return from_cuda(launch_group(device_plan, host_plan, pdl, (cudaStream_t)stream));
+}
+
+size_t bit1_group_tc_plan_bytes(int count) { return tcg_plan_bytes(count); }
+
+size_t bit1_group_tc_workspace_bytes(const bit1_gemv_problem* problems, int count, int B) {
+    return tcg_workspace_bytes(problems, count, B);
+}
+
+bit1_status bit1_group_plan_tc(const bit1_gemv_problem* problems, int count, int B, void* workspace,
+                               size_t ws_bytes, void* host_plan, size_t plan_bytes) {
+    return tcg_plan(problems, count, B, workspace, ws_bytes, host_plan, plan_bytes);
 }
 
 }  // extern "C"

@@ -67,9 +67,11 @@ struct GHeader {            // 128 bytes
     uint32_t off_xraw;      // raw bf16 activations of the next phase (bulk copy target)
     uint32_t off_pinfo;     // per-problem {RB, G, nch, N} of the CTA's range
     int layout;             // sign-bit layout of every problem (kLayoutCanonical or kLayoutG128x)
-    int pad[15];
+    int kind;               // kPlanKindTables
+    int pad[14];
 };
 static_assert(sizeof(GHeader) == 128, "header size");
+static_assert(offsetof(GHeader, kind) == kPlanKindOffset, "kind offset");
 
 struct GRange {             // blocks from (p0, b0) up to, not including, (p1, b1)
     int p0, b0, p1, b1;
@@ -797,6 +799,7 @@ const void* group_kernel(int nb, int S) { return group_kernel_s<L>(nb, S == 2); 
 
 cudaError_t launch_group(const void* device_plan, const void* host_plan, bool pdl, cudaStream_t stream) {
     const GHeader* h = static_cast<const GHeader*>(host_plan);
+    if (h->kind != kPlanKindTables) return cudaErrorInvalidValue;
     if (h->S != 1 && h->S != 2) return cudaErrorInvalidValue;
     if (h->layout != kLayoutCanonical && h->layout != kLayoutG128x) return cudaErrorInvalidValue;
     const void* fn = h->layout == kLayoutG128x ? group_kernel<kLayoutG128x>(h->nb, h->S)

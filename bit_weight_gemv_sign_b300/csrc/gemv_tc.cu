@@ -55,15 +55,14 @@
 #include "common.cuh"
 #include "internal.h"
 #include "t6_common.cuh"
+#include "tc_common.cuh"
 
 namespace bit1 {
 
 __device__ unsigned int g_tc_wait_timeouts = 0;
 
 constexpr int kTcRows = 256;              // weight rows per CTA (two M = 128 MMAs)
-constexpr int kTcStepK = 128;             // inputs per pipeline step (one scale group)
 constexpr int kTcStages = 3;              // max A (tensor memory) / B (shared memory) stages
-constexpr int kTcChunkSteps = 4;          // sign-bit box: 64 bytes of each row = 4 steps
 constexpr int kTcWSlots = 4;              // sign-bit ring slots
 constexpr uint32_t kTcWSlotBytes = kTcRows * 16 * kTcChunkSteps;   // 16 KB
 constexpr int kTcMaxB = 64;               // batch rows per chunk with two accumulators per half
@@ -71,8 +70,6 @@ constexpr int kTcWideB = 128;             // rows per chunk with one accumulator
 constexpr int kTcUnpackWarps = 8;
 constexpr int kTcMmaWarps = 4;
 constexpr int kTcThreads = 32 * (kTcUnpackWarps + 2 + kTcMmaWarps);
-constexpr int kTcPrepThreads = 512;
-constexpr int kTcPrepUnits = 8;           // 16-byte units of x per prep thread held in registers
 
 struct TcParams {
     const uint16_t* scales;
@@ -86,23 +83,6 @@ struct TcParams {
 };
 
 // ---------------------------------------------------------------- helpers
-__device__ __forceinline__ void tc_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle (8-row x
-// 128-byte atoms, consecutive atoms 1024 bytes apart), descriptor version 1.
-__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t saddr) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity));
-}
-__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
 __device__ __forceinline__ float4 ld_cluster_v4(uint32_t remote_addr) {
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote_addr) : "memory");
@@ -132,104 +112,16 @@ __device__ __forceinline__ void store_h(const TcParams& p, int b, int unit, floa
 __device__ __forceinline__ void store_h_fast(const TcParams& p, int b, int unit, float g, float u) {
     put_h(p, b, unit, __fdividef(g, 1.f + __expf(-g)) * u);
 }
-__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, uint32_t bar) {
-    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-                 ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar) : "memory");
-}
-__device__ __forceinline__ uint32_t bf16_mag(uint32_t v) {   // |x| bits; NaN -> 0 (does not set the scale)
-    v &= 0x7fffu;
-    return v > 0x7f80u ? 0u : v;
-}
-__device__ __forceinline__ uint32_t bf16x2_max_mag(uint32_t w) { return max(bf16_mag(w & 0xffffu), bf16_mag(w >> 16)); }
-__device__ __forceinline__ uint32_t pack_h2(uint32_t lo_bf16, uint32_t hi_bf16, float finv) {
-    const __half2 h = __floats2half2_rn(bf16_bits_to_f32(lo_bf16) * finv, bf16_bits_to_f32(hi_bf16) * finv);
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
-
 // ---------------------------------------------------------------- prep
-// One CTA per padded batch row b: xp[b][32q + 2j + h] = fp16(x[b][32q + j + 16h]
-// * 2^-m_b) and xscale[b] = 2^m_b, with m_b chosen so that max|x * 2^-m_b| lies
-// in [2^14, 2^15) (exact: bf16 keeps 8 significant bits, fp16 11).  Rows b >= B
-// are zero.
-// Thread layout: 16-byte unit u = 8 consecutive inputs; the four units of a
-// 32-input block sit in four consecutive lanes, and lanes p and p^2 exchange
-// their units to form the (j, j+16) pairs.
+// One CTA per padded batch row b (tc_prep_row): xp[b] = the permuted,
+// prescaled fp16 copy of x[b], xscale[b] = 2^m_b; rows b >= B are zero.
 __global__ void __launch_bounds__(kTcPrepThreads) k_tc_prep(const uint16_t* __restrict__ x, int B, int K,
                                                             uint16_t* __restrict__ xp, float* __restrict__ xscale) {
     pdl_wait();
     pdl_launch_dependents();   // the main kernel may start: everything before this one has completed
     const int b = blockIdx.x;
     __shared__ uint32_t red[kTcPrepThreads / 32];
-    uint4* out = reinterpret_cast<uint4*>(xp + (size_t)b * K);
-    const int units = K / 8;
-    if (b >= B) {
-        for (int i = threadIdx.x; i < units; i += blockDim.x) out[i] = make_uint4(0, 0, 0, 0);
-        if (threadIdx.x == 0) xscale[b] = 1.f;
-        return;
-    }
-    const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)b * K);
-    const bool resident = units <= kTcPrepThreads * kTcPrepUnits;
-    uint4 v[kTcPrepUnits];
-    uint32_t m = 0;
-    if (resident) {
-#pragma unroll
-        for (int i = 0; i < kTcPrepUnits; ++i) {
-            const int u = threadIdx.x + i * kTcPrepThreads;
-            v[i] = u < units ? in[u] : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int i = 0; i < kTcPrepUnits; ++i)
-            m = max(m, max(max(bf16x2_max_mag(v[i].x), bf16x2_max_mag(v[i].y)),
-                           max(bf16x2_max_mag(v[i].z), bf16x2_max_mag(v[i].w))));
-    } else {
-        for (int u = threadIdx.x; u < units; u += blockDim.x) {
-            const uint4 t = in[u];
-            m = max(m, max(max(bf16x2_max_mag(t.x), bf16x2_max_mag(t.y)), max(bf16x2_max_mag(t.z), bf16x2_max_mag(t.w))));
-        }
-    }
-    m = __reduce_max_sync(0xffffffffu, m);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-    __syncthreads();
-    m = red[0];
-#pragma unroll
-    for (int i = 1; i < kTcPrepThreads / 32; ++i) m = max(m, red[i]);
-    int mb = 0;
-    if (m != 0) {
-        const int e = (int)(m >> 7) - 127;            // exponent of max|x| (subnormal -> -127)
-        mb = min(max(e - 14, -126), 126);
-    }
-    const float finv = __uint_as_float((uint32_t)(127 - mb) << 23);
-    if (threadIdx.x == 0) xscale[b] = __uint_as_float((uint32_t)(mb + 127) << 23);
-    const int p = threadIdx.x & 3;                     // unit position within its 32-input block
-    auto emit = [&](int u, uint4 own) {
-        uint4 oth;
-        oth.x = __shfl_xor_sync(0xffffffffu, own.x, 2);
-        oth.y = __shfl_xor_sync(0xffffffffu, own.y, 2);
-        oth.z = __shfl_xor_sync(0xffffffffu, own.z, 2);
-        oth.w = __shfl_xor_sync(0xffffffffu, own.w, 2);
-        // p = 0/1: inputs 8p..8p+7 (low of the pair) with 16+8p.. (high): pairs 8p..8p+3
-        // p = 2/3: partner's low with own high: pairs 8(p-2)+4..+7
-        const uint4 lo = (p < 2) ? own : oth, hi = (p < 2) ? oth : own;
-        const uint32_t l0 = (p < 2) ? lo.x : lo.z, l1 = (p < 2) ? lo.y : lo.w;
-        const uint32_t h0 = (p < 2) ? hi.x : hi.z, h1 = (p < 2) ? hi.y : hi.w;
-        uint4 r;
-        r.x = pack_h2(l0 & 0xffffu, h0 & 0xffffu, finv);
-        r.y = pack_h2(l0 >> 16, h0 >> 16, finv);
-        r.z = pack_h2(l1 & 0xffffu, h1 & 0xffffu, finv);
-        r.w = pack_h2(l1 >> 16, h1 >> 16, finv);
-        const int q = u >> 2;
-        const int slot = (p == 0) ? 0 : (p == 2) ? 1 : (p == 1) ? 2 : 3;   // 16-byte slot in the block's 64 output bytes
-        if (u < units) out[4 * q + slot] = r;
-    };
-    if (resident) {
-#pragma unroll
-        for (int i = 0; i < kTcPrepUnits; ++i) {
-            const int u = threadIdx.x + i * kTcPrepThreads;
-            if (i * kTcPrepThreads < units) emit(u, v[i]);   // warp-uniform (units is a multiple of 128)
-        }
-    } else {
-        for (int u = threadIdx.x; u < units; u += blockDim.x) emit(u, in[u]);
-    }
+    tc_prep_row(b < B ? x + (size_t)b * K : nullptr, K, xp + (size_t)b * K, xscale + b, red);
 }
 
 // ---------------------------------------------------------------- main kernel
@@ -323,24 +215,7 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
             const uint32_t wsel = (step & 4) ? ((step & 2) ? sc_cur.w : sc_cur.z) : ((step & 2) ? sc_cur.y : sc_cur.x);
             const uint32_t s16 = (step & 1) ? (wsel >> 16) : (wsel & 0xffffu);
             const uint32_t s2 = live ? (s16 | (s16 << 16)) : 0u;
-            const uint32_t words[4] = {~w.x, ~w.y, ~w.z, ~w.w};
-            const uint32_t col0 = abase + 128u * st + 64u * h;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t v[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    // bits j and j+16 to the fp16 sign positions 15 and 31 (bit 1 -> +s); the
-                    // shift is written as a multiply so that it can issue on the FMA pipe
-                    uint32_t t;
-                    asm("mul.lo.u32 %0, %1, %2;" : "=r"(t) : "r"(words[q]), "r"(1u << (15 - j)));
-                    v[j] = (t & 0x80008000u) | s2;
-                }
-                asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-                             ::"r"(tmem + lane_base + col0 + 16u * q), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]),
-                               "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]),
-                               "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]) : "memory");
-            }
+            tc_unpack_step(w, s2, tmem + lane_base + abase + 128u * st + 64u * h);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;");
             __syncwarp();
@@ -355,19 +230,9 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
             asm volatile("tcgen05.fence::after_thread_sync;");
             for (int cb = 0; cb < p.Bp; cb += 16) {
                 uint32_t d[16], e[16];
-                asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-                             : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]), "=r"(d[4]), "=r"(d[5]), "=r"(d[6]),
-                               "=r"(d[7]), "=r"(d[8]), "=r"(d[9]), "=r"(d[10]), "=r"(d[11]), "=r"(d[12]), "=r"(d[13]),
-                               "=r"(d[14]), "=r"(d[15])
-                             : "r"(tmem + lane_base + (uint32_t)((wide ? h : 2 * h) * p.Bp + cb)) : "memory");
-                if (!wide) {
-                    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-                                 : "=r"(e[0]), "=r"(e[1]), "=r"(e[2]), "=r"(e[3]), "=r"(e[4]), "=r"(e[5]), "=r"(e[6]),
-                                   "=r"(e[7]), "=r"(e[8]), "=r"(e[9]), "=r"(e[10]), "=r"(e[11]), "=r"(e[12]), "=r"(e[13]),
-                                   "=r"(e[14]), "=r"(e[15])
-                                 : "r"(tmem + lane_base + (uint32_t)((2 * h + 1) * p.Bp + cb)) : "memory");
-                }
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                tc_ld16(tmem + lane_base + (uint32_t)((wide ? h : 2 * h) * p.Bp + cb), d);
+                if (!wide) tc_ld16(tmem + lane_base + (uint32_t)((2 * h + 1) * p.Bp + cb), e);
+                tc_wait_ld();
                 if (!wide) {
 #pragma unroll
                     for (int k = 0; k < 16; ++k) d[k] = __float_as_uint(__uint_as_float(d[k]) + __uint_as_float(e[k]));
@@ -439,10 +304,7 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
         // wide mode: warp (h, 0) issues every slice into the one accumulator of half h
         const int kk0 = wide ? 0 : q, kkd = wide ? 1 : 2;
         if (lane == 0 && !(wide && q == 1)) {
-            const uint32_t idesc = (1u << 4)                         // D: fp32
-                                   | (0u << 7) | (0u << 10)          // A, B: fp16
-                                   | ((uint32_t)(p.Bp >> 3) << 17)   // N
-                                   | ((uint32_t)(128 >> 4) << 24);   // M
+            const uint32_t idesc = tc_idesc_f16(p.Bp);
             const uint32_t d_addr = tmem + (uint32_t)((wide ? h : 2 * h + q) * p.Bp);
             for (int s = 0; s < nst; ++s) {
                 const int st = s % nstg;
@@ -454,18 +316,10 @@ k_gemv_tc(const __grid_constant__ CUtensorMap tm_bits, const __grid_constant__ C
                 asm volatile("tcgen05.fence::after_thread_sync;");
                 const uint32_t bst = bring + st * bstage;
                 const uint32_t a0 = tmem + abase + 128u * st + 64u * h;
-#pragma unroll
-                for (int kk = kk0; kk < kTcStepK / 16; kk += kkd) {
-                    const uint64_t bdesc = tc_desc_sw128(bst + (kk >> 2) * btile + (kk & 3) * 32);
-                    const uint32_t acc = (s > 0 || kk > kk0) ? 1u : 0u;
-                    asm volatile("{.reg .pred pa; setp.ne.b32 pa, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;}"
-                                 ::"r"(d_addr), "r"(a0 + 8u * kk), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
-                }
-                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                             ::"r"(freed + 8 * st) : "memory");
+                tc_mma_step(d_addr, a0, bst, btile, idesc, kk0, kkd, s == 0);
+                tc_commit(freed + 8 * st);
             }
-            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                         ::"r"(d_done) : "memory");
+            tc_commit(d_done);
             // no MMA may still be running when the tensor memory is released
             if (!mbar_wait(d_done, 0)) atomicOr(&g_tc_wait_timeouts, 8u);
         }

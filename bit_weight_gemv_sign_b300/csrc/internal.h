@@ -61,6 +61,12 @@ unsigned int t6_take_timeouts();
 // One kernel whose bounded wait runs out on purpose (sets *d_done = 1 on exit).
 cudaError_t launch_wait_selftest(unsigned int* d_done, cudaStream_t stream);
 
+// Grouped plans: the int at byte kPlanKindOffset of a plan's 128-byte
+// header says which grouped kernel it is for.
+constexpr int kPlanKindOffset = 68;
+constexpr int kPlanKindTables = 0;        // gemv_group.cu (CUDA cores, B <= 6)
+constexpr int kPlanKindTensor = 1;        // gemv_tc_group.cu (tensor cores, B <= 64)
+
 // Grouped persistent kernel (gemv_group.cu).
 size_t group_plan_bytes(int count);
 bit1_status group_plan(const bit1_gemv_problem* problems, int count, int nb, int layout, void* host_plan,
@@ -79,6 +85,15 @@ size_t tc_min_workspace_bytes(int64_t B, int64_t N, int64_t K);  // one 64-row c
 int tc_launch_count(int64_t B, int64_t N, int64_t K);
 cudaError_t launch_gemv_tc(const GemvArgs& a);
 unsigned int tc_take_timeouts();
+
+// Grouped persistent tensor-core kernel (gemv_tc_group.cu): B <= 64 rows per
+// problem, a caller-owned workspace for the activations' fp16 copies.
+size_t tcg_plan_bytes(int count);
+size_t tcg_workspace_bytes(const bit1_gemv_problem* problems, int count, int B);
+bit1_status tcg_plan(const bit1_gemv_problem* problems, int count, int B, void* workspace, size_t ws_bytes,
+                     void* host_plan, size_t bytes);
+cudaError_t launch_tc_group(const void* device_plan, const void* host_plan, bool pdl, cudaStream_t stream);
+unsigned int tcg_take_timeouts();
 
 // Ternary weights in 2-bit slots (ternary.cu).
 cudaError_t launch_ternary_planes(const int8_t* codes, int64_t N, int64_t K, uint8_t* a, uint8_t* b,

@@ -249,9 +249,40 @@ bit1_status bit1_group_plan_batched(const bit1_gemv_problem *problems, int count
 bit1_status bit1_group_plan_ex(const bit1_gemv_problem *problems, int count, int B,
                                int layout, void *host_plan, size_t plan_bytes);
 
-/* flags: BIT1_FLAG_PDL or 0. */
+/* Runs a plan made by any bit1_group_plan* call above or below (the plan
+ * records which kernel it is for).  flags: BIT1_FLAG_PDL or 0. */
 bit1_status bit1_gemv_group(const void *device_plan, const void *host_plan,
                             unsigned flags, bit1_stream_t stream);
+
+/* Grouped products on the tensor cores: the same problems (bit1_gemv_problem,
+ * same rules: K a multiple of 1024, 16-byte aligned device pointers, row-major
+ * x [B][K] bf16 and y [B][N] or [B][N/2] with BIT1_EPI_SWIGLU) at a batch of
+ * 1 <= B <= 64 rows shared by every problem (else BIT1_ESHAPE), for the
+ * multi-row verify pass of speculative decoding (the Bonsai 27B page,
+ * section "DSpark: 추측 디코딩으로 한 번 더 가속") and batched decode.  The
+ * arithmetic is bit1_gemv's BIT1_GEMV_TC path: weights +-s in fp16, the
+ * activations as fp16 with an exact per-row power-of-two prescale, fp32
+ * accumulation on the tensor cores; results equal BIT1_GEMV_TC's within the
+ * same tolerance (the summation order inside an MMA is the hardware's).
+ *
+ * Use: a caller-owned DEVICE workspace of bit1_group_tc_workspace_bytes()
+ * bytes (256-byte aligned; it receives the activations' fp16 copies on every
+ * run) and a HOST plan buffer of bit1_group_tc_plan_bytes(count) bytes
+ * (128-byte aligned); bit1_group_plan_tc() fills the plan, which the caller
+ * copies unchanged into a device buffer of the same size and runs with
+ * bit1_gemv_group (two launches: the activation prep, then one persistent
+ * kernel over all problems).  The plan embeds the problems' pointers and the
+ * workspace's: valid while those buffers are; runs of one plan must not
+ * overlap in time (they share the workspace).  Errors: BIT1_EINVAL for null
+ * or misaligned buffers or a workspace or plan buffer that is too small;
+ * BIT1_ESHAPE for a problem outside the rules or B outside [1, 64];
+ * BIT1_ECUDA if a tensor map cannot be encoded.  bit1_group_tc_workspace_bytes
+ * returns 0 on invalid arguments. */
+size_t bit1_group_tc_plan_bytes(int count);
+size_t bit1_group_tc_workspace_bytes(const bit1_gemv_problem *problems, int count, int B);
+bit1_status bit1_group_plan_tc(const bit1_gemv_problem *problems, int count, int B,
+                               void *workspace, size_t ws_bytes, void *host_plan,
+                               size_t plan_bytes);
 
 /* ------------------------------------------------------------------------
  * bit1_repack_g128x / bit1_unpack_g128x -- convert packed sign bits between

@@ -234,6 +234,41 @@ def test_group_plan_epilogue_checked_on_host(lib):
         assert lib.bit1_group_plan(ctypes.byref(p), 1, plan.ctypes.data, n) == b1.ESHAPE, (N, epi)
 
 
+def test_group_tc_plan_checked_on_host(lib):
+    """Tensor-core grouped plans: sizes and argument checks, all before any
+    CUDA call (a fake, aligned workspace address is never dereferenced)."""
+    import numpy as np
+    assert lib.bit1_group_tc_plan_bytes(0) == 0
+    n = lib.bit1_group_tc_plan_bytes(3)
+    assert n >= 3 * 256 + 128
+    raw = np.zeros(n + 128, dtype=np.uint8)
+    off = (-raw.ctypes.data) % 128
+    plan = raw[off:off + n]
+    probs = (b1._Problem * 2)(b1._Problem(FAKE, FAKE, FAKE, FAKE, 300, 4096, b1.F32, 0),
+                              b1._Problem(FAKE, FAKE, FAKE, FAKE, 64, 17408, b1.BF16, b1.EPI_SWIGLU))
+    # x' [Bp][K] fp16 and Bp scale factors per problem, each rounded up to 256 bytes
+    for B, Bp in ((1, 16), (5, 16), (16, 16), (17, 32), (64, 64)):
+        want = sum(Bp * K * 2 + (Bp * 4 + 255) // 256 * 256 for K in (4096, 17408))
+        assert lib.bit1_group_tc_workspace_bytes(probs, 2, B) == want, B
+    for B in (0, 65, -1):
+        assert lib.bit1_group_tc_workspace_bytes(probs, 2, B) == 0
+    ws = lib.bit1_group_tc_workspace_bytes(probs, 2, 16)
+    call = lambda B=16, w=FAKE, wsz=ws, pl=plan.ctypes.data, nb=n, pr=probs, c=2: \
+        lib.bit1_group_plan_tc(pr, c, B, w, wsz, pl, nb)
+    assert call(B=0) == b1.ESHAPE and call(B=65) == b1.ESHAPE
+    assert call(w=FAKE + 128) == b1.EINVAL                     # workspace not 256-byte aligned
+    assert call(w=None) == b1.EINVAL
+    assert call(wsz=ws - 1) == b1.EINVAL                        # workspace too small
+    assert call(nb=lib.bit1_group_tc_plan_bytes(2) - 1) == b1.EINVAL   # plan buffer too small
+    assert call(pl=plan.ctypes.data + 8, nb=n - 8) == b1.EINVAL  # plan not 128-byte aligned
+    assert call(c=0) == b1.EINVAL
+    bad = (b1._Problem * 1)(b1._Problem(FAKE, FAKE, FAKE, FAKE, 300, 1152, b1.F32, 0))   # K % 1024 != 0
+    assert lib.bit1_group_tc_workspace_bytes(bad, 1, 16) == 0
+    assert call(pr=bad, c=1) == b1.ESHAPE
+    odd = (b1._Problem * 1)(b1._Problem(FAKE, FAKE, FAKE, FAKE, 63, 1024, b1.F32, b1.EPI_SWIGLU))
+    assert call(pr=odd, c=1) == b1.ESHAPE
+
+
 def test_sweep_feeds_swiglu_output_to_the_next_matrix():
     """Host wiring of the fused chain: the matrix after a SwiGLU matrix reads
     its h; a grouped plan over such a sweep is refused (its problems run
