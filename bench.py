@@ -649,27 +649,36 @@ def extra_t5(torch, b1, reps=20):
     return out
 
 
-def extra_verify_sweep_8b(torch, b1, B=5, steps=20):
-    """A speculative-decoding verify pass on the 8B-class sweep: every matrix
-    multiplies B = 5 rows (four drafted tokens plus one) in one grouped launch,
-    against the same 253 products as per-matrix batched launches (graph + PDL)
-    and the batch-1 sweep."""
-    from bit_weight_gemv_sign_b300 import synth
-    from bit_weight_gemv_sign_b300.sweep import Sweep
-    sw = Sweep(synth.sweep_8b(), seed0=0, batch=B, y_dtype=b1.BF16).fill_device(55)
-    plan = sw.group_plan()
+def _time_plan(torch, plan, steps, flags=0):
+    """Mean ms of plan.run() over `steps` back-to-back runs on a side stream."""
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         for _ in range(3):
-            plan.run(stream=s)
+            plan.run(flags=flags, stream=s)
         s.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
         for _ in range(steps):
-            plan.run(stream=s)
+            plan.run(flags=flags, stream=s)
         e1.record(s)
         e1.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+    return e0.elapsed_time(e1) / steps
+
+
+def extra_verify_sweep_8b(torch, b1, B=5, steps=20):
+    """A speculative-decoding verify pass on the 8B-class sweep: every matrix
+    multiplies B = 5 rows (four drafted tokens plus one), as one grouped
+    table-lookup launch and as one grouped tensor-core plan (prep + persistent
+    tcgen05 kernel), against the same 253 products as per-matrix batched
+    launches (graph + PDL) and the batch-1 sweep."""
+    from bit_weight_gemv_sign_b300 import synth
+    from bit_weight_gemv_sign_b300.sweep import Sweep
+    sw = Sweep(synth.sweep_8b(), seed0=0, batch=B, y_dtype=b1.BF16).fill_device(55)
+    plan = sw.group_plan()
+    ms = _time_plan(torch, plan, steps)
+    tc_plan = sw.group_plan(tensor_cores=True)
+    ms_tc = _time_plan(torch, tc_plan, steps, flags=b1.FLAG_PDL)
+    del tc_plan
     sw.capture(pdl=True)
     with torch.cuda.stream(sw.stream):       # graph replays run on the current stream
         for _ in range(2):
@@ -684,12 +693,40 @@ def extra_verify_sweep_8b(torch, b1, B=5, steps=20):
     ms_chain = c0.elapsed_time(c1) / 5
     hbm, _ = _peaks()
     gbs = sw.weight_bytes / (ms * 1e-3) / 1e9
-    out = {"batch_rows": B, "weight_bytes": sw.weight_bytes, "ms_per_verify_step": ms,
-           "ms_per_token_row": ms / B, "weight_gbs": gbs, "hbm_frac": gbs / hbm,
+    gbs_tc = sw.weight_bytes / (ms_tc * 1e-3) / 1e9
+    best = min(ms, ms_tc)
+    out = {"batch_rows": B, "weight_bytes": sw.weight_bytes, "ms_per_verify_step": best,
+           "ms_per_token_row": best / B, "weight_gbs": sw.weight_bytes / (best * 1e-3) / 1e9,
+           "hbm_frac": sw.weight_bytes / (best * 1e-3) / 1e9 / hbm,
+           "table_lookups_grouped": {"ms_per_verify_step": ms, "ms_per_token_row": ms / B, "weight_gbs": gbs,
+                                     "launches_per_step": 1},
+           "tensor_cores_grouped": {"ms_per_verify_step": ms_tc, "ms_per_token_row": ms_tc / B,
+                                    "weight_gbs": gbs_tc, "launches_per_step": 2},
            "ms_per_step_per_matrix_launches": ms_chain, "launches_per_step_per_matrix": sw.launches_per_step(),
-           "note": "one grouped launch per step; compare ms_per_token_row with the batch-1 sweep's ms_per_step"}
+           "note": "best of the two grouped plans; compare ms_per_token_row with the batch-1 sweep's ms_per_step"}
     del sw, plan
     torch.cuda.empty_cache()
+    return out
+
+
+def extra_batched_sweep_8b(torch, b1, batches=(16, 64), steps=10):
+    """Batched decode on the 8B-class sweep: every matrix multiplies B rows in
+    one grouped tensor-core plan (prep + persistent tcgen05 kernel)."""
+    from bit_weight_gemv_sign_b300 import synth
+    from bit_weight_gemv_sign_b300.sweep import Sweep
+    hbm, _ = _peaks()
+    out = {}
+    for B in batches:
+        sw = Sweep(synth.sweep_8b(), seed0=0, batch=B, y_dtype=b1.BF16).fill_device(60 + B)
+        plan = sw.group_plan(tensor_cores=True)
+        ms = _time_plan(torch, plan, steps, flags=b1.FLAG_PDL)
+        gbs = sw.weight_bytes / (ms * 1e-3) / 1e9
+        flops = 2.0 * B * sum(m.N * m.K for m in sw.mats)
+        out[f"B{B}"] = {"ms_per_step": ms, "ms_per_token_row": ms / B, "weight_gbs": gbs, "hbm_frac": gbs / hbm,
+                        "tflops": flops / (ms * 1e-3) / 1e12, "launches_per_step": 2}
+        del sw, plan
+        torch.cuda.empty_cache()
+    out["note"] = "weight_gbs counts each weight byte once per step (B rows per read)"
     return out
 
 
@@ -958,6 +995,7 @@ def run_mine(args):
                          "ternary_sweep_8b": extra_ternary_sweep_8b(torch, b1),
                          "ternary_t5": extra_t5(torch, b1),
                          "verify_sweep_8b_b5": extra_verify_sweep_8b(torch, b1),
+                         "batched_sweep_8b_tc": extra_batched_sweep_8b(torch, b1),
                          "fused_mlp_sweep_8b": extra_fused_mlp_sweep_8b(torch, b1)}
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
