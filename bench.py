@@ -668,9 +668,10 @@ def _time_plan(torch, plan, steps, flags=0):
 def extra_verify_sweep_8b(torch, b1, B=5, steps=20):
     """A speculative-decoding verify pass on the 8B-class sweep: every matrix
     multiplies B = 5 rows (four drafted tokens plus one), as one grouped
-    table-lookup launch and as one grouped tensor-core plan (prep + persistent
-    tcgen05 kernel), against the same 253 products as per-matrix batched
-    launches (graph + PDL) and the batch-1 sweep."""
+    table-lookup launch, as one grouped launch on register-sourced MMAs, and
+    as one grouped tensor-core plan (prep + persistent tcgen05 kernel),
+    against the same 253 products as per-matrix batched launches (graph +
+    PDL) and the batch-1 sweep."""
     from bit_weight_gemv_sign_b300 import synth
     from bit_weight_gemv_sign_b300.sweep import Sweep
     sw = Sweep(synth.sweep_8b(), seed0=0, batch=B, y_dtype=b1.BF16).fill_device(55)
@@ -679,6 +680,9 @@ def extra_verify_sweep_8b(torch, b1, B=5, steps=20):
     tc_plan = sw.group_plan(tensor_cores=True)
     ms_tc = _time_plan(torch, tc_plan, steps, flags=b1.FLAG_PDL)
     del tc_plan
+    mma_plan = sw.group_plan(mma=True)
+    ms_mma = _time_plan(torch, mma_plan, steps, flags=b1.FLAG_PDL)
+    del mma_plan
     sw.capture(pdl=True)
     with torch.cuda.stream(sw.stream):       # graph replays run on the current stream
         for _ in range(2):
@@ -694,7 +698,7 @@ def extra_verify_sweep_8b(torch, b1, B=5, steps=20):
     hbm, _ = _peaks()
     gbs = sw.weight_bytes / (ms * 1e-3) / 1e9
     gbs_tc = sw.weight_bytes / (ms_tc * 1e-3) / 1e9
-    best = min(ms, ms_tc)
+    best = min(ms, ms_tc, ms_mma)
     out = {"batch_rows": B, "weight_bytes": sw.weight_bytes, "ms_per_verify_step": best,
            "ms_per_token_row": best / B, "weight_gbs": sw.weight_bytes / (best * 1e-3) / 1e9,
            "hbm_frac": sw.weight_bytes / (best * 1e-3) / 1e9 / hbm,
@@ -702,8 +706,10 @@ def extra_verify_sweep_8b(torch, b1, B=5, steps=20):
                                      "launches_per_step": 1},
            "tensor_cores_grouped": {"ms_per_verify_step": ms_tc, "ms_per_token_row": ms_tc / B,
                                     "weight_gbs": gbs_tc, "launches_per_step": 2},
+           "mma_engine_grouped": {"ms_per_verify_step": ms_mma, "ms_per_token_row": ms_mma / B,
+                                  "weight_gbs": sw.weight_bytes / (ms_mma * 1e-3) / 1e9, "launches_per_step": 1},
            "ms_per_step_per_matrix_launches": ms_chain, "launches_per_step_per_matrix": sw.launches_per_step(),
-           "note": "best of the two grouped plans; compare ms_per_token_row with the batch-1 sweep's ms_per_step"}
+           "note": "best of the three grouped plans; compare ms_per_token_row with the batch-1 sweep's ms_per_step"}
     del sw, plan
     torch.cuda.empty_cache()
     return out

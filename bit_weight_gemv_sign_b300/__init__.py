@@ -103,6 +103,8 @@ def load():
         lib.bit1_group_plan_batched.restype = i32
         lib.bit1_group_plan_ex.argtypes = [ctypes.POINTER(_Problem), i32, i32, i32, p, sz]
         lib.bit1_group_plan_ex.restype = i32
+        lib.bit1_group_plan_mma.argtypes = [ctypes.POINTER(_Problem), i32, i32, p, sz]
+        lib.bit1_group_plan_mma.restype = i32
         lib.bit1_repack_g128x.argtypes = [p, i64, i64, p, p]
         lib.bit1_repack_g128x.restype = i32
         lib.bit1_unpack_g128x.argtypes = [p, i64, i64, p, p]
@@ -333,14 +335,19 @@ def bit1_group_plan_tc(problems, B: int, workspace, host_plan_ptr: int, plan_byt
 
 
 def bit1_group_plan(problems, host_plan_ptr: int, plan_bytes: int, B: int = 1,
-                    layout: int = LAYOUT_CANONICAL) -> None:
+                    layout: int = LAYOUT_CANONICAL, mma: bool = False) -> None:
     """problems: sequence of (bits, scales, x, y) or (bits, scales, x, y,
     epilogue) CUDA tensors; x is [B, K] (or [K] at B = 1) bf16 and y [B, N]
     ([B, N/2] with EPI_SWIGLU, the rows then interleaved gate/up pairs).
     B > 1 calls bit1_group_plan_batched; a non-canonical ``layout`` (every
-    problem's bits converted with bit1_repack_g128x) bit1_group_plan_ex."""
+    problem's bits converted with bit1_repack_g128x) bit1_group_plan_ex;
+    ``mma`` bit1_group_plan_mma (register-sourced MMAs, B <= 16)."""
     arr = _problem_array(problems)
-    if layout != LAYOUT_CANONICAL:
+    if mma:
+        if layout != LAYOUT_CANONICAL:
+            raise ValueError("the MMA engine takes the canonical layout")
+        st = load().bit1_group_plan_mma(arr, len(problems), int(B), host_plan_ptr, plan_bytes)
+    elif layout != LAYOUT_CANONICAL:
         st = load().bit1_group_plan_ex(arr, len(problems), int(B), int(layout), host_plan_ptr, plan_bytes)
     elif B == 1:
         st = load().bit1_group_plan(arr, len(problems), host_plan_ptr, plan_bytes)
@@ -383,10 +390,11 @@ class GroupPlan:
     """A grouped-GEMV plan: the encoded host copy and its device copy (both
     128-byte aligned).  The tensors named in ``problems`` must stay alive and
     in place while the plan is used.  ``tensor_cores``: the tcgen05 grouped
-    kernel (B <= 64, canonical layout; the plan owns its workspace)."""
+    kernel (B <= 64, canonical layout; the plan owns its workspace); ``mma``:
+    the grouped kernel's register-sourced MMA engine (B <= 16)."""
 
     def __init__(self, problems, device="cuda", B: int = 1, layout: int = LAYOUT_CANONICAL,
-                 tensor_cores: bool = False):
+                 tensor_cores: bool = False, mma: bool = False):
         import numpy as np
         import torch
         self.problems = list(problems)
@@ -409,7 +417,7 @@ class GroupPlan:
         if self.tensor_cores:
             bit1_group_plan_tc(self.problems, self.B, self.workspace, self.host.ctypes.data, self.nbytes)
         else:
-            bit1_group_plan(self.problems, self.host.ctypes.data, self.nbytes, self.B, self.layout)
+            bit1_group_plan(self.problems, self.host.ctypes.data, self.nbytes, self.B, self.layout, mma=mma)
         self._dev_raw = torch.empty(self.nbytes + 128, dtype=torch.uint8, device=device)
         doff = (-self._dev_raw.data_ptr()) % 128
         self.dev = self._dev_raw[doff: doff + self.nbytes]

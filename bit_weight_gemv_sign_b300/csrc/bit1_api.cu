@@ -279,18 +279,23 @@ size_t bit1_group_plan_bytes(int count) { return group_plan_bytes(count); }
 
 bit1_status bit1_group_plan(const bit1_gemv_problem* problems, int count, void* host_plan,
                             size_t plan_bytes) {
-    return group_plan(problems, count, 1, BIT1_LAYOUT_CANONICAL, host_plan, plan_bytes);
+    return group_plan(problems, count, 1, BIT1_LAYOUT_CANONICAL, 0, host_plan, plan_bytes);
 }
 
 bit1_status bit1_group_plan_batched(const bit1_gemv_problem* problems, int count, int B, void* host_plan,
                                     size_t plan_bytes) {
-    return group_plan(problems, count, B, BIT1_LAYOUT_CANONICAL, host_plan, plan_bytes);
+    return group_plan(problems, count, B, BIT1_LAYOUT_CANONICAL, 0, host_plan, plan_bytes);
+}
+
+bit1_status bit1_group_plan_mma(const bit1_gemv_problem* problems, int count, int B, void* host_plan,
+                                size_t plan_bytes) {
+    return group_plan(problems, count, B, BIT1_LAYOUT_CANONICAL, 1, host_plan, plan_bytes);
 }
 
 bit1_status bit1_group_plan_ex(const bit1_gemv_problem* problems, int count, int B, int layout, void* host_plan,
                                size_t plan_bytes) {
     if (layout != BIT1_LAYOUT_CANONICAL && layout != BIT1_LAYOUT_G128X) return BIT1_EINVAL;
-    return group_plan(problems, count, B, layout, host_plan, plan_bytes);
+    return group_plan(problems, count, B, layout, 0, host_plan, plan_bytes);
 }
 
 bit1_status bit1_repack_g128x(const uint8_t* bits, int64_t N, int64_t K, uint8_t* out, bit1_stream_t stream) {

@@ -48,7 +48,10 @@ constexpr int kGWarps = 20;
 constexpr int kGMaxSmem = 227 * 1024;
 constexpr int kGSegBlocks = 128;             // sub-segment cap: 4096 rows of partials
 constexpr int kGMaxProbsPerCta = 64;         // problems one CTA's range may touch
-constexpr int kGMaxNB = 6;                   // batch rows per grouped launch
+constexpr int kGMaxNB = 6;                   // batch rows per grouped launch (table engine)
+constexpr int kGMaxNBMma = 16;               // batch rows per grouped launch (MMA engine)
+constexpr int kGEngineTables = 0;            // 6-bit tables, one lookup per six inputs and batch row
+constexpr int kGEngineMma = 1;               // register-sourced mma.sync, batch rows as the MMA's N
 
 // K chunk (groups) at nb batch rows: the tables of all rows, nb * CG * 2816
 // bytes, stay at about 90 KB.
@@ -68,7 +71,8 @@ struct GHeader {            // 128 bytes
     uint32_t off_pinfo;     // per-problem {RB, G, nch, N} of the CTA's range
     int layout;             // sign-bit layout of every problem (kLayoutCanonical or kLayoutG128x)
     int kind;               // kPlanKindTables
-    int pad[14];
+    int engine;             // kGEngineTables or kGEngineMma
+    int pad[13];
 };
 static_assert(sizeof(GHeader) == 128, "header size");
 static_assert(offsetof(GHeader, kind) == kPlanKindOffset, "kind offset");
@@ -540,6 +544,290 @@ __device__ __forceinline__ void g_body(const uint8_t* plan) {
     }
 }
 
+// ---------------------------------------------------------------- MMA engine
+// Several batch rows (2..16) on register-sourced tensor-core MMAs
+// (mma.sync m16n8k16, fp16 operands, fp32 accumulators).  The table engine's
+// lookups grow with the batch rows; here the per-weight work (forming +-s as
+// fp16 in a register: one multiply-as-shift and one LOP3 per two weights) is
+// the same for every batch up to the MMA's N = 8 (NT = 1) or 16 (NT = 2).
+// The A fragments never leave registers, so nothing is written to shared or
+// tensor memory per weight, and each warp's MMAs depend on nothing but its own
+// stage: no cross-warp hand-off per step.
+//
+// Within each 32-bit sign word, inputs k and k + 16 share one fp16x2
+// register (sign bits 15 and 31 of s | s << 16), pair j = (k, k + 16) for
+// j = 0..15.  Of a word's 16 pairs, MMA k-step h (two per word) takes pairs
+// 8h..8h+7: slot pair c of the fragment (thread c = lane % 4) holds pair
+// 8h + c, slot pair c + 4 holds pair 8h + c + 4.  The activations are laid
+// out in the same K order, so the contraction is unchanged.  Per phase, the
+// CTA converts its K chunk of activations to fp16 fragments with one
+// power-of-two prescale per batch row (max |x'| in [2^14, 2^15), exact for
+// every bf16 value within 2^29 of the chunk's largest), and the per-chunk
+// sums are scaled back before they join the row's other chunks.  The chunk
+// is read straight from global memory (L2) at the phase boundary: with 4096
+// inputs per chunk a CTA has only a few phases, and the shared memory a
+// staged copy would take goes to larger sub-segments instead.
+__host__ __device__ constexpr int g_mma_nt(int nb) { return nb <= 8 ? 1 : 2; }
+// K chunk: 4096 inputs (B <= 8) or 2048 (B > 8), 64 KB of fragments either way;
+// sub-segments of multi-chunk problems: 64 KB of partials.
+__host__ __device__ constexpr int g_mma_chunk_groups(int nb) { return nb <= 8 ? 32 : 16; }
+__host__ __device__ constexpr int g_mma_seg_blocks(int nb) { return nb <= 4 ? 128 : nb <= 8 ? 64 : 32; }
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint2 b) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b.x), "r"(b.y));
+}
+// Pair j of the sign word w as an fp16x2 +-s: bits j and j + 16 moved to the
+// sign positions 15 and 31 (a multiply by mul = 2^(15 - j), so the shift can
+// issue on the FMA pipe; both come from real bits of w since j <= 15), then
+// inverted (bit 0 -> negative) and applied to s2 = s | s << 16 in one LOP3.
+__device__ __forceinline__ uint32_t g_pair(uint32_t w, uint32_t mul, uint32_t s2) {
+    uint32_t t;
+    asm("mul.lo.u32 %0, %1, %2;" : "=r"(t) : "r"(w), "r"(mul));
+    return (~t & 0x80008000u) ^ s2;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+
+template <int NT, int CG, int S>
+__device__ __forceinline__ void g_body_mma(const uint8_t* plan) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (base - raw);
+
+    const GHeader* H = reinterpret_cast<const GHeader*>(plan);
+    const int W = H->W, prows = H->part_rows, NB = H->nb;
+    GCtx<CG, false> cx;
+    cx.P = reinterpret_cast<const GProb*>(plan + H->probs_off);
+    cx.R = reinterpret_cast<const GRange*>(plan + H->ranges_off)[blockIdx.x];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    cx.w = warp;
+    cx.W = W;
+    cx.seg_blocks = H->seg_blocks;
+    int4* pinfo = reinterpret_cast<int4*>(sm + H->off_pinfo);
+    for (int i = threadIdx.x; i <= cx.R.p1 - cx.R.p0 && i < kGMaxProbsPerCta; i += blockDim.x) {
+        const GProb& q = cx.P[cx.R.p0 + i];
+        pinfo[i] = make_int4(q.RB, q.G, q.nch, q.N);
+    }
+    cx.I = pinfo;
+    __syncthreads();
+    const GProb* P = cx.P;
+    const uint32_t bars = base + H->off_bars + (uint32_t)(warp * S) * 8u;
+    const uint32_t stages = base + (uint32_t)(warp * S) * kGStageBytes;
+
+    GIter prod = cx.first();
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(bars + 8u * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int s = 0; s < S && !cx.done(prod); ++s) {
+            g_issue(prod, stages + (uint32_t)s * kGStageBytes, bars + 8u * s);
+            cx.next(prod);
+        }
+    } else {
+        for (int s = 0; s < S && !cx.done(prod); ++s) cx.next(prod);
+    }
+    __syncwarp();
+
+    pdl_wait();     // x may come from the preceding kernel
+    float* fac = reinterpret_cast<float*>(sm + H->off_fac);     // [0, 16): 2^-m_b; [16, 32): 2^m_b
+    float* part = reinterpret_cast<float*>(sm + H->off_part);
+    uint2* xf = reinterpret_cast<uint2*>(sm + H->off_tables);    // [NT][CG * 8 k-steps][32 lanes]
+    const uint32_t xf_s = base + H->off_tables;
+
+    const int g = lane >> 2, c = lane & 3;
+    const uint32_t mul0 = 1u << (15 - c), mul1 = 1u << (11 - c), mul2 = 1u << (7 - c), mul3 = 1u << (3 - c);
+    const uint32_t swz = (uint32_t)g << 4;           // rows g, g + 8, 16 + g, 24 + g: swizzle (row % 8) = g
+    int k = 0, sk = 0;
+    uint32_t ph = 0;
+    int kfail = -1;
+    bool ok = true;
+    for (int p = cx.R.p0; p <= cx.R.p1; ++p) {
+      const GProb& pr = P[p];
+      const int4 pi = cx.info(p);             // RB, G, nch, N
+      for (int sb = cx.bs(p); sb < cx.be(p); sb += cx.mb(p)) {
+        const int be = cx.se(p, sb);
+        for (int ch = 0; ch < pi.z; ++ch) {
+            const int cg = min(CG, pi.y - CG * ch);
+            const uint16_t* xc = pr.x + (size_t)ch * CG * 128;   // this chunk of batch row 0; row b at + b K
+            __syncthreads();                                   // old fragments no longer read
+            // per batch row: largest finite |x| of the chunk -> prescale 2^-m
+            for (int b = warp; b < NB; b += W) {
+                uint32_t m = 0;
+                for (int u = lane; u < cg * 16; u += 32) {     // 16-byte units of the row's chunk
+                    const uint4 v = *reinterpret_cast<const uint4*>(xc + (size_t)b * pr.K + 8 * u);
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t lo = w4[i] & 0x7fffu, hi = (w4[i] >> 16) & 0x7fffu;
+                        m = max(m, max(lo > 0x7f80u ? 0u : lo, hi > 0x7f80u ? 0u : hi));
+                    }
+                }
+                m = __reduce_max_sync(0xffffffffu, m);
+                int mb = 0;
+                if (m != 0) mb = min(max((int)(m >> 7) - 127 - 14, -126), 126);
+                if (lane == 0) {
+                    fac[b] = __uint_as_float((uint32_t)(127 - mb) << 23);
+                    fac[16 + b] = __uint_as_float((uint32_t)(127 + mb) << 23);
+                }
+            }
+            __syncthreads();
+            // fragments: entry (nt, q, l) = batch row 8 nt + l / 4, k-step q of the chunk
+            {
+                const int per_nt = cg * 8 * 32;
+                for (int e = threadIdx.x; e < NT * per_nt; e += blockDim.x) {
+                    const int nt = e / per_nt, rem = e - nt * per_nt, q = rem >> 5, l = rem & 31;
+                    const int n = 8 * nt + (l >> 2), cc = l & 3;
+                    uint2 v = make_uint2(0u, 0u);
+                    if (n < NB) {
+                        const int kb = (q >> 3) * 128 + 32 * ((q & 7) >> 1) + 8 * (q & 1) + cc;
+                        const uint16_t* xs = xc + (size_t)n * pr.K + kb;
+                        const float f = fac[n];
+                        const __half2 h0 = __floats2half2_rn(bf16_bits_to_f32(xs[0]) * f, bf16_bits_to_f32(xs[16]) * f);
+                        const __half2 h1 = __floats2half2_rn(bf16_bits_to_f32(xs[4]) * f, bf16_bits_to_f32(xs[20]) * f);
+                        v.x = *reinterpret_cast<const uint32_t*>(&h0);
+                        v.y = *reinterpret_cast<const uint32_t*>(&h1);
+                    }
+                    xf[(nt * CG * 8 + q) * 32 + l] = v;
+                }
+            }
+            __syncthreads();
+            if (p == cx.R.p0 && sb == cx.bs(p) && ch == 0) pdl_launch_dependents();
+
+            const int nsl = cg >> 3;
+            // One stage (32 rows x 8 groups): 2 row tiles x 64 k-steps of MMAs.
+            auto consume = [&](int j, float (&acc)[2][NT][4]) {
+                if (ok && !mbar_wait(bars + 8u * sk, ph)) {
+                    if (lane == 0) atomicOr(&g_group_wait_timeouts, 1u);
+                    ok = false;
+                    kfail = k;
+                }
+                {
+                    const uint32_t st = stages + (uint32_t)sk * kGStageBytes;
+                    uint32_t sw[4];     // scales of groups jj, jj + 1 (jj even) of rows g, g + 8, 16 + g, 24 + g
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        uint4 w[4];
+                        uint32_t s2[4];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            w[r] = lds128(st + (uint32_t)(g + 8 * r) * 128u + (((uint32_t)jj << 4) ^ swz));
+                            if (!(jj & 1)) sw[r] = lds32(st + 4096u + 16u * (uint32_t)(g + 8 * r) + 2u * (uint32_t)jj);
+                            s2[r] = __byte_perm(sw[r], 0u, (jj & 1) ? 0x3232u : 0x1010u);   // s | s << 16
+                        }
+                        const uint32_t q0 = (uint32_t)((8 * j + jj) * 8);       // first k-step of the group in the chunk
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            uint32_t nw[4];
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) nw[r] = i == 0 ? w[r].x : i == 1 ? w[r].y : i == 2 ? w[r].z : w[r].w;
+#pragma unroll
+                            for (int hh = 0; hh < 2; ++hh) {
+                                const uint32_t ma = hh ? mul2 : mul0, mc = hh ? mul3 : mul1;
+                                uint2 bf[NT];
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt)
+                                    bf[nt] = lds64(xf_s + (((uint32_t)nt * CG * 8u + q0 + 2u * i + hh) * 32u + lane) * 8u);
+#pragma unroll
+                                for (int mt = 0; mt < 2; ++mt) {
+                                    const int r0 = 2 * mt, r1 = 2 * mt + 1;     // rows 16 mt + g and 16 mt + g + 8
+                                    const uint32_t a0 = g_pair(nw[r0], ma, s2[r0]), a1 = g_pair(nw[r1], ma, s2[r1]);
+                                    const uint32_t a2 = g_pair(nw[r0], mc, s2[r0]), a3 = g_pair(nw[r1], mc, s2[r1]);
+#pragma unroll
+                                    for (int nt = 0; nt < NT; ++nt) mma16816(acc[mt][nt], a0, a1, a2, a3, bf[nt]);
+                                }
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                g_issue_pred(prod, stages + (uint32_t)sk * kGStageBytes, bars + 8u * sk,
+                             lane == 0 && ok && !cx.done(prod));
+                if (!cx.done(prod)) cx.next(prod);
+                ++k;
+                if (++sk == S) {
+                    sk = 0;
+                    ph ^= 1u;
+                }
+            };
+            // Block b's sums for this chunk, scaled back by 2^m per batch row:
+            // carried in `part` to the next chunk or written to y.
+            auto finish = [&](int b, float (&acc)[2][NT][4]) {
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int rl = 16 * mt + g + 8 * (e >> 1);       // row within the block
+                            const int bb = 8 * nt + 2 * c + (e & 1);         // batch row
+                            const int row = b * 32 + rl;
+                            const int li = (b - sb) * 32 + rl;
+                            float v = acc[mt][nt][e] * fac[16 + (bb < NB ? bb : 0)];
+                            if (pi.z > 1) {
+                                const int pl = bb * prows + li;
+                                if (bb < NB && ch > 0) v += part[pl];
+                                if (ch + 1 < pi.z) {
+                                    if (bb < NB) part[pl] = v;
+                                    continue;
+                                }
+                            }
+                            if (pr.swiglu) {
+                                // rows 2u (gate) and 2u + 1 (up) sit in lanes 4 apart
+                                const float u = __shfl_xor_sync(0xffffffffu, v, 4);
+                                if (!(g & 1) && bb < NB && row < pi.w) {
+                                    const float h = v / (1.f + expf(-v)) * u;
+                                    const int64_t o = (int64_t)bb * (pi.w >> 1) + (row >> 1);
+                                    if (pr.y_bf16) reinterpret_cast<uint16_t*>(pr.y)[o] = f32_to_bf16_bits(h);
+                                    else reinterpret_cast<float*>(pr.y)[o] = h;
+                                }
+                            } else if (bb < NB && row < pi.w) {
+                                const int64_t o = (int64_t)bb * pi.w + row;
+                                if (pr.y_bf16) reinterpret_cast<uint16_t*>(pr.y)[o] = f32_to_bf16_bits(v);
+                                else reinterpret_cast<float*>(pr.y)[o] = v;
+                            }
+                        }
+                    }
+                }
+            };
+            const int n = be - sb;
+            const int q = cx.full_blocks(n);
+            for (int i = 0; i < q; ++i) {
+                float acc[2][NT][4];
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
+                for (int j = 0; j < nsl; ++j) consume(j, acc);
+                finish(sb + warp + W * i, acc);
+            }
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+        for (int kk = kfail + 1; kk < kfail + S; ++kk)
+            (void)mbar_wait(bars + 8u * (kk % S), (uint32_t)(kk / S) & 1u);
+    }
+}
+
+// NT: 8-column MMA tiles (1: up to 8 batch rows, 2: up to 16); canonical layout
+// only; at most 16 warps, so 128 registers a thread.
+template <int NT, int S>
+__global__ void __launch_bounds__(16 * 32, 1) k_gemv_group_mma(const uint8_t* __restrict__ plan) {
+    g_body_mma<NT, g_mma_chunk_groups(8 * NT), S>(plan);
+}
+
 // S: TMA stages per warp ring (the plan's H->S); L: the sign-bit layout (the
 // plan's H->layout).  One instantiation per value the planner can choose.
 template <int S, int L>
@@ -580,7 +868,10 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode() {
     return fn;
 }
 
-bool encode_prob(GProb& g, const bit1_gemv_problem& pb, int nb) {
+int chunk_groups(int nb, int engine) { return engine == kGEngineMma ? g_mma_chunk_groups(nb) : g_chunk_groups(nb); }
+int seg_blocks(int nb, int engine) { return engine == kGEngineMma ? g_mma_seg_blocks(nb) : g_seg_blocks(nb); }
+
+bool encode_prob(GProb& g, const bit1_gemv_problem& pb, int nb, int engine) {
     auto enc = g_encode();
     if (!enc) return false;
     const int64_t G = pb.K / 128;
@@ -612,7 +903,7 @@ bool encode_prob(GProb& g, const bit1_gemv_problem& pb, int nb) {
     g.RB = (int)((pb.N + 31) / 32);
     g.y_bf16 = pb.y_dtype == BIT1_BF16;
     g.swiglu = pb.epilogue == BIT1_EPI_SWIGLU;
-    const int cg = g_chunk_groups(nb);
+    const int cg = chunk_groups(nb, engine);
     g.nch = (int)((G + cg - 1) / cg);
     return true;
 }
@@ -632,22 +923,28 @@ constexpr double kGPhaseFixed = 6.0 * 4096;   // batch 1: a phase's barriers, ac
 constexpr double kGPhaseTables = 6.0 * 4096;  // batch 1: building a full chunk's tables (32 groups)
 
 // Cost of the table builds of one pass over all K chunks of problem p.
-double phase_cost(const GProb& pr, int nb) {
+double phase_cost(const GProb& pr, int nb, int engine) {
+    if (engine == kGEngineMma) return kGPhaseFixed * pr.nch;     // barriers, prescales, fragment build
     if (nb > 1) return kGBuildCost * pr.nch * (nb * g_chunk_groups(nb) / 32.0);
     return kGPhaseFixed * pr.nch + kGPhaseTables * (double)pr.G / g_chunk_groups(1);
 }
+// Cost of a 32-row block per input, relative to batch 1's table lookups.
+double row_factor(int nb, int engine) {
+    if (engine == kGEngineMma) return g_mma_nt(nb) == 1 ? 1.5 : 2.5;   // per weight, not per batch row
+    return 1.0 + 0.8 * (nb - 1);                  // lookups grow with the batch, the weight reads do not
+}
 
-int partition(const std::vector<GProb>& probs, double T, std::vector<GRange>* out, int nb) {
+int partition(const std::vector<GProb>& probs, double T, std::vector<GRange>* out, int nb, int engine) {
     const int n = (int)probs.size();
-    const int seg = g_seg_blocks(nb);
-    const double rowf = 1.0 + 0.8 * (nb - 1);     // lookups grow with the batch, the weight reads do not
+    const int seg = seg_blocks(nb, engine);
+    const double rowf = row_factor(nb, engine);
     int ctas = 1;
     double cur = 0.0;
     GRange r{0, 0, 0, 0};
     for (int p = 0; p < n; ++p) {
         int taken = 0;
         const double c = (double)probs[p].K * rowf;
-        const double build = phase_cost(probs[p], nb);
+        const double build = phase_cost(probs[p], nb, engine);
         for (int b = 0; b < probs[p].RB; ++b) {
             double add = c;
             if (taken == 0 || (probs[p].nch > 1 && taken % seg == 0)) add += build;
@@ -667,21 +964,22 @@ int partition(const std::vector<GProb>& probs, double T, std::vector<GRange>* ou
     return ctas;
 }
 
-bool plan_layout(const std::vector<GProb>& probs, int nctas, int nb, GHeader& h, std::vector<GRange>& ranges) {
+bool plan_layout(const std::vector<GProb>& probs, int nctas, int nb, int engine, GHeader& h,
+                 std::vector<GRange>& ranges) {
     const int n = (int)probs.size();
-    const int CG = g_chunk_groups(nb), seg = g_seg_blocks(nb);
-    const double rowf = 1.0 + 0.8 * (nb - 1);
+    const int CG = chunk_groups(nb, engine), seg = seg_blocks(nb, engine);
+    const double rowf = row_factor(nb, engine);
     double total = 0.0;
     for (int p = 0; p < n; ++p)
-        total += (double)probs[p].RB * probs[p].K * rowf + phase_cost(probs[p], nb);
+        total += (double)probs[p].RB * probs[p].K * rowf + phase_cost(probs[p], nb, engine);
     double lo = total / nctas, hi = total + (kGBuildCost + kGPhaseFixed + kGPhaseTables) * nb * 8;
     for (int it = 0; it < 60 && hi - lo > 1e-4 * lo; ++it) {
         const double mid = 0.5 * (lo + hi);
-        if (partition(probs, mid, nullptr, nb) <= nctas) hi = mid;
+        if (partition(probs, mid, nullptr, nb, engine) <= nctas) hi = mid;
         else lo = mid;
     }
     ranges.clear();
-    partition(probs, hi, &ranges, nb);
+    partition(probs, hi, &ranges, nb, engine);
     while ((int)ranges.size() < nctas)            // CTAs without work
         ranges.push_back(GRange{n - 1, probs[n - 1].RB, n - 1, probs[n - 1].RB});
     for (const GRange& r : ranges)
@@ -698,18 +996,20 @@ bool plan_layout(const std::vector<GProb>& probs, int nctas, int nb, GHeader& h,
     h.nb = nb;
     h.part_rows = part_rows;
     h.seg_blocks = seg;
-    const int tables = nb * CG * kT6GroupBytes;
+    h.engine = engine;
+    // table engine: every batch row's tables; MMA engine: the chunk's activation fragments
+    const int tables = engine == kGEngineMma ? g_mma_nt(nb) * CG * 8 * 32 * 8 : nb * CG * kT6GroupBytes;
     // (warps, stages per warp) in order of preference; the first that fits
     // wins.  Several batch rows: at most 16 warps (the kernel's register cap).
     static const int kCfg[][2] = {{20, 1}, {16, 1}, {12, 1}, {8, 2}, {8, 1}};
     for (const auto& cf : kCfg) {
         const int W = cf[0], S = cf[1];
-        if (nb > 1 && W > 16) continue;
+        if ((nb > 1 || engine == kGEngineMma) && W > 16) continue;   // those kernels: at most 16 warps
         {
             uint32_t off = (uint32_t)(W * S * kGStageBytes);
             const uint32_t off_tables = off;  off += tables;
-            const uint32_t off_fac = off;     off += nb * CG * 8;      // 2^m_g and 2^-m_g per row
-            const uint32_t off_xraw = off;    off += nb * CG * 128 * 2;
+            const uint32_t off_fac = off;     off += std::max(nb * CG * 8, 32 * 4);   // table engine: 2^m_g and 2^-m_g per row and group; MMA engine: 2^-m_b, 2^m_b
+            const uint32_t off_xraw = off;    off += engine == kGEngineMma ? 0 : nb * CG * 128 * 2;
             const uint32_t off_pinfo = off;   off += kGMaxProbsPerCta * 16;
             const uint32_t off_part = off;    off += (uint32_t)(part_rows * nb) * 4;
             if (nb == 1) off += (uint32_t)((W - 1) * (CG / 8) * 32) * 4;   // unit partials (see GCtx)
@@ -754,21 +1054,23 @@ size_t group_plan_bytes(int count) {
     return probs_off + (size_t)count * sizeof(GProb);
 }
 
-bit1_status group_plan(const bit1_gemv_problem* problems, int count, int nb, int layout, void* host_plan,
-                       size_t bytes) {
+bit1_status group_plan(const bit1_gemv_problem* problems, int count, int nb, int layout, int engine,
+                       void* host_plan, size_t bytes) {
     if (count < 1 || !problems || !host_plan) return BIT1_EINVAL;
-    if (nb < 1 || nb > kGMaxNB) return BIT1_ESHAPE;
+    if (engine != kGEngineTables && engine != kGEngineMma) return BIT1_EINVAL;
+    if (nb < 1 || nb > (engine == kGEngineMma ? kGMaxNBMma : kGMaxNB)) return BIT1_ESHAPE;
     if (layout != kLayoutCanonical && layout != kLayoutG128x) return BIT1_EINVAL;
+    if (engine == kGEngineMma && layout != kLayoutCanonical) return BIT1_EINVAL;
     if (bytes < group_plan_bytes(count) || ((uintptr_t)host_plan & 127)) return BIT1_EINVAL;
     for (int i = 0; i < count; ++i)
         if (!problem_ok(problems[i])) return BIT1_ESHAPE;
     std::vector<GProb> probs(count);
     for (int i = 0; i < count; ++i)
-        if (!encode_prob(probs[i], problems[i], nb)) return BIT1_ECUDA;
+        if (!encode_prob(probs[i], problems[i], nb, engine)) return BIT1_ECUDA;
     GHeader h{};
     std::vector<GRange> ranges;
     const int nctas = std::min(sm_count(), kGMaxCtas);
-    if (!plan_layout(probs, nctas, nb, h, ranges)) return BIT1_ESHAPE;
+    if (!plan_layout(probs, nctas, nb, engine, h, ranges)) return BIT1_ESHAPE;
     h.layout = layout;
     const size_t r_off = sizeof(GHeader);
     const size_t p_off = (r_off + (size_t)kGMaxCtas * sizeof(GRange) + 127) & ~(size_t)127;
@@ -802,8 +1104,15 @@ cudaError_t launch_group(const void* device_plan, const void* host_plan, bool pd
     if (h->kind != kPlanKindTables) return cudaErrorInvalidValue;
     if (h->S != 1 && h->S != 2) return cudaErrorInvalidValue;
     if (h->layout != kLayoutCanonical && h->layout != kLayoutG128x) return cudaErrorInvalidValue;
-    const void* fn = h->layout == kLayoutG128x ? group_kernel<kLayoutG128x>(h->nb, h->S)
-                                               : group_kernel<kLayoutCanonical>(h->nb, h->S);
+    const void* fn = nullptr;
+    if (h->engine == kGEngineMma) {
+        if (h->layout != kLayoutCanonical || h->nb < 1 || h->nb > kGMaxNBMma) return cudaErrorInvalidValue;
+        fn = g_mma_nt(h->nb) == 1 ? (h->S == 2 ? (const void*)k_gemv_group_mma<1, 2> : (const void*)k_gemv_group_mma<1, 1>)
+                                  : (h->S == 2 ? (const void*)k_gemv_group_mma<2, 2> : (const void*)k_gemv_group_mma<2, 1>);
+    } else if (h->engine == kGEngineTables) {
+        fn = h->layout == kLayoutG128x ? group_kernel<kLayoutG128x>(h->nb, h->S)
+                                       : group_kernel<kLayoutCanonical>(h->nb, h->S);
+    }
     if (!fn) return cudaErrorInvalidValue;
     cudaError_t e = set_smem_attr(fn);
     if (e != cudaSuccess) return e;
@@ -865,11 +1174,11 @@ cudaError_t launch_gemv_group1(const GemvArgs& a) {
         pb.epilogue = a.swiglu ? BIT1_EPI_SWIGLU : BIT1_EPI_NONE;
         if (!problem_ok(pb)) return cudaErrorInvalidValue;
         std::vector<GProb> probs(1);
-        if (!encode_prob(probs[0], pb, nb)) return cudaErrorInvalidValue;
+        if (!encode_prob(probs[0], pb, nb, kGEngineTables)) return cudaErrorInvalidValue;
         std::memset(&single, 0, sizeof(single));
         std::vector<GRange> ranges;
         const int nctas = std::min(sm_count(), kGMaxCtas);
-        if (!plan_layout(probs, nctas, nb, single.h, ranges)) return cudaErrorInvalidValue;
+        if (!plan_layout(probs, nctas, nb, kGEngineTables, single.h, ranges)) return cudaErrorInvalidValue;
         single.h.layout = kLayoutCanonical;
         single.h.ranges_off = (int)offsetof(GSingle, r);
         single.h.probs_off = (int)offsetof(GSingle, p);

@@ -69,8 +69,10 @@ constexpr int kPlanKindTensor = 1;        // gemv_tc_group.cu (tensor cores, B <
 
 // Grouped persistent kernel (gemv_group.cu).
 size_t group_plan_bytes(int count);
-bit1_status group_plan(const bit1_gemv_problem* problems, int count, int nb, int layout, void* host_plan,
-                       size_t bytes);
+// engine: 0 = 6-bit tables (1 <= nb <= 6, either layout), 1 = register-sourced
+// MMAs (1 <= nb <= 16, canonical layout).
+bit1_status group_plan(const bit1_gemv_problem* problems, int count, int nb, int layout, int engine,
+                       void* host_plan, size_t bytes);
 cudaError_t launch_group(const void* device_plan, const void* host_plan, bool pdl, cudaStream_t stream);
 bool group1_supported(int64_t B, int64_t N, int64_t K);
 int group1_launch_count(int64_t B);          // ceil(B / 6): up to 6 rows per launch

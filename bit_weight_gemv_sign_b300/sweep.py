@@ -173,7 +173,7 @@ class Sweep:
         self.layout = LAYOUT_CANONICAL
         return self
 
-    def group_plan(self, x=None, y=None, tensor_cores: bool = False):
+    def group_plan(self, x=None, y=None, tensor_cores: bool = False, mma: bool = False):
         """One grouped launch over every matrix of the sweep (each with its own
         input, ``batch`` rows of it): the plan is built once; run() is one
         kernel launch (two with ``tensor_cores``: the activation prep and the
@@ -185,7 +185,7 @@ class Sweep:
         probs = [(self.bits_of(i), self.scales_of(i), self.x_of(i, x), self.y_of(i, y),
                   EPI_SWIGLU if m.swiglu else EPI_NONE) for i, m in enumerate(self.mats)]
         return GroupPlan(probs, device=self.device, B=self.B, layout=getattr(self, "layout", LAYOUT_CANONICAL),
-                         tensor_cores=tensor_cores)
+                         tensor_cores=tensor_cores, mma=mma)
 
     def apply_patch(self, entries, proj_count: int = 7):
         """Apply (or, applied again, remove) a list of (layer, projection, row)

@@ -249,6 +249,18 @@ bit1_status bit1_group_plan_batched(const bit1_gemv_problem *problems, int count
 bit1_status bit1_group_plan_ex(const bit1_gemv_problem *problems, int count, int B,
                                int layout, void *host_plan, size_t plan_bytes);
 
+/* The same batched grouped product (canonical layout, 1 <= B <= 16, else
+ * BIT1_ESHAPE) on register-sourced tensor-core MMAs (mma.sync m16n8k16,
+ * fp16 operands, fp32 accumulation): weights become +-s in fp16 registers,
+ * each problem's activations are converted per K chunk of 2048 (B <= 8) or
+ * 1024 inputs (B > 8) to fp16 with an exact per-row power-of-two prescale,
+ * and the batch rows are the MMA's columns, so the work per weight does not
+ * grow with B.  Same plan buffer size and the same bit1_gemv_group call;
+ * results agree with the table engine within the GEMV tolerance (different
+ * summation order) and are deterministic run to run. */
+bit1_status bit1_group_plan_mma(const bit1_gemv_problem *problems, int count, int B,
+                                void *host_plan, size_t plan_bytes);
+
 /* Runs a plan made by any bit1_group_plan* call above or below (the plan
  * records which kernel it is for).  flags: BIT1_FLAG_PDL or 0. */
 bit1_status bit1_gemv_group(const void *device_plan, const void *host_plan,
