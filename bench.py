@@ -1016,6 +1016,42 @@ def run_mine(args):
     return 0
 
 
+def run_profile_case(args):
+    """One grouped plan over the 8B-class sweep (or its first --layers layers)
+    at --batch rows on --engine, run --warmup + --steps times: the small,
+    short command that the ncu summaries under profiles/ capture.  Prints one
+    JSON line (a profiling run, not the benchmark)."""
+    import torch
+    import bit_weight_gemv_sign_b300 as b1
+    from bit_weight_gemv_sign_b300 import synth
+    from bit_weight_gemv_sign_b300.sweep import Sweep
+    b1.load()
+    mats = synth.sweep_8b()
+    if args.layers is not None:
+        mats = mats[:7 * args.layers] + mats[-1:]
+    sw = Sweep(mats, seed0=0, batch=args.batch, y_dtype=b1.BF16).fill_device(5)
+    if args.engine == "tables" and args.batch == 1:
+        sw.to_g128x()
+    plan = sw.group_plan(tensor_cores=args.engine == "tc", mma=args.engine == "mma")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(max(1, args.warmup)):
+            plan.run(flags=b1.FLAG_PDL, stream=s)
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(args.steps):
+            plan.run(flags=b1.FLAG_PDL, stream=s)
+        e1.record(s)
+        e1.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    print(json.dumps({"profile_case": f"{len(mats)} GEMVs of the 8B-class sweep", "engine": args.engine,
+                      "batch": args.batch, "ms_per_step": ms, "weight_bytes": sw.weight_bytes,
+                      "weight_gbs": sw.weight_bytes / (ms * 1e-3) / 1e9,
+                      "device_wait_timeouts": b1.bit1_device_wait_timeouts()}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1027,9 +1063,14 @@ def main():
                     help="profiling: only the first L decoder layers of the sweep and its LM head")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the other configurations (tiny, projections, crossover, 27B sweep)")
+    ap.add_argument("--engine", default=None, choices=["tables", "mma", "tc"],
+                    help="profiling: time only one grouped plan at --batch rows on this engine")
+    ap.add_argument("--batch", type=int, default=1, help="batch rows per matrix for --engine")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.engine is not None:
+        return run_profile_case(args)
     return run_mine(args)
 
 

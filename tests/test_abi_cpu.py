@@ -269,6 +269,23 @@ def test_group_tc_plan_checked_on_host(lib):
     assert call(pr=odd, c=1) == b1.ESHAPE
 
 
+def test_group_plan_mma_checked_on_host(lib):
+    """The MMA-engine grouped plan: B outside [1, 16] and bad problems are
+    refused on the host, before any CUDA call."""
+    import numpy as np
+    n = lib.bit1_group_plan_bytes(1)
+    raw = np.zeros(n + 128, dtype=np.uint8)
+    off = (-raw.ctypes.data) % 128
+    plan = raw[off:off + n]
+    p = b1._Problem(FAKE, FAKE, FAKE, FAKE, 300, 4096, b1.F32, 0)
+    for B in (0, 17, -3):
+        assert lib.bit1_group_plan_mma(ctypes.byref(p), 1, B, plan.ctypes.data, n) == b1.ESHAPE, B
+    bad = b1._Problem(FAKE, FAKE, FAKE, FAKE, 300, 1152, b1.F32, 0)       # K % 1024 != 0
+    assert lib.bit1_group_plan_mma(ctypes.byref(bad), 1, 4, plan.ctypes.data, n) == b1.ESHAPE
+    assert lib.bit1_group_plan_mma(ctypes.byref(p), 1, 4, plan.ctypes.data, n - 1) == b1.EINVAL
+    assert lib.bit1_group_plan_mma(ctypes.byref(p), 0, 4, plan.ctypes.data, n) == b1.EINVAL
+
+
 def test_sweep_feeds_swiglu_output_to_the_next_matrix():
     """Host wiring of the fused chain: the matrix after a SwiGLU matrix reads
     its h; a grouped plan over such a sweep is refused (its problems run
