@@ -112,7 +112,6 @@ __global__ void __launch_bounds__(kTcPrepThreads) k_tcg_prep(const uint8_t* __re
 // with a latency of several steps, and the A stages are bounded by tensor
 // memory.
 // Tensor memory: accumulator (half h, slice parity q) at columns (2h + q) Bp;
-// Tensor memory: accumulator (half h, slice parity q) at columns (2h + q) Bp;
 // A stage st, half h at abase + 128 st + 64 h, abase = 4 Bp rounded up to 128.
 //
 // MMA issue: one thread issues a tcgen05.mma about every 150-200 cycles (the
@@ -120,7 +119,7 @@ __global__ void __launch_bounds__(kTcPrepThreads) k_tcg_prep(const uint8_t* __re
 // step (2 halves x 8 slices of 16 inputs) are spread over 4 issuer warps,
 // each with its own accumulator.  (Eight issuers with eight accumulators
 // measured no faster: the step time is set by the stage round trip, see
-// the notes on the pipeline below.)
+// the notes at the top of this file.)
 __global__ void __launch_bounds__(kTgThreads, 1) k_gemv_tc_group(const uint8_t* __restrict__ plan) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = (uint32_t)__cvta_generic_to_shared(smem_raw);
@@ -310,7 +309,7 @@ __global__ void __launch_bounds__(kTgThreads, 1) k_gemv_tc_group(const uint8_t* 
                 for (int t = ts(p); t < te(p) && ok; ++t) {
                     for (int c = 0; c < nch; ++c, ++gc) {
                         const int ws = gc % kTgWSlots;
-                        if (gc >= kTgWSlots && !mbar_wait(wempty + 8 * ws, (uint32_t)(gc / kTgWSlots - 1) & 1u)) {
+                        if (gc >= kTgWSlots && !mbar_wait_sleep(wempty + 8 * ws, (uint32_t)(gc / kTgWSlots - 1) & 1u)) {
                             ok = false;
                             break;
                         }
@@ -336,7 +335,7 @@ __global__ void __launch_bounds__(kTgThreads, 1) k_gemv_tc_group(const uint8_t* 
                 const int nst = pr.K / kTcStepK;
                 for (int t = ts(p); t < te(p) && ok; ++t) {
                     for (int s = 0; s < nst; ++s, ++gs) {
-                        if (use > 0 && !mbar_wait(bfree + 8 * st, (uint32_t)(use - 1) & 1u)) {
+                        if (use > 0 && !mbar_wait_sleep(bfree + 8 * st, (uint32_t)(use - 1) & 1u)) {
                             ok = false;
                             break;
                         }
@@ -377,8 +376,8 @@ __global__ void __launch_bounds__(kTgThreads, 1) k_gemv_tc_group(const uint8_t* 
                 const int nst = P[p].K / kTcStepK;
                 for (int t = ts(p); t < te(p) && ok; ++t) {
                     for (int s = 0; s < nst; ++s) {
-                        if (!mbar_wait(afull + 8 * st, (uint32_t)ause & 1u) ||
-                            !mbar_wait(bfull + 8 * bs, (uint32_t)buse & 1u)) {
+                        if (!mbar_wait_sleep(afull + 8 * st, (uint32_t)ause & 1u) ||
+                            !mbar_wait_sleep(bfull + 8 * bs, (uint32_t)buse & 1u)) {
                             ok = false;
                             break;
                         }

@@ -30,6 +30,20 @@ __device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t saddr) {
 __device__ __forceinline__ uint32_t tc_idesc_f16(int n) {
     return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
+// Bounded wait for a single waiting thread that is expected to block for a
+// while (a producer or an MMA issuer): each try_wait may suspend the thread
+// for up to 20 us until the phase completes, so the waiting thread does not
+// spend its sub-partition's issue slots on polling; 2^19 polls bound the wait
+// (seconds).
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < (1u << 19); ++i) {
+        uint32_t done;
+        asm volatile("{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p;}"
+                     : "=r"(done) : "r"(bar), "r"(parity), "r"(20000u) : "memory");
+        if (done) return true;
+    }
+    return false;
+}
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
