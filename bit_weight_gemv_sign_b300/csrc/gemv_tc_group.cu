@@ -21,8 +21,8 @@
 // problem over its whole K.  The concatenated tiles of all problems are cut
 // into one contiguous, cost-balanced range per CTA (one CTA per SM); every
 // role walks the same tile sequence, and the rings (sign bits: 4 slots of 4
-// steps; A in tensor memory and B in shared memory: 2-3 stages) run on
-// without draining at tile boundaries.  After a tile's last step the unpack
+// steps; A in tensor memory: 2-3 steps; activations in shared memory: up to
+// 32 steps) run on without draining at tile boundaries.  After a tile's last step the unpack
 // warps wait for its accumulators, read them back and write y (or the SwiGLU
 // output); the next tile's first MMA overwrites the accumulators only after
 // that (its A operand is written after the read-back).  No split K: every
