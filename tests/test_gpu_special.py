@@ -59,3 +59,24 @@ def test_non_finite_activations(orc, variant, B):
         torch.cuda.synchronize()
         _compare(y, ref, bound, f"variant {variant} B={B} y_dtype={ydt}")
     assert b1.bit1_device_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("engine,B", [("mma", 5), ("mma", 12), ("tc", 5), ("tc", 16)])
+def test_non_finite_activations_grouped_engines(orc, engine, B):
+    """The same rows through the batched grouped engines (register-sourced
+    MMAs, tcgen05 plan): a non-finite input must not hide the other batch
+    rows' products (each row has its own prescale), and its own row follows
+    the oracle's Inf / NaN pattern."""
+    N, K = 512, 4096
+    bits, scales, x = _inputs(N, K, B, 9100 + B)
+    ref = orc.gemv(bits, scales, x, B, N, K)
+    with np.errstate(invalid="ignore"):
+        bound = abs_bound(scales, x, K)
+    for ydt in (b1.F32, b1.BF16):
+        y = torch.empty((B, N), dtype=torch.bfloat16 if ydt == b1.BF16 else torch.float32, device="cuda")
+        plan = b1.GroupPlan([(dev_u8(bits), dev_u16(scales), dev_bf16(x).view(B, K), y)], B=B,
+                            mma=engine == "mma", tensor_cores=engine == "tc")
+        plan.run()
+        torch.cuda.synchronize()
+        _compare(y, ref, bound, f"grouped {engine} B={B} y_dtype={ydt}")
+    assert b1.bit1_device_wait_timeouts() == 0
