@@ -14,7 +14,7 @@ import threading
 
 __all__ = [
     "Bit1Error", "OK", "EINVAL", "ESHAPE", "ERANGE", "ECUDA", "ENAN",
-    "F32", "BF16", "F16", "AUTO", "SIMPLE", "LUT", "SPLITK", "TC", "LUT6", "STREAM", "FLAG_PDL",
+    "F32", "BF16", "F16", "AUTO", "SIMPLE", "LUT", "SPLITK", "TC", "LUT6", "STREAM", "MMA", "FLAG_PDL",
     "FLAG_SWIGLU", "EPI_NONE", "EPI_SWIGLU",
     "bit1_pack", "bit1_pack_flags_status", "bit1_gemv", "bit1_gemv_ex",
     "bit1_gemv_workspace_bytes", "bit1_gemv_pick", "bit1_gemv_launches",
@@ -31,7 +31,7 @@ __all__ = [
 
 OK, EINVAL, ESHAPE, ERANGE, ECUDA, ENAN = 0, 1, 2, 3, 4, 5
 F32, BF16, F16 = 0, 1, 2
-AUTO, SIMPLE, LUT, SPLITK, TC, LUT6, STREAM = 0, 1, 2, 3, 4, 5, 6
+AUTO, SIMPLE, LUT, SPLITK, TC, LUT6, STREAM, MMA = 0, 1, 2, 3, 4, 5, 6, 7
 FLAG_PDL = 1
 FLAG_SWIGLU = 2
 EPI_NONE, EPI_SWIGLU = 0, 1

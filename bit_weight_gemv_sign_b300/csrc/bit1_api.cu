@@ -96,15 +96,21 @@ bool tc_beats_tables(int64_t B, int64_t N, int64_t K, bool t6_ok) {
 // Batch 1 below 65536 rows: the nibble-table kernel (one launch of it is the
 // shortest for the projection sizes of 8B-27B models: less set-up than the
 // cluster kernel); otherwise the 6-bit-table kernel (up to 8 batch rows per
-// launch); shapes it cannot split (K = 17408): the grouped kernel with the
-// one problem (up to 6 rows per launch, any K that is a multiple of 1024);
-// what none of them takes: one warp per row.
+// launch), or the register-MMA engine with the one problem from 12 rows at
+// K <= 4096; shapes the 6-bit kernel cannot split (K = 17408): the grouped
+// kernel with the one problem, on the register-MMA engine from 3 rows and on
+// tables below; what none of them takes: one warp per row (per-call times
+// measured on one B300).
 int pick_variant(int64_t B, int64_t N, int64_t K, size_t ws_bytes) {
     const bool t6_ok = t6_supported(B, N, K);
     if (tc_supported(B, N, K) && ws_bytes >= tc_min_workspace_bytes(B, N, K) && tc_beats_tables(B, N, K, t6_ok))
         return BIT1_GEMV_TC;
     if (B == 1 && N < 65536 && lut_supported(B, N, K)) return BIT1_GEMV_LUT;
-    if (t6_ok) return BIT1_GEMV_LUT6;
+    // Without the tensor cores, the register-MMA engine from 12 rows at
+    // K <= 4096 (its work per weight does not grow with the rows; the tables'
+    // does), and from 3 rows where the 6-bit tables cannot split K.
+    if (t6_ok) return (B >= 12 && K <= 4096 && mma1_supported(B, N, K)) ? BIT1_GEMV_MMA : BIT1_GEMV_LUT6;
+    if (B >= 3 && mma1_supported(B, N, K)) return BIT1_GEMV_MMA;
     if (group1_supported(B, N, K)) return BIT1_GEMV_STREAM;
     if (lut_supported(B, N, K)) return BIT1_GEMV_LUT;
     return BIT1_GEMV_SIMPLE;
@@ -161,6 +167,7 @@ bit1_status gemv_check(const uint8_t* bits, const uint16_t* scales, const uint16
         case BIT1_GEMV_SIMPLE: return BIT1_OK;
         case BIT1_GEMV_LUT: return lut_supported(B, N, K) ? BIT1_OK : BIT1_ESHAPE;
         case BIT1_GEMV_STREAM: return group1_supported(B, N, K) ? BIT1_OK : BIT1_ESHAPE;
+        case BIT1_GEMV_MMA: return mma1_supported(B, N, K) ? BIT1_OK : BIT1_ESHAPE;
         case BIT1_GEMV_TC:
             if (!tc_supported(B, N, K)) return BIT1_ESHAPE;
             return ws_bytes < tc_min_workspace_bytes(B, N, K) ? BIT1_EINVAL : BIT1_OK;
@@ -188,6 +195,7 @@ bit1_status gemv_run(const uint8_t* bits, const uint16_t* scales, const uint16_t
         case BIT1_GEMV_SPLITK:
         case BIT1_GEMV_LUT6: return from_cuda(launch_gemv_t6(a));
         case BIT1_GEMV_STREAM: return from_cuda(launch_gemv_group1(a));
+        case BIT1_GEMV_MMA: return from_cuda(launch_gemv_mma1(a));
         case BIT1_GEMV_TC: return from_cuda(launch_gemv_tc(a));
         default: return BIT1_EINVAL;
     }
@@ -238,6 +246,7 @@ int bit1_gemv_launches(int64_t B, int64_t N, int64_t K, int variant) {
         case BIT1_GEMV_SPLITK:
         case BIT1_GEMV_LUT6: return t6_launch_count(B, N, K);
         case BIT1_GEMV_STREAM: return group1_supported(B, N, K) ? group1_launch_count(B) : 0;
+        case BIT1_GEMV_MMA: return mma1_supported(B, N, K) ? mma1_launch_count(B) : 0;
         case BIT1_GEMV_TC: return tc_launch_count(B, N, K);
         default: return 0;
     }

@@ -828,6 +828,13 @@ __global__ void __launch_bounds__(16 * 32, 1) k_gemv_group_mma(const uint8_t* __
     g_body_mma<NT, g_mma_chunk_groups(8 * NT), S>(plan);
 }
 
+// One problem on the MMA engine with its plan passed by value (bit1_gemv_ex
+// with BIT1_GEMV_MMA).
+template <int NT, int S>
+__global__ void __launch_bounds__(16 * 32, 1) k_gemv_group1_mma(const __grid_constant__ GSingle plan) {
+    g_body_mma<NT, g_mma_chunk_groups(8 * NT), S>(reinterpret_cast<const uint8_t*>(&plan));
+}
+
 // S: TMA stages per warp ring (the plan's H->S); L: the sign-bit layout (the
 // plan's H->layout).  One instantiation per value the planner can choose.
 template <int S, int L>
@@ -1172,7 +1179,13 @@ cudaError_t launch_gemv_group1(const GemvArgs& a) {
         pb.K = a.K;
         pb.y_dtype = a.y_bf16 ? BIT1_BF16 : BIT1_F32;
         pb.epilogue = a.swiglu ? BIT1_EPI_SWIGLU : BIT1_EPI_NONE;
+        // y of a later launch starts b0 rows in, which need not be 16-byte
+        // aligned; the kernels store y element by element, so the caller's
+        // (checked) base pointer is what the shape check sees.
+        void* const y_rows = pb.y;
+        pb.y = a.y;
         if (!problem_ok(pb)) return cudaErrorInvalidValue;
+        pb.y = y_rows;
         std::vector<GProb> probs(1);
         if (!encode_prob(probs[0], pb, nb, kGEngineTables)) return cudaErrorInvalidValue;
         std::memset(&single, 0, sizeof(single));
@@ -1187,6 +1200,65 @@ cudaError_t launch_gemv_group1(const GemvArgs& a) {
         if (single.h.S != 1 && single.h.S != 2) return cudaErrorInvalidValue;
         const void* fn = group1_kernel_nb(nb, single.h.S);
         if (!fn) return cudaErrorInvalidValue;
+        cudaError_t e = set_smem_attr(fn);
+        if (e != cudaSuccess) return e;
+        void* args[] = {(void*)&single};
+        e = launch(fn, dim3((unsigned)single.h.nctas), dim3((unsigned)(single.h.W * 32)), (size_t)single.h.smem_bytes,
+                   a.stream, a.pdl, args);
+        if (e != cudaSuccess) return e;
+        b0 += nb;
+    }
+    return cudaSuccess;
+}
+
+bool mma1_supported(int64_t B, int64_t N, int64_t K) { return group1_supported(B, N, K); }
+
+int mma1_launch_count(int64_t B) { return (int)((B + kGMaxNBMma - 1) / kGMaxNBMma); }
+
+// One problem on the MMA engine: B rows in ceil(B / 16) launches of balanced
+// row counts, each with its plan passed by value.
+cudaError_t launch_gemv_mma1(const GemvArgs& a) {
+    if (!mma1_supported(a.B, a.N, a.K)) return cudaErrorInvalidValue;
+    const int launches = mma1_launch_count(a.B);
+    const int64_t out_n = a.swiglu ? a.N / 2 : a.N;
+    const size_t ysz = a.y_bf16 ? 2 : 4;
+    static GSingle single;  // large: keep off the stack; filled and copied into each launch
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    int64_t b0 = 0;
+    for (int l = 0; l < launches; ++l) {
+        const int nb = (int)((a.B - b0 + (launches - l) - 1) / (launches - l));
+        bit1_gemv_problem pb{};
+        pb.bits = a.bits;
+        pb.scales = a.scales;
+        pb.x = a.x + b0 * a.K;
+        pb.y = static_cast<uint8_t*>(a.y) + (size_t)b0 * (size_t)out_n * ysz;
+        pb.N = a.N;
+        pb.K = a.K;
+        pb.y_dtype = a.y_bf16 ? BIT1_BF16 : BIT1_F32;
+        pb.epilogue = a.swiglu ? BIT1_EPI_SWIGLU : BIT1_EPI_NONE;
+        // y of a later launch starts b0 rows in, which need not be 16-byte
+        // aligned; the kernels store y element by element, so the caller's
+        // (checked) base pointer is what the shape check sees.
+        void* const y_rows = pb.y;
+        pb.y = a.y;
+        if (!problem_ok(pb)) return cudaErrorInvalidValue;
+        pb.y = y_rows;
+        std::vector<GProb> probs(1);
+        if (!encode_prob(probs[0], pb, nb, kGEngineMma)) return cudaErrorInvalidValue;
+        std::memset(&single, 0, sizeof(single));
+        std::vector<GRange> ranges;
+        const int nctas = std::min(sm_count(), kGMaxCtas);
+        if (!plan_layout(probs, nctas, nb, kGEngineMma, single.h, ranges)) return cudaErrorInvalidValue;
+        single.h.layout = kLayoutCanonical;
+        single.h.ranges_off = (int)offsetof(GSingle, r);
+        single.h.probs_off = (int)offsetof(GSingle, p);
+        std::memcpy(single.r, ranges.data(), ranges.size() * sizeof(GRange));
+        single.p = probs[0];
+        if (single.h.S != 1 && single.h.S != 2) return cudaErrorInvalidValue;
+        const bool one = g_mma_nt(nb) == 1;
+        const void* fn = one ? (single.h.S == 2 ? (const void*)k_gemv_group1_mma<1, 2> : (const void*)k_gemv_group1_mma<1, 1>)
+                             : (single.h.S == 2 ? (const void*)k_gemv_group1_mma<2, 2> : (const void*)k_gemv_group1_mma<2, 1>);
         cudaError_t e = set_smem_attr(fn);
         if (e != cudaSuccess) return e;
         void* args[] = {(void*)&single};

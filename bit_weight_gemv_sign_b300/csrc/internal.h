@@ -77,6 +77,11 @@ cudaError_t launch_group(const void* device_plan, const void* host_plan, bool pd
 bool group1_supported(int64_t B, int64_t N, int64_t K);
 int group1_launch_count(int64_t B);          // ceil(B / 6): up to 6 rows per launch
 cudaError_t launch_gemv_group1(const GemvArgs& a);
+// One problem on the grouped kernel's register-sourced MMA engine (up to 16
+// rows per launch, ceil(B / 16) launches).
+bool mma1_supported(int64_t B, int64_t N, int64_t K);
+int mma1_launch_count(int64_t B);
+cudaError_t launch_gemv_mma1(const GemvArgs& a);
 unsigned int group_take_timeouts();
 
 // tcgen05 tensor-core batched kernel (gemv_tc.cu): K a multiple of 1024;

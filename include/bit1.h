@@ -68,8 +68,9 @@ enum bit1_dtype {
  * one B300: the tensor cores when the workspace allows them and they are the
  * faster (B >= 16; B >= 8; B >= 4 for N <= 8192; B >= 5 for N*K >= 64M;
  * any B >= 2 where the 6-bit tables cannot split K), else at batch 1 the
- * nibble-table kernel below 65536 rows, else the 6-bit tables, else the
- * grouped kernel with the one problem (STREAM), else one warp per row. */
+ * nibble-table kernel below 65536 rows, else the 6-bit tables (the MMA
+ * variant from B = 12 at K <= 4096), else the grouped kernel with the one
+ * problem (MMA from B = 3, STREAM below), else one warp per row. */
 enum bit1_gemv_variant {
     BIT1_GEMV_AUTO = 0,
     BIT1_GEMV_SIMPLE = 1,  /* any shape; one warp per row (reference-quality) */
@@ -84,12 +85,17 @@ enum bit1_gemv_variant {
                               tables per batch row, TMA-staged weights, K split
                               over a thread-block cluster; up to 8 batch rows
                               per launch (larger batches: several launches) */
-    BIT1_GEMV_STREAM = 6   /* K a multiple of 1024: the grouped kernel below
+    BIT1_GEMV_STREAM = 6,  /* K a multiple of 1024: the grouped kernel below
                               with the one problem (one CTA per SM streaming a
                               contiguous row range, full-K tables, no clusters;
                               no workspace); up to 6 batch rows per launch
                               (larger batches: ceil(B / 6) launches of
                               balanced row counts) */
+    BIT1_GEMV_MMA = 7      /* K a multiple of 1024: the grouped kernel with the
+                              one problem on register-sourced tensor-core MMAs
+                              (bit1_group_plan_mma's engine; no workspace); up
+                              to 16 batch rows per launch (larger batches:
+                              ceil(B / 16) launches of balanced row counts) */
 };
 
 /* bit1_gemv_ex flags. */

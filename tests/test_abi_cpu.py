@@ -100,7 +100,10 @@ def test_pick_and_launch_counts(lib):
     assert b1.bit1_gemv_workspace_bytes(1, 4096, 100) == 0
     # batched: the table kernel without scratch, the tensor cores from 16 rows with it
     assert b1.bit1_gemv_pick(4, 12288, 4096) == b1.LUT6
-    assert b1.bit1_gemv_pick(16, 12288, 4096) == b1.LUT6
+    assert b1.bit1_gemv_pick(16, 12288, 4096) == b1.MMA     # no scratch, many rows, K <= 4096: register MMAs
+    assert b1.bit1_gemv_pick(12, 4096, 4096) == b1.MMA
+    assert b1.bit1_gemv_pick(11, 4096, 4096) == b1.LUT6
+    assert b1.bit1_gemv_pick(16, 4096, 12288) == b1.LUT6    # K = 12288: the 6-bit tables stay faster
     ws = b1.bit1_gemv_workspace_bytes(16, 12288, 4096)
     assert ws > 0 and b1.bit1_gemv_pick(16, 12288, 4096, ws) == b1.TC
     # the measured crossover with scratch: 12288x4096 from 8 rows, N <= 8192 from 4,
@@ -116,7 +119,9 @@ def test_pick_and_launch_counts(lib):
     assert b1.bit1_gemv_pick(2, 5120, 17408, big) == b1.TC
     assert b1.bit1_gemv_pick(1, 5120, 17408, big) == b1.STREAM
     # without scratch, K = 17408 at 2-8 rows: the grouped kernel, up to 6 rows a launch
-    assert b1.bit1_gemv_pick(4, 5120, 17408) == b1.STREAM
+    assert b1.bit1_gemv_pick(4, 5120, 17408) == b1.MMA      # no 6-bit split, no scratch: register MMAs from 3 rows
+    assert b1.bit1_gemv_pick(2, 5120, 17408) == b1.STREAM
+    assert b1.bit1_gemv_launches(20, 5120, 17408, b1.MMA) == 2
     assert b1.bit1_gemv_launches(6, 5120, 17408, b1.STREAM) == 1
     assert b1.bit1_gemv_launches(8, 5120, 17408, b1.STREAM) == 2
     assert b1.bit1_gemv_launches(4, 12288, 4096, b1.LUT6) == 1

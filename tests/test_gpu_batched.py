@@ -7,7 +7,7 @@ import torch
 
 import bit_weight_gemv_sign_b300 as b1
 from bit_weight_gemv_sign_b300 import synth
-from tests.helpers import abs_bound, assert_gemv_close, dev_bf16, dev_u8, dev_u16
+from tests.helpers import abs_bound, assert_gemv_close, assert_swiglu_close, dev_bf16, dev_u8, dev_u16
 
 pytestmark = pytest.mark.gpu
 
@@ -103,14 +103,14 @@ def test_splitk_names_the_cluster_split_kernel():
 def test_k17408_small_batch_grouped_and_tensor_cores(orc, B):
     N, K = 5120, 17408
     bits, scales, x = _problem(N, K, B, 8200 + B)
-    assert b1.bit1_gemv_pick(B, N, K) == b1.STREAM
+    assert b1.bit1_gemv_pick(B, N, K) == (b1.STREAM if B < 3 else b1.MMA)
     assert b1.bit1_gemv_launches(B, N, K, b1.STREAM) == (B + 5) // 6
     # with bit1_gemv_workspace_bytes of scratch AUTO takes the tensor cores
     assert b1.bit1_gemv_launches(B, N, K, b1.AUTO) == b1.bit1_gemv_launches(B, N, K, b1.TC)
     ref = orc.gemv(bits, scales, x, B, N, K)
     bound = abs_bound(scales, x, K)
     y = _run(bits, scales, x, N, K, B, variant=b1.AUTO)
-    assert_gemv_close(y, ref, bound, f"grouped N={N} K={K} B={B}")
+    assert_gemv_close(y, ref, bound, f"AUTO without workspace N={N} K={K} B={B}")
     yb = _run(bits, scales, x, N, K, B, variant=b1.STREAM, y_dtype=b1.BF16)
     assert_gemv_close(yb, ref, bound, f"grouped bf16 N={N} K={K} B={B}")
     ws = torch.empty(b1.bit1_gemv_workspace_bytes(B, N, K), dtype=torch.uint8, device="cuda")
@@ -119,6 +119,15 @@ def test_k17408_small_batch_grouped_and_tensor_cores(orc, B):
     torch.cuda.synchronize()
     assert_gemv_close(yt, ref, bound, f"tensor cores N={N} K={K} B={B}")
     assert b1.bit1_device_wait_timeouts() == 0
+
+
+def test_stream_rows_split_with_unaligned_output_rows(orc):
+    """Seven rows as 4 + 3 over N = 513 bf16 outputs: the second launch's y
+    starts 4 * 513 * 2 bytes in (not 16-byte aligned)."""
+    N, K, B = 513, 4096, 7
+    bits, scales, x = _problem(N, K, B, 8220)
+    y = _run(bits, scales, x, N, K, B, variant=b1.STREAM, y_dtype=b1.BF16)
+    assert_gemv_close(y, orc.gemv(bits, scales, x, B, N, K), abs_bound(scales, x, K), "stream 4 + 3, N = 513")
 
 
 def test_stream_rows_split_over_launches():
@@ -131,3 +140,34 @@ def test_stream_rows_split_over_launches():
     y4 = _run(bits, scales, x[:4], N, K, 4, variant=b1.STREAM)
     y3 = _run(bits, scales, x[4:], N, K, 3, variant=b1.STREAM)
     assert torch.equal(y7[:4], y4) and torch.equal(y7[4:], y3)
+
+
+# (N, K, B): one chunk and several, ragged N, one and two 8-column tiles, two launches (B > 16)
+MMA1_SHAPES = [(1000, 4096, 1), (300, 12288, 3), (4096, 4096, 5), (777, 5120, 8), (129, 17408, 9),
+               (2048, 2048, 16), (513, 4096, 20)]
+
+
+@pytest.mark.parametrize("N,K,B", MMA1_SHAPES)
+def test_single_call_mma_variant_matches_oracle(orc, N, K, B):
+    """bit1_gemv_ex with BIT1_GEMV_MMA: the grouped kernel's register-MMA engine
+    with the one problem, fp32 and bf16 output, against the oracle."""
+    bits, scales, x = _problem(N, K, B, 8300 + B)
+    assert b1.bit1_gemv_launches(B, N, K, b1.MMA) == (B + 15) // 16
+    ref = orc.gemv(bits, scales, x, B, N, K)
+    bound = abs_bound(scales, x, K)
+    for ydt in (b1.F32, b1.BF16):
+        y = _run(bits, scales, x, N, K, B, variant=b1.MMA, y_dtype=ydt)
+        assert_gemv_close(y, ref, bound, f"mma variant N={N} K={K} B={B} y={ydt}")
+    assert b1.bit1_device_wait_timeouts() == 0
+
+
+def test_single_call_mma_variant_swiglu(orc):
+    N, K, B = 1026, 4096, 6
+    bits, scales, x = _problem(N, K, B, 8400)
+    yo = orc.gemv(bits, scales, x, B, N, K)
+    h = orc.gemv_swiglu(bits, scales, x, B, N, K)
+    bd = abs_bound(scales, x, K)
+    y = b1.bit1_gemv_ex(dev_u8(bits), dev_u16(scales), dev_bf16(x).view(B, K), variant=b1.MMA,
+                        flags=b1.FLAG_SWIGLU, N=N, K=K)
+    torch.cuda.synchronize()
+    assert_swiglu_close(y, h, yo[:, 0::2], yo[:, 1::2], bd[:, 0::2], bd[:, 1::2], "mma variant SwiGLU")
