@@ -463,7 +463,8 @@ def extra_c2_projections(torch, b1):
 
 def extra_c4_crossover(torch, b1):
     """CUDA-core path (6-bit tables, up to 8 batch rows per launch) vs the
-    tcgen05 path on the 8B MLP shapes."""
+    tcgen05 path on the 8B MLP shapes, with the register-MMA variant (no
+    workspace) beside them."""
     out = {}
     for N, K, name in ((12288, 4096, "up_gate"), (4096, 12288, "down")):
         rows = {}
@@ -471,7 +472,9 @@ def extra_c4_crossover(torch, b1):
         for B in (1, 4, 16, 32, 64):
             cc = _time_calls(torch, b1, N, K, B, b1.LUT6)
             tc = _time_calls(torch, b1, N, K, B, b1.TC)
-            rows[str(B)] = {"cuda_core": _shape_entry(N, K, B, cc), "tcgen05": _shape_entry(N, K, B, tc)}
+            mma = _time_calls(torch, b1, N, K, B, b1.MMA)
+            rows[str(B)] = {"cuda_core": _shape_entry(N, K, B, cc), "tcgen05": _shape_entry(N, K, B, tc),
+                            "mma_no_workspace": _shape_entry(N, K, B, mma)}
             if cross is None and cc is not None and tc is not None and tc < cc:
                 cross = B
         out[name] = {"shape": [N, K], "by_batch": rows, "tcgen05_faster_from_batch": cross}
