@@ -84,7 +84,7 @@ def test_verify_sweep_8b_b5_sampled_parity(orc):
 
 
 # ---------------------------------------------------------------- MMA engine
-MMA_SHAPES = SHAPES + [(514, 2048)]
+MMA_SHAPES = SHAPES + [(514, 8192)]      # the SwiGLU pair: two (B <= 8) or four (B > 8) K chunks
 
 
 def _mma_problems(B, seed, ydt, swiglu_last=True):
